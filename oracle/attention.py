@@ -1,0 +1,235 @@
+"""Exact attention, its gradient and the log-sum-exp merge, in float64.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).  Plain definitions,
+full score rows, no online softmax.  Query rows are independent of one another
+by definition (each row has its own softmax), so long sequences are processed
+in blocks of whole query rows purely to bound memory; within a block every
+row sees all of its keys at once.
+
+Notation: ``S = scale * Q K^T``, ``P = softmax_rows(S)`` over the visible keys,
+``O = P V``, ``LSE_i = log sum_j exp(S_ij)`` (natural log).  Backward for the
+loss ``<O, dO>``: ``dV = P^T dO``, ``dP = dO V^T``,
+``dS = P * (dP - rowsum(P * dP))`` (the softmax Jacobian applied row by row),
+``dQ = scale * dS K``, ``dK = scale * dS^T Q``.
+
+Readings where the pages are silent (each listed in the design doc):
+* scale is an explicit argument (the DISTFLASHATTN review writes
+  ``softmax(QK^T)V`` with no scale);
+* causal visibility uses global positions: key ``j`` is visible to query ``i``
+  iff ``kv_offset + j <= q_offset + i``;
+* a query row with no visible key has ``O = 0``, ``LSE = -inf`` and zero
+  gradients;
+* grouped-query attention maps query head ``h`` to key/value head
+  ``h // (Hq // Hkv)``, and dK/dV sum over the query heads of a group;
+* block-sparse: a kept ``block x block`` block is dense, a dropped one is
+  masked out entirely (FlashAttention abstract; BurstAttention author
+  responses: sparse attention only changes the mask matrix).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import numpy as np
+
+ROW_BLOCK = 1024  # query rows per block when a head is processed in pieces
+
+
+@dataclass(frozen=True)
+class MaskSpec:
+    """Which keys a query may see.
+
+    kind: ``"none"``, ``"causal"`` or ``"block_sparse"``.
+    block_mask: for ``block_sparse``, a boolean ``[ceil(Nq/block), ceil(Nk/block)]``
+        array shared by every batch and head; ``True`` keeps the block.
+    causal_in_blocks: for ``block_sparse``, additionally apply the element
+        causal rule inside kept blocks.
+    """
+
+    kind: str = "none"
+    block_mask: Optional[np.ndarray] = None
+    block: int = 128
+    causal_in_blocks: bool = False
+
+    def __post_init__(self):
+        if self.kind not in ("none", "causal", "block_sparse"):
+            raise ValueError(f"unknown mask kind {self.kind!r}")
+        if self.kind == "block_sparse" and self.block_mask is None:
+            raise ValueError("block_sparse needs a block_mask")
+
+
+def visible(rows: np.ndarray, nk: int, mask: MaskSpec,
+            q_offset: int = 0, kv_offset: int = 0) -> np.ndarray:
+    """Boolean ``[len(rows), nk]``: True where key ``j`` is visible to query ``rows[i]``.
+
+    ``rows`` are local query indices of this call; positions used by the
+    causal rule are ``q_offset + row`` and ``kv_offset + j``.
+    """
+    rows = np.asarray(rows, dtype=np.int64)
+    cols = np.arange(nk, dtype=np.int64)
+    vis = np.ones((rows.size, nk), dtype=bool)
+    causal = mask.kind == "causal" or (mask.kind == "block_sparse" and mask.causal_in_blocks)
+    if causal:
+        vis &= (kv_offset + cols)[None, :] <= (q_offset + rows)[:, None]
+    if mask.kind == "block_sparse":
+        bm = np.asarray(mask.block_mask, dtype=bool)
+        vis &= bm[(rows // mask.block)[:, None], (cols // mask.block)[None, :]]
+    return vis
+
+
+def head_forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
+                 vis: np.ndarray):
+    """One head, a set of query rows: returns ``(O [r, d], LSE [r])``.
+
+    ``q`` is ``[r, d]`` (the query rows), ``k``/``v`` are ``[nk, d]``, ``vis``
+    is the boolean ``[r, nk]`` visibility of each key.
+    """
+    s = scale * (q @ k.T)
+    s = np.where(vis, s, -np.inf)
+    m = s.max(axis=1) if s.shape[1] else np.full(s.shape[0], -np.inf)
+    has = np.isfinite(m)
+    m0 = np.where(has, m, 0.0)
+    e = np.exp(s - m0[:, None])            # exp(-inf) = 0 for hidden keys
+    l = e.sum(axis=1)
+    p = e / np.where(has, l, 1.0)[:, None]
+    o = p @ v
+    lse = np.where(has, m0 + np.log(np.where(has, l, 1.0)), -np.inf)
+    return o, lse
+
+
+def _probs(q, k, scale, vis):
+    s = scale * (q @ k.T)
+    s = np.where(vis, s, -np.inf)
+    m = s.max(axis=1) if s.shape[1] else np.full(s.shape[0], -np.inf)
+    has = np.isfinite(m)
+    e = np.exp(s - np.where(has, m, 0.0)[:, None])
+    l = e.sum(axis=1)
+    return e / np.where(has, l, 1.0)[:, None]
+
+
+def head_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, do: np.ndarray,
+                  scale: float, vis: np.ndarray):
+    """One head, a set of query rows: returns ``(dQ [r,d], dK [nk,d], dV [nk,d])``.
+
+    dK and dV are the contributions of these rows only (sum them over row sets
+    and over the query heads of a group).
+    """
+    p = _probs(q, k, scale, vis)
+    dv = p.T @ do
+    dp = do @ v.T
+    # softmax Jacobian-vector product, row by row: dS = P * (dP - <P, dP>)
+    ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+    dq = scale * (ds @ k)
+    dk = scale * (ds.T @ q)
+    return dq, dk, dv
+
+
+def _group(hq: int, hkv: int) -> int:
+    if hq % hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    return hq // hkv
+
+
+def attention_forward(q, k, v, scale: float, mask: MaskSpec = MaskSpec(),
+                      q_offset: int = 0, kv_offset: int = 0,
+                      heads: Optional[Sequence] = None,
+                      rows: Optional[np.ndarray] = None):
+    """Exact attention forward in float64.
+
+    ``q`` is ``[B, Hq, Nq, d]``, ``k``/``v`` are ``[B, Hkv, Nk, d]``.
+    Without ``heads``/``rows`` returns full ``O [B,Hq,Nq,d]`` and
+    ``LSE [B,Hq,Nq]``.  With ``heads`` (a list of ``(b, h)``) and ``rows``
+    (local query indices) returns ``O [len(heads), len(rows), d]`` and
+    ``LSE [len(heads), len(rows)]`` for that sample only.
+    """
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    g = _group(Hq, Hkv)
+    sample = heads is not None
+    if heads is None:
+        heads = [(b, h) for b in range(B) for h in range(Hq)]
+    rows = np.arange(Nq) if rows is None else np.asarray(rows, np.int64)
+    o_out = np.zeros((len(heads), rows.size, d))
+    l_out = np.zeros((len(heads), rows.size))
+    for n, (b, h) in enumerate(heads):
+        kk, vv = k[b, h // g], v[b, h // g]
+        for s0 in range(0, rows.size, ROW_BLOCK):
+            r = rows[s0:s0 + ROW_BLOCK]
+            vis = visible(r, Nk, mask, q_offset, kv_offset)
+            o, l = head_forward(q[b, h, r], kk, vv, scale, vis)
+            o_out[n, s0:s0 + r.size] = o
+            l_out[n, s0:s0 + r.size] = l
+    if sample:
+        return o_out, l_out
+    return o_out.reshape(B, Hq, rows.size, d), l_out.reshape(B, Hq, rows.size)
+
+
+def attention_backward(q, k, v, do, scale: float, mask: MaskSpec = MaskSpec(),
+                       q_offset: int = 0, kv_offset: int = 0,
+                       kv_heads: Optional[Sequence] = None):
+    """Exact gradient of ``<O, dO>`` with respect to Q, K, V, in float64.
+
+    Without ``kv_heads`` returns full ``dQ [B,Hq,Nq,d]``, ``dK``/``dV``
+    ``[B,Hkv,Nk,d]``.  With ``kv_heads`` (a list of ``(b, hkv)``) computes only
+    those key/value heads and the query heads of their groups, returning
+    ``dQ [len, g, Nq, d]``, ``dK [len, Nk, d]``, ``dV [len, Nk, d]``.
+    """
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64); do = np.asarray(do, np.float64)
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    g = _group(Hq, Hkv)
+    sample = kv_heads is not None
+    if kv_heads is None:
+        kv_heads = [(b, hk) for b in range(B) for hk in range(Hkv)]
+    dq = np.zeros((len(kv_heads), g, Nq, d))
+    dk = np.zeros((len(kv_heads), Nk, d))
+    dv = np.zeros((len(kv_heads), Nk, d))
+    for n, (b, hk) in enumerate(kv_heads):
+        for j in range(g):
+            h = hk * g + j
+            for s0 in range(0, Nq, ROW_BLOCK):
+                r = np.arange(s0, min(Nq, s0 + ROW_BLOCK))
+                vis = visible(r, Nk, mask, q_offset, kv_offset)
+                a, bk, bv = head_backward(q[b, h, r], k[b, hk], v[b, hk], do[b, h, r], scale, vis)
+                dq[n, j, r] = a
+                dk[n] += bk
+                dv[n] += bv
+    if sample:
+        return dq, dk, dv
+    return dq.reshape(B, Hq, Nq, d), dk.reshape(B, Hkv, Nk, d), dv.reshape(B, Hkv, Nk, d)
+
+
+def attention_backward_dq_rows(q, k, v, do, scale: float, b: int, h: int, rows,
+                               mask: MaskSpec = MaskSpec(), q_offset: int = 0,
+                               kv_offset: int = 0):
+    """dQ for selected query rows of one head (each dQ row depends on its own row only)."""
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64); do = np.asarray(do, np.float64)
+    g = _group(q.shape[1], k.shape[1])
+    rows = np.asarray(rows, np.int64)
+    vis = visible(rows, k.shape[2], mask, q_offset, kv_offset)
+    dq, _, _ = head_backward(q[b, h, rows], k[b, h // g], v[b, h // g], do[b, h, rows], scale, vis)
+    return dq
+
+
+def merge_partials(o_parts, lse_parts):
+    """Combine partial attention results over disjoint key sets.
+
+    Each part ``c`` holds ``O_c`` (normalised over its own keys) and
+    ``LSE_c``.  The result over the union of keys is
+    ``LSE = log sum_c exp(LSE_c)`` and ``O = sum_c exp(LSE_c - LSE) O_c``;
+    a part with ``LSE_c = -inf`` weighs zero, and a row where every part is
+    ``-inf`` gives ``O = 0``, ``LSE = -inf``.
+    (BurstAttention author responses: online-softmax combination of local
+    attention results across devices.)
+    """
+    lse = np.stack([np.asarray(x, np.float64) for x in lse_parts])
+    o = np.stack([np.asarray(x, np.float64) for x in o_parts])
+    total = np.logaddexp.reduce(lse, axis=0)
+    fin = np.isfinite(total)
+    with np.errstate(invalid="ignore"):
+        w = np.where(fin[None], np.exp(lse - np.where(fin, total, 0.0)[None]), 0.0)
+    out = (w[..., None] * o).sum(axis=0)
+    return out, total

@@ -1,0 +1,107 @@
+"""Integer work schedules, restated in plain Python.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).  These are the
+bookkeeping rules the CUDA library follows; tests compare the library's
+exported builders with these element by element.
+
+Readings (the pages describe load balancing only in words: DISTFLASHATTN
+reviews, first review points 1-2 and third review summary; FlashAttention-2
+reviews, fourth review on causal block skipping; none prints the schedule):
+
+* Forward work unit = one CTA = 256 query rows (two 128-row tiles) of one
+  (batch, query head).  Units are launched heaviest first: unit ``i`` takes
+  query chunk ``nqc - 1 - i // (B*Hq)`` of head ``i % (B*Hq)``.  Under a
+  causal mask the later query chunks see more key tiles, so this is the
+  longest-processing-time-first order that the hardware block scheduler then
+  assigns greedily to free SMs.
+* A unit's key tiles are the union of the key tiles its two query tiles see.
+* Chunk pairs for chunked causal attention: every ``(qc, kc)`` with
+  ``kc <= qc``; an off-diagonal pair costs 2, a diagonal pair (half masked)
+  costs 1.  Pairs are sorted by (cost desc, qc desc, kc asc) and each is given
+  to the least-loaded of ``n_lanes`` virtual lanes (lowest lane on ties);
+  the output interleaves the lanes round-robin by position.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+TILE = 128          # rows of a query tile / key tile
+UNIT_ROWS = 256     # query rows of one forward work unit
+
+
+def _cdiv(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def kv_tile_range_causal(r_first: int, r_last: int, nk: int,
+                         q_offset: int, kv_offset: int) -> int:
+    """Number of leading key tiles with any key visible to query rows
+    ``r_first..r_last`` (local, inclusive) under the causal rule."""
+    nkt = _cdiv(nk, TILE)
+    if r_last < r_first:
+        return 0
+    last_pos = q_offset + r_last
+    if last_pos < kv_offset:
+        return 0
+    return min(nkt, (last_pos - kv_offset) // TILE + 1)
+
+
+def _tile_kv_set(t_row: int, nq: int, nk: int, kind: str, q_offset: int,
+                 kv_offset: int, block_mask, causal_in_blocks: bool):
+    """Set of key tiles visible to query tile ``t_row`` (row-block index)."""
+    nkt = _cdiv(nk, TILE)
+    r0 = t_row * TILE
+    if r0 >= nq:
+        return set()
+    r1 = min(nq, r0 + TILE) - 1
+    if kind == "none":
+        return set(range(nkt))
+    lim = kv_tile_range_causal(r0, r1, nk, q_offset, kv_offset)
+    if kind == "causal":
+        return set(range(lim))
+    bm = np.asarray(block_mask, dtype=bool)
+    keep = {kt for kt in range(nkt) if bm[t_row, kt]}
+    if causal_in_blocks:
+        keep = {kt for kt in keep if kt < lim}
+    return keep
+
+
+def fwd_work_units(kind: str, B: int, Hq: int, nq: int, nk: int,
+                   q_offset: int = 0, kv_offset: int = 0, block_mask=None,
+                   causal_in_blocks: bool = False):
+    """Forward work units in launch order: list of ``(bh, qchunk, n_kv_tiles)``."""
+    bh_n = B * Hq
+    nqc = _cdiv(nq, UNIT_ROWS)
+    out = []
+    for i in range(bh_n * nqc):
+        qc = nqc - 1 - i // bh_n
+        bh = i % bh_n
+        kv = set()
+        for t in range(2):
+            kv |= _tile_kv_set(2 * qc + t, nq, nk, kind, q_offset, kv_offset,
+                               block_mask, causal_in_blocks)
+        out.append((bh, qc, len(kv)))
+    return out
+
+
+def chunk_pair_schedule(n_chunks: int, n_lanes: int = 0):
+    """Load-balanced order of the causal (q-chunk, kv-chunk) pairs."""
+    if n_chunks <= 0:
+        return []
+    lanes = n_lanes if n_lanes > 0 else n_chunks
+    pairs = [(qc, kc) for qc in range(n_chunks) for kc in range(qc + 1)]
+    cost = {p: (1 if p[0] == p[1] else 2) for p in pairs}
+    pairs.sort(key=lambda p: (-cost[p], -p[0], p[1]))
+    load = [0] * lanes
+    per_lane = [[] for _ in range(lanes)]
+    for p in pairs:
+        best = min(range(lanes), key=lambda l: (load[l], l))
+        load[best] += cost[p]
+        per_lane[best].append(p)
+    out = []
+    depth = max(len(x) for x in per_lane)
+    for pos in range(depth):
+        for l in range(lanes):
+            if pos < len(per_lane[l]):
+                out.append(per_lane[l][pos])
+    return out

@@ -1,0 +1,398 @@
+"""Pins for the fp64 oracle: each check ties it to something other than itself.
+
+Closed forms (Q = 0, constant V, one dominant logit, a single key), hand-worked
+golden fixtures, central finite differences, a library softmax and PyTorch's
+float64 scaled-dot-product attention with autograd, and invariants (chunked
+merge == monolithic, GQA == repeated MHA, all-ones block mask == dense,
+block-triangular + causal == causal).  ``test_planted_mistakes`` shows that a
+plausible slip in the oracle (a dropped term, a sign, an off-by-one, a
+transposed operand, a missing merge weight) fails at least one pin.
+"""
+import glob
+import json
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+from oracle import MaskSpec
+from oracle import attention as oa
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+RNG = np.random.default_rng(7)
+
+
+def rnd(*shape, rng=None):
+    return (rng or RNG).standard_normal(shape)
+
+
+def masks_for(n, block=4, rng=None):
+    rng = rng or np.random.default_rng(3)
+    nb = -(-n // block)
+    bm = rng.random((nb, nb)) < 0.5
+    bm[np.arange(nb), np.arange(nb)] = True
+    return [MaskSpec("none"), MaskSpec("causal"),
+            MaskSpec("block_sparse", bm, block),
+            MaskSpec("block_sparse", bm, block, causal_in_blocks=True)]
+
+
+# ---------------------------------------------------------------- closed forms
+
+def check_q_zero(fwd):
+    for nq, nk, qo, ko in [(7, 7, 0, 0), (5, 9, 4, 0), (6, 6, 0, 2), (9, 5, 3, 3)]:
+        for mask in masks_for(max(nq, nk)):
+            if mask.kind == "block_sparse" and (qo or ko):
+                continue
+            q = np.zeros((1, 1, nq, 3))
+            k = rnd(1, 1, nk, 3)
+            v = rnd(1, 1, nk, 3)
+            o, lse = fwd(q, k, v, 0.37, mask, qo, ko)
+            for i in range(nq):
+                vis = []
+                for j in range(nk):
+                    ok = True
+                    if mask.kind == "causal" or mask.causal_in_blocks:
+                        ok = ok and ko + j <= qo + i
+                    if mask.kind == "block_sparse":
+                        ok = ok and bool(mask.block_mask[i // mask.block, j // mask.block])
+                    if ok:
+                        vis.append(j)
+                if not vis:
+                    assert np.all(o[0, 0, i] == 0) and lse[0, 0, i] == -np.inf
+                else:
+                    np.testing.assert_allclose(o[0, 0, i], v[0, 0, vis].mean(axis=0), rtol=0, atol=1e-13)
+                    assert abs(lse[0, 0, i] - np.log(len(vis))) < 1e-13
+
+
+def test_q_zero_gives_mean_of_visible_rows():
+    check_q_zero(oracle.attention_forward)
+
+
+def test_constant_v_rows():
+    q, k = rnd(1, 2, 9, 4), rnd(1, 1, 9, 4)
+    vrow = rnd(4)
+    v = np.broadcast_to(vrow, (1, 1, 9, 4)).copy()
+    do = rnd(1, 2, 9, 4)
+    for mask in masks_for(9):
+        o, _ = oracle.attention_forward(q, k, v, 0.5, mask)
+        np.testing.assert_allclose(o, np.broadcast_to(vrow, o.shape), atol=1e-13)
+        dq, dk, _ = oracle.attention_backward(q, k, v, do, 0.5, mask)
+        assert np.abs(dq).max() < 1e-12 and np.abs(dk).max() < 1e-12
+
+
+def test_dominant_logit():
+    n, d, i, js = 16, 8, 5, 11
+    q, k, v = rnd(1, 1, n, d), rnd(1, 1, n, d), rnd(1, 1, n, d)
+    scale = 0.35
+    others = scale * (q[0, 0, i] @ np.delete(k[0, 0], js, axis=0).T)
+    qq = q[0, 0, i] @ q[0, 0, i]
+    alpha = (others.max() + 40.0) / (scale * qq)
+    k[0, 0, js] = alpha * q[0, 0, i]
+    o, lse = oracle.attention_forward(q, k, v, scale)
+    assert np.abs(o[0, 0, i] - v[0, 0, js]).max() < 1e-15 * 1e2 + n * np.exp(-40.0) * np.abs(v).max()
+    assert abs(lse[0, 0, i] - scale * alpha * qq) < 1e-12
+
+
+def test_single_key():
+    q, k, v = rnd(2, 3, 1, 8), rnd(2, 3, 1, 8), rnd(2, 3, 1, 8)
+    o, lse = oracle.attention_forward(q, k, v, 0.125)
+    np.testing.assert_allclose(o, v, atol=1e-15)
+    np.testing.assert_allclose(lse, 0.125 * (q * k).sum(-1), atol=1e-14)
+
+
+def test_lse_bounds_and_rows_sum_to_one():
+    q, k, v = rnd(1, 2, 33, 8), rnd(1, 2, 33, 8), rnd(1, 2, 33, 8)
+    for mask in masks_for(33):
+        o, lse = oracle.attention_forward(q, k, v, 0.4, mask)
+        # P rows sum to one: attention of a constant-one value column is one
+        ones = np.ones((1, 2, 33, 1))
+        o1, _ = oracle.attention_forward(q, k, ones, 0.4, mask)
+        for h in range(2):
+            vis = oracle.visible(np.arange(33), 33, mask)
+            s = np.where(vis, 0.4 * q[0, h] @ k[0, h].T, -np.inf)
+            smax = s.max(1)
+            cnt = vis.sum(1)
+            ok = cnt > 0
+            assert np.all(lse[0, h, ok] >= smax[ok] - 1e-12)
+            assert np.all(lse[0, h, ok] <= smax[ok] + np.log(cnt[ok]) + 1e-12)
+            np.testing.assert_allclose(o1[0, h, ok, 0], 1.0, atol=1e-14)
+
+
+# ---------------------------------------------------------------- golden files
+
+def _mask_from(g, n):
+    if g.get("mask", "none") == "block_sparse":
+        return MaskSpec("block_sparse", np.array(g["block_mask"], bool), g["block"])
+    return MaskSpec(g.get("mask", "none"))
+
+
+@pytest.mark.parametrize("path", sorted(glob.glob(os.path.join(HERE, "golden", "*.json"))),
+                         ids=os.path.basename)
+def test_golden(path):
+    g = json.load(open(path))
+    assert g["source"]
+    if "o_parts" in g:
+        o, lse = oracle.merge_partials([np.array(x) for x in g["o_parts"]],
+                                       [np.array(x) for x in g["lse_parts"]])
+        np.testing.assert_allclose(o, g["o"], atol=1e-12)
+        np.testing.assert_allclose(lse, g["lse"], atol=1e-12)
+        return
+    q = np.array(g["q"])[None, None]
+    k = np.array(g["k"])[None, None]
+    v = np.array(g["v"])[None, None]
+    mask = _mask_from(g, q.shape[2])
+    o, lse = oracle.attention_forward(q, k, v, g["scale"], mask)
+    np.testing.assert_allclose(o[0, 0], g["o"], atol=1e-12)
+    if "lse" in g:
+        np.testing.assert_allclose(lse[0, 0], g["lse"], atol=1e-12)
+    if "dq" in g:
+        do = np.array(g["do"])[None, None]
+        dq, dk, dv = oracle.attention_backward(q, k, v, do, g["scale"], mask)
+        np.testing.assert_allclose(dq[0, 0], g["dq"], atol=1e-12)
+        np.testing.assert_allclose(dk[0, 0], g["dk"], atol=1e-12)
+        np.testing.assert_allclose(dv[0, 0], g["dv"], atol=1e-12)
+
+
+# ---------------------------------------------------------------- finite differences
+
+def fd_check(fwd, bwd, mask, qo=0, ko=0, nq=6, nk=6, hq=2, hkv=1, d=3, seed=11):
+    rng = np.random.default_rng(seed)
+    q, k, v = rnd(1, hq, nq, d, rng=rng), rnd(1, hkv, nk, d, rng=rng), rnd(1, hkv, nk, d, rng=rng)
+    do = rnd(1, hq, nq, d, rng=rng)
+    scale = 0.6
+
+    def loss(q_, k_, v_):
+        o, _ = fwd(q_, k_, v_, scale, mask, qo, ko)
+        return float((o * do).sum())
+
+    dq, dk, dv = bwd(q, k, v, do, scale, mask, qo, ko)
+    h = 1e-6
+    for x, gx in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = x[idx]
+            x[idx] = old + h
+            fp = loss(q, k, v)
+            x[idx] = old - h
+            fm = loss(q, k, v)
+            x[idx] = old
+            num[idx] = (fp - fm) / (2 * h)
+        scale_ref = max(1.0, np.abs(num).max())
+        err = np.abs(num - gx).max() / scale_ref
+        assert err < 1e-7, (mask.kind, err)
+
+
+@pytest.mark.parametrize("mi", range(4))
+def test_finite_difference_gradients(mi):
+    mask = masks_for(8, block=3)[mi]
+    fd_check(oracle.attention_forward, oracle.attention_backward, mask, nq=8, nk=8)
+
+
+def test_finite_difference_gradients_offsets():
+    fd_check(oracle.attention_forward, oracle.attention_backward, MaskSpec("causal"),
+             qo=5, ko=2, nq=5, nk=7)
+
+
+# ---------------------------------------------------------------- library routines
+
+def test_library_softmax_scipy():
+    q, k, v = rnd(1, 2, 40, 8), rnd(1, 2, 40, 8), rnd(1, 2, 40, 8)
+    for mask in masks_for(40, block=8):
+        o, lse = oracle.attention_forward(q, k, v, 0.3, mask)
+        for h in range(2):
+            vis = np.zeros((40, 40), bool)
+            for i in range(40):
+                for j in range(40):
+                    ok = True
+                    if mask.kind == "causal" or mask.causal_in_blocks:
+                        ok &= j <= i
+                    if mask.kind == "block_sparse":
+                        ok &= bool(mask.block_mask[i // 8, j // 8])
+                    vis[i, j] = ok
+            s = np.where(vis, 0.3 * np.einsum("id,jd->ij", q[0, h], k[0, h]), -np.inf)
+            p = scipy.special.softmax(s, axis=1)
+            np.testing.assert_allclose(o[0, h], p @ v[0, h], atol=1e-12)
+            np.testing.assert_allclose(lse[0, h], scipy.special.logsumexp(s, axis=1), atol=1e-12)
+
+
+def test_library_torch_sdpa_fwd_bwd():
+    """PyTorch's float64 CPU scaled_dot_product_attention and its autograd agree."""
+    F = torch.nn.functional
+    for causal, hq, hkv in [(False, 4, 4), (True, 4, 4), (True, 4, 2), (False, 6, 2)]:
+        q, k, v, do = rnd(2, hq, 24, 16), rnd(2, hkv, 24, 16), rnd(2, hkv, 24, 16), rnd(2, hq, 24, 16)
+        mask = MaskSpec("causal" if causal else "none")
+        o, _ = oracle.attention_forward(q, k, v, 0.25, mask)
+        dq, dk, dv = oracle.attention_backward(q, k, v, do, 0.25, mask)
+        tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+        g = hq // hkv
+        to = F.scaled_dot_product_attention(tq, tk.repeat_interleave(g, 1), tv.repeat_interleave(g, 1),
+                                            is_causal=causal, scale=0.25)
+        to.backward(torch.tensor(do))
+        np.testing.assert_allclose(o, to.detach().numpy(), atol=1e-12)
+        np.testing.assert_allclose(dq, tq.grad.numpy(), atol=1e-11)
+        np.testing.assert_allclose(dk, tk.grad.numpy(), atol=1e-11)
+        np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-11)
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_chunked_merge_equals_monolithic():
+    n, d = 48, 8
+    q, k, v = rnd(1, 2, n, d), rnd(1, 1, n, d), rnd(1, 1, n, d)
+    full_o, full_l = oracle.attention_forward(q, k, v, 0.3, MaskSpec("causal"))
+    for nc in (1, 2, 3, 4, 6, 8, 12, 16, 24, 48):
+        c = n // nc
+        for qc in range(nc):
+            qs = slice(qc * c, (qc + 1) * c)
+            parts = []
+            for kc in range(qc + 1):
+                ks = slice(kc * c, (kc + 1) * c)
+                parts.append(oracle.attention_forward(q[:, :, qs], k[:, :, ks], v[:, :, ks], 0.3,
+                                                      MaskSpec("causal"), qc * c, kc * c))
+            o, l = oracle.merge_partials([p[0] for p in parts], [p[1] for p in parts])
+            np.testing.assert_allclose(o, full_o[:, :, qs], atol=1e-12)
+            np.testing.assert_allclose(l, full_l[:, :, qs], atol=1e-12)
+
+
+def test_merge_with_empty_parts():
+    o1, l1 = rnd(3, 4), rnd(3)
+    o, l = oracle.merge_partials([o1, rnd(3, 4)], [l1, np.full(3, -np.inf)])
+    np.testing.assert_allclose(o, o1, atol=1e-15)
+    np.testing.assert_allclose(l, l1, atol=1e-15)
+    o, l = oracle.merge_partials([o1, o1], [np.full(3, -np.inf)] * 2)
+    assert np.all(o == 0) and np.all(l == -np.inf)
+
+
+def test_gqa_equals_repeated_mha():
+    q, k, v, do = rnd(2, 6, 10, 4), rnd(2, 2, 10, 4), rnd(2, 2, 10, 4), rnd(2, 6, 10, 4)
+    for mask in masks_for(10):
+        o, l = oracle.attention_forward(q, k, v, 0.5, mask)
+        kr, vr = np.repeat(k, 3, axis=1), np.repeat(v, 3, axis=1)
+        o2, l2 = oracle.attention_forward(q, kr, vr, 0.5, mask)
+        np.testing.assert_allclose(o, o2, atol=1e-14)
+        np.testing.assert_allclose(l, l2, atol=1e-14)
+        dq, dk, dv = oracle.attention_backward(q, k, v, do, 0.5, mask)
+        dq2, dk2, dv2 = oracle.attention_backward(q, kr, vr, do, 0.5, mask)
+        np.testing.assert_allclose(dq, dq2, atol=1e-13)
+        np.testing.assert_allclose(dk, dk2.reshape(2, 2, 3, 10, 4).sum(2), atol=1e-13)
+        np.testing.assert_allclose(dv, dv2.reshape(2, 2, 3, 10, 4).sum(2), atol=1e-13)
+
+
+def test_block_mask_special_cases():
+    q, k, v, do = rnd(1, 2, 20, 4), rnd(1, 2, 20, 4), rnd(1, 2, 20, 4), rnd(1, 2, 20, 4)
+    ones = MaskSpec("block_sparse", np.ones((5, 5), bool), 4)
+    tri = MaskSpec("block_sparse", np.tril(np.ones((5, 5), bool)), 4, causal_in_blocks=True)
+    for sparse, dense in ((ones, MaskSpec("none")), (tri, MaskSpec("causal"))):
+        a = oracle.attention_forward(q, k, v, 0.5, sparse)
+        b = oracle.attention_forward(q, k, v, 0.5, dense)
+        np.testing.assert_allclose(a[0], b[0], atol=1e-14)
+        np.testing.assert_allclose(a[1], b[1], atol=1e-14)
+        ga = oracle.attention_backward(q, k, v, do, 0.5, sparse)
+        gb = oracle.attention_backward(q, k, v, do, 0.5, dense)
+        for x, y in zip(ga, gb):
+            np.testing.assert_allclose(x, y, atol=1e-13)
+
+
+def test_backward_identities():
+    """rowsum(dO*O) equals rowsum(P*dP), and sum_j dS_ij = 0 (so dQ is unchanged
+    when one vector is added to every key)."""
+    q, k, v, do = rnd(1, 1, 12, 5), rnd(1, 1, 12, 5), rnd(1, 1, 12, 5), rnd(1, 1, 12, 5)
+    for mask in masks_for(12):
+        o, _ = oracle.attention_forward(q, k, v, 0.7, mask)
+        vis = oracle.visible(np.arange(12), 12, mask)
+        s = np.where(vis, 0.7 * q[0, 0] @ k[0, 0].T, -np.inf)
+        p = scipy.special.softmax(s, axis=1)
+        dp = do[0, 0] @ v[0, 0].T
+        np.testing.assert_allclose((do * o).sum(-1)[0, 0], (p * dp).sum(1), atol=1e-13)
+        dq, _, _ = oracle.attention_backward(q, k, v, do, 0.7, mask)
+        dq2, _, _ = oracle.attention_backward(q, k + rnd(5), v, do, 0.7, mask)
+        np.testing.assert_allclose(dq, dq2, atol=1e-12)
+
+
+def test_sampled_rows_match_full():
+    q, k, v, do = rnd(2, 4, 30, 8), rnd(2, 2, 30, 8), rnd(2, 2, 30, 8), rnd(2, 4, 30, 8)
+    mask = MaskSpec("causal")
+    o, l = oracle.attention_forward(q, k, v, 0.3, mask)
+    rows = np.array([0, 7, 29])
+    os_, ls_ = oracle.attention_forward(q, k, v, 0.3, mask, heads=[(1, 3), (0, 0)], rows=rows)
+    np.testing.assert_allclose(os_[0], o[1, 3, rows], atol=0)
+    np.testing.assert_allclose(ls_[1], l[0, 0, rows], atol=0)
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, 0.3, mask)
+    dqs = oracle.attention_backward_dq_rows(q, k, v, do, 0.3, 1, 3, rows, mask)
+    np.testing.assert_allclose(dqs, dq[1, 3, rows], atol=1e-14)
+    dqg, dks, dvs = oracle.attention_backward(q, k, v, do, 0.3, mask, kv_heads=[(1, 1)])
+    np.testing.assert_allclose(dks[0], dk[1, 1], atol=1e-14)
+    np.testing.assert_allclose(dvs[0], dv[1, 1], atol=1e-14)
+    np.testing.assert_allclose(dqg[0], dq[1, 2:4], atol=1e-14)
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+def _fails(fn):
+    try:
+        fn()
+    except AssertionError:
+        return True
+    return False
+
+
+def test_planted_mistakes(monkeypatch):
+    """Each plausible slip in the oracle fails at least one of the pins above."""
+    good_bwd = oa.head_backward
+    good_vis = oa.visible
+    good_fwd = oa.head_forward
+
+    def bwd_no_rowsum(q, k, v, do, scale, vis):          # dropped term in dS
+        p = oa._probs(q, k, scale, vis)
+        dp = do @ v.T
+        ds = p * dp
+        return scale * (ds @ k), scale * (ds.T @ q), p.T @ do
+
+    def bwd_sign(q, k, v, do, scale, vis):               # wrong sign in dS
+        dq, dk, dv = good_bwd(q, k, v, do, scale, vis)
+        return -dq, dk, dv
+
+    def bwd_transposed(q, k, v, do, scale, vis):         # dV from P instead of P^T
+        dq, dk, dv = good_bwd(q, k, v, do, scale, vis)
+        p = oa._probs(q, k, scale, vis)
+        return dq, dk, (p @ do) if p.shape[0] == p.shape[1] else dv * 1.5
+
+    def vis_off_by_one(rows, nk, mask, q_offset=0, kv_offset=0):   # strict causal
+        m = good_vis(rows, nk, mask, q_offset, kv_offset)
+        if mask.kind == "causal":
+            rows = np.asarray(rows)
+            m &= (kv_offset + np.arange(nk))[None, :] < (q_offset + rows)[:, None]
+        return m
+
+    def fwd_no_scale_in_lse(q, k, v, scale, vis):        # LSE of unscaled logits
+        o, lse = good_fwd(q, k, v, scale, vis)
+        o2, lse2 = good_fwd(q, k, v, 1.0, vis)
+        return o, lse2
+
+    def merge_no_weights(o_parts, lse_parts):            # plain average of parts
+        return (np.mean(np.stack(o_parts), 0),
+                np.logaddexp.reduce(np.stack(lse_parts), axis=0))
+
+    checks_bwd = [lambda: fd_check(oracle.attention_forward, oracle.attention_backward, MaskSpec("none")),
+                  lambda: fd_check(oracle.attention_forward, oracle.attention_backward, MaskSpec("causal"))]
+    for bad in (bwd_no_rowsum, bwd_sign, bwd_transposed):
+        monkeypatch.setattr(oa, "head_backward", bad)
+        assert any(_fails(c) for c in checks_bwd + [test_library_torch_sdpa_fwd_bwd]), bad.__name__
+        monkeypatch.setattr(oa, "head_backward", good_bwd)
+
+    monkeypatch.setattr(oa, "visible", vis_off_by_one)
+    assert _fails(test_q_zero_gives_mean_of_visible_rows)
+    monkeypatch.setattr(oa, "visible", good_vis)
+
+    monkeypatch.setattr(oa, "head_forward", fwd_no_scale_in_lse)
+    assert _fails(test_library_softmax_scipy)
+    monkeypatch.setattr(oa, "head_forward", good_fwd)
+
+    monkeypatch.setattr(oa, "merge_partials", merge_no_weights)
+    monkeypatch.setattr(oracle, "merge_partials", merge_no_weights)
+    assert _fails(test_chunked_merge_equals_monolithic)
