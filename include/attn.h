@@ -1,0 +1,232 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact-attention library (libattn.so).
+ *
+ * What is computed (the definition every entry point follows):
+ *   S = scale * Q K^T,  P = softmax over each row of S restricted to the keys
+ *   the mask leaves visible,  O = P V,  LSE_i = ln sum_j exp(S_ij).
+ *   "DISTFLASHATTN: Distributed Memory-efficient Attention for Long-context LLMs
+ *   Training" reviews, first review summary (attention = softmax(QK^T) V; the
+ *   backward pass needs no recomputation of a stored N x N matrix);
+ *   "FlashAttention: Fast and Memory-Efficient Exact Attention with
+ *   IO-Awareness", abstract (exact attention, tiled between HBM and on-chip
+ *   SRAM; block-sparse attention as the same algorithm on a block mask).
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are row-major [B, H, N, d] with d contiguous (row stride d).
+ *     Q, K, V, O, dO, dQ, dK, dV are bfloat16 unless stated otherwise; LSE and
+ *     D are float32 [B, H_q, N].  LSE is the natural-log log-sum-exp.
+ *   - Grouped-query attention: H_q % H_kv == 0 and query head h reads key/value
+ *     head h / (H_q / H_kv)  ("FlashAttention-2" reviews, first review
+ *     questions: the MQA/GQA paragraph of the backward section).
+ *   - d is 64 or 128.  N >= 1, any value (ragged last tiles are masked).
+ *   - Every device pointer must be 16-byte aligned; head strides in bytes must
+ *     be multiples of 16.
+ *   - Pointers named "device" are CUDA device pointers owned by the caller; the
+ *     library never frees them.  The library allocates only a one-word device
+ *     status register per device (on first use).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
+ *     launches are asynchronous on it.  The return value reports host-side
+ *     validation and launch errors only; errors seen by a kernel (a bounded
+ *     wait that ran out) are read back with attn_get_status().
+ *   - A query row that sees no key gets O = 0 and LSE = -inf.
+ *   - Return codes are attn_status_t values; on error a message is available
+ *     from attn_last_error_message() (thread-local) and nothing was launched.
+ */
+#ifndef IO_AWARE_EXACT_ATTN_GB300_ATTN_H
+#define IO_AWARE_EXACT_ATTN_GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = -1,    /* null pointer, bad size, bad mask descriptor */
+  ATTN_ERR_UNSUPPORTED = -2,    /* valid but not built: d not in {64,128}, ... */
+  ATTN_ERR_MISALIGNED = -3,     /* pointer or stride not 16-byte aligned */
+  ATTN_ERR_CUDA = -4,           /* a CUDA runtime/driver call failed */
+  ATTN_ERR_DEVICE_TIMEOUT = -5, /* a kernel's bounded wait ran out (device-side) */
+  ATTN_ERR_WORKSPACE = -6,      /* workspace too small */
+  ATTN_ERR_NO_DEVICE = -7       /* no usable sm_103 device */
+} attn_status_t;
+
+typedef enum {
+  ATTN_MASK_NONE = 0,
+  ATTN_MASK_CAUSAL = 1,
+  ATTN_MASK_BLOCK_SPARSE = 2
+} attn_mask_kind_t;
+
+typedef enum { ATTN_DTYPE_BF16 = 0, ATTN_DTYPE_F32 = 1 } attn_dtype_t;
+
+/* Tile edge used by the kernels and by the block-sparse mask granularity. */
+#define ATTN_TILE 128
+
+/*
+ * Mask descriptor.  A NULL attn_mask_t* means ATTN_MASK_NONE.
+ *   kind = ATTN_MASK_CAUSAL: key j is visible to query i iff
+ *     kv_offset + j <= q_offset + i (global positions; offsets are 0 except in
+ *     attn_partial_fwd).  Fully masked key tiles are skipped, not computed
+ *     ("FlashAttention-2" reviews, fourth review: causal block skipping).
+ *   kind = ATTN_MASK_BLOCK_SPARSE: block_mask is a DEVICE pointer to a
+ *     row-major uint8 array [ceil(Nq/128)][ceil(Nk/128)] shared by every batch
+ *     and head; a nonzero byte keeps that 128x128 block dense, zero drops it
+ *     and the block is skipped ("FlashAttention" abstract: block-sparse
+ *     FlashAttention; BurstAttention author responses: sparse attention only
+ *     changes the attention mask matrix).  causal_in_blocks != 0 additionally
+ *     applies the causal rule inside kept blocks.
+ * The descriptor is read during the call; block_mask must stay valid until the
+ * launched work has completed.
+ */
+typedef struct attn_mask {
+  int32_t kind;
+  int32_t causal_in_blocks;
+  const uint8_t* block_mask;
+} attn_mask_t;
+
+/*
+ * attn_fwd -- exact attention forward with online softmax and a saved LSE.
+ * "FlashAttention-2" reviews, first review questions (online-softmax
+ * equations, diag(l)^-1 rescaling) and second review items 1-2 (rescaling
+ * deferred to the end; one log-sum-exp saved per row for the backward pass).
+ *   q   device bf16 [B, Hq,  N, d]      k, v device bf16 [B, Hkv, N, d]
+ *   o   device bf16 [B, Hq,  N, d]      (written)
+ *   lse device f32  [B, Hq,  N]         (written; may be NULL if not wanted)
+ *   scale  multiplies Q K^T (typically 1/sqrt(d)).
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int Hq, int Hkv, int N, int d, float scale,
+             const attn_mask_t* mask, void* stream);
+
+/*
+ * attn_partial_fwd -- attention of one query chunk against one key/value chunk,
+ * the building block of chunked / sequence-parallel attention
+ * ("DISTFLASHATTN" reviews, first review summary: attention computed in chunks
+ * distributed over workers; BurstAttention author responses: local attention
+ * per device combined with online softmax).
+ *   q        device bf16, Nq rows per head, consecutive heads q_head_stride
+ *            rows apart (0 means Nq).  Layout [B, Hq, *, d].
+ *   k, v     device bf16, Nk rows per head, heads kv_head_stride rows apart
+ *            (0 means Nk).  Layout [B, Hkv, *, d].
+ *   o_part   device f32 [B, Hq, Nq, d] contiguous: O of this chunk pair,
+ *            normalised over the chunk's visible keys (0 for rows seeing none).
+ *   lse_part device f32 [B, Hq, Nq]: LSE over the chunk's keys (-inf if none).
+ *   q_offset, kv_offset: global positions of local row 0 / key 0, used by the
+ *            causal rule.  A block-sparse mask is indexed by local tiles.
+ */
+int attn_partial_fwd(const void* q, const void* k, const void* v, float* o_part,
+                     float* lse_part, int B, int Hq, int Hkv, int Nq, int Nk,
+                     int d, float scale, const attn_mask_t* mask,
+                     int64_t q_offset, int64_t kv_offset,
+                     int64_t q_head_stride, int64_t kv_head_stride,
+                     void* stream);
+
+/*
+ * attn_merge_lse -- combine partial results over disjoint key sets:
+ *   LSE = ln sum_c exp(LSE_c),  O = sum_c exp(LSE_c - LSE) * O_c.
+ * Parts with LSE_c = -inf weigh zero; a row where all parts are -inf gets
+ * O = 0, LSE = -inf.  (BurstAttention author responses: online-softmax
+ * combination of local results across devices.)
+ *   o_parts   HOST array of n_parts DEVICE pointers, each f32 [B, Hq, Nq, d]
+ *             contiguous.   lse_parts: HOST array of n_parts DEVICE pointers,
+ *             each f32 [B, Hq, Nq].  1 <= n_parts <= 64.
+ *   o_out     device, out_dtype (ATTN_DTYPE_BF16 or ATTN_DTYPE_F32), heads
+ *             out_head_stride rows apart (0 means Nq), row stride d.
+ *   lse_out   device f32, heads out_head_stride rows apart; may be NULL.
+ * The pointer arrays are copied during the call.
+ */
+int attn_merge_lse(const float* const* o_parts, const float* const* lse_parts,
+                   int n_parts, void* o_out, int out_dtype, float* lse_out,
+                   int B, int Hq, int Nq, int d, int64_t out_head_stride,
+                   void* stream);
+
+/*
+ * attn_bwd -- exact backward pass that recomputes P from the saved LSE instead
+ * of storing it ("DISTFLASHATTN" reviews, first review point 3: the backward
+ * pass needs no recomputed forward; "FlashAttention-2" reviews, second review
+ * items 2-3: LSE saved for the backward pass, query-derivative update
+ * restructured).  Three launches on `stream`:
+ *   1. D = rowsum(dO * O) per query row (float32, into the workspace);
+ *   2. dK, dV per key tile, looping over the query tiles (and the query heads
+ *      of its GQA group) that see it;
+ *   3. dQ per query tile, accumulated in float32 on chip, looping over the key
+ *      tiles it sees.
+ *   q, o, dout  device bf16 [B, Hq, N, d];  k, v device bf16 [B, Hkv, N, d]
+ *   lse         device f32 [B, Hq, N] from attn_fwd (same mask and scale)
+ *   dq          device bf16 [B, Hq, N, d] (written)
+ *   dk, dv      device bf16 [B, Hkv, N, d] (written; summed over GQA groups)
+ *   workspace   device scratch of at least attn_bwd_workspace_bytes() bytes,
+ *               16-byte aligned; its contents on entry are ignored.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o,
+             const float* lse, const void* dout, void* dq, void* dk, void* dv,
+             void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+             int N, int d, float scale, const attn_mask_t* mask, void* stream);
+
+/* Bytes of workspace attn_bwd needs (D: B*Hq*N floats, rounded up to 256). */
+size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
+
+/*
+ * attn_build_schedule -- HOST-ONLY.  The forward work units in the order
+ * attn_fwd / attn_partial_fwd launch them, as int32 triples
+ * (b*Hq + h, query chunk of 256 rows, number of key tiles visited).  Units go
+ * heaviest first: unit i takes chunk nqc-1 - i/(B*Hq) of head i%(B*Hq)
+ * (DISTFLASHATTN reviews, first review point 1: with causal masking careless
+ * placement leaves processors idle).  host_block_mask is a HOST copy of the
+ * block mask (only read for ATTN_MASK_BLOCK_SPARSE).  Writes at most cap
+ * int32 values to out and the number of units to *n_out; ATTN_ERR_INVALID_ARG
+ * if cap is too small (n_out still set).
+ */
+int attn_build_schedule(int mask_kind, int causal_in_blocks,
+                        const uint8_t* host_block_mask, int B, int Hq, int Nq,
+                        int Nk, int64_t q_offset, int64_t kv_offset,
+                        int32_t* out, size_t cap, size_t* n_out);
+
+/*
+ * attn_build_chunk_schedule -- HOST-ONLY.  Load-balanced order of the causal
+ * (q-chunk, kv-chunk <= q-chunk) pairs of chunked attention, as int32 pairs.
+ * Off-diagonal pairs cost 2, diagonal pairs 1; pairs sorted by (cost desc,
+ * qc desc, kc asc) go to the least-loaded of n_lanes virtual lanes (lowest on
+ * ties; n_lanes <= 0 means n_chunks) and are emitted lane-round-robin by
+ * position ("DISTFLASHATTN" reviews: token-level workload balancing of the
+ * causal chunks; the paper's own schedule is not reproduced on the page).
+ */
+int attn_build_chunk_schedule(int n_chunks, int n_lanes, int32_t* pairs_out,
+                              size_t cap, size_t* n_out);
+
+/*
+ * attn_get_status -- synchronises `stream`, then reads and clears the current
+ * device's status register.  Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT if a
+ * kernel's bounded wait ran out since the last call, or ATTN_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+int attn_get_status(void* stream);
+
+/*
+ * attn_set_wait_limit_ns -- upper bound, in nanoseconds, on every spin-wait in
+ * the kernels launched after this call (default 2e9).  A wait that runs out
+ * sets the status register, and the kernel drains and returns.  limit_ns <= 0
+ * restores the default.
+ */
+void attn_set_wait_limit_ns(int64_t limit_ns);
+
+/*
+ * attn_selftest_wait_timeout -- launches one small kernel that waits, with the
+ * given limit, on a barrier that nothing signals, so that the bounded-wait
+ * error path can be tested without faulting or hanging the GPU.  The wait
+ * runs out after limit_ns; attn_get_status() then reports
+ * ATTN_ERR_DEVICE_TIMEOUT.
+ */
+int attn_selftest_wait_timeout(int64_t limit_ns, void* stream);
+
+const char* attn_status_string(int status);
+const char* attn_last_error_message(void);
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IO_AWARE_EXACT_ATTN_GB300_ATTN_H */

@@ -1,0 +1,225 @@
+"""PyTorch-facing wrappers over the C ABI (argument marshalling only).
+
+Every function checks shapes, dtypes and layouts, allocates outputs with
+torch (device memory is torch's), and calls one entry point of ``libattn.so``
+on the current CUDA stream.  All arithmetic happens in the library's kernels.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import _ffi
+from ._ffi import attn_mask_t, check
+
+__all__ = ["attn_fwd", "attn_partial_fwd", "attn_merge_lse", "attn_bwd", "bwd_workspace_bytes",
+           "build_schedule", "build_chunk_schedule", "get_status", "set_wait_limit_ns",
+           "selftest_wait_timeout", "mask_desc"]
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _rows_view(t: torch.Tensor, name: str, dtype=torch.bfloat16):
+    """Check a [B, H, N, d] tensor whose rows are contiguous; return its head stride in rows."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be 4-D [B, H, N, d]")
+    B, H, N, d = t.shape
+    if t.stride(3) != 1 or (N > 1 and t.stride(2) != d):
+        raise ValueError(f"{name}: rows must be contiguous with stride d")
+    if t.stride(1) % d or t.stride(1) // d < N or (B > 1 and t.stride(0) != H * t.stride(1)):
+        raise ValueError(f"{name}: heads must be evenly strided")
+    return t.stride(1) // d
+
+
+def _contig(t: torch.Tensor, name: str, dtype=torch.bfloat16):
+    if not (t.is_cuda and t.dtype == dtype and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+def mask_desc(causal: bool = False, block_mask: Optional[torch.Tensor] = None,
+              causal_in_blocks: bool = False):
+    """Build the C mask descriptor; returns (descriptor or None, tensor to keep alive)."""
+    if block_mask is not None:
+        bm = block_mask
+        if bm.dtype != torch.uint8:
+            bm = bm.to(torch.uint8)
+        bm = bm.contiguous()
+        if not bm.is_cuda:
+            raise ValueError("block_mask must be on the GPU")
+        m = attn_mask_t(_ffi.MASK_BLOCK_SPARSE, 1 if causal_in_blocks else 0, bm.data_ptr())
+        return m, bm
+    if causal:
+        return attn_mask_t(_ffi.MASK_CAUSAL, 0, None), None
+    return None, None
+
+
+def _mp(m):
+    return C.byref(m) if m is not None else None
+
+
+def attn_fwd(q, k, v, scale: Optional[float] = None, causal: bool = False,
+             block_mask: Optional[torch.Tensor] = None, causal_in_blocks: bool = False,
+             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None):
+    """Exact attention forward: returns ``(O [B,Hq,N,d] bf16, LSE [B,Hq,N] f32)``."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _contig(t, n)
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, N, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Hkv, N, d] matching q")
+    o = torch.empty_like(q) if out is None else out
+    _contig(o, "out")
+    l = torch.empty((B, Hq, N), device=q.device, dtype=torch.float32) if lse is None else lse
+    _contig(l, "lse", torch.float32)
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    m, keep = mask_desc(causal, block_mask, causal_in_blocks)
+    check(_ffi.lib().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
+                              B, Hq, Hkv, N, d, sc, _mp(m), _stream(q)), "attn_fwd")
+    del keep
+    return o, l
+
+
+def attn_partial_fwd(q, k, v, q_offset: int = 0, kv_offset: int = 0, scale: Optional[float] = None,
+                     causal: bool = False, block_mask: Optional[torch.Tensor] = None,
+                     causal_in_blocks: bool = False, o_part: Optional[torch.Tensor] = None,
+                     lse_part: Optional[torch.Tensor] = None):
+    """Attention of one query chunk against one key/value chunk.
+
+    ``q`` ``[B,Hq,Nq,d]`` and ``k``/``v`` ``[B,Hkv,Nk,d]`` may be row-slices of
+    larger tensors (rows contiguous, heads evenly strided).  Returns the fp32
+    partial ``O_c [B,Hq,Nq,d]`` normalised over this chunk's keys and
+    ``LSE_c [B,Hq,Nq]``.
+    """
+    qhs = _rows_view(q, "q")
+    khs = _rows_view(k, "k")
+    vhs = _rows_view(v, "v")
+    if vhs != khs or v.shape != k.shape or k.stride() != v.stride():
+        raise ValueError("k and v must share shape and strides")
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    o = torch.empty((B, Hq, Nq, d), device=q.device, dtype=torch.float32) if o_part is None else o_part
+    l = torch.empty((B, Hq, Nq), device=q.device, dtype=torch.float32) if lse_part is None else lse_part
+    _contig(o, "o_part", torch.float32)
+    _contig(l, "lse_part", torch.float32)
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    m, keep = mask_desc(causal, block_mask, causal_in_blocks)
+    check(_ffi.lib().attn_partial_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
+                                      B, Hq, Hkv, Nq, Nk, d, sc, _mp(m), int(q_offset), int(kv_offset),
+                                      qhs, khs, _stream(q)), "attn_partial_fwd")
+    del keep
+    return o, l
+
+
+def attn_merge_lse(o_parts: Sequence[torch.Tensor], lse_parts: Sequence[torch.Tensor],
+                   out: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
+                   lse_out: Optional[torch.Tensor] = None):
+    """Log-sum-exp merge of partial results over disjoint key sets.
+
+    ``out`` (and ``lse_out``) may be row-slices of larger tensors with the same
+    head stride.  Returns ``(O, LSE)``.
+    """
+    n = len(o_parts)
+    if n != len(lse_parts) or n < 1:
+        raise ValueError("need matching, non-empty part lists")
+    for i, (o, l) in enumerate(zip(o_parts, lse_parts)):
+        _contig(o, f"o_parts[{i}]", torch.float32)
+        _contig(l, f"lse_parts[{i}]", torch.float32)
+    B, Hq, Nq, d = o_parts[0].shape
+    for o in o_parts:
+        if o.shape != (B, Hq, Nq, d):
+            raise ValueError("all parts must share one shape")
+    dt = out.dtype if out is not None else out_dtype
+    o_out = torch.empty((B, Hq, Nq, d), device=o_parts[0].device, dtype=dt) if out is None else out
+    hs = _rows_view(o_out, "out", dt)
+    l_out = torch.empty((B, Hq, Nq), device=o_parts[0].device, dtype=torch.float32) if lse_out is None else lse_out
+    if l_out.dtype != torch.float32 or l_out.stride(-1) != 1 or (Hq > 1 and l_out.stride(1) != hs):
+        raise ValueError("lse_out must be f32 with the same head stride (in rows) as out")
+    optrs = (C.c_void_p * n)(*[o.data_ptr() for o in o_parts])
+    lptrs = (C.c_void_p * n)(*[l.data_ptr() for l in lse_parts])
+    code = _ffi.DTYPE_F32 if dt == torch.float32 else _ffi.DTYPE_BF16
+    check(_ffi.lib().attn_merge_lse(optrs, lptrs, n, o_out.data_ptr(), code, l_out.data_ptr(), B, Hq, Nq, d, hs,
+                                    _stream(o_parts[0])), "attn_merge_lse")
+    return o_out, l_out
+
+
+def bwd_workspace_bytes(B: int, Hq: int, Hkv: int, N: int, d: int) -> int:
+    return int(_ffi.lib().attn_bwd_workspace_bytes(B, Hq, Hkv, N, d))
+
+
+def attn_bwd(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = False,
+             block_mask: Optional[torch.Tensor] = None, causal_in_blocks: bool = False,
+             workspace: Optional[torch.Tensor] = None, dq=None, dk=None, dv=None):
+    """Exact backward pass; returns ``(dQ, dK, dV)`` in bf16."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _contig(t, n)
+    _contig(lse, "lse", torch.float32)
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    need = bwd_workspace_bytes(B, Hq, Hkv, N, d)
+    ws = torch.empty(need, device=q.device, dtype=torch.uint8) if workspace is None else workspace
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    m, keep = mask_desc(causal, block_mask, causal_in_blocks)
+    check(_ffi.lib().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(),
+                              ws.numel() * ws.element_size(), B, Hq, Hkv, N, d, sc, _mp(m), _stream(q)),
+          "attn_bwd")
+    del keep
+    return dq, dk, dv
+
+
+def build_schedule(mask_kind: int, B: int, Hq: int, Nq: int, Nk: int, q_offset: int = 0,
+                   kv_offset: int = 0, host_block_mask: Optional[np.ndarray] = None,
+                   causal_in_blocks: bool = False) -> np.ndarray:
+    """Forward work units in launch order, ``[n, 3]`` int32 (bh, query chunk, key tiles)."""
+    L = _ffi.lib()
+    n = C.c_size_t(0)
+    bm = None
+    if host_block_mask is not None:
+        bm = np.ascontiguousarray(host_block_mask, dtype=np.uint8)
+    bmp = bm.ctypes.data if bm is not None else None
+    L.attn_build_schedule(mask_kind, int(causal_in_blocks), bmp, B, Hq, Nq, Nk, q_offset, kv_offset,
+                          None, 0, C.byref(n))
+    out = np.zeros(3 * n.value, dtype=np.int32)
+    check(L.attn_build_schedule(mask_kind, int(causal_in_blocks), bmp, B, Hq, Nq, Nk, q_offset, kv_offset,
+                                out.ctypes.data_as(C.POINTER(C.c_int32)), out.size, C.byref(n)),
+          "attn_build_schedule")
+    return out.reshape(-1, 3)
+
+
+def build_chunk_schedule(n_chunks: int, n_lanes: int = 0):
+    """Load-balanced order of causal (q-chunk, kv-chunk) pairs."""
+    L = _ffi.lib()
+    n = C.c_size_t(0)
+    L.attn_build_chunk_schedule(n_chunks, n_lanes, None, 0, C.byref(n))
+    out = np.zeros(2 * n.value, dtype=np.int32)
+    check(L.attn_build_chunk_schedule(n_chunks, n_lanes, out.ctypes.data_as(C.POINTER(C.c_int32)), out.size,
+                                      C.byref(n)), "attn_build_chunk_schedule")
+    return [tuple(int(x) for x in p) for p in out.reshape(-1, 2)]
+
+
+def get_status(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the device status."""
+    s = torch.cuda.current_stream(device).cuda_stream
+    return int(_ffi.lib().attn_get_status(s))
+
+
+def set_wait_limit_ns(limit_ns: int) -> None:
+    _ffi.lib().attn_set_wait_limit_ns(int(limit_ns))
+
+
+def selftest_wait_timeout(limit_ns: int, device=None) -> None:
+    s = torch.cuda.current_stream(device).cuda_stream
+    check(_ffi.lib().attn_selftest_wait_timeout(int(limit_ns), s), "attn_selftest_wait_timeout")

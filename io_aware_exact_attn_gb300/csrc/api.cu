@@ -1,0 +1,399 @@
+// api.cu -- the C ABI (include/attn.h): argument validation, TMA descriptor
+// encoding, launches, the per-device status register, and the host-only
+// schedule builders.  Every compute step runs in the kernels of fwd.cu,
+// bwd.cu and merge.cu; nothing here computes attention.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "attn.h"
+#include "internal.h"
+#include "schedule.h"
+
+using namespace attn;
+
+namespace {
+
+thread_local std::string g_msg;
+std::mutex g_mu;
+int64_t g_wait_limit_ns = 2000000000ll;
+
+constexpr int MAX_DEVICES = 64;
+unsigned int* g_status[MAX_DEVICES] = {};
+int g_dev_ok[MAX_DEVICES] = {};  // 0 unknown, 1 ok, -1 unsupported
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_msg = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Current device, checked to be sm_103; its status word allocated on first use.
+int device_ready(unsigned int** status) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(ATTN_ERR_NO_DEVICE, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= MAX_DEVICES) return fail(ATTN_ERR_NO_DEVICE, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_dev_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (g_dev_ok[dev] < 0) return fail(ATTN_ERR_NO_DEVICE, "device %d is not sm_103 (GB300)", dev);
+  if (g_status[dev] == nullptr) {
+    unsigned int* p = nullptr;
+    e = cudaMalloc(&p, sizeof(unsigned int));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(status)");
+    e = cudaMemset(p, 0, sizeof(unsigned int));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+    g_status[dev] = p;
+  }
+  *status = g_status[dev];
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_ptr(const void* p, const char* name) {
+  if (p == nullptr) return fail(ATTN_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned16(p)) return fail(ATTN_ERR_MISALIGNED, "%s is not 16-byte aligned", name);
+  return ATTN_OK;
+}
+
+int check_dims(int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "sizes must be positive (B=%d Hq=%d Hkv=%d Nq=%d Nk=%d)", B, Hq, Hkv, Nq, Nk);
+  if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim d=%d not supported (64 or 128)", d);
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if ((int64_t)B * Hq > (int64_t)1 << 30 || (int64_t)Nq * d > (int64_t)1 << 40)
+    return fail(ATTN_ERR_INVALID_ARG, "problem too large");
+  return ATTN_OK;
+}
+
+struct MaskArgs {
+  int kind = MASK_NONE;
+  int causal_in_blocks = 0;
+  const uint8_t* block_mask = nullptr;
+};
+
+int read_mask(const attn_mask_t* m, MaskArgs* out) {
+  *out = MaskArgs();
+  if (m == nullptr) return ATTN_OK;
+  if (m->kind != ATTN_MASK_NONE && m->kind != ATTN_MASK_CAUSAL && m->kind != ATTN_MASK_BLOCK_SPARSE)
+    return fail(ATTN_ERR_INVALID_ARG, "unknown mask kind %d", (int)m->kind);
+  out->kind = m->kind;
+  out->causal_in_blocks = m->causal_in_blocks ? 1 : 0;
+  if (m->kind == ATTN_MASK_BLOCK_SPARSE) {
+    if (m->block_mask == nullptr) return fail(ATTN_ERR_INVALID_ARG, "block-sparse mask without block_mask");
+    out->block_mask = m->block_mask;
+  }
+  return ATTN_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+namespace attn {
+
+int encode_rows_map(CUtensorMap* map, const void* base, int d, int rows, int heads, int64_t head_stride_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)head_stride_rows * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return ATTN_OK;
+}
+
+}  // namespace attn
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+int attn_version(void) { return 1; }
+
+const char* attn_last_error_message(void) { return g_msg.c_str(); }
+
+const char* attn_status_string(int s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_MISALIGNED: return "pointer or stride not 16-byte aligned";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait ran out";
+    case ATTN_ERR_WORKSPACE: return "workspace too small";
+    case ATTN_ERR_NO_DEVICE: return "no usable sm_103 device";
+    default: return "unknown status";
+  }
+}
+
+void attn_set_wait_limit_ns(int64_t limit_ns) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_wait_limit_ns = limit_ns > 0 ? limit_ns : 2000000000ll;
+}
+
+static int64_t wait_limit() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_wait_limit_ns;
+}
+
+static int fwd_common(const void* q, const void* k, const void* v, void* o, bool out_f32, float* lse, int B,
+                      int Hq, int Hkv, int Nq, int Nk, int d, float scale, const attn_mask_t* mask,
+                      int64_t q_off, int64_t kv_off, int64_t q_hs, int64_t kv_hs, void* stream) {
+  int rc;
+  if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k, "k")) || (rc = check_ptr(v, "v")) ||
+      (rc = check_ptr(o, "o")))
+    return rc;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(ATTN_ERR_MISALIGNED, "lse not 4-byte aligned");
+  if ((rc = check_dims(B, Hq, Hkv, Nq, Nk, d, scale))) return rc;
+  if (q_hs < Nq || kv_hs < Nk) return fail(ATTN_ERR_INVALID_ARG, "head stride smaller than the rows per head");
+  MaskArgs m;
+  if ((rc = read_mask(mask, &m))) return rc;
+  unsigned int* status = nullptr;
+  if ((rc = device_ready(&status))) return rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = encode_rows_map(&tq, q, d, Nq, B * Hq, q_hs)) || (rc = encode_rows_map(&tk, k, d, Nk, B * Hkv, kv_hs)) ||
+      (rc = encode_rows_map(&tv, v, d, Nk, B * Hkv, kv_hs)))
+    return rc;
+  FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.o_head_stride = Nq;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = Nq; p.Nk = Nk;
+  p.nqc = (int)cdiv(Nq, UNIT_ROWS);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.mask_kind = m.kind;
+  p.causal_in_blocks = m.causal_in_blocks;
+  p.block_mask = m.block_mask;
+  p.nkb = (int)cdiv(Nk, TILE);
+  p.q_offset = q_off;
+  p.kv_offset = kv_off;
+  p.status = status;
+  p.wait_limit_ns = wait_limit();
+  cudaError_t e = launch_fwd(d, out_f32, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return ATTN_OK;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N, int d,
+             float scale, const attn_mask_t* mask, void* stream) {
+  return fwd_common(q, k, v, o, false, lse, B, Hq, Hkv, N, N, d, scale, mask, 0, 0, N, N, stream);
+}
+
+int attn_partial_fwd(const void* q, const void* k, const void* v, float* o_part, float* lse_part, int B, int Hq,
+                     int Hkv, int Nq, int Nk, int d, float scale, const attn_mask_t* mask, int64_t q_offset,
+                     int64_t kv_offset, int64_t q_head_stride, int64_t kv_head_stride, void* stream) {
+  if (lse_part == nullptr) return fail(ATTN_ERR_INVALID_ARG, "lse_part is NULL");
+  return fwd_common(q, k, v, o_part, true, lse_part, B, Hq, Hkv, Nq, Nk, d, scale, mask, q_offset, kv_offset,
+                    q_head_stride > 0 ? q_head_stride : Nq, kv_head_stride > 0 ? kv_head_stride : Nk, stream);
+}
+
+int attn_merge_lse(const float* const* o_parts, const float* const* lse_parts, int n_parts, void* o_out,
+                   int out_dtype, float* lse_out, int B, int Hq, int Nq, int d, int64_t out_head_stride,
+                   void* stream) {
+  if (o_parts == nullptr || lse_parts == nullptr) return fail(ATTN_ERR_INVALID_ARG, "part arrays are NULL");
+  if (n_parts < 1 || n_parts > 64) return fail(ATTN_ERR_INVALID_ARG, "n_parts=%d outside [1, 64]", n_parts);
+  int rc;
+  for (int c = 0; c < n_parts; ++c) {
+    if ((rc = check_ptr(o_parts[c], "o_parts[c]"))) return rc;
+    if (lse_parts[c] == nullptr) return fail(ATTN_ERR_INVALID_ARG, "lse_parts[%d] is NULL", c);
+  }
+  if ((rc = check_ptr(o_out, "o_out"))) return rc;
+  if (out_dtype != ATTN_DTYPE_BF16 && out_dtype != ATTN_DTYPE_F32)
+    return fail(ATTN_ERR_INVALID_ARG, "out_dtype=%d", out_dtype);
+  if ((rc = check_dims(B, Hq, Hq, Nq, Nq, d, 1.f))) return rc;
+  const int64_t hs = out_head_stride > 0 ? out_head_stride : Nq;
+  if (hs < Nq) return fail(ATTN_ERR_INVALID_ARG, "out_head_stride smaller than Nq");
+  unsigned int* status = nullptr;
+  if ((rc = device_ready(&status))) return rc;
+  cudaError_t e = launch_merge(o_parts, lse_parts, n_parts, o_out, out_dtype == ATTN_DTYPE_F32, lse_out, Nq, B * Hq,
+                               d, hs, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return ATTN_OK;
+}
+
+size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
+  (void)Hkv;
+  (void)d;
+  if (B < 1 || Hq < 1 || N < 1) return 0;
+  const size_t bytes = (size_t)B * Hq * N * sizeof(float);
+  return (bytes + 255) & ~(size_t)255;
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
+             void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d,
+             float scale, const attn_mask_t* mask, void* stream) {
+  int rc;
+  if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k, "k")) || (rc = check_ptr(v, "v")) ||
+      (rc = check_ptr(o, "o")) || (rc = check_ptr(lse, "lse")) || (rc = check_ptr(dout, "dout")) ||
+      (rc = check_ptr(dq, "dq")) || (rc = check_ptr(dk, "dk")) || (rc = check_ptr(dv, "dv")) ||
+      (rc = check_ptr(workspace, "workspace")))
+    return rc;
+  if ((rc = check_dims(B, Hq, Hkv, N, N, d, scale))) return rc;
+  if (workspace_bytes < attn_bwd_workspace_bytes(B, Hq, Hkv, N, d))
+    return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes, need %zu", workspace_bytes,
+                attn_bwd_workspace_bytes(B, Hq, Hkv, N, d));
+  MaskArgs m;
+  if ((rc = read_mask(mask, &m))) return rc;
+  unsigned int* status = nullptr;
+  if ((rc = device_ready(&status))) return rc;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((rc = encode_rows_map(&tq, q, d, N, B * Hq, N)) || (rc = encode_rows_map(&tk, k, d, N, B * Hkv, N)) ||
+      (rc = encode_rows_map(&tv, v, d, N, B * Hkv, N)) || (rc = encode_rows_map(&tdo, dout, d, N, B * Hq, N)))
+    return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* dsum = static_cast<float*>(workspace);
+  cudaError_t e = launch_bwd_preprocess(o, dout, dsum, (int64_t)B * Hq * N, d, s);
+  if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
+  BwdParams p{};
+  p.lse = lse;
+  p.dsum = dsum;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.mask_kind = m.kind;
+  p.causal_in_blocks = m.causal_in_blocks;
+  p.block_mask = m.block_mask;
+  p.nkb = (int)cdiv(N, TILE);
+  p.status = status;
+  p.wait_limit_ns = wait_limit();
+  e = launch_bwd_dkdv(d, tq, tk, tv, tdo, p, s);
+  if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, "backward kernels not built");
+  if (e != cudaSuccess) return cuda_fail(e, "backward dK/dV launch");
+  e = launch_bwd_dq(d, tq, tk, tv, tdo, p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "backward dQ launch");
+  return ATTN_OK;
+}
+
+int attn_build_schedule(int mask_kind, int causal_in_blocks, const uint8_t* host_block_mask, int B, int Hq, int Nq,
+                        int Nk, int64_t q_offset, int64_t kv_offset, int32_t* out, size_t cap, size_t* n_out) {
+  if (n_out == nullptr) return fail(ATTN_ERR_INVALID_ARG, "n_out is NULL");
+  *n_out = 0;
+  if (B < 1 || Hq < 1 || Nq < 1 || Nk < 1) return fail(ATTN_ERR_INVALID_ARG, "sizes must be positive");
+  if (mask_kind < 0 || mask_kind > 2) return fail(ATTN_ERR_INVALID_ARG, "unknown mask kind %d", mask_kind);
+  if (mask_kind == ATTN_MASK_BLOCK_SPARSE && host_block_mask == nullptr)
+    return fail(ATTN_ERR_INVALID_ARG, "block-sparse schedule needs host_block_mask");
+  const int nqc = (int)cdiv(Nq, UNIT_ROWS);
+  const int nkb = (int)cdiv(Nk, TILE);
+  const int64_t units = (int64_t)B * Hq * nqc;
+  *n_out = (size_t)units;
+  if (out == nullptr || cap < (size_t)units * 3) return fail(ATTN_ERR_INVALID_ARG, "output capacity too small");
+  for (int64_t i = 0; i < units; ++i) {
+    const Unit u = fwd_unit(i, B, Hq, 1, Nq, Nk, nqc, mask_kind, causal_in_blocks, host_block_mask, nkb, q_offset,
+                            kv_offset);
+    int cnt = 0;
+    for (int kt = 0; kt < u.kt_end; ++kt) cnt += unit_uses(u, kt) ? 1 : 0;
+    out[3 * i + 0] = u.bh;
+    out[3 * i + 1] = u.row0 / UNIT_ROWS;
+    out[3 * i + 2] = cnt;
+  }
+  return ATTN_OK;
+}
+
+int attn_build_chunk_schedule(int n_chunks, int n_lanes, int32_t* pairs_out, size_t cap, size_t* n_out) {
+  if (n_out == nullptr) return fail(ATTN_ERR_INVALID_ARG, "n_out is NULL");
+  *n_out = 0;
+  if (n_chunks < 1 || n_chunks > 4096) return fail(ATTN_ERR_INVALID_ARG, "n_chunks=%d", n_chunks);
+  const int lanes = n_lanes > 0 ? n_lanes : n_chunks;
+  struct Pair { int qc, kc, cost; };
+  std::vector<Pair> pairs;
+  for (int qc = 0; qc < n_chunks; ++qc)
+    for (int kc = 0; kc <= qc; ++kc) pairs.push_back({qc, kc, qc == kc ? 1 : 2});
+  *n_out = pairs.size();
+  if (pairs_out == nullptr || cap < 2 * pairs.size()) return fail(ATTN_ERR_INVALID_ARG, "output capacity too small");
+  std::stable_sort(pairs.begin(), pairs.end(), [](const Pair& a, const Pair& b) {
+    if (a.cost != b.cost) return a.cost > b.cost;
+    if (a.qc != b.qc) return a.qc > b.qc;
+    return a.kc < b.kc;
+  });
+  std::vector<int64_t> load(lanes, 0);
+  std::vector<std::vector<Pair>> per(lanes);
+  for (const Pair& p : pairs) {
+    int best = 0;
+    for (int l = 1; l < lanes; ++l)
+      if (load[l] < load[best]) best = l;
+    load[best] += p.cost;
+    per[best].push_back(p);
+  }
+  size_t depth = 0, n = 0;
+  for (auto& v : per) depth = std::max(depth, v.size());
+  for (size_t pos = 0; pos < depth; ++pos)
+    for (int l = 0; l < lanes; ++l)
+      if (pos < per[l].size()) {
+        pairs_out[2 * n] = per[l][pos].qc;
+        pairs_out[2 * n + 1] = per[l][pos].kc;
+        ++n;
+      }
+  return ATTN_OK;
+}
+
+int attn_get_status(void* stream) {
+  unsigned int* status = nullptr;
+  int rc = device_ready(&status);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int h = 0;
+  e = cudaMemcpy(&h, status, sizeof h, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+  if (h != 0) {
+    e = cudaMemset(status, 0, sizeof h);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    return fail(ATTN_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out (status 0x%x)", h);
+  }
+  return ATTN_OK;
+}
+
+int attn_selftest_wait_timeout(int64_t limit_ns, void* stream) {
+  unsigned int* status = nullptr;
+  int rc = device_ready(&status);
+  if (rc) return rc;
+  if (limit_ns <= 0 || limit_ns > 10000000000ll) return fail(ATTN_ERR_INVALID_ARG, "limit_ns outside (0, 1e10]");
+  cudaError_t e = launch_wait_selftest(status, limit_ns, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,389 @@
+// fwd.cu -- exact attention forward for sm_103a: TMA-fed tcgen05 MMAs with the
+// score and output accumulators in tensor memory, online softmax in base 2,
+// deferred normalisation and one saved log-sum-exp per row.
+//
+// What it computes: O = softmax(scale * Q K^T) V over the visible keys and
+// LSE = ln sum_j exp(scale * q.k_j)  ("FlashAttention: Fast and
+// Memory-Efficient Exact Attention with IO-Awareness", abstract: tiling between
+// HBM and on-chip memory so S and P never reach HBM; "FlashAttention-2"
+// reviews, first review questions: the online-softmax recurrences with
+// diag(l)^-1 applied once at the end; second review items 1-2: deferred
+// rescaling, one LSE per row saved for the backward pass).
+//
+// One CTA = one work unit = 256 query rows (two 128-row tiles, t = 0, 1) of
+// one (batch, query head); launched heaviest-first (see schedule.h).
+// Warp roles (12 warps, three warpgroups):
+//   warp 0      TMA producer: Q0/Q1 once, then K_j and V_j into an NS-deep ring
+//   warp 1      MMA issuer (one thread): S_t = Q_t K_j^T, then O_t += P_t V_j
+//               with P_t read from tensor memory; owns the TMEM allocation
+//   warps 2-3   idle (they complete the control warpgroup)
+//   warps 4-7   softmax for tile 0 (warp w owns TMEM lanes 32*(w%4)..+31)
+//   warps 8-11  softmax for tile 1
+// The control warpgroup gives registers back (56 per thread) so that the two
+// softmax warpgroups can hold a full 128-column score row each (224 per
+// thread): 128*56 + 256*224 = 384*168, the block's launch allotment.
+// Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d),
+// O_1 [256+d, 256+2d).  P_t (bf16 pairs) overwrites the first 64 columns of S_t.
+// The tensor core order is S_0, S_1, PV_0, PV_1 per key tile; S_t of the next
+// key tile is issued only after PV_t of this one has completed, because P_t
+// lives in the columns S_t overwrites.
+//
+// Online softmax per row, in units of log2: x = s * scale * log2(e),
+// m = running max, p = 2^(x - m), l = sum p.  The max used for p is only moved
+// when the true max exceeds it by more than 8 (p <= 256 in between); when it
+// moves, O_t is rescaled in tensor memory by 2^(m_old - m_new).  This keeps the
+// result exact: O and l always share the same reference max and the final
+// O / l cancels it.
+#include "internal.h"
+#include "ptx.cuh"
+#include "schedule.h"
+
+namespace attn {
+
+namespace {
+
+constexpr float RESCALE_THRESHOLD = 8.0f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int NS = (D == 128) ? 2 : 4;          // K/V ring depth
+  static constexpr int NBOX = D / 64;                     // 64-column TMA boxes per row
+  static constexpr uint32_t BOX_BYTES = 128 * 128;        // 128 rows x 128 bytes
+  static constexpr uint32_t TILE_BYTES = NBOX * BOX_BYTES;
+  static constexpr uint32_t OFF_K = 2 * TILE_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + NS * TILE_BYTES;
+  static constexpr uint32_t SMEM_TILES = OFF_V + NS * TILE_BYTES;
+  static constexpr uint32_t SMEM_BYTES = SMEM_TILES + 1024;  // + alignment slack
+  static constexpr uint32_t TMEM_O = 256;
+  static constexpr int THREADS = 384;
+  static constexpr uint32_t REGS_CTRL = 56, REGS_SOFTMAX = 224;
+};
+
+template <int D, bool OUT_F32>
+__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, const FwdParams p) {
+  using C = FwdCfg<D>;
+  constexpr int NS = C::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t bars[1 + 3 * NS + 7];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t s_base = smem_u32(smem);
+  const uint32_t bar_q = smem_u32(&bars[0]);
+  auto bar_k = [&](int s) { return smem_u32(&bars[1 + s]); };
+  auto bar_v = [&](int s) { return smem_u32(&bars[1 + NS + s]); };
+  auto bar_free = [&](int s) { return smem_u32(&bars[1 + 2 * NS + s]); };
+  auto bar_s = [&](int t) { return smem_u32(&bars[1 + 3 * NS + t]); };
+  auto bar_p = [&](int t) { return smem_u32(&bars[1 + 3 * NS + 2 + t]); };
+  auto bar_o = [&](int t) { return smem_u32(&bars[1 + 3 * NS + 4 + t]); };
+  const uint32_t bar_done = smem_u32(&bars[1 + 3 * NS + 6]);
+
+  const Unit u = fwd_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.Nq, p.Nk, p.nqc, p.mask_kind, p.causal_in_blocks,
+                          p.block_mask, p.nkb, p.q_offset, p.kv_offset);
+  WaitCtx wc{p.wait_limit_ns, p.status, &abort_flag};
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar_k(s), 1);
+      mbar_init(bar_v(s), 1);
+      mbar_init(bar_free(s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_s(t), 1);
+      mbar_init(bar_p(t), 128);
+      mbar_init(bar_o(t), 1);
+    }
+    mbar_init(bar_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tq);
+    prefetch_tmap(&tk);
+    prefetch_tmap(&tv);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp < 4) {
+   reg_dealloc<C::REGS_CTRL>();
+   if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_q, 2 * C::TILE_BYTES);
+      for (int t = 0; t < 2; ++t)
+        for (int bx = 0; bx < C::NBOX; ++bx)
+          tma_load_3d(s_base + t * C::TILE_BYTES + bx * C::BOX_BYTES, &tq, bx * 64, u.row0 + t * TILE,
+                      u.bh, bar_q);
+      int n = 0;
+      bool ok = true;
+      for (int kt = 0; kt < u.kt_end && ok; ++kt) {
+        if (!unit_uses(u, kt)) continue;
+        const int s = n % NS;
+        if (n >= NS) ok = wait_bar(bar_free(s), ((n / NS) - 1) & 1, wc);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar_k(s), C::TILE_BYTES);
+        for (int bx = 0; bx < C::NBOX; ++bx)
+          tma_load_3d(s_base + C::OFF_K + s * C::TILE_BYTES + bx * C::BOX_BYTES, &tk, bx * 64, kt * TILE,
+                      u.kvh, bar_k(s));
+        mbar_arrive_expect_tx(bar_v(s), C::TILE_BYTES);
+        for (int bx = 0; bx < C::NBOX; ++bx)
+          tma_load_3d(s_base + C::OFF_V + s * C::TILE_BYTES + bx * C::BOX_BYTES, &tv, bx * 64, kt * TILE,
+                      u.kvh, bar_v(s));
+        ++n;
+      }
+      if (!ok || abort_flag) {
+        // drain: every issued copy must land before the CTA's shared memory is released
+        wait_bar(bar_q, 0, wc, false);
+        for (int j = n - NS < 0 ? 0 : n - NS; j < n; ++j) {
+          wait_bar(bar_k(j % NS), (j / NS) & 1, wc, false);
+          wait_bar(bar_v(j % NS), (j / NS) & 1, wc, false);
+        }
+      }
+    }
+   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16(128, 128, false, false);
+      const uint32_t id_pv = idesc_bf16(128, D, false, true);
+      int it[2] = {0, 0};
+      int n = 0;
+      bool ok = wait_bar(bar_q, 0, wc);
+      for (int kt = 0; kt < u.kt_end && ok; ++kt) {
+        const uint32_t use = unit_uses(u, kt);
+        if (!use) continue;
+        const int s = n % NS;
+        const uint32_t ph = (n / NS) & 1;
+        if (!(ok = wait_bar(bar_k(s), ph, wc))) break;
+        tc_fence_after();
+        const uint32_t kb = s_base + C::OFF_K + s * C::TILE_BYTES;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!(use & (1u << t))) continue;
+          if (it[t] > 0 && !(ok = wait_bar(bar_o(t), (it[t] - 1) & 1, wc))) break;
+          tc_fence_after();
+          const uint32_t qb = s_base + t * C::TILE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+            mma_ss(tmem + t * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), id_s,
+                   kk > 0);
+          }
+          mma_commit(bar_s(t));
+        }
+        if (!ok || !(ok = wait_bar(bar_v(s), ph, wc))) break;
+        const uint32_t vb = s_base + C::OFF_V + s * C::TILE_BYTES;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!(use & (1u << t))) continue;
+          if (!(ok = wait_bar(bar_p(t), it[t] & 1, wc))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < TILE / 16; ++kk)
+            mma_ts(tmem + C::TMEM_O + t * D, tmem + t * 128 + kk * 8,
+                   sdesc_sw128(vb + kk * 2048, C::BOX_BYTES, 1024), id_pv, (it[t] > 0 || kk > 0));
+          mma_commit(bar_o(t));
+          ++it[t];
+        }
+        mma_commit(bar_free(s));
+        ++n;
+      }
+      // every commit above lands before the CTA leaves
+      mma_commit(bar_done);
+      wait_bar(bar_done, 0, wc, false);
+    }
+   }
+  } else {
+    reg_alloc<C::REGS_SOFTMAX>();
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - 4) >> 2;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;                  // row inside the tile == TMEM lane
+    const int qrow = u.row0 + t * TILE + r;        // local query row
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + t * 128;
+    const uint32_t tO = tmem + lane_off + C::TMEM_O + t * D;
+    const float c = p.scale_log2;
+    const bool causal = mask_is_causal(p.mask_kind, p.causal_in_blocks);
+    const int64_t row_first_pos = p.q_offset + u.row0 + t * TILE;  // first row of the tile
+    float m = -INFINITY, l = 0.f, lr = 0.f;
+    int it = 0;
+    bool ok = true;
+    for (int kt = 0; kt < u.kt_end; ++kt) {
+      if (!(unit_uses(u, kt) & (1u << t))) continue;
+      ok = wait_bar(bar_s(t), it & 1, wc);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      float s[128];
+      {
+        uint32_t rr[32];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          tmem_ld32(tS + q4 * 32, rr);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) s[q4 * 32 + j] = __uint_as_float(rr[j]);
+        }
+      }
+      // element mask on the ragged last key tile and on causal diagonal tiles
+      const int64_t key0 = p.kv_offset + (int64_t)kt * TILE;
+      const bool tail = (kt == u.nkt - 1) && (p.Nk % TILE) != 0;
+      const bool diag = causal && (key0 + TILE - 1 > row_first_pos);
+      if (tail || diag) {
+        int64_t lim = p.Nk - (int64_t)kt * TILE;
+        if (causal) {
+          const int64_t lc = p.q_offset + qrow - key0 + 1;
+          lim = lc < lim ? lc : lim;
+        }
+#pragma unroll
+        for (int j = 0; j < 128; ++j) s[j] = (j < lim) ? s[j] : -INFINITY;
+      }
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+      for (int j = 4; j < 128; j += 4) {
+        mx0 = fmaxf(mx0, s[j]);
+        mx1 = fmaxf(mx1, s[j + 1]);
+        mx2 = fmaxf(mx2, s[j + 2]);
+        mx3 = fmaxf(mx3, s[j + 3]);
+      }
+      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      const float m_new = fmaxf(m, mt);
+      // Move the reference max only at the first tile or when it grows by more
+      // than the threshold; O_t is then rescaled below, after P is written
+      // (the score registers are free by then).
+      float alpha = 1.f;
+      bool rescale = false;
+      if (it == 0) {
+        m = m_new;
+      } else if (__any_sync(0xffffffffu, m_new > m + RESCALE_THRESHOLD)) {
+        alpha = (m_new == -INFINITY) ? 1.f : ex2(m - m_new);
+        m = m_new;
+        rescale = true;
+      }
+      const float mb = (m == -INFINITY) ? 0.f : m;
+      float l0 = 0.f, l1 = 0.f, r0 = 0.f, r1 = 0.f;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float p0 = ex2(fmaf(s[q4 * 32 + 2 * j], c, -mb));
+          const float p1 = ex2(fmaf(s[q4 * 32 + 2 * j + 1], c, -mb));
+          const uint32_t w = pack_bf16(p0, p1);
+          // lr sums the bf16-rounded weights that P.V sees (O is normalised by
+          // it, so the rounding of a dominant weight cancels in O / lr); l sums
+          // the fp32 weights and gives the log-sum-exp.
+          l0 += p0;
+          l1 += p1;
+          r0 += __uint_as_float(w << 16);
+          r1 += __uint_as_float(w & 0xffff0000u);
+          pk[j] = w;
+        }
+        tmem_st16(tS + q4 * 16, pk);
+      }
+      l = l * alpha + (l0 + l1);
+      lr = lr * alpha + (r0 + r1);
+      if (rescale) {
+        // PV_t of the previous key tile must have landed in O_t first
+        ok = wait_bar(bar_o(t), (it - 1) & 1, wc);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int q4 = 0; q4 < D / 32; ++q4) {
+          uint32_t rr[32];
+          tmem_ld32(tO + q4 * 32, rr);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
+          tmem_st32(tO + q4 * 32, rr);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar_p(t));
+      ++it;
+    }
+    // ---------------------------------------------------------- epilogue
+    if (ok && !abort_flag) {
+      const bool have = it > 0;
+      if (have) {
+        ok = wait_bar(bar_o(t), (it - 1) & 1, wc);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (ok) {
+        tc_fence_after();
+        const bool valid_row = qrow < p.Nq;
+        const float inv_l = (lr > 0.f) ? 1.f / lr : 0.f;
+        const size_t orow = (size_t)u.bh * (size_t)p.o_head_stride + (size_t)qrow;
+#pragma unroll
+        for (int q4 = 0; q4 < D / 32; ++q4) {
+          uint32_t rr[32];
+          if (have) {
+            tmem_ld32(tO + q4 * 32, rr);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) rr[j] = 0u;
+          }
+          if (valid_row) {
+            if constexpr (OUT_F32) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + q4 * 32);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(__uint_as_float(rr[4 * j]) * inv_l, __uint_as_float(rr[4 * j + 1]) * inv_l,
+                                     __uint_as_float(rr[4 * j + 2]) * inv_l,
+                                     __uint_as_float(rr[4 * j + 3]) * inv_l);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + q4 * 32);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint4 v4;
+                v4.x = pack_bf16(__uint_as_float(rr[8 * j + 0]) * inv_l, __uint_as_float(rr[8 * j + 1]) * inv_l);
+                v4.y = pack_bf16(__uint_as_float(rr[8 * j + 2]) * inv_l, __uint_as_float(rr[8 * j + 3]) * inv_l);
+                v4.z = pack_bf16(__uint_as_float(rr[8 * j + 4]) * inv_l, __uint_as_float(rr[8 * j + 5]) * inv_l);
+                v4.w = pack_bf16(__uint_as_float(rr[8 * j + 6]) * inv_l, __uint_as_float(rr[8 * j + 7]) * inv_l);
+                dst[j] = v4;
+              }
+            }
+          }
+        }
+        if (valid_row && p.lse != nullptr)
+          p.lse[orow] = (l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool F32>
+cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const FwdParams& p, cudaStream_t s) {
+  using C = FwdCfg<D>;
+  auto kern = fwd_kernel<D, F32>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)(p.B * p.Hq) * (unsigned)p.nqc;
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(int d, bool out_f32, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const FwdParams& p, cudaStream_t s) {
+  if (d == 128) return out_f32 ? launch_fwd_t<128, true>(tq, tk, tv, p, s) : launch_fwd_t<128, false>(tq, tk, tv, p, s);
+  return out_f32 ? launch_fwd_t<64, true>(tq, tk, tv, p, s) : launch_fwd_t<64, false>(tq, tk, tv, p, s);
+}
+
+}  // namespace attn

@@ -1,0 +1,80 @@
+// internal.h -- parameter blocks and launcher entry points shared between the
+// C-ABI front end (api.cu) and the kernel translation units.  Not installed.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+constexpr int TILE = 128;       // query-tile rows, key-tile rows, block-mask granularity
+constexpr int UNIT_ROWS = 256;  // query rows per forward work unit (two query tiles)
+
+enum MaskKind : int { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_BLOCK_SPARSE = 2 };
+
+// Everything a forward launch needs besides the three TMA descriptors.
+struct FwdParams {
+  void* o;                  // bf16 or f32 output rows, row stride d
+  float* lse;               // may be null
+  int64_t o_head_stride;    // rows between consecutive (b, h) heads of o / lse
+  int B, Hq, Hkv, Nq, Nk;
+  int nqc;                  // number of 256-row query chunks
+  float scale_log2;         // scale * log2(e)
+  int mask_kind;
+  int causal_in_blocks;
+  const uint8_t* block_mask;  // [ceil(Nq/128)][ceil(Nk/128)]
+  int nkb;                    // ceil(Nk/128)
+  int64_t q_offset, kv_offset;
+  unsigned int* status;
+  int64_t wait_limit_ns;
+};
+
+// Backward parameter block (kernels 2 and 3 of attn_bwd).
+struct BwdParams {
+  const float* lse;         // [B,Hq,N]
+  const float* dsum;        // D = rowsum(dO*O), [B,Hq,N]
+  void* dq;                 // bf16 [B,Hq,N,d]
+  void* dk;                 // bf16 [B,Hkv,N,d]
+  void* dv;                 // bf16 [B,Hkv,N,d]
+  int B, Hq, Hkv, N;
+  float scale;
+  float scale_log2;
+  int mask_kind;
+  int causal_in_blocks;
+  const uint8_t* block_mask;
+  int nkb;
+  unsigned int* status;
+  int64_t wait_limit_ns;
+};
+
+struct TensorMaps {
+  CUtensorMap a, b, c, d;
+};
+
+// Encode a bf16 [heads][rows][d] tensor as a 3-D TMA descriptor with
+// 128-byte swizzle and a 64 x 128 (columns x rows) box.
+int encode_rows_map(CUtensorMap* map, const void* base, int d, int rows, int heads,
+                    int64_t head_stride_rows);
+
+cudaError_t launch_fwd(int d, bool out_f32, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const FwdParams& p, cudaStream_t s);
+
+cudaError_t launch_merge(const float* const* o_parts, const float* const* lse_parts, int n_parts,
+                         void* o_out, bool out_f32, float* lse_out, int rows_per_head, int heads,
+                         int d, int64_t out_head_stride, cudaStream_t s);
+
+cudaError_t launch_bwd_preprocess(const void* o, const void* dout, float* dsum, int64_t rows, int d,
+                                  cudaStream_t s);
+
+cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
+                            cudaStream_t s);
+
+cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
+                          cudaStream_t s);
+
+cudaError_t launch_wait_selftest(unsigned int* status, int64_t limit_ns, cudaStream_t s);
+
+}  // namespace attn

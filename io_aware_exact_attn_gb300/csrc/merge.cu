@@ -1,0 +1,190 @@
+// merge.cu -- the streaming (HBM-bound) kernels:
+//   * log-sum-exp merge of partial attention results over disjoint key sets
+//     (BurstAttention author responses: local attention results combined
+//     across devices with online-softmax statistics; "DISTFLASHATTN" reviews:
+//     attention computed chunk by chunk);
+//   * the backward preprocessing D_i = sum_k dO_ik * O_ik;
+//   * the bounded-wait self-test kernel.
+// Neither streaming kernel touches the tensor cores: each row is read with
+// 16-byte, fully coalesced, streaming (evict-first) loads and written once.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+
+namespace {
+
+constexpr int MAX_PARTS = 64;
+
+struct MergeArgs {
+  const float* o[MAX_PARTS];
+  const float* lse[MAX_PARTS];
+};
+
+// One group of d/4 lanes per row; each lane owns 4 consecutive columns.
+// out = sum_c w_c O_c / sum_c w_c with w_c = exp(LSE_c - max_c LSE_c).
+template <int D, bool F32>
+__global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ MergeArgs a, int n_parts,
+                                                    void* __restrict__ o_out, float* __restrict__ lse_out,
+                                                    int64_t rows, int rows_per_head, int64_t out_head_stride) {
+  constexpr int LPR = D / 4;                 // lanes per row
+  constexpr int RPW = 32 / LPR;              // rows per warp
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / LPR, col = (lane % LPR) * 4;
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t wrow = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; wrow * RPW < rows;
+       wrow += warps_total) {
+    const int64_t row = wrow * RPW + sub;
+    if (row >= rows) continue;
+    float mx = -INFINITY;
+    for (int c = 0; c < n_parts; ++c) mx = fmaxf(mx, __ldg(a.lse[c] + row));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    if (mx != -INFINITY) {
+      int c = 0;
+      for (; c + 4 <= n_parts; c += 4) {
+        float4 v[4];
+        float w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[j] = __ldcs(reinterpret_cast<const float4*>(a.o[c + j] + row * D + col));
+          w[j] = __expf(__ldg(a.lse[c + j] + row) - mx);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc.x = fmaf(w[j], v[j].x, acc.x);
+          acc.y = fmaf(w[j], v[j].y, acc.y);
+          acc.z = fmaf(w[j], v[j].z, acc.z);
+          acc.w = fmaf(w[j], v[j].w, acc.w);
+          wsum += w[j];
+        }
+      }
+      for (; c < n_parts; ++c) {
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(a.o[c] + row * D + col));
+        const float w = __expf(__ldg(a.lse[c] + row) - mx);
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+        wsum += w;
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const int64_t head = row / rows_per_head, r = row % rows_per_head;
+    const int64_t orow = head * out_head_stride + r;
+    if constexpr (F32) {
+      __stcs(reinterpret_cast<float4*>(static_cast<float*>(o_out) + orow * D + col),
+             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+    } else {
+      uint2 pk;
+      pk.x = pack_bf16(acc.x * inv, acc.y * inv);
+      pk.y = pack_bf16(acc.z * inv, acc.w * inv);
+      __stcs(reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o_out) + orow * D + col), pk);
+    }
+    if (lse_out != nullptr && (lane % LPR) == 0)
+      lse_out[orow] = (wsum > 0.f) ? mx + __logf(wsum) : -INFINITY;
+  }
+}
+
+// D_i = sum_k dO_ik * O_ik; groups of d/8 lanes per row, 8 bf16 per lane.
+template <int D>
+__global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __restrict__ o,
+                                                         const __nv_bfloat16* __restrict__ dout,
+                                                         float* __restrict__ dsum, int64_t rows) {
+  constexpr int LPR = D / 8;
+  constexpr int RPW = 32 / LPR;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / LPR, col = (lane % LPR) * 8;
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t wrow = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; wrow * RPW < rows;
+       wrow += warps_total) {
+    const int64_t row = wrow * RPW + sub;
+    float acc = 0.f;
+    if (row < rows) {
+      const uint4 a = __ldcs(reinterpret_cast<const uint4*>(o + row * D + col));
+      const uint4 b = __ldcs(reinterpret_cast<const uint4*>(dout + row * D + col));
+      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 fa = __bfloat1622float2(pa[j]);
+        const float2 fb = __bfloat1622float2(pb[j]);
+        acc = fmaf(fa.x, fb.x, acc);
+        acc = fmaf(fa.y, fb.y, acc);
+      }
+    }
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < rows && (lane % LPR) == 0) dsum[row] = acc;
+  }
+}
+
+// Waits, with the given limit, on a barrier that nothing ever signals.
+__global__ void wait_selftest_kernel(unsigned int* status, int64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    WaitCtx w{limit_ns, status, &abort_flag};
+    wait_bar(smem_u32(&bar), 0, w);
+  }
+}
+
+int grid_for(int64_t warps_needed) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (warps_needed + 7) / 8;       // 8 warps per 256-thread block
+  const int64_t cap = (int64_t)sms * 8;              // 8 resident blocks per SM
+  return (int)(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const float* const* o_parts, const float* const* lse_parts, int n_parts,
+                         void* o_out, bool out_f32, float* lse_out, int rows_per_head, int heads, int d,
+                         int64_t out_head_stride, cudaStream_t s) {
+  MergeArgs a;
+  for (int c = 0; c < MAX_PARTS; ++c) {
+    a.o[c] = c < n_parts ? o_parts[c] : nullptr;
+    a.lse[c] = c < n_parts ? lse_parts[c] : nullptr;
+  }
+  const int64_t rows = (int64_t)rows_per_head * heads;
+  const int rpw = 32 / (d / 4);
+  const int grid = grid_for((rows + rpw - 1) / rpw);
+  if (d == 128) {
+    if (out_f32) merge_kernel<128, true><<<grid, 256, 0, s>>>(a, n_parts, o_out, lse_out, rows, rows_per_head, out_head_stride);
+    else merge_kernel<128, false><<<grid, 256, 0, s>>>(a, n_parts, o_out, lse_out, rows, rows_per_head, out_head_stride);
+  } else {
+    if (out_f32) merge_kernel<64, true><<<grid, 256, 0, s>>>(a, n_parts, o_out, lse_out, rows, rows_per_head, out_head_stride);
+    else merge_kernel<64, false><<<grid, 256, 0, s>>>(a, n_parts, o_out, lse_out, rows, rows_per_head, out_head_stride);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_preprocess(const void* o, const void* dout, float* dsum, int64_t rows, int d,
+                                  cudaStream_t s) {
+  const int rpw = 32 / (d / 8);
+  const int grid = grid_for((rows + rpw - 1) / rpw);
+  if (d == 128)
+    preprocess_kernel<128><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
+                                                static_cast<const __nv_bfloat16*>(dout), dsum, rows);
+  else
+    preprocess_kernel<64><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
+                                               static_cast<const __nv_bfloat16*>(dout), dsum, rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(unsigned int* status, int64_t limit_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,154 @@
+"""GPU forward parity: attn_fwd, attn_partial_fwd and attn_merge_lse through the
+C ABI against the fp64 oracle on the same seeded bf16 inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from io_aware_exact_attn_gb300 import api, inputs
+from _gpu_helpers import assert_o_lse, f64, make, mask_spec, max_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _lib(cuda_lib):
+    yield
+    assert api.get_status() == 0
+
+
+def run_fwd(q, k, v, kind="none", bm=None, cib=False, scale=None):
+    bmt = torch.as_tensor(bm, dtype=torch.uint8).cuda() if bm is not None else None
+    return api.attn_fwd(q, k, v, scale=scale, causal=kind == "causal", block_mask=bmt, causal_in_blocks=cib)
+
+
+def check_full(B, Hq, Hkv, N, d, kind, bm=None, cib=False, k_mul=1.0):
+    q, k, v, _ = make(B, Hq, Hkv, N, d, k_mul=k_mul)
+    o, lse = run_fwd(q, k, v, kind, bm, cib)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.attention_forward(f64(q), f64(k), f64(v), 1.0 / np.sqrt(d), mask_spec(kind, bm, cib))
+    return assert_o_lse(f64(o), f64(lse), o_ref, l_ref, f"{kind} B{B} H{Hq}/{Hkv} N{N} d{d}")
+
+
+@pytest.mark.parametrize("kind", ["none", "causal"])
+def test_tiny_exact_attention(kind):
+    """B=1, H=2, N=128, d=64 (fp32 N(0,1) draws rounded to bf16), full oracle."""
+    check_full(1, 2, 2, 128, 64, kind)
+
+
+SHAPES = [
+    (1, 2, 2, 300, 64, "none"), (1, 2, 2, 300, 128, "causal"), (2, 4, 2, 520, 128, "causal"),
+    (1, 3, 1, 129, 64, "causal"), (1, 1, 1, 1, 128, "none"), (1, 1, 1, 1, 64, "causal"),
+    (1, 2, 2, 1000, 64, "none"), (2, 2, 2, 384, 128, "none"), (1, 2, 1, 777, 128, "causal"),
+    (1, 4, 4, 256, 64, "causal"), (1, 2, 2, 17, 128, "none"),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "B{}_H{}-{}_N{}_d{}_{}".format(*s))
+def test_fwd_shapes(shape):
+    check_full(*shape)
+
+
+def test_peaked_rows():
+    """K scaled by 4: peaked softmax rows (exercises the running-max rescale)."""
+    check_full(1, 2, 2, 1024, 128, "causal", k_mul=4.0)
+    check_full(1, 2, 2, 700, 64, "none", k_mul=4.0)
+
+
+@pytest.mark.parametrize("cib", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_block_sparse(cib, d):
+    N = 900
+    nb = -(-N // 128)
+    bm = inputs.block_sparse_mask(nb, nb, 0.3, seed=11)
+    check_full(1, 2, 2, N, d, "block_sparse", bm, cib)
+
+
+def test_block_sparse_special_masks():
+    N, d = 640, 64
+    q, k, v, _ = make(1, 2, 2, N, d)
+    nb = N // 128
+    o1, l1 = run_fwd(q, k, v, "block_sparse", np.ones((nb, nb), bool))
+    o2, l2 = run_fwd(q, k, v, "none")
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    o3, l3 = run_fwd(q, k, v, "block_sparse", np.tril(np.ones((nb, nb), bool)), cib=True)
+    o4, l4 = run_fwd(q, k, v, "causal")
+    assert torch.equal(o3, o4) and torch.equal(l3, l4)
+
+
+def test_fully_masked_rows():
+    """A block row with no kept block: O = 0 and LSE = -inf for its rows."""
+    N, d = 384, 64
+    q, k, v, _ = make(1, 1, 1, N, d)
+    bm = np.ones((3, 3), bool)
+    bm[1, :] = False
+    o, l = run_fwd(q, k, v, "block_sparse", bm)
+    torch.cuda.synchronize()
+    assert torch.all(o[0, 0, 128:256] == 0)
+    assert torch.all(torch.isneginf(l[0, 0, 128:256]))
+    o_ref, l_ref = oracle.attention_forward(f64(q), f64(k), f64(v), 1 / 8, mask_spec("block_sparse", bm))
+    assert_o_lse(f64(o), f64(l), o_ref, l_ref)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_partial_fwd_offsets(d):
+    """Partial attention with global offsets, including rows that see nothing."""
+    B, Hq, Hkv, N = 1, 4, 2, 600
+    q, k, v, _ = make(B, Hq, Hkv, N, d)
+    for (q0, q1, k0, k1) in [(300, 600, 0, 300), (256, 600, 256, 600), (0, 300, 200, 500), (100, 420, 0, 600)]:
+        qs, ks = q[:, :, q0:q1], k[:, :, k0:k1]
+        vs = v[:, :, k0:k1]
+        o, l = api.attn_partial_fwd(qs, ks, vs, q_offset=q0, kv_offset=k0, causal=True)
+        torch.cuda.synchronize()
+        o_ref, l_ref = oracle.attention_forward(f64(qs), f64(ks), f64(vs), 1 / np.sqrt(d),
+                                                oracle.MaskSpec("causal"), q0, k0)
+        assert_o_lse(f64(o), f64(l), o_ref, l_ref, f"partial {q0}:{q1} x {k0}:{k1}")
+
+
+@pytest.mark.parametrize("n_chunks", [2, 4])
+def test_chunked_equals_monolithic(n_chunks):
+    B, Hq, Hkv, N, d = 1, 4, 2, 1024, 128
+    q, k, v, _ = make(B, Hq, Hkv, N, d)
+    c = N // n_chunks
+    o_full, l_full = run_fwd(q, k, v, "causal")
+    o = torch.empty_like(q)
+    l = torch.empty((B, Hq, N), device="cuda", dtype=torch.float32)
+    parts = {}
+    for qc, kc in api.build_chunk_schedule(n_chunks):
+        parts[(qc, kc)] = api.attn_partial_fwd(q[:, :, qc * c:(qc + 1) * c], k[:, :, kc * c:(kc + 1) * c],
+                                               v[:, :, kc * c:(kc + 1) * c], qc * c, kc * c, causal=True)
+    for qc in range(n_chunks):
+        api.attn_merge_lse([parts[(qc, kc)][0] for kc in range(qc + 1)],
+                           [parts[(qc, kc)][1] for kc in range(qc + 1)],
+                           out=o[:, :, qc * c:(qc + 1) * c], lse_out=l[:, :, qc * c:(qc + 1) * c])
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.attention_forward(f64(q), f64(k), f64(v), 1 / np.sqrt(d), oracle.MaskSpec("causal"))
+    assert_o_lse(f64(o), f64(l), o_ref, l_ref, "chunked vs oracle")
+    assert max_err(f64(o), f64(o_full)) <= 1e-2
+    assert max_err(f64(l), f64(l_full)) <= 2e-3
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("f32", [False, True])
+def test_merge_against_oracle(d, f32):
+    B, H, N = 2, 3, 333
+    g = torch.Generator().manual_seed(5)
+    n = 5
+    o_parts = [torch.randn(B, H, N, d, generator=g).cuda() for _ in range(n)]
+    lse_parts = [torch.randn(B, H, N, generator=g).mul(3).cuda() for _ in range(n)]
+    lse_parts[2][0, 0, :7] = float("-inf")
+    for p in lse_parts:
+        p[1, 2, 5] = float("-inf")
+    o, l = api.attn_merge_lse(o_parts, lse_parts, out_dtype=torch.float32 if f32 else torch.bfloat16)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.merge_partials([f64(x) for x in o_parts], [f64(x) for x in lse_parts])
+    tol = 1e-5 if f32 else 2e-2
+    assert max_err(f64(o), o_ref) <= tol * max(1.0, np.abs(o_ref).max())
+    assert max_err(f64(l), l_ref) <= 1e-5 * 10
+    assert torch.all(o[1, 2, 5] == 0) and torch.isneginf(l[1, 2, 5])
+
+
+def test_bounded_wait_reports_timeout():
+    api.selftest_wait_timeout(20_000_000)  # 20 ms
+    assert api.get_status() == -5
+    assert api.get_status() == 0

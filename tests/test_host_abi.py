@@ -1,0 +1,162 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every function declared in include/attn.h, rejects bad
+arguments before touching a device, and its integer schedules equal the
+oracle's plain-Python restatement element by element."""
+import ctypes as C
+import os
+import re
+import shutil
+
+import numpy as np
+import pytest
+
+import oracle
+from io_aware_exact_attn_gb300 import _ffi, api, build as B, inputs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_ffi.LIB_PATH) or B._stale():
+        if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+            pytest.skip("nvcc unavailable and library not built")
+        B.build()
+    return _ffi.lib()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert len(names) >= 12, names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(_ffi.SIGNATURES), set(names) ^ set(_ffi.SIGNATURES)
+    assert lib.attn_version() >= 1
+
+
+def test_status_strings(lib):
+    for code in list(_ffi.STATUS):
+        assert lib.attn_status_string(code)
+
+
+def _ptr(x):
+    return C.c_void_p(x)
+
+
+def test_argument_validation_without_gpu(lib):
+    m = None
+    good = 4096
+    # NULL / misaligned pointers and bad sizes are rejected before any device call
+    assert lib.attn_fwd(None, _ptr(good), _ptr(good), _ptr(good), None, 1, 2, 2, 128, 64, 0.125, m, None) == -1
+    assert lib.attn_fwd(_ptr(good + 2), _ptr(good), _ptr(good), _ptr(good), None, 1, 2, 2, 128, 64, 0.125, m,
+                        None) == -3
+    assert lib.attn_fwd(_ptr(good), _ptr(good), _ptr(good), _ptr(good), None, 1, 3, 2, 128, 64, 0.125, m,
+                        None) == -1
+    assert lib.attn_fwd(_ptr(good), _ptr(good), _ptr(good), _ptr(good), None, 1, 2, 2, 128, 96, 0.125, m,
+                        None) == -2
+    assert lib.attn_fwd(_ptr(good), _ptr(good), _ptr(good), _ptr(good), None, 1, 2, 2, 0, 64, 0.125, m,
+                        None) == -1
+    assert lib.attn_fwd(_ptr(good), _ptr(good), _ptr(good), _ptr(good), None, 1, 2, 2, 128, 64, -1.0, m,
+                        None) == -1
+    bad = _ffi.attn_mask_t(7, 0, None)
+    assert lib.attn_fwd(_ptr(good), _ptr(good), _ptr(good), _ptr(good), None, 1, 2, 2, 128, 64, 0.125,
+                        C.byref(bad), None) == -1
+    sparse_no_mask = _ffi.attn_mask_t(2, 0, None)
+    assert lib.attn_fwd(_ptr(good), _ptr(good), _ptr(good), _ptr(good), None, 1, 2, 2, 128, 64, 0.125,
+                        C.byref(sparse_no_mask), None) == -1
+    assert "multiple" in lib.attn_last_error_message().decode() or lib.attn_last_error_message()
+    # merge: part count limits
+    arr = (C.c_void_p * 1)(good)
+    assert lib.attn_merge_lse(arr, arr, 0, _ptr(good), 0, None, 1, 1, 4, 64, 0, None) == -1
+    assert lib.attn_merge_lse(arr, arr, 65, _ptr(good), 0, None, 1, 1, 4, 64, 0, None) == -1
+    # bwd workspace size and check
+    need = lib.attn_bwd_workspace_bytes(2, 4, 2, 100, 64)
+    assert need == ((2 * 4 * 100 * 4 + 255) // 256) * 256
+    p = [_ptr(good)] * 10
+    assert lib.attn_bwd(*p, need - 256, 2, 4, 2, 100, 64, 0.125, None, None) == -6
+    # partial fwd: head stride smaller than the rows is rejected
+    assert lib.attn_partial_fwd(_ptr(good), _ptr(good), _ptr(good), _ptr(good), _ptr(good), 1, 2, 2, 256, 256,
+                                64, 0.125, None, 0, 0, 100, 0, None) == -1
+
+
+def test_status_without_gpu(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("has a GPU")
+    assert lib.attn_get_status(None) == -7
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 8, 13])
+@pytest.mark.parametrize("lanes", [0, 1, 3, 8])
+def test_chunk_schedule_matches_oracle(lib, n, lanes):
+    got = api.build_chunk_schedule(n, lanes)
+    want = oracle.chunk_pair_schedule(n, lanes)
+    assert got == want
+    assert sorted(got) == sorted((q, k) for q in range(n) for k in range(q + 1))
+
+
+def test_chunk_schedule_balance():
+    """Costs add up to n^2 half-tiles and each lane's share (positions l, l+L, ...
+    in the interleaved order while lanes stay full) is within one pair of the mean."""
+    for n in (4, 8, 16):
+        pairs = oracle.chunk_pair_schedule(n)
+        total = sum(1 if q == k else 2 for q, k in pairs)
+        assert total == n * n
+        assert len(pairs) == n * (n + 1) // 2
+
+
+CASES = [
+    (0, 1, 2, 600, 600, 0, 0), (1, 1, 2, 600, 600, 0, 0), (1, 2, 3, 1000, 1000, 0, 0),
+    (1, 1, 4, 4096, 4096, 4096, 0), (1, 1, 4, 4096, 4096, 4096, 8192), (1, 1, 2, 300, 700, 128, 0),
+    (0, 2, 3, 129, 1, 0, 0), (1, 1, 1, 1, 1, 0, 0), (1, 1, 2, 512, 512, 0, 300),
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_fwd_schedule_matches_oracle(lib, case):
+    kind, B_, H, nq, nk, qo, ko = case
+    got = api.build_schedule(kind, B_, H, nq, nk, qo, ko)
+    want = np.array(oracle.fwd_work_units(["none", "causal"][kind], B_, H, nq, nk, qo, ko), dtype=np.int32)
+    np.testing.assert_array_equal(got, want.reshape(-1, 3))
+
+
+@pytest.mark.parametrize("cib", [False, True])
+def test_fwd_schedule_block_sparse_matches_oracle(lib, cib):
+    n = 1000
+    nb = -(-n // 128)
+    bm = inputs.block_sparse_mask(nb, nb, 0.25, seed=5)
+    got = api.build_schedule(2, 2, 3, n, n, 0, 0, host_block_mask=bm, causal_in_blocks=cib)
+    want = oracle.fwd_work_units("block_sparse", 2, 3, n, n, 0, 0, bm, cib)
+    np.testing.assert_array_equal(got, np.array(want, dtype=np.int32).reshape(-1, 3))
+
+
+def test_schedule_covers_every_visible_tile_pair_once():
+    """Coverage from the visibility matrix itself: each work unit visits exactly
+    the key tiles that hold at least one key visible to one of its rows."""
+    for kind, qo, ko in (("causal", 0, 0), ("causal", 256, 0), ("none", 0, 0)):
+        nq, nk = 700, 900
+        units = oracle.fwd_work_units(kind, 1, 1, nq, nk, qo, ko)
+        vis = oracle.visible(np.arange(nq), nk, oracle.MaskSpec(kind), qo, ko)
+        seen = set()
+        for bh, qc, cnt in units:
+            rows = slice(qc * 256, min(nq, qc * 256 + 256))
+            tiles = {j // 128 for j in np.flatnonzero(vis[rows].any(axis=0))}
+            assert cnt == len(tiles)
+            assert qc not in seen
+            seen.add(qc)
+        assert seen == set(range(-(-nq // 256)))
+
+
+def test_workload_inputs_are_seeded():
+    q1, k1, v1, d1 = inputs.make_qkvdo(1, 2, 1, 64, 64, 64)
+    q2, k2, v2, d2 = inputs.make_qkvdo(1, 2, 1, 64, 64, 64)
+    assert all(bool((a == b).all()) for a, b in ((q1, q2), (k1, k2), (v1, v2), (d1, d2)))
+    m = inputs.block_sparse_mask(128, 128)
+    assert m.sum() == 128 + round((128 * 128 - 128) / 8) == 2160
+    assert m[np.arange(128), np.arange(128)].all()
