@@ -165,7 +165,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o,
              void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
              int N, int d, float scale, const attn_mask_t* mask, void* stream);
 
-/* Bytes of workspace attn_bwd needs (D: B*Hq*N floats, rounded up to 256). */
+/* Bytes of workspace attn_bwd needs: two float arrays (D and LSE*log2 e) of
+ * B*Hq*ceil(N/128)*128 entries, rounded up to 256 bytes. */
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
 
 /*

@@ -254,7 +254,8 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
   (void)Hkv;
   (void)d;
   if (B < 1 || Hq < 1 || N < 1) return 0;
-  const size_t bytes = (size_t)B * Hq * N * sizeof(float);
+  // D and LSE*log2(e), one float per query row each, rows padded to whole tiles
+  const size_t bytes = 2 * (size_t)B * Hq * (size_t)cdiv(N, TILE) * TILE * sizeof(float);
   return (bytes + 255) & ~(size_t)255;
 }
 
@@ -280,12 +281,15 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
       (rc = encode_rows_map(&tv, v, d, N, B * Hkv, N)) || (rc = encode_rows_map(&tdo, dout, d, N, B * Hq, N)))
     return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int Np = (int)(cdiv(N, TILE) * TILE);
   float* dsum = static_cast<float*>(workspace);
-  cudaError_t e = launch_bwd_preprocess(o, dout, dsum, (int64_t)B * Hq * N, d, s);
+  float* lse2 = dsum + (size_t)B * Hq * Np;
+  cudaError_t e = launch_bwd_preprocess(o, dout, lse, dsum, lse2, (int64_t)B * Hq, N, Np, d, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
   BwdParams p{};
-  p.lse = lse;
+  p.lse2 = lse2;
   p.dsum = dsum;
+  p.Np = Np;
   p.dq = dq; p.dk = dk; p.dv = dv;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N;
   p.scale = scale;
@@ -297,7 +301,6 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   p.status = status;
   p.wait_limit_ns = wait_limit();
   e = launch_bwd_dkdv(d, tq, tk, tv, tdo, p, s);
-  if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, "backward kernels not built");
   if (e != cudaSuccess) return cuda_fail(e, "backward dK/dV launch");
   e = launch_bwd_dq(d, tq, tk, tv, tdo, p, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward dQ launch");

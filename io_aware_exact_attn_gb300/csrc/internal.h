@@ -32,8 +32,9 @@ struct FwdParams {
 
 // Backward parameter block (kernels 2 and 3 of attn_bwd).
 struct BwdParams {
-  const float* lse;         // [B,Hq,N]
-  const float* dsum;        // D = rowsum(dO*O), [B,Hq,N]
+  const float* lse2;        // LSE * log2(e), [B*Hq][Np], +inf on padding rows
+  const float* dsum;        // D = rowsum(dO*O), [B*Hq][Np], 0 on padding rows
+  int Np;                   // N rounded up to a multiple of 128
   void* dq;                 // bf16 [B,Hq,N,d]
   void* dk;                 // bf16 [B,Hkv,N,d]
   void* dv;                 // bf16 [B,Hkv,N,d]
@@ -64,8 +65,8 @@ cudaError_t launch_merge(const float* const* o_parts, const float* const* lse_pa
                          void* o_out, bool out_f32, float* lse_out, int rows_per_head, int heads,
                          int d, int64_t out_head_stride, cudaStream_t s);
 
-cudaError_t launch_bwd_preprocess(const void* o, const void* dout, float* dsum, int64_t rows, int d,
-                                  cudaStream_t s);
+cudaError_t launch_bwd_preprocess(const void* o, const void* dout, const float* lse, float* dsum, float* lse2,
+                                  int64_t heads, int N, int Np, int d, cudaStream_t s);
 
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,

@@ -88,21 +88,32 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
   }
 }
 
-// D_i = sum_k dO_ik * O_ik; groups of d/8 lanes per row, 8 bf16 per lane.
+// D_i = sum_k dO_ik * O_ik and lse2_i = LSE_i * log2(e) for the backward
+// kernels; groups of d/8 lanes per row, 8 bf16 per lane.  Both outputs are
+// [heads][Np] with Np = N rounded up to a whole tile; rows past N (and rows
+// whose LSE is -inf, i.e. that saw no key) get D = 0 and lse2 = +inf, which
+// makes every recomputed probability of such a row exactly 0.
 template <int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ dout,
-                                                         float* __restrict__ dsum, int64_t rows) {
+                                                         const float* __restrict__ lse,
+                                                         float* __restrict__ dsum, float* __restrict__ lse2,
+                                                         int64_t heads, int N, int Np) {
   constexpr int LPR = D / 8;
   constexpr int RPW = 32 / LPR;
   const int lane = threadIdx.x & 31;
   const int sub = lane / LPR, col = (lane % LPR) * 8;
+  const int64_t rows = heads * Np;
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x / 32);
   for (int64_t wrow = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; wrow * RPW < rows;
        wrow += warps_total) {
-    const int64_t row = wrow * RPW + sub;
+    const int64_t prow = wrow * RPW + sub;        // padded row index
+    const int64_t head = prow / Np;
+    const int r = (int)(prow - head * Np);
+    const bool valid = prow < rows && r < N;
+    const int64_t row = head * N + r;             // dense row index
     float acc = 0.f;
-    if (row < rows) {
+    if (valid) {
       const uint4 a = __ldcs(reinterpret_cast<const uint4*>(o + row * D + col));
       const uint4 b = __ldcs(reinterpret_cast<const uint4*>(dout + row * D + col));
       const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
@@ -117,7 +128,15 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
     }
 #pragma unroll
     for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (row < rows && (lane % LPR) == 0) dsum[row] = acc;
+    if (prow < rows && (lane % LPR) == 0) {
+      float l2 = INFINITY;
+      if (valid) {
+        const float L = lse[row];
+        l2 = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
+      }
+      dsum[prow] = valid ? acc : 0.f;
+      lse2[prow] = l2;
+    }
   }
 }
 
@@ -169,16 +188,18 @@ cudaError_t launch_merge(const float* const* o_parts, const float* const* lse_pa
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_preprocess(const void* o, const void* dout, float* dsum, int64_t rows, int d,
-                                  cudaStream_t s) {
+cudaError_t launch_bwd_preprocess(const void* o, const void* dout, const float* lse, float* dsum, float* lse2,
+                                  int64_t heads, int N, int Np, int d, cudaStream_t s) {
   const int rpw = 32 / (d / 8);
-  const int grid = grid_for((rows + rpw - 1) / rpw);
+  const int grid = grid_for((heads * Np + rpw - 1) / rpw);
   if (d == 128)
     preprocess_kernel<128><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
-                                                static_cast<const __nv_bfloat16*>(dout), dsum, rows);
+                                                static_cast<const __nv_bfloat16*>(dout), lse, dsum, lse2, heads,
+                                                N, Np);
   else
     preprocess_kernel<64><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
-                                               static_cast<const __nv_bfloat16*>(dout), dsum, rows);
+                                               static_cast<const __nv_bfloat16*>(dout), lse, dsum, lse2, heads,
+                                               N, Np);
   return cudaGetLastError();
 }
 

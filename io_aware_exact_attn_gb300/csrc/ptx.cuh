@@ -118,6 +118,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int c
       : "memory");
 }
 
+// Plain (untiled) bulk copy global -> shared: both addresses 16-byte aligned,
+// bytes a multiple of 16; no bounds checking, so the source must be in range.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // Make generic-proxy shared-memory writes visible to the async proxy (TMA, MMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -77,7 +77,7 @@ def test_argument_validation_without_gpu(lib):
     assert lib.attn_merge_lse(arr, arr, 65, _ptr(good), 0, None, 1, 1, 4, 64, 0, None) == -1
     # bwd workspace size and check
     need = lib.attn_bwd_workspace_bytes(2, 4, 2, 100, 64)
-    assert need == ((2 * 4 * 100 * 4 + 255) // 256) * 256
+    assert need == ((2 * 2 * 4 * 128 * 4 + 255) // 256) * 256
     p = [_ptr(good)] * 10
     assert lib.attn_bwd(*p, need - 256, 2, 4, 2, 100, 64, 0.125, None, None) == -6
     # partial fwd: head stride smaller than the rows is rejected
