@@ -1,0 +1,470 @@
+#!/usr/bin/env python3
+"""Exact-attention benchmark on GB300: forward + backward TFLOP/s.
+
+One step = one forward (attn_fwd) and one backward (attn_bwd: preprocessing,
+dK/dV, dQ) pass over the causal GPT-style workload B=2, H=32, N=8192, d=128
+with seeded synthetic bf16 inputs resident in HBM.  FLOPs follow the
+published convention: 4*B*H*N^2*d for the forward, 2.5x that for the
+backward, halved under a causal mask.
+
+Printed (rank 0): one JSON line with the headline value, per-kernel roofline of
+the dominant kernel (durations from CUDA events the library records around its
+own launches, on the launching stream), the chunked partial-forward + LSE-merge
+rows measured in the same run, an end-to-end number through the public API
+with host buffers, the fp64 CPU oracle timed on a bounded sample, and the SM
+clocks sampled during the timed region.
+
+``--impl reference`` times the fp64 CPU oracle itself (the only reference this
+method has: the pages hold no runnable implementation) on a bounded sample of
+the same workload.  Multi-GPU (torchrun, one rank per GPU): every rank runs its
+own independent batch (weak scaling, no collective on the data path); the
+slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd+bwd TFLOP/s (bf16, causal-adjusted) and % of GB300 dense BF16 peak"
+WORKLOAD = dict(name="gpt_causal", B=2, Hq=32, Hkv=32, N=8192, d=128, mask="causal")
+CHUNKED = dict(name="chunked_gqa", B=1, Hq=32, Hkv=8, N=32768, d=128, chunks=8)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = {
+    "fwd": ["fwd.cu", "ptx.cuh", "schedule.h", "internal.h"],
+    "partial_fwd": ["fwd.cu", "ptx.cuh", "schedule.h", "internal.h"],
+    "bwd_dkdv": ["bwd.cu", "ptx.cuh", "internal.h"],
+    "bwd_dq": ["bwd.cu", "ptx.cuh", "internal.h"],
+    "bwd_preprocess": ["merge.cu", "ptx.cuh", "internal.h"],
+    "merge": ["merge.cu", "ptx.cuh", "internal.h"],
+}
+
+
+def fwd_flops(B, H, N, d, causal):
+    return 4.0 * B * H * N * N * d * (0.5 if causal else 1.0)
+
+
+def step_flops(w):
+    f = fwd_flops(w["B"], w["Hq"], w["N"], w["d"], w["mask"] == "causal")
+    return f, 2.5 * f
+
+
+def kernel_work(w):
+    """Algorithmic work per launch of each kernel of one step."""
+    B, H, N, d = w["B"], w["Hq"], w["N"], w["d"]
+    cf = 0.5 if w["mask"] == "causal" else 1.0
+    gemm = 2.0 * B * H * N * N * d * cf          # one N x N x d product over all heads
+    Np = -(-N // 128) * 128
+    return {
+        "fwd": ("tensor", 2 * gemm),                 # S = QK^T, O = PV
+        "bwd_dkdv": ("tensor", 4 * gemm),            # S^T, dP^T, dV, dK
+        "bwd_dq": ("tensor", 1 * gemm),              # dQ (S and dP are recomputed, not counted)
+        "bwd_preprocess": ("hbm", 2 * B * H * N * d * 2 + 4 * B * H * N + 2 * 4 * B * H * Np),
+    }
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(kernel):
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES.get(kernel, []):
+        with open(os.path.join(ROOT, "io_aware_exact_attn_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+    for path in glob.glob(os.path.join(ROOT, "profiles", f"{kernel}_{workload}*.txt")):
+        text = open(path).read()
+        m_hash = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+        m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+        if m_hash and m_bytes and m_hash.group(1) == source_hash(kernel):
+            return float(m_bytes.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def start(self):
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+            if self.gpu_id is not None:
+                cmd += ["-i", str(self.gpu_id)]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        loaded = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+# ------------------------------------------------------------------ oracle leg
+
+def oracle_sample(seconds, rank=0):
+    """Time the fp64 oracle (fwd + bwd) on heads of the workload cut to their first
+    NS positions (causal), head after head, for about `seconds` seconds."""
+    import numpy as np
+    import oracle
+    from io_aware_exact_attn_gb300 import inputs
+    w = WORKLOAD
+    NS = 2048
+    scale = 1.0 / math.sqrt(w["d"])
+    q, k, v, do = inputs.make_qkvdo(1, 4, 4, NS, NS, w["d"], seed=inputs.SEED + 100 * rank)
+    q, k, v, do = (inputs.to_f64(t) for t in (q, k, v, do))
+    mask = oracle.MaskSpec("causal")
+    t0 = time.perf_counter()
+    heads = 0
+    while True:
+        h = heads % 4
+        sl = slice(h, h + 1)
+        oracle.attention_forward(q[:, sl], k[:, sl], v[:, sl], scale, mask)
+        oracle.attention_backward(q[:, sl], k[:, sl], v[:, sl], do[:, sl], scale, mask)
+        heads += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    f, b = fwd_flops(1, 1, NS, w["d"], True), 2.5 * fwd_flops(1, 1, NS, w["d"], True)
+    return dict(value=heads * (f + b) / el / 1e12, unit="TFLOP/s", cores=os.cpu_count(), kind="oracle",
+                sample=f"{heads} head(s) of the causal d={w['d']} workload cut to the first {NS} positions, "
+                       f"fp64 NumPy fwd+bwd with full score rows, {el:.1f} s; BLAS threads = default "
+                       f"(all {os.cpu_count()} host cores)",
+                seconds=el, heads=heads)
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import oracle  # noqa: F401
+    for _ in range(args.warmup):
+        oracle_sample(0.0)
+    times = []
+    flops = None
+    for _ in range(args.steps):
+        r = oracle_sample(0.0)
+        times.append(r["seconds"])
+        flops = r["value"] * r["seconds"] * 1e12
+    total = sum(times)
+    value = args.steps * flops / total / 1e12
+    cpu = dict(value=value, unit="TFLOP/s", cores=os.cpu_count(), kind="oracle",
+               sample=f"each step: one head of the causal d={WORKLOAD['d']} workload cut to its first 2048 "
+                      f"positions, fp64 NumPy oracle fwd+bwd on the host cores")
+    line = dict(metric=METRIC, value=value, unit="TFLOP/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
+                ms_per_step=1e3 * total / args.steps, higher_is_better=True, scaling="weak", vs_baseline=None,
+                dtype="f64", data="synthetic", impl="reference",
+                config=dict(workload=workload_desc(WORKLOAD), sample="first 2048 positions of one head per step"),
+                cpu_baseline=cpu, e2e=dict(value=value, unit="TFLOP/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_desc(w):
+    return (f"{w['name']}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} N={w['N']} d={w['d']} {w['mask']}, "
+            f"bf16 N(0,1) inputs, scale 1/sqrt(d)")
+
+
+# ------------------------------------------------------------------ GPU leg
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-extras", action="store_true", help="skip the e2e, chunked and CPU legs")
+    ap.add_argument("--profile-pass", action="store_true",
+                    help="one untimed step only (for profiler launch lists); prints nothing")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if args.warmup < 3 and not args.profile_pass:
+        raise SystemExit("--warmup must be at least 3")
+
+    import numpy as np
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import oracle
+    from io_aware_exact_attn_gb300 import api, inputs
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    w = WORKLOAD
+    causal = w["mask"] == "causal"
+    q, k, v, do = (t.cuda() for t in inputs.make_qkvdo(w["B"], w["Hq"], w["Hkv"], w["N"], w["N"], w["d"],
+                                                       seed=inputs.SEED + 100 * rank))
+    o = torch.empty_like(q)
+    lse = torch.empty(w["B"], w["Hq"], w["N"], device="cuda", dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(api.bwd_workspace_bytes(w["B"], w["Hq"], w["Hkv"], w["N"], w["d"]), device="cuda",
+                     dtype=torch.uint8)
+
+    def step():
+        api.attn_fwd(q, k, v, causal=causal, out=o, lse=lse)
+        api.attn_bwd(q, k, v, o, lse, do, causal=causal, workspace=ws, dq=dq, dk=dk, dv=dv)
+
+    if args.profile_pass:
+        step()
+        torch.cuda.synchronize()
+        return 0
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert api.get_status() == 0
+
+    props = torch.cuda.get_device_properties(local)
+    gpu_id = None
+    uuid = getattr(props, "uuid", None)
+    if uuid is not None:
+        gpu_id = "GPU-" + str(uuid) if not str(uuid).startswith("GPU-") else str(uuid)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+    api.trace_enable(8 * args.steps + 64)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+    api.trace_disable()
+    clocks = sampler.stop()
+    recs, n_launch = api.trace_read(8 * args.steps + 64)
+    status = api.get_status()
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    f_fwd, f_bwd = step_flops(w)
+    ms_step = elapsed_ms / args.steps
+    value = world * args.steps * (f_fwd + f_bwd) / (elapsed_ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    peak_burst = peaks["bf16_tflops"]
+
+    # per-kernel durations (CUDA events on the launching stream, inside the timed region)
+    per = {}
+    for name, ms in recs:
+        per.setdefault(name, []).append(ms)
+    work = kernel_work(w)
+    kernels = {}
+    for name, lst in per.items():
+        avg = sum(lst) / len(lst)
+        kind, amount = work.get(name, ("?", 0.0))
+        entry = dict(launches=len(lst), avg_ms=avg, share=sum(lst) / sum(sum(x) for x in per.values()))
+        if kind == "tensor":
+            entry["tflops"] = amount / (avg * 1e-3) / 1e12
+        elif kind == "hbm":
+            entry["gbs"] = amount / (avg * 1e-3) / 1e9
+        kernels[name] = entry
+    dom = max(kernels, key=lambda n: kernels[n]["share"])
+    kind, amount = work[dom]
+    if kind == "tensor":
+        ach = kernels[dom]["tflops"]
+        roof = dict(bound="tensor", achieved=ach, peak=peak_sus, unit="TFLOP/s", frac=ach / peak_sus,
+                    traffic=profile_traffic(dom, w["name"]), kernel=dom,
+                    peak_source=f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step loop)",
+                    frac_of_burst_peak=ach / peak_burst)
+    else:
+        ach = kernels[dom]["gbs"]
+        roof = dict(bound="hbm", achieved=ach, peak=peaks["hbm_gbs"], unit="GB/s", frac=ach / peaks["hbm_gbs"],
+                    traffic=profile_traffic(dom, w["name"]), kernel=dom, peak_source=f"{peak_src} hbm_gbs")
+    fwd_ms = kernels.get("fwd", {}).get("avg_ms", float("nan"))
+    bwd_ms = sum(kernels.get(n, {}).get("avg_ms", 0.0) for n in ("bwd_preprocess", "bwd_dkdv", "bwd_dq"))
+    split = dict(fwd_tflops=f_fwd / (fwd_ms * 1e-3) / 1e12, bwd_tflops=f_bwd / (bwd_ms * 1e-3) / 1e12)
+    split["fwd_frac_of_burst_peak"] = split["fwd_tflops"] / peak_burst
+    split["bwd_frac_of_burst_peak"] = split["bwd_tflops"] / peak_burst
+
+    # parity spot check on the bench's own outputs (sampled rows vs the oracle)
+    rows = np.array([0, 1, 127, 128, 4095, 8191])
+    f64 = inputs.to_f64
+    qh, kh, vh, doh = (f64(t[:1, :2]) for t in (q, k, v, do))
+    o_ref, l_ref = oracle.attention_forward(qh, kh, vh, 1 / math.sqrt(w["d"]), oracle.MaskSpec("causal"),
+                                            heads=[(0, 0), (0, 1)], rows=rows)
+    o_err = float(np.abs(f64(o[0, :2, rows]) - o_ref).max())
+    l_err = float(np.abs(f64(lse[0, :2, rows]) - l_ref).max())
+    dq_ref = oracle.attention_backward_dq_rows(qh, kh, vh, doh, 1 / math.sqrt(w["d"]), 0, 1, rows,
+                                               oracle.MaskSpec("causal"))
+    dq_err = float(np.abs(f64(dq[0, 1, rows]) - dq_ref).max() / np.abs(dq_ref).max())
+    parity = dict(rows_checked=int(2 * rows.size), o_max_abs=o_err, lse_max_abs=l_err, dq_rel=dq_err,
+                  ok=bool(o_err <= 1e-2 and l_err <= 2e-3 and dq_err <= 3e-2 and status == 0))
+
+    out = dict(metric=METRIC, value=value, unit="TFLOP/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
+               ms_per_step=ms_step, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
+               data="synthetic",
+               config=dict(workload=workload_desc(w), B=w["B"], Hq=w["Hq"], Hkv=w["Hkv"], N=w["N"], d=w["d"],
+                           mask=w["mask"], per_rank="one independent batch per GPU",
+                           l2="inputs larger than L2 (Q, K, V, O, dO are 134 MB each; L2 is 129 MB), no flush"),
+               roofline=roof, kernels=kernels, split=split, gpu_launches=n_launch, parity=parity,
+               pct_of_burst_peak=value / world / peak_burst)
+    if clocks is not None:
+        out["clocks"] = clocks
+
+    if not args.no_extras:
+        out["e2e"] = e2e_leg(api, inputs, torch, w, causal, rank)
+        out["chunked_gqa"] = chunked_leg(api, inputs, torch, peaks, rank)
+        if rank == 0:
+            out["cpu_baseline"] = {k_: v_ for k_, v_ in oracle_sample(args.cpu_seconds).items()
+                                   if k_ in ("value", "unit", "cores", "kind", "sample")}
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    return 0
+
+
+def e2e_leg(api, inputs, torch, w, causal, rank, steps=6):
+    """Same metric through the public API with pinned HOST buffers: every step copies
+    Q, K, V, dO to the device and O, LSE, dQ, dK, dV back."""
+    hq, hk, hv, hdo = (t.pin_memory() for t in inputs.make_qkvdo(w["B"], w["Hq"], w["Hkv"], w["N"], w["N"],
+                                                                  w["d"], seed=inputs.SEED + 100 * rank + 7))
+    outs = [torch.empty(w["B"], w["Hq"], w["N"], w["d"], dtype=torch.bfloat16).pin_memory(),
+            torch.empty(w["B"], w["Hq"], w["N"], dtype=torch.float32).pin_memory(),
+            torch.empty(w["B"], w["Hq"], w["N"], w["d"], dtype=torch.bfloat16).pin_memory(),
+            torch.empty(w["B"], w["Hkv"], w["N"], w["d"], dtype=torch.bfloat16).pin_memory(),
+            torch.empty(w["B"], w["Hkv"], w["N"], w["d"], dtype=torch.bfloat16).pin_memory()]
+
+    def one():
+        q, k, v, do = (t.to("cuda", non_blocking=True) for t in (hq, hk, hv, hdo))
+        o, lse = api.attn_fwd(q, k, v, causal=causal)
+        dq, dk, dv = api.attn_bwd(q, k, v, o, lse, do, causal=causal)
+        for dst, src in zip(outs, (o, lse, dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    el = time.perf_counter() - t0
+    f_fwd, f_bwd = step_flops(w)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    return dict(value=steps * (f_fwd + f_bwd) / el / 1e12, unit="TFLOP/s", h2d_bytes_per_step=h2d,
+                d2h_bytes_per_step=d2h, steps=steps, ms_per_step=1e3 * el / steps)
+
+
+def chunked_leg(api, inputs, torch, peaks, rank, reps=3):
+    """Chunked causal GQA (B=1, Hq=32, Hkv=8, N=32768, d=128, 8 chunks): the 36
+    partial forwards in load-balanced order, then one LSE merge per query chunk."""
+    c = CHUNKED
+    B, Hq, Hkv, N, d, nc = c["B"], c["Hq"], c["Hkv"], c["N"], c["d"], c["chunks"]
+    L = N // nc
+    q, k, v, _ = (t.cuda() for t in inputs.make_qkvdo(B, Hq, Hkv, N, N, d, seed=inputs.SEED + 100 * rank + 3))
+    sched = api.build_chunk_schedule(nc)
+    parts = {p: (torch.empty(B, Hq, L, d, device="cuda"), torch.empty(B, Hq, L, device="cuda")) for p in sched}
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, N, device="cuda")
+
+    def run():
+        for qc, kc in sched:
+            api.attn_partial_fwd(q[:, :, qc * L:(qc + 1) * L], k[:, :, kc * L:(kc + 1) * L],
+                                 v[:, :, kc * L:(kc + 1) * L], qc * L, kc * L, causal=True,
+                                 o_part=parts[(qc, kc)][0], lse_part=parts[(qc, kc)][1])
+        for qc in range(nc):
+            api.attn_merge_lse([parts[(qc, kc)][0] for kc in range(qc + 1)],
+                               [parts[(qc, kc)][1] for kc in range(qc + 1)],
+                               out=o[:, :, qc * L:(qc + 1) * L], lse_out=lse[:, :, qc * L:(qc + 1) * L])
+
+    run()
+    torch.cuda.synchronize()
+    api.trace_enable(64 * reps)
+    for _ in range(reps):
+        run()
+    torch.cuda.synchronize()
+    api.trace_disable()
+    recs, _ = api.trace_read(64 * reps)
+    part_ms = sum(ms for n, ms in recs if n == "partial_fwd") / reps
+    merge_ms = sum(ms for n, ms in recs if n == "merge") / reps
+    flops = fwd_flops(B, Hq, N, d, True)
+    merge_bytes = sum((qc + 1) * (B * Hq * L * (d * 4 + 4)) for qc in range(nc)) + B * Hq * N * (d * 2 + 4)
+    # monolithic causal forward on the same tensors, and agreement with the chunked result
+    o_m, l_m = api.attn_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    agree = dict(o_max_abs=float((o.float() - o_m.float()).abs().max()),
+                 lse_max_abs=float((lse - l_m).abs().max()))
+    gbs = merge_bytes / (merge_ms * 1e-3) / 1e9
+    return dict(workload=f"B={B} Hq={Hq} Hkv={Hkv} N={N} d={d} causal, {nc} chunks, {len(sched)} pairs",
+                partial_fwd_ms=part_ms, partial_fwd_tflops=flops / (part_ms * 1e-3) / 1e12,
+                merge_ms=merge_ms, merge_bytes=merge_bytes, merge_gbs=gbs, merge_frac_of_hbm=gbs / peaks["hbm_gbs"],
+                chunked_vs_monolithic=agree)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -222,6 +222,36 @@ void attn_set_wait_limit_ns(int64_t limit_ns);
  */
 int attn_selftest_wait_timeout(int64_t limit_ns, void* stream);
 
+/*
+ * Launch tracing.  While enabled, every kernel the library launches is
+ * bracketed by two CUDA events recorded on the launching stream, so each
+ * kernel's device time can be read back afterwards.  Kernel ids:
+ */
+typedef enum {
+  ATTN_KERNEL_FWD = 1,            /* attn_fwd forward kernel */
+  ATTN_KERNEL_PARTIAL_FWD = 2,    /* attn_partial_fwd forward kernel (f32 output) */
+  ATTN_KERNEL_MERGE = 3,          /* attn_merge_lse */
+  ATTN_KERNEL_BWD_PREPROCESS = 4, /* attn_bwd step 1: D and LSE*log2 e */
+  ATTN_KERNEL_BWD_DKDV = 5,       /* attn_bwd step 2: dK, dV */
+  ATTN_KERNEL_BWD_DQ = 6,         /* attn_bwd step 3: dQ */
+  ATTN_KERNEL_SELFTEST = 7        /* attn_selftest_wait_timeout */
+} attn_kernel_id_t;
+
+typedef struct attn_trace_record {
+  int32_t kernel; /* attn_kernel_id_t */
+  float ms;       /* device time between the two events */
+} attn_trace_record_t;
+
+/* Start recording (dropping earlier records); at most `capacity` launches are
+ * kept (1 <= capacity <= 1<<20).  Tracing is process-wide. */
+int attn_trace_enable(int capacity);
+/* Stop recording; records already taken stay readable. */
+int attn_trace_disable(void);
+/* Wait for the recorded events, copy up to cap records in launch order to
+ * out (HOST), set *n_out to the number recorded, and clear them.  Launches
+ * beyond the capacity are counted in *n_out but not stored. */
+int attn_trace_read(attn_trace_record_t* out, int cap, int* n_out);
+
 const char* attn_status_string(int status);
 const char* attn_last_error_message(void);
 int attn_version(void);

@@ -16,6 +16,9 @@ from .api import (  # noqa: F401
     set_wait_limit_ns,
     selftest_wait_timeout,
     mask_desc,
+    trace_enable,
+    trace_disable,
+    trace_read,
 )
 
 __version__ = "0.1.0"

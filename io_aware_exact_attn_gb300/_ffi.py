@@ -15,6 +15,14 @@ LIB_PATH = os.path.join(_PKG, "libattn.so")
 c_void_p, c_int, c_float, c_int64, c_size_t = C.c_void_p, C.c_int, C.c_float, C.c_int64, C.c_size_t
 
 
+class attn_trace_record_t(C.Structure):
+    _fields_ = [("kernel", C.c_int32), ("ms", C.c_float)]
+
+
+KERNEL_NAMES = {1: "fwd", 2: "partial_fwd", 3: "merge", 4: "bwd_preprocess", 5: "bwd_dkdv", 6: "bwd_dq",
+                7: "selftest"}
+
+
 class attn_mask_t(C.Structure):
     _fields_ = [("kind", C.c_int32), ("causal_in_blocks", C.c_int32), ("block_mask", C.c_void_p)]
 
@@ -44,6 +52,9 @@ SIGNATURES = {
     "attn_get_status": (c_int, [c_void_p]),
     "attn_set_wait_limit_ns": (None, [c_int64]),
     "attn_selftest_wait_timeout": (c_int, [c_int64, c_void_p]),
+    "attn_trace_enable": (c_int, [c_int]),
+    "attn_trace_disable": (c_int, []),
+    "attn_trace_read": (c_int, [C.POINTER(attn_trace_record_t), c_int, C.POINTER(c_int)]),
     "attn_status_string": (C.c_char_p, [c_int]),
     "attn_last_error_message": (C.c_char_p, []),
     "attn_version": (c_int, []),

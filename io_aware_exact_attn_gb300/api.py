@@ -18,7 +18,7 @@ from ._ffi import attn_mask_t, check
 
 __all__ = ["attn_fwd", "attn_partial_fwd", "attn_merge_lse", "attn_bwd", "bwd_workspace_bytes",
            "build_schedule", "build_chunk_schedule", "get_status", "set_wait_limit_ns",
-           "selftest_wait_timeout", "mask_desc"]
+           "selftest_wait_timeout", "mask_desc", "trace_enable", "trace_disable", "trace_read"]
 
 
 def _stream(t: torch.Tensor) -> int:
@@ -223,3 +223,22 @@ def set_wait_limit_ns(limit_ns: int) -> None:
 def selftest_wait_timeout(limit_ns: int, device=None) -> None:
     s = torch.cuda.current_stream(device).cuda_stream
     check(_ffi.lib().attn_selftest_wait_timeout(int(limit_ns), s), "attn_selftest_wait_timeout")
+
+
+def trace_enable(capacity: int = 4096) -> None:
+    """Record CUDA events around every kernel the library launches from now on."""
+    check(_ffi.lib().attn_trace_enable(int(capacity)), "attn_trace_enable")
+
+
+def trace_disable() -> None:
+    _ffi.lib().attn_trace_disable()
+
+
+def trace_read(capacity: int = 1 << 16):
+    """Return ``(records, n_launched)``: records are ``(kernel_name, ms)`` in launch order."""
+    buf = (_ffi.attn_trace_record_t * capacity)()
+    n = C.c_int(0)
+    check(_ffi.lib().attn_trace_read(buf, capacity, C.byref(n)), "attn_trace_read")
+    recs = [(_ffi.KERNEL_NAMES.get(buf[i].kernel, str(buf[i].kernel)), float(buf[i].ms))
+            for i in range(min(n.value, capacity))]
+    return recs, n.value

@@ -123,6 +123,51 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// ---- launch tracing: event pairs recorded on the launching stream
+struct TraceEntry {
+  int kernel;
+  cudaEvent_t start, stop;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+int g_trace_cap = 0;
+int64_t g_trace_count = 0;
+std::vector<TraceEntry> g_trace;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Brackets one launch; a no-op unless tracing is enabled.
+struct TraceScope {
+  int slot = -1;
+  cudaStream_t s;
+  TraceScope(int kernel, cudaStream_t stream) : s(stream) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (!g_trace_on) return;
+    ++g_trace_count;
+    if ((int)g_trace.size() >= g_trace_cap) return;
+    TraceEntry t{kernel, take_event(), take_event()};
+    if (t.start == nullptr || t.stop == nullptr) return;
+    cudaEventRecord(t.start, s);
+    g_trace.push_back(t);
+    slot = (int)g_trace.size() - 1;
+  }
+  ~TraceScope() {
+    if (slot < 0) return;
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (slot < (int)g_trace.size()) cudaEventRecord(g_trace[slot].stop, s);
+  }
+};
+
 }  // namespace
 
 namespace attn {
@@ -208,7 +253,11 @@ static int fwd_common(const void* q, const void* k, const void* v, void* o, bool
   p.kv_offset = kv_off;
   p.status = status;
   p.wait_limit_ns = wait_limit();
-  cudaError_t e = launch_fwd(d, out_f32, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  {
+    TraceScope ts(out_f32 ? ATTN_KERNEL_PARTIAL_FWD : ATTN_KERNEL_FWD, static_cast<cudaStream_t>(stream));
+    e = launch_fwd(d, out_f32, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  }
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return ATTN_OK;
 }
@@ -244,8 +293,12 @@ int attn_merge_lse(const float* const* o_parts, const float* const* lse_parts, i
   if (hs < Nq) return fail(ATTN_ERR_INVALID_ARG, "out_head_stride smaller than Nq");
   unsigned int* status = nullptr;
   if ((rc = device_ready(&status))) return rc;
-  cudaError_t e = launch_merge(o_parts, lse_parts, n_parts, o_out, out_dtype == ATTN_DTYPE_F32, lse_out, Nq, B * Hq,
-                               d, hs, static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  {
+    TraceScope ts(ATTN_KERNEL_MERGE, static_cast<cudaStream_t>(stream));
+    e = launch_merge(o_parts, lse_parts, n_parts, o_out, out_dtype == ATTN_DTYPE_F32, lse_out, Nq, B * Hq, d, hs,
+                     static_cast<cudaStream_t>(stream));
+  }
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return ATTN_OK;
 }
@@ -284,7 +337,11 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   const int Np = (int)(cdiv(N, TILE) * TILE);
   float* dsum = static_cast<float*>(workspace);
   float* lse2 = dsum + (size_t)B * Hq * Np;
-  cudaError_t e = launch_bwd_preprocess(o, dout, lse, dsum, lse2, (int64_t)B * Hq, N, Np, d, s);
+  cudaError_t e;
+  {
+    TraceScope ts(ATTN_KERNEL_BWD_PREPROCESS, s);
+    e = launch_bwd_preprocess(o, dout, lse, dsum, lse2, (int64_t)B * Hq, N, Np, d, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
   BwdParams p{};
   p.lse2 = lse2;
@@ -300,9 +357,15 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   p.nkb = (int)cdiv(N, TILE);
   p.status = status;
   p.wait_limit_ns = wait_limit();
-  e = launch_bwd_dkdv(d, tq, tk, tv, tdo, p, s);
+  {
+    TraceScope ts(ATTN_KERNEL_BWD_DKDV, s);
+    e = launch_bwd_dkdv(d, tq, tk, tv, tdo, p, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "backward dK/dV launch");
-  e = launch_bwd_dq(d, tq, tk, tv, tdo, p, s);
+  {
+    TraceScope ts(ATTN_KERNEL_BWD_DQ, s);
+    e = launch_bwd_dq(d, tq, tk, tv, tdo, p, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "backward dQ launch");
   return ATTN_OK;
 }
@@ -394,9 +457,57 @@ int attn_selftest_wait_timeout(int64_t limit_ns, void* stream) {
   int rc = device_ready(&status);
   if (rc) return rc;
   if (limit_ns <= 0 || limit_ns > 10000000000ll) return fail(ATTN_ERR_INVALID_ARG, "limit_ns outside (0, 1e10]");
-  cudaError_t e = launch_wait_selftest(status, limit_ns, static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  {
+    TraceScope ts(ATTN_KERNEL_SELFTEST, static_cast<cudaStream_t>(stream));
+    e = launch_wait_selftest(status, limit_ns, static_cast<cudaStream_t>(stream));
+  }
   if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
   return ATTN_OK;
+}
+
+int attn_trace_enable(int capacity) {
+  if (capacity < 1 || capacity > (1 << 20)) return fail(ATTN_ERR_INVALID_ARG, "trace capacity %d", capacity);
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  for (auto& t : g_trace) {
+    g_event_pool.push_back(t.start);
+    g_event_pool.push_back(t.stop);
+  }
+  g_trace.clear();
+  g_trace.reserve(capacity);
+  g_trace_cap = capacity;
+  g_trace_count = 0;
+  g_trace_on = true;
+  return ATTN_OK;
+}
+
+int attn_trace_disable(void) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_on = false;
+  return ATTN_OK;
+}
+
+int attn_trace_read(attn_trace_record_t* out, int cap, int* n_out) {
+  if (n_out == nullptr) return fail(ATTN_ERR_INVALID_ARG, "n_out is NULL");
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  *n_out = (int)g_trace_count;
+  int rc = ATTN_OK;
+  for (size_t i = 0; i < g_trace.size(); ++i) {
+    TraceEntry& t = g_trace[i];
+    cudaError_t e = cudaEventSynchronize(t.stop);
+    float ms = -1.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, t.start, t.stop);
+    if (e != cudaSuccess) rc = cuda_fail(e, "reading a trace event");
+    if (out != nullptr && (int)i < cap) {
+      out[i].kernel = t.kernel;
+      out[i].ms = ms;
+    }
+    g_event_pool.push_back(t.start);
+    g_event_pool.push_back(t.stop);
+  }
+  g_trace.clear();
+  g_trace_count = 0;
+  return rc;
 }
 
 }  // extern "C"
