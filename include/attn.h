@@ -165,6 +165,37 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o,
              void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
              int N, int d, float scale, const attn_mask_t* mask, void* stream);
 
+/*
+ * attn_bwd_static_scratch -- the same backward pass as attn_bwd, for callers
+ * that must not allocate device memory: code running where cudaMalloc is not
+ * allowed or would break a memory budget fixed up front (an allocator or
+ * runtime that owns every device allocation, a pre-reserved serving process,
+ * a host that has set up its memory pools before the hot loop).  It takes no
+ * workspace and allocates nothing: its scratch (D and LSE*log2 e) lives in a
+ * static device array of ATTN_STATIC_SCRATCH_BYTES inside the library, which
+ * every GPU that loads the library holds until the process exits.  The pages
+ * describe no such variant; it is an integration aid only.
+ *   Arguments, layouts and results are those of attn_bwd.
+ *   Limit: 2 * B*Hq*ceil(N/128)*128 floats must fit in the array, i.e.
+ *   B*Hq*ceil(N/128)*128 <= 2^21 query rows; larger calls return
+ *   ATTN_ERR_WORKSPACE and launch nothing.
+ *   The first call on each device looks up the array's device address (and
+ *   the device status word next to it) with cudaGetSymbolAddress while that
+ *   device is current; make that first call before any stream capture.
+ *   All calls on a device share the one array: calls that may overlap on the
+ *   GPU (other streams, other host threads) race and must be serialised by
+ *   the caller.  Nothing in the array needs clearing: each call overwrites
+ *   every entry it later reads.
+ *   A kernel wait that runs out during this call is recorded in the static
+ *   status word, not in the one attn_get_status() reads; dQ, dK and dV are
+ *   then incomplete.
+ */
+#define ATTN_STATIC_SCRATCH_BYTES (16u << 20)
+int attn_bwd_static_scratch(const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dout, void* dq, void* dk,
+                            void* dv, int B, int Hq, int Hkv, int N, int d, float scale,
+                            const attn_mask_t* mask, void* stream);
+
 /* Bytes of workspace attn_bwd needs: two float arrays (D and LSE*log2 e) of
  * B*Hq*ceil(N/128)*128 entries, rounded up to 256 bytes. */
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);

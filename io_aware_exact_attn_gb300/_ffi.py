@@ -45,6 +45,9 @@ SIGNATURES = {
     "attn_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                          c_void_p, c_void_p, c_size_t, c_int, c_int, c_int, c_int, c_int, c_float,
                          C.POINTER(attn_mask_t), c_void_p]),
+    "attn_bwd_static_scratch": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                        c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float,
+                                        C.POINTER(attn_mask_t), c_void_p]),
     "attn_bwd_workspace_bytes": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
     "attn_build_schedule": (c_int, [c_int, c_int, c_void_p, c_int, c_int, c_int, c_int, c_int64, c_int64,
                                     C.POINTER(C.c_int32), c_size_t, C.POINTER(c_size_t)]),

@@ -511,3 +511,99 @@ int attn_trace_read(attn_trace_record_t* out, int cap, int* n_out) {
 }
 
 }  // extern "C"
+
+// ============================================================ static scratch
+// attn_bwd_static_scratch: attn_bwd without a caller workspace and without any
+// device allocation, for callers that cannot call cudaMalloc.  The scratch is a
+// file-scope static device array; host code never passes the array's name to a
+// kernel (in host code that name is only a host-side stand-in) but its device
+// address, looked up once per device with cudaGetSymbolAddress.
+namespace {
+
+static __device__ __align__(256) float g_static_scratch[ATTN_STATIC_SCRATCH_BYTES / sizeof(float)];
+static __device__ unsigned int g_static_status;
+
+struct StaticScratch {
+  float* scratch = nullptr;
+  unsigned int* status = nullptr;
+};
+StaticScratch g_static_dev[MAX_DEVICES];
+std::mutex g_static_mu;
+
+// Device addresses of the static scratch and status word on the current device.
+int static_scratch_for_current_device(StaticScratch* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(ATTN_ERR_NO_DEVICE, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= MAX_DEVICES) return fail(ATTN_ERR_NO_DEVICE, "device index %d out of range", dev);
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (!(major == 10 && minor == 3)) return fail(ATTN_ERR_NO_DEVICE, "device %d is not sm_103 (GB300)", dev);
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  StaticScratch& st = g_static_dev[dev];
+  if (st.scratch == nullptr) {
+    void* ps = nullptr;
+    void* pw = nullptr;
+    e = cudaGetSymbolAddress(&ps, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    e = cudaGetSymbolAddress(&pw, g_static_status);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static status)");
+    st.scratch = static_cast<float*>(ps);
+    st.status = static_cast<unsigned int*>(pw);
+  }
+  *out = st;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int attn_bwd_static_scratch(const void* q, const void* k, const void* v, const void* o,
+                                       const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                                       int Hq, int Hkv, int N, int d, float scale, const attn_mask_t* mask,
+                                       void* stream) {
+  int rc;
+  if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k, "k")) || (rc = check_ptr(v, "v")) ||
+      (rc = check_ptr(o, "o")) || (rc = check_ptr(lse, "lse")) || (rc = check_ptr(dout, "dout")) ||
+      (rc = check_ptr(dq, "dq")) || (rc = check_ptr(dk, "dk")) || (rc = check_ptr(dv, "dv")))
+    return rc;
+  if ((rc = check_dims(B, Hq, Hkv, N, N, d, scale))) return rc;
+  const int64_t Np = cdiv(N, TILE) * TILE;
+  const int64_t rows = (int64_t)B * Hq * Np;
+  if (2 * rows * (int64_t)sizeof(float) > (int64_t)ATTN_STATIC_SCRATCH_BYTES)
+    return fail(ATTN_ERR_WORKSPACE,
+                "B*Hq*ceil(N/128)*128 = %lld query rows exceed the static scratch limit of %lld rows",
+                (long long)rows, (long long)(ATTN_STATIC_SCRATCH_BYTES / (2 * sizeof(float))));
+  MaskArgs m;
+  if ((rc = read_mask(mask, &m))) return rc;
+  StaticScratch st;
+  if ((rc = static_scratch_for_current_device(&st))) return rc;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((rc = encode_rows_map(&tq, q, d, N, B * Hq, N)) || (rc = encode_rows_map(&tk, k, d, N, B * Hkv, N)) ||
+      (rc = encode_rows_map(&tv, v, d, N, B * Hkv, N)) || (rc = encode_rows_map(&tdo, dout, d, N, B * Hq, N)))
+    return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* dsum = st.scratch;
+  float* lse2 = st.scratch + rows;
+  cudaError_t e = launch_bwd_preprocess(o, dout, lse, dsum, lse2, (int64_t)B * Hq, N, (int)Np, d, s);
+  if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
+  BwdParams p{};
+  p.lse2 = lse2;
+  p.dsum = dsum;
+  p.Np = (int)Np;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.mask_kind = m.kind;
+  p.causal_in_blocks = m.causal_in_blocks;
+  p.block_mask = m.block_mask;
+  p.nkb = (int)cdiv(N, TILE);
+  p.status = st.status;
+  p.wait_limit_ns = wait_limit();
+  e = launch_bwd_dkdv(d, tq, tk, tv, tdo, p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "backward dK/dV launch");
+  e = launch_bwd_dq(d, tq, tk, tv, tdo, p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "backward dQ launch");
+  return ATTN_OK;
+}

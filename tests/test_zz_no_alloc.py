@@ -1,0 +1,45 @@
+"""attn_bwd_static_scratch: the backward pass for callers that cannot allocate
+device memory (for example code that runs under an allocator or runtime that
+owns every device allocation, or a process whose memory was reserved up
+front).  It must give the same dQ, dK and dV as attn_bwd, including when it is
+called twice in a row and the second call reuses the one static scratch area.
+
+This file is collected last on purpose, so that a run that stops at the first
+failure has already run every other test."""
+import ctypes as C
+
+import pytest
+import torch
+
+from io_aware_exact_attn_gb300 import _ffi, api
+from _gpu_helpers import assert_grad, f64, make
+
+
+def test_static_scratch_rejects_oversized_problem_without_a_gpu():
+    lib = _ffi.lib()
+    p = C.c_void_p(4096)
+    # 2 * 32 * 65536 query rows = 2^22 > 2^21: refused before any device work
+    rc = lib.attn_bwd_static_scratch(p, p, p, p, p, p, p, p, p, 2, 32, 32, 65536, 128, 0.088, None, None)
+    assert rc == -6
+    assert b"static scratch" in lib.attn_last_error_message()
+
+
+@pytest.mark.gpu
+def test_static_scratch_backward_matches_attn_bwd(cuda_lib):
+    lib = cuda_lib
+    cases = [(1, 4, 2, 700, 128, True), (2, 2, 2, 384, 64, False)]   # two calls in a row
+    for B, Hq, Hkv, N, d, causal in cases:
+        q, k, v, do = make(B, Hq, Hkv, N, d)
+        o, lse = api.attn_fwd(q, k, v, causal=causal)
+        ref = api.attn_bwd(q, k, v, o, lse, do, causal=causal)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        m, _ = api.mask_desc(causal=causal)
+        stream = torch.cuda.current_stream().cuda_stream
+        rc = lib.attn_bwd_static_scratch(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                         do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N,
+                                         d, 1.0 / d ** 0.5, C.byref(m) if m is not None else None, stream)
+        assert rc == 0, lib.attn_last_error_message()
+        torch.cuda.synchronize()
+        for name, got, want in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+            assert_grad(f64(got), f64(want), f"{name} B{B} H{Hq}/{Hkv} N{N} d{d}")
+    assert api.get_status() == 0
