@@ -203,17 +203,19 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
 /*
  * attn_build_schedule -- HOST-ONLY.  The forward work units in the order
  * attn_fwd / attn_partial_fwd launch them, as int32 triples
- * (b*Hq + h, query chunk of 256 rows, number of key tiles visited).  Units go
- * heaviest first: unit i takes chunk nqc-1 - i/(B*Hq) of head i%(B*Hq)
- * (DISTFLASHATTN reviews, first review point 1: with causal masking careless
- * placement leaves processors idle).  host_block_mask is a HOST copy of the
- * block mask (only read for ATTN_MASK_BLOCK_SPARSE).  Writes at most cap
- * int32 values to out and the number of units to *n_out; ATTN_ERR_INVALID_ARG
- * if cap is too small (n_out still set).
+ * (b*Hq + h, query chunk of 256 rows, number of key tiles visited).
+ * Heads are taken in groups of G = clamp((Hq/Hkv) * floor(64 MiB / (4*Nk*d)),
+ * 1, B*Hq) consecutive (b, h) so that the group's K and V stay in L2; inside a
+ * group the latest (heaviest) query chunk of every head comes first, then the
+ * next, and so on (DISTFLASHATTN reviews, first review point 1: with causal
+ * masking careless placement leaves processors idle).  host_block_mask is a
+ * HOST copy of the block mask (only read for ATTN_MASK_BLOCK_SPARSE).  Writes
+ * at most cap int32 values to out and the number of units to *n_out;
+ * ATTN_ERR_INVALID_ARG if cap is too small (n_out still set).
  */
 int attn_build_schedule(int mask_kind, int causal_in_blocks,
-                        const uint8_t* host_block_mask, int B, int Hq, int Nq,
-                        int Nk, int64_t q_offset, int64_t kv_offset,
+                        const uint8_t* host_block_mask, int B, int Hq, int Hkv,
+                        int Nq, int Nk, int d, int64_t q_offset, int64_t kv_offset,
                         int32_t* out, size_t cap, size_t* n_out);
 
 /*

@@ -49,8 +49,8 @@ SIGNATURES = {
                                         c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float,
                                         C.POINTER(attn_mask_t), c_void_p]),
     "attn_bwd_workspace_bytes": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
-    "attn_build_schedule": (c_int, [c_int, c_int, c_void_p, c_int, c_int, c_int, c_int, c_int64, c_int64,
-                                    C.POINTER(C.c_int32), c_size_t, C.POINTER(c_size_t)]),
+    "attn_build_schedule": (c_int, [c_int, c_int, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int64,
+                                    c_int64, C.POINTER(C.c_int32), c_size_t, C.POINTER(c_size_t)]),
     "attn_build_chunk_schedule": (c_int, [c_int, c_int, C.POINTER(C.c_int32), c_size_t, C.POINTER(c_size_t)]),
     "attn_get_status": (c_int, [c_void_p]),
     "attn_set_wait_limit_ns": (None, [c_int64]),

@@ -182,18 +182,19 @@ def attn_bwd(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = 
 
 def build_schedule(mask_kind: int, B: int, Hq: int, Nq: int, Nk: int, q_offset: int = 0,
                    kv_offset: int = 0, host_block_mask: Optional[np.ndarray] = None,
-                   causal_in_blocks: bool = False) -> np.ndarray:
+                   causal_in_blocks: bool = False, Hkv: Optional[int] = None, d: int = 128) -> np.ndarray:
     """Forward work units in launch order, ``[n, 3]`` int32 (bh, query chunk, key tiles)."""
     L = _ffi.lib()
+    hkv = Hq if Hkv is None else Hkv
     n = C.c_size_t(0)
     bm = None
     if host_block_mask is not None:
         bm = np.ascontiguousarray(host_block_mask, dtype=np.uint8)
     bmp = bm.ctypes.data if bm is not None else None
-    L.attn_build_schedule(mask_kind, int(causal_in_blocks), bmp, B, Hq, Nq, Nk, q_offset, kv_offset,
+    L.attn_build_schedule(mask_kind, int(causal_in_blocks), bmp, B, Hq, hkv, Nq, Nk, d, q_offset, kv_offset,
                           None, 0, C.byref(n))
     out = np.zeros(3 * n.value, dtype=np.int32)
-    check(L.attn_build_schedule(mask_kind, int(causal_in_blocks), bmp, B, Hq, Nq, Nk, q_offset, kv_offset,
+    check(L.attn_build_schedule(mask_kind, int(causal_in_blocks), bmp, B, Hq, hkv, Nq, Nk, d, q_offset, kv_offset,
                                 out.ctypes.data_as(C.POINTER(C.c_int32)), out.size, C.byref(n)),
           "attn_build_schedule")
     return out.reshape(-1, 3)

@@ -244,6 +244,7 @@ static int fwd_common(const void* q, const void* k, const void* v, void* o, bool
   p.o_head_stride = Nq;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = Nq; p.Nk = Nk;
   p.nqc = (int)cdiv(Nq, UNIT_ROWS);
+  p.head_group = kv_stream_group(B, Hq, Hkv, Nk, d);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.mask_kind = m.kind;
   p.causal_in_blocks = m.causal_in_blocks;
@@ -355,6 +356,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   p.causal_in_blocks = m.causal_in_blocks;
   p.block_mask = m.block_mask;
   p.nkb = (int)cdiv(N, TILE);
+  p.kv_group = q_stream_group(B, Hq, Hkv, N, d);
+  p.q_group = kv_stream_group(B, Hq, Hkv, N, d);
   p.status = status;
   p.wait_limit_ns = wait_limit();
   {
@@ -370,22 +373,25 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   return ATTN_OK;
 }
 
-int attn_build_schedule(int mask_kind, int causal_in_blocks, const uint8_t* host_block_mask, int B, int Hq, int Nq,
-                        int Nk, int64_t q_offset, int64_t kv_offset, int32_t* out, size_t cap, size_t* n_out) {
+int attn_build_schedule(int mask_kind, int causal_in_blocks, const uint8_t* host_block_mask, int B, int Hq, int Hkv,
+                        int Nq, int Nk, int d, int64_t q_offset, int64_t kv_offset, int32_t* out, size_t cap,
+                        size_t* n_out) {
   if (n_out == nullptr) return fail(ATTN_ERR_INVALID_ARG, "n_out is NULL");
   *n_out = 0;
-  if (B < 1 || Hq < 1 || Nq < 1 || Nk < 1) return fail(ATTN_ERR_INVALID_ARG, "sizes must be positive");
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || d < 1) return fail(ATTN_ERR_INVALID_ARG, "sizes must be positive");
+  if (Hq % Hkv) return fail(ATTN_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
   if (mask_kind < 0 || mask_kind > 2) return fail(ATTN_ERR_INVALID_ARG, "unknown mask kind %d", mask_kind);
   if (mask_kind == ATTN_MASK_BLOCK_SPARSE && host_block_mask == nullptr)
     return fail(ATTN_ERR_INVALID_ARG, "block-sparse schedule needs host_block_mask");
   const int nqc = (int)cdiv(Nq, UNIT_ROWS);
   const int nkb = (int)cdiv(Nk, TILE);
   const int64_t units = (int64_t)B * Hq * nqc;
+  const int group = kv_stream_group(B, Hq, Hkv, Nk, d);
   *n_out = (size_t)units;
   if (out == nullptr || cap < (size_t)units * 3) return fail(ATTN_ERR_INVALID_ARG, "output capacity too small");
   for (int64_t i = 0; i < units; ++i) {
-    const Unit u = fwd_unit(i, B, Hq, 1, Nq, Nk, nqc, mask_kind, causal_in_blocks, host_block_mask, nkb, q_offset,
-                            kv_offset);
+    const Unit u = fwd_unit(i, B, Hq, Hkv, Nq, Nk, nqc, group, mask_kind, causal_in_blocks, host_block_mask, nkb,
+                            q_offset, kv_offset);
     int cnt = 0;
     for (int kt = 0; kt < u.kt_end; ++kt) cnt += unit_uses(u, kt) ? 1 : 0;
     out[3 * i + 0] = u.bh;
@@ -599,6 +605,8 @@ extern "C" int attn_bwd_static_scratch(const void* q, const void* k, const void*
   p.causal_in_blocks = m.causal_in_blocks;
   p.block_mask = m.block_mask;
   p.nkb = (int)cdiv(N, TILE);
+  p.kv_group = q_stream_group(B, Hq, Hkv, N, d);
+  p.q_group = kv_stream_group(B, Hq, Hkv, N, d);
   p.status = st.status;
   p.wait_limit_ns = wait_limit();
   e = launch_bwd_dkdv(d, tq, tk, tv, tdo, p, s);

@@ -25,6 +25,7 @@
 // (warp w owns TMEM lanes 32*(w%4)..+31; one thread per tile row).
 #include "internal.h"
 #include "ptx.cuh"
+#include "schedule.h"
 
 namespace attn {
 
@@ -103,9 +104,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const uint32_t bar_dk = smem_u32(&bars[1 + 2 * NS + 5]);
   const uint32_t bar_done = smem_u32(&bars[1 + 2 * NS + 6]);
 
-  const int BHkv = p.B * p.Hkv;
-  const int kt = (int)(blockIdx.x / BHkv);
-  const int bkv = (int)(blockIdx.x % BHkv);
+  const int nkt_all = (p.N + TILE - 1) / TILE;
+  int kt = 0, bkv = 0;
+  grouped_unit(blockIdx.x, p.B * p.Hkv, nkt_all, p.kv_group, &bkv, &kt);  // key tiles ascending: heaviest first
   const int b = bkv / p.Hkv, hkv = bkv % p.Hkv;
   const int g = p.Hq / p.Hkv;
   const int nqt = (p.N + TILE - 1) / TILE;
@@ -144,37 +145,41 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const uint32_t tmem = tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------------------------------------------------------- producer
-      mbar_arrive_expect_tx(bar_kv, 2 * C::TILE_BYTES);
-      for (int bx = 0; bx < C::NBOX; ++bx) {
-        tma_load_3d(s_base + bx * C::BOX_BYTES, &tk, bx * 64, kt * TILE, bkv, bar_kv);
-        tma_load_3d(s_base + OFF_V + bx * C::BOX_BYTES, &tv, bx * 64, kt * TILE, bkv, bar_kv);
-      }
-      int n = 0;
-      bool ok = true;
-      for (int h = 0; h < g && ok; ++h) {
-        const int bh = b * p.Hq + hkv * g + h;
-        for (int qt = qt_first; qt < nqt && ok; ++qt) {
-          if (!tile_pair_visible(p, qt, kt)) continue;
-          const int s = n % NS;
-          if (n >= NS && !(ok = wait_bar(bar_qfree(s), ((n / NS) - 1) & 1, wc))) break;
-          const uint32_t st = s_base + OFF_RING + s * STAGE;
-          mbar_arrive_expect_tx(bar_q(s), 2 * C::TILE_BYTES + 1024);
-          for (int bx = 0; bx < C::NBOX; ++bx) {
-            tma_load_3d(st + bx * C::BOX_BYTES, &tq, bx * 64, qt * TILE, bh, bar_q(s));
-            tma_load_3d(st + C::TILE_BYTES + bx * C::BOX_BYTES, &tdo, bx * 64, qt * TILE, bh, bar_q(s));
-          }
-          const size_t roff = (size_t)bh * p.Np + (size_t)qt * TILE;
+    // ---------------------------------------------------------- producer
+    // one lane per TMA copy (copies issued by one thread are serialised)
+    if (lane == 0) mbar_arrive_expect_tx(bar_kv, 2 * C::TILE_BYTES);
+    __syncwarp();
+    if (lane < C::NBOX) tma_load_3d(s_base + lane * C::BOX_BYTES, &tk, lane * 64, kt * TILE, bkv, bar_kv);
+    else if (lane < 2 * C::NBOX)
+      tma_load_3d(s_base + OFF_V + (lane - C::NBOX) * C::BOX_BYTES, &tv, (lane - C::NBOX) * 64, kt * TILE, bkv, bar_kv);
+    int n = 0;
+    bool ok = true;
+    for (int h = 0; h < g && ok; ++h) {
+      const int bh = b * p.Hq + hkv * g + h;
+      for (int qt = qt_first; qt < nqt && ok; ++qt) {
+        if (!tile_pair_visible(p, qt, kt)) continue;
+        const int s = n % NS;
+        if (n >= NS) ok = wait_bar(bar_qfree(s), ((n / NS) - 1) & 1, wc);
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
+        const uint32_t st = s_base + OFF_RING + s * STAGE;
+        if (lane == 0) mbar_arrive_expect_tx(bar_q(s), 2 * C::TILE_BYTES + 1024);
+        __syncwarp();
+        const size_t roff = (size_t)bh * p.Np + (size_t)qt * TILE;
+        if (lane < C::NBOX)
+          tma_load_3d(st + lane * C::BOX_BYTES, &tq, lane * 64, qt * TILE, bh, bar_q(s));
+        else if (lane < 2 * C::NBOX)
+          tma_load_3d(st + C::TILE_BYTES + (lane - C::NBOX) * C::BOX_BYTES, &tdo, (lane - C::NBOX) * 64, qt * TILE, bh,
+                      bar_q(s));
+        else if (lane == 2 * C::NBOX)
           bulk_load(st + 2 * C::TILE_BYTES, p.lse2 + roff, 512, bar_q(s));
+        else if (lane == 2 * C::NBOX + 1)
           bulk_load(st + 2 * C::TILE_BYTES + 512, p.dsum + roff, 512, bar_q(s));
-          ++n;
-        }
+        ++n;
       }
-      if (!ok || abort_flag) {
-        wait_bar(bar_kv, 0, wc, false);
-        for (int j = n - NS < 0 ? 0 : n - NS; j < n; ++j) wait_bar(bar_q(j % NS), (j / NS) & 1, wc, false);
-      }
+    }
+    if ((!ok || abort_flag) && lane == 0) {
+      wait_bar(bar_kv, 0, wc, false);
+      for (int j = n - NS < 0 ? 0 : n - NS; j < n; ++j) wait_bar(bar_q(j % NS), (j / NS) & 1, wc, false);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -248,45 +253,56 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         const bool diag = causal && qt == kt;       // key r sees query column j iff r <= j
-        float pr[128];
+        const float4* l4 = reinterpret_cast<const float4*>(lse2);
+        const float4* d4 = reinterpret_cast<const float4*>(dsum);
+        // phase A: P^T = 2^(S^T c - lse2) -> bf16 pairs into the first 64 S^T columns
+        uint32_t pk[64];
+        {
+          uint32_t sr[128];
+          tmem_ld128(tmem + lane_off, sr);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t sr[32];
-          tmem_ld32(tmem + lane_off + q4 * 32, sr);
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const int col = q4 * 32 + j;
-            float p0 = ex2(fmaf(__uint_as_float(sr[j]), c, -lse2[col]));
-            float p1 = ex2(fmaf(__uint_as_float(sr[j + 1]), c, -lse2[col + 1]));
+          for (int j4 = 0; j4 < 32; ++j4) {
+            const float4 L = l4[j4];
+            const int col = 4 * j4;
+            float p0 = ex2(fmaf(__uint_as_float(sr[col + 0]), c, -L.x));
+            float p1 = ex2(fmaf(__uint_as_float(sr[col + 1]), c, -L.y));
+            float p2 = ex2(fmaf(__uint_as_float(sr[col + 2]), c, -L.z));
+            float p3 = ex2(fmaf(__uint_as_float(sr[col + 3]), c, -L.w));
             if (diag) {
-              p0 = (r <= col) ? p0 : 0.f;
+              p0 = (r <= col + 0) ? p0 : 0.f;
               p1 = (r <= col + 1) ? p1 : 0.f;
+              p2 = (r <= col + 2) ? p2 : 0.f;
+              p3 = (r <= col + 3) ? p3 : 0.f;
             }
-            pr[col] = p0;
-            pr[col + 1] = p1;
-            pk[j >> 1] = pack_bf16(p0, p1);
+            pk[2 * j4] = pack_bf16(p0, p1);
+            pk[2 * j4 + 1] = pack_bf16(p2, p3);
           }
-          tmem_st16(tmem + lane_off + q4 * 16, pk);
         }
+        tmem_st64(tmem + lane_off, pk);
         tc_fence_before();
         mbar_arrive(bar_p);
         ok = wait_bar(bar_dp, i & 1, wc);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
+        // phase B: dS^T = P^T * (dP^T - D), in two 64-column halves; the bf16
+        // pairs go over the dP^T columns already read
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t dr[32];
-          tmem_ld32(tmem + lane_off + 128 + q4 * 32, dr);
-          uint32_t pk[16];
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t dr[64];
+          tmem_ld64(tmem + lane_off + 128 + hh * 64, dr);
+          uint32_t ds[32];
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const int col = q4 * 32 + j;
-            const float d0 = pr[col] * (__uint_as_float(dr[j]) - dsum[col]);
-            const float d1 = pr[col + 1] * (__uint_as_float(dr[j + 1]) - dsum[col + 1]);
-            pk[j >> 1] = pack_bf16(d0, d1);
+          for (int j4 = 0; j4 < 16; ++j4) {
+            const float4 Dv = d4[hh * 16 + j4];
+            const uint32_t pa = pk[hh * 32 + 2 * j4], pb = pk[hh * 32 + 2 * j4 + 1];
+            const float d0 = __uint_as_float(pa << 16) * (__uint_as_float(dr[4 * j4 + 0]) - Dv.x);
+            const float d1 = __uint_as_float(pa & 0xffff0000u) * (__uint_as_float(dr[4 * j4 + 1]) - Dv.y);
+            const float d2 = __uint_as_float(pb << 16) * (__uint_as_float(dr[4 * j4 + 2]) - Dv.z);
+            const float d3 = __uint_as_float(pb & 0xffff0000u) * (__uint_as_float(dr[4 * j4 + 3]) - Dv.w);
+            ds[2 * j4] = pack_bf16(d0, d1);
+            ds[2 * j4 + 1] = pack_bf16(d2, d3);
           }
-          tmem_st16(tmem + lane_off + 128 + q4 * 16, pk);
+          tmem_st32(tmem + lane_off + 128 + hh * 32, ds);
         }
         tc_fence_before();
         mbar_arrive(bar_ds);
@@ -370,10 +386,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const uint32_t bar_dq = smem_u32(&bars[1 + 3 * NS + 4]);
   const uint32_t bar_done = smem_u32(&bars[1 + 3 * NS + 5]);
 
-  const int BH = p.B * p.Hq;
   const int nqt = (p.N + TILE - 1) / TILE;
-  const int qt = nqt - 1 - (int)(blockIdx.x / BH);
-  const int bh = (int)(blockIdx.x % BH);
+  int bh = 0, qpos = 0;
+  grouped_unit(blockIdx.x, p.B * p.Hq, nqt, p.q_group, &bh, &qpos);
+  const int qt = nqt - 1 - qpos;  // latest query tile first: heaviest under a causal mask
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int bkv = b * p.Hkv + h / (p.Hq / p.Hkv);
   const int nkt = (p.N + TILE - 1) / TILE;
@@ -412,34 +428,39 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const uint32_t tmem = tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------------------------------------------------------- producer
-      mbar_arrive_expect_tx(bar_qdo, 2 * C::TILE_BYTES);
-      for (int bx = 0; bx < C::NBOX; ++bx) {
-        tma_load_3d(s_base + bx * C::BOX_BYTES, &tq, bx * 64, qt * TILE, bh, bar_qdo);
-        tma_load_3d(s_base + OFF_DO + bx * C::BOX_BYTES, &tdo, bx * 64, qt * TILE, bh, bar_qdo);
-      }
-      int n = 0;
-      bool ok = true;
-      for (int kt = 0; kt < kt_end && ok; ++kt) {
-        if (!tile_pair_visible(p, qt, kt)) continue;
-        const int s = n % NS;
-        if (n >= NS && !(ok = wait_bar(bar_free(s), ((n / NS) - 1) & 1, wc))) break;
-        const uint32_t st = s_base + OFF_RING + s * STAGE;
+    // ---------------------------------------------------------- producer
+    // one lane per TMA copy (copies issued by one thread are serialised)
+    if (lane == 0) mbar_arrive_expect_tx(bar_qdo, 2 * C::TILE_BYTES);
+    __syncwarp();
+    if (lane < C::NBOX) tma_load_3d(s_base + lane * C::BOX_BYTES, &tq, lane * 64, qt * TILE, bh, bar_qdo);
+    else if (lane < 2 * C::NBOX)
+      tma_load_3d(s_base + OFF_DO + (lane - C::NBOX) * C::BOX_BYTES, &tdo, (lane - C::NBOX) * 64, qt * TILE, bh,
+                  bar_qdo);
+    int n = 0;
+    bool ok = true;
+    for (int kt = 0; kt < kt_end && ok; ++kt) {
+      if (!tile_pair_visible(p, qt, kt)) continue;
+      const int s = n % NS;
+      if (n >= NS) ok = wait_bar(bar_free(s), ((n / NS) - 1) & 1, wc);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      const uint32_t st = s_base + OFF_RING + s * STAGE;
+      if (lane == 0) {
         mbar_arrive_expect_tx(bar_k(s), C::TILE_BYTES);
-        for (int bx = 0; bx < C::NBOX; ++bx)
-          tma_load_3d(st + bx * C::BOX_BYTES, &tk, bx * 64, kt * TILE, bkv, bar_k(s));
         mbar_arrive_expect_tx(bar_v(s), C::TILE_BYTES);
-        for (int bx = 0; bx < C::NBOX; ++bx)
-          tma_load_3d(st + C::TILE_BYTES + bx * C::BOX_BYTES, &tv, bx * 64, kt * TILE, bkv, bar_v(s));
-        ++n;
       }
-      if (!ok || abort_flag) {
-        wait_bar(bar_qdo, 0, wc, false);
-        for (int j = n - NS < 0 ? 0 : n - NS; j < n; ++j) {
-          wait_bar(bar_k(j % NS), (j / NS) & 1, wc, false);
-          wait_bar(bar_v(j % NS), (j / NS) & 1, wc, false);
-        }
+      __syncwarp();
+      if (lane < C::NBOX)
+        tma_load_3d(st + lane * C::BOX_BYTES, &tk, lane * 64, kt * TILE, bkv, bar_k(s));
+      else if (lane < 2 * C::NBOX)
+        tma_load_3d(st + C::TILE_BYTES + (lane - C::NBOX) * C::BOX_BYTES, &tv, (lane - C::NBOX) * 64, kt * TILE, bkv,
+                    bar_v(s));
+      ++n;
+    }
+    if ((!ok || abort_flag) && lane == 0) {
+      wait_bar(bar_qdo, 0, wc, false);
+      for (int j = n - NS < 0 ? 0 : n - NS; j < n; ++j) {
+        wait_bar(bar_k(j % NS), (j / NS) & 1, wc, false);
+        wait_bar(bar_v(j % NS), (j / NS) & 1, wc, false);
       }
     }
   } else if (warp == 1) {
@@ -542,14 +563,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       int lim = p.N - kt * TILE;
       if (causal && kt == qt) lim = min(lim, r + 1);
       float pr[128];
+      {
+        uint32_t sr[128];
+        tmem_ld128(tmem + lane_off + T_S, sr);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t sr[32];
-        tmem_ld32(tmem + lane_off + T_S + q4 * 32, sr);
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int col = q4 * 32 + jj;
-          const float pv = ex2(fmaf(__uint_as_float(sr[jj]), c, -l2));
+        for (int col = 0; col < 128; ++col) {
+          const float pv = ex2(fmaf(__uint_as_float(sr[col]), c, -l2));
           pr[col] = (col < lim) ? pv : 0.f;
         }
       }
@@ -559,17 +578,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t dpr[32];
-        tmem_ld32(tmem + lane_off + T_DP + q4 * 32, dpr);
-        uint32_t pk[16];
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t dpr[64];
+        tmem_ld64(tmem + lane_off + T_DP + hh * 64, dpr);
+        uint32_t pk[32];
 #pragma unroll
-        for (int jj = 0; jj < 32; jj += 2) {
-          const int col = q4 * 32 + jj;
-          pk[jj >> 1] = pack_bf16(pr[col] * (__uint_as_float(dpr[jj]) - dr),
-                                  pr[col + 1] * (__uint_as_float(dpr[jj + 1]) - dr));
+        for (int jj = 0; jj < 32; ++jj) {
+          const int col = hh * 64 + 2 * jj;
+          pk[jj] = pack_bf16(pr[col] * (__uint_as_float(dpr[2 * jj]) - dr),
+                             pr[col + 1] * (__uint_as_float(dpr[2 * jj + 1]) - dr));
         }
-        tmem_st16(tmem + lane_off + T_DS + q4 * 16, pk);
+        tmem_st32(tmem + lane_off + T_DS + hh * 32, pk);
       }
       tc_fence_before();
       mbar_arrive(bar_ds);

@@ -13,7 +13,8 @@
 // One CTA = one work unit = 256 query rows (two 128-row tiles, t = 0, 1) of
 // one (batch, query head); launched heaviest-first (see schedule.h).
 // Warp roles (12 warps, three warpgroups):
-//   warp 0      TMA producer: Q0/Q1 once, then K_j and V_j into an NS-deep ring
+//   warp 0      TMA producer: Q0/Q1 once, then K_j and V_j into NS-deep rings;
+//               one lane per 16 KB box, K slots released after the S MMAs
 //   warp 1      MMA issuer (one thread): S_t = Q_t K_j^T, then O_t += P_t V_j
 //               with P_t read from tensor memory; owns the TMEM allocation
 //   warps 2-3   idle (they complete the control warpgroup)
@@ -67,7 +68,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bars[1 + 3 * NS + 7];
+  __shared__ __align__(8) uint64_t bars[1 + 4 * NS + 7];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -76,13 +77,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   const uint32_t bar_q = smem_u32(&bars[0]);
   auto bar_k = [&](int s) { return smem_u32(&bars[1 + s]); };
   auto bar_v = [&](int s) { return smem_u32(&bars[1 + NS + s]); };
-  auto bar_free = [&](int s) { return smem_u32(&bars[1 + 2 * NS + s]); };
-  auto bar_s = [&](int t) { return smem_u32(&bars[1 + 3 * NS + t]); };
-  auto bar_p = [&](int t) { return smem_u32(&bars[1 + 3 * NS + 2 + t]); };
-  auto bar_o = [&](int t) { return smem_u32(&bars[1 + 3 * NS + 4 + t]); };
-  const uint32_t bar_done = smem_u32(&bars[1 + 3 * NS + 6]);
+  auto bar_kfree = [&](int s) { return smem_u32(&bars[1 + 2 * NS + s]); };  // K slot read by both S MMAs
+  auto bar_vfree = [&](int s) { return smem_u32(&bars[1 + 3 * NS + s]); };  // V slot read by both PV MMAs
+  auto bar_s = [&](int t) { return smem_u32(&bars[1 + 4 * NS + t]); };
+  auto bar_p = [&](int t) { return smem_u32(&bars[1 + 4 * NS + 2 + t]); };
+  auto bar_o = [&](int t) { return smem_u32(&bars[1 + 4 * NS + 4 + t]); };
+  const uint32_t bar_done = smem_u32(&bars[1 + 4 * NS + 6]);
 
-  const Unit u = fwd_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.Nq, p.Nk, p.nqc, p.mask_kind, p.causal_in_blocks,
+  const Unit u = fwd_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.Nq, p.Nk, p.nqc, p.head_group, p.mask_kind, p.causal_in_blocks,
                           p.block_mask, p.nkb, p.q_offset, p.kv_offset);
   WaitCtx wc{p.wait_limit_ns, p.status, &abort_flag};
 
@@ -92,7 +94,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar_k(s), 1);
       mbar_init(bar_v(s), 1);
-      mbar_init(bar_free(s), 1);
+      mbar_init(bar_kfree(s), 1);
+      mbar_init(bar_vfree(s), 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_s(t), 1);
@@ -120,36 +123,43 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
    reg_dealloc<C::REGS_CTRL>();
    if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar_q, 2 * C::TILE_BYTES);
-      for (int t = 0; t < 2; ++t)
-        for (int bx = 0; bx < C::NBOX; ++bx)
-          tma_load_3d(s_base + t * C::TILE_BYTES + bx * C::BOX_BYTES, &tq, bx * 64, u.row0 + t * TILE,
-                      u.bh, bar_q);
-      int n = 0;
-      bool ok = true;
-      for (int kt = 0; kt < u.kt_end && ok; ++kt) {
-        if (!unit_uses(u, kt)) continue;
-        const int s = n % NS;
-        if (n >= NS) ok = wait_bar(bar_free(s), ((n / NS) - 1) & 1, wc);
-        if (!ok) break;
-        mbar_arrive_expect_tx(bar_k(s), C::TILE_BYTES);
-        for (int bx = 0; bx < C::NBOX; ++bx)
-          tma_load_3d(s_base + C::OFF_K + s * C::TILE_BYTES + bx * C::BOX_BYTES, &tk, bx * 64, kt * TILE,
-                      u.kvh, bar_k(s));
-        mbar_arrive_expect_tx(bar_v(s), C::TILE_BYTES);
-        for (int bx = 0; bx < C::NBOX; ++bx)
-          tma_load_3d(s_base + C::OFF_V + s * C::TILE_BYTES + bx * C::BOX_BYTES, &tv, bx * 64, kt * TILE,
-                      u.kvh, bar_v(s));
-        ++n;
-      }
-      if (!ok || abort_flag) {
-        // drain: every issued copy must land before the CTA's shared memory is released
-        wait_bar(bar_q, 0, wc, false);
-        for (int j = n - NS < 0 ? 0 : n - NS; j < n; ++j) {
-          wait_bar(bar_k(j % NS), (j / NS) & 1, wc, false);
-          wait_bar(bar_v(j % NS), (j / NS) & 1, wc, false);
-        }
+    // Each box of a tile is issued by its own lane: TMA copies issued by one
+    // thread are processed one after another, so spreading them over lanes is
+    // what lets several 16 KB boxes stream into the SM at the same time.
+    if (lane == 0) mbar_arrive_expect_tx(bar_q, 2 * C::TILE_BYTES);
+    __syncwarp();
+    if (lane < 2 * C::NBOX) {
+      const int t = lane / C::NBOX, bx = lane % C::NBOX;
+      tma_load_3d(s_base + t * C::TILE_BYTES + bx * C::BOX_BYTES, &tq, bx * 64, u.row0 + t * TILE, u.bh, bar_q);
+    }
+    int n = 0;
+    bool ok = true;
+    for (int kt = 0; kt < u.kt_end && ok; ++kt) {
+      if (!unit_uses(u, kt)) continue;
+      const int s = n % NS;
+      const uint32_t fph = ((n / NS) - 1) & 1;
+      if (n >= NS) ok = wait_bar(bar_kfree(s), fph, wc);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      if (lane == 0) mbar_arrive_expect_tx(bar_k(s), C::TILE_BYTES);
+      __syncwarp();
+      if (lane < C::NBOX)
+        tma_load_3d(s_base + C::OFF_K + s * C::TILE_BYTES + lane * C::BOX_BYTES, &tk, lane * 64, kt * TILE, u.kvh,
+                    bar_k(s));
+      if (n >= NS) ok = wait_bar(bar_vfree(s), fph, wc);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      if (lane == 0) mbar_arrive_expect_tx(bar_v(s), C::TILE_BYTES);
+      __syncwarp();
+      if (lane >= C::NBOX && lane < 2 * C::NBOX)
+        tma_load_3d(s_base + C::OFF_V + s * C::TILE_BYTES + (lane - C::NBOX) * C::BOX_BYTES, &tv,
+                    (lane - C::NBOX) * 64, kt * TILE, u.kvh, bar_v(s));
+      ++n;
+    }
+    if ((!ok || abort_flag) && lane == 0) {
+      // drain: every issued copy must land before the CTA's shared memory is released
+      wait_bar(bar_q, 0, wc, false);
+      for (int j = n - NS < 0 ? 0 : n - NS; j < n; ++j) {
+        wait_bar(bar_k(j % NS), (j / NS) & 1, wc, false);
+        wait_bar(bar_v(j % NS), (j / NS) & 1, wc, false);
       }
     }
    } else if (warp == 1) {
@@ -181,7 +191,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           }
           mma_commit(bar_s(t));
         }
-        if (!ok || !(ok = wait_bar(bar_v(s), ph, wc))) break;
+        if (!ok) break;
+        mma_commit(bar_kfree(s));   // K slot free once both S MMAs have read it
+        if (!(ok = wait_bar(bar_v(s), ph, wc))) break;
         const uint32_t vb = s_base + C::OFF_V + s * C::TILE_BYTES;
         for (int t = 0; t < 2 && ok; ++t) {
           if (!(use & (1u << t))) continue;
@@ -194,7 +206,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           mma_commit(bar_o(t));
           ++it[t];
         }
-        mma_commit(bar_free(s));
+        mma_commit(bar_vfree(s));
         ++n;
       }
       // every commit above lands before the CTA leaves
@@ -223,91 +235,101 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       ok = wait_bar(bar_s(t), it & 1, wc);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      float s[128];
-      {
-        uint32_t rr[32];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          tmem_ld32(tS + q4 * 32, rr);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) s[q4 * 32 + j] = __uint_as_float(rr[j]);
-        }
-      }
       // element mask on the ragged last key tile and on causal diagonal tiles
       const int64_t key0 = p.kv_offset + (int64_t)kt * TILE;
       const bool tail = (kt == u.nkt - 1) && (p.Nk % TILE) != 0;
       const bool diag = causal && (key0 + TILE - 1 > row_first_pos);
+      int lim = 128;
       if (tail || diag) {
-        int64_t lim = p.Nk - (int64_t)kt * TILE;
+        int64_t l64 = p.Nk - (int64_t)kt * TILE;
         if (causal) {
           const int64_t lc = p.q_offset + qrow - key0 + 1;
-          lim = lc < lim ? lc : lim;
+          l64 = lc < l64 ? lc : l64;
         }
-#pragma unroll
-        for (int j = 0; j < 128; ++j) s[j] = (j < lim) ? s[j] : -INFINITY;
+        lim = (int)(l64 < 0 ? 0 : (l64 > 128 ? 128 : l64));
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      auto load_scores = [&](float (&sc)[128]) {
+        uint32_t rr[128];
+        tmem_ld128(tS, rr);   // the whole score row in one round trip
 #pragma unroll
-      for (int j = 4; j < 128; j += 4) {
-        mx0 = fmaxf(mx0, s[j]);
-        mx1 = fmaxf(mx1, s[j + 1]);
-        mx2 = fmaxf(mx2, s[j + 2]);
-        mx3 = fmaxf(mx3, s[j + 3]);
+        for (int j = 0; j < 128; ++j) sc[j] = __uint_as_float(rr[j]);
+        if (tail || diag) {
+#pragma unroll
+          for (int j = 0; j < 128; ++j) sc[j] = (j < lim) ? sc[j] : -INFINITY;
+        }
+      };
+      // p = 2^(s*c - mb), two lanes per packed FMA; in place
+      auto exponentials = [&](float (&sc)[128], float mb) {
+#pragma unroll
+        for (int j = 0; j < 128; j += 2) {
+          float x0, x1;
+          fma2(x0, x1, sc[j], sc[j + 1], c, c, -mb, -mb);
+          sc[j] = ex2(x0);
+          sc[j + 1] = ex2(x1);
+        }
+      };
+      float s[128];
+      load_scores(s);
+      // Row max of the tile alongside exponentials taken against the current
+      // reference max: the usual case (max moved by at most the threshold)
+      // needs no second pass and the max is off the critical path.
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 128; j += 4) {
+        mx0 = max3(mx0, s[j], s[j + 1]);
+        mx1 = max3(mx1, s[j + 2], s[j + 3]);
       }
-      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
-      const float m_new = fmaxf(m, mt);
-      // Move the reference max only at the first tile or when it grows by more
-      // than the threshold; O_t is then rescaled below, after P is written
-      // (the score registers are free by then).
+      exponentials(s, (m == -INFINITY) ? 0.f : m);
+      const float m_new = fmaxf(m, fmaxf(mx0, mx1) * c);
       float alpha = 1.f;
       bool rescale = false;
-      if (it == 0) {
-        m = m_new;
-      } else if (__any_sync(0xffffffffu, m_new > m + RESCALE_THRESHOLD)) {
-        alpha = (m_new == -INFINITY) ? 1.f : ex2(m - m_new);
-        m = m_new;
-        rescale = true;
-      }
-      const float mb = (m == -INFINITY) ? 0.f : m;
-      float l0 = 0.f, l1 = 0.f, r0 = 0.f, r1 = 0.f;
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float p0 = ex2(fmaf(s[q4 * 32 + 2 * j], c, -mb));
-          const float p1 = ex2(fmaf(s[q4 * 32 + 2 * j + 1], c, -mb));
-          const uint32_t w = pack_bf16(p0, p1);
-          // lr sums the bf16-rounded weights that P.V sees (O is normalised by
-          // it, so the rounding of a dominant weight cancels in O / lr); l sums
-          // the fp32 weights and gives the log-sum-exp.
-          l0 += p0;
-          l1 += p1;
-          r0 += __uint_as_float(w << 16);
-          r1 += __uint_as_float(w & 0xffff0000u);
-          pk[j] = w;
+      if (__any_sync(0xffffffffu, it == 0 || m_new > m + RESCALE_THRESHOLD)) {
+        // the reference max moves: O_t (if any) is rescaled by 2^(m_old - m_new)
+        // below, and the exponentials are redone from the scores still in TMEM
+        if (it > 0) {
+          alpha = (m_new == -INFINITY) ? 1.f : ex2(m - m_new);
+          rescale = true;
         }
-        tmem_st16(tS + q4 * 16, pk);
+        m = m_new;
+        load_scores(s);
+        exponentials(s, (m == -INFINITY) ? 0.f : m);
       }
-      l = l * alpha + (l0 + l1);
-      lr = lr * alpha + (r0 + r1);
+      // l sums the fp32 weights (for the log-sum-exp); lr, below, sums the
+      // bf16-rounded weights P.V sees, so O / lr cancels the rounding of a
+      // dominant weight
+      uint32_t pk[64];
+      float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        pk[j] = pack_bf16(s[2 * j], s[2 * j + 1]);
+        add2(l0, l1, l0, l1, s[2 * j], s[2 * j + 1]);
+      }
+      tmem_st64(tS, pk);    // P_t (bf16 pairs) over the first 64 columns of S_t
       if (rescale) {
         // PV_t of the previous key tile must have landed in O_t first
         ok = wait_bar(bar_o(t), (it - 1) & 1, wc);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int q4 = 0; q4 < D / 32; ++q4) {
-          uint32_t rr[32];
-          tmem_ld32(tO + q4 * 32, rr);
+        for (int h64 = 0; h64 < D / 64; ++h64) {
+          uint32_t rr[64];
+          tmem_ld64(tO + h64 * 64, rr);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
-          tmem_st32(tO + q4 * 32, rr);
+          for (int j = 0; j < 64; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
+          tmem_st64(tO + h64 * 64, rr);
         }
       }
       tc_fence_before();
       mbar_arrive(bar_p(t));
       ++it;
+      // rounded-weight sum after P has been handed to the tensor core
+      float r0 = 0.f, r1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 64; ++j)
+        add2(r0, r1, r0, r1, __uint_as_float(pk[j] << 16), __uint_as_float(pk[j] & 0xffff0000u));
+      l = l * alpha + (l0 + l1);
+      lr = lr * alpha + (r0 + r1);
+
     }
     // ---------------------------------------------------------- epilogue
     if (ok && !abort_flag) {
@@ -322,26 +344,26 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const float inv_l = (lr > 0.f) ? 1.f / lr : 0.f;
         const size_t orow = (size_t)u.bh * (size_t)p.o_head_stride + (size_t)qrow;
 #pragma unroll
-        for (int q4 = 0; q4 < D / 32; ++q4) {
-          uint32_t rr[32];
+        for (int h64 = 0; h64 < D / 64; ++h64) {
+          uint32_t rr[64];
           if (have) {
-            tmem_ld32(tO + q4 * 32, rr);
+            tmem_ld64(tO + h64 * 64, rr);
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) rr[j] = 0u;
+            for (int j = 0; j < 64; ++j) rr[j] = 0u;
           }
           if (valid_row) {
             if constexpr (OUT_F32) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + q4 * 32);
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + h64 * 64);
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
+              for (int j = 0; j < 16; ++j)
                 dst[j] = make_float4(__uint_as_float(rr[4 * j]) * inv_l, __uint_as_float(rr[4 * j + 1]) * inv_l,
                                      __uint_as_float(rr[4 * j + 2]) * inv_l,
                                      __uint_as_float(rr[4 * j + 3]) * inv_l);
             } else {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + q4 * 32);
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + h64 * 64);
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
+              for (int j = 0; j < 8; ++j) {
                 uint4 v4;
                 v4.x = pack_bf16(__uint_as_float(rr[8 * j + 0]) * inv_l, __uint_as_float(rr[8 * j + 1]) * inv_l);
                 v4.y = pack_bf16(__uint_as_float(rr[8 * j + 2]) * inv_l, __uint_as_float(rr[8 * j + 3]) * inv_l);

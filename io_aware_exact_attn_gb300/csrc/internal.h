@@ -20,6 +20,7 @@ struct FwdParams {
   int64_t o_head_stride;    // rows between consecutive (b, h) heads of o / lse
   int B, Hq, Hkv, Nq, Nk;
   int nqc;                  // number of 256-row query chunks
+  int head_group;           // heads per L2 group (schedule.h)
   float scale_log2;         // scale * log2(e)
   int mask_kind;
   int causal_in_blocks;
@@ -45,6 +46,8 @@ struct BwdParams {
   int causal_in_blocks;
   const uint8_t* block_mask;
   int nkb;
+  int kv_group;             // kv heads per L2 group of the dK/dV kernel
+  int q_group;              // query heads per L2 group of the dQ kernel
   unsigned int* status;
   int64_t wait_limit_ns;
 };

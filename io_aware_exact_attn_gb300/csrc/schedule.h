@@ -3,13 +3,14 @@
 // follow.
 //
 // A forward work unit is 256 query rows (two 128-row tiles) of one
-// (batch, query head).  Units are taken heaviest first: unit i covers query
-// chunk nqc-1 - i/(B*Hq) of head i%(B*Hq).  Under a causal mask later chunks
-// see more key tiles, so this is a longest-processing-time-first list that the
-// hardware block scheduler hands greedily to free SMs ("DISTFLASHATTN"
-// reviews, first review point 1: with causal masking, careless placement of
-// the chunks leaves processors idle; "FlashAttention-2" reviews, fourth
-// review: fully masked blocks are skipped).
+// (batch, query head).  Within each head-group (see grouped_unit) units are
+// taken heaviest first: the latest query chunk of every head of the group,
+// then the next latest, and so on.  Under a causal mask later chunks see more
+// key tiles, so this is a longest-processing-time-first list that the hardware
+// block scheduler hands greedily to free SMs ("DISTFLASHATTN" reviews, first
+// review point 1: with causal masking, careless placement of the chunks leaves
+// processors idle; "FlashAttention-2" reviews, fourth review: fully masked
+// blocks are skipped).
 #pragma once
 
 #include <stdint.h>
@@ -46,14 +47,58 @@ ATTN_HD bool mask_is_causal(int kind, int causal_in_blocks) {
   return kind == MASK_CAUSAL || (kind == MASK_BLOCK_SPARSE && causal_in_blocks);
 }
 
+// Work units are taken head-group by head-group so that the operand a group
+// streams (K/V for the forward and dQ kernels, Q/dO for dK/dV) stays resident
+// in L2 while every unit of the group re-reads it: groups hold as many heads as
+// fit in L2_GROUP_BYTES of streamed bf16 operands.
+constexpr int64_t L2_GROUP_BYTES = 64ll << 20;
+
+ATTN_HD int clamp_group(int64_t g, int heads) {
+  return (int)(g < 1 ? 1 : (g > heads ? heads : g));
+}
+
+// Query heads per group for kernels that stream one kv head's K and V
+// (forward, dQ): the g query heads of a GQA group share them.
+ATTN_HD int kv_stream_group(int B, int Hq, int Hkv, int Nk, int d) {
+  const int64_t kv_bytes = 4ll * Nk * d;  // K + V of one kv head, bf16
+  return clamp_group((int64_t)(Hq / Hkv) * (L2_GROUP_BYTES / kv_bytes), B * Hq);
+}
+
+// Kv heads per group for the dK/dV kernel, which streams Q and dO of the g
+// query heads of each kv head.
+ATTN_HD int q_stream_group(int B, int Hq, int Hkv, int Nq, int d) {
+  const int64_t q_bytes = 4ll * Nq * d * (Hq / Hkv);
+  return clamp_group(L2_GROUP_BYTES / q_bytes, B * Hkv);
+}
+
+// Unit i of `heads` x `per_head` units in grouped order: head-groups of
+// `group` heads (the last may be smaller), inside a group position-major with
+// the heads inner.  Returns the head and the position (0 = first taken).
+ATTN_HD void grouped_unit(int64_t i, int heads, int per_head, int group, int* head, int* pos) {
+  const int64_t full = heads / group;
+  const int64_t per_full = (int64_t)group * per_head;
+  int64_t grp, j, gs;
+  if (i < full * per_full) {
+    grp = i / per_full;
+    j = i % per_full;
+    gs = group;
+  } else {
+    grp = full;
+    j = i - full * per_full;
+    gs = heads - full * group;
+  }
+  *pos = (int)(j / gs);
+  *head = (int)(grp * group + j % gs);
+}
+
 // `block_mask` may be a host or a device pointer, matching the caller.
-ATTN_HD Unit fwd_unit(int64_t i, int B, int Hq, int Hkv, int Nq, int Nk, int nqc, int mask_kind,
+ATTN_HD Unit fwd_unit(int64_t i, int B, int Hq, int Hkv, int Nq, int Nk, int nqc, int head_group, int mask_kind,
                       int causal_in_blocks, const uint8_t* block_mask, int nkb, int64_t q_off,
                       int64_t kv_off) {
   Unit u;
-  const int64_t BH = (int64_t)B * Hq;
-  const int qc = nqc - 1 - (int)(i / BH);
-  u.bh = (int)(i % BH);
+  int pos = 0;
+  grouped_unit(i, B * Hq, nqc, head_group, &u.bh, &pos);
+  const int qc = nqc - 1 - pos;   // heaviest (latest) query chunk first
   const int b = u.bh / Hq, h = u.bh % Hq;
   u.kvh = b * Hkv + h / (Hq / Hkv);
   u.row0 = qc * UNIT_ROWS;

@@ -9,9 +9,12 @@ reviews, first review points 1-2 and third review summary; FlashAttention-2
 reviews, fourth review on causal block skipping; none prints the schedule):
 
 * Forward work unit = one CTA = 256 query rows (two 128-row tiles) of one
-  (batch, query head).  Units are launched heaviest first: unit ``i`` takes
-  query chunk ``nqc - 1 - i // (B*Hq)`` of head ``i % (B*Hq)``.  Under a
-  causal mask the later query chunks see more key tiles, so this is the
+  (batch, query head).  Heads are taken in groups of
+  ``G = clamp((Hq/Hkv) * floor(64 MiB / (4*Nk*d)), 1, B*Hq)`` consecutive heads
+  (the last group may be smaller), so that a group's K and V fit in L2.  Inside
+  a group units go heaviest first: the latest query chunk of each head of the
+  group (heads in order), then the next latest, and so on.  Under a causal
+  mask later query chunks see more key tiles, so this is a
   longest-processing-time-first order that the hardware block scheduler then
   assigns greedily to free SMs.
 * A unit's key tiles are the union of the key tiles its two query tiles see.
@@ -66,16 +69,31 @@ def _tile_kv_set(t_row: int, nq: int, nk: int, kind: str, q_offset: int,
     return keep
 
 
+L2_GROUP_BYTES = 64 * 2 ** 20
+
+
+def head_group(B: int, Hq: int, Hkv: int, nk: int, d: int) -> int:
+    """Heads per group: as many query heads as share <= 64 MiB of K and V."""
+    g = (Hq // Hkv) * (L2_GROUP_BYTES // (4 * nk * d))
+    return max(1, min(B * Hq, g))
+
+
 def fwd_work_units(kind: str, B: int, Hq: int, nq: int, nk: int,
                    q_offset: int = 0, kv_offset: int = 0, block_mask=None,
-                   causal_in_blocks: bool = False):
+                   causal_in_blocks: bool = False, Hkv: int = None, d: int = 128):
     """Forward work units in launch order: list of ``(bh, qchunk, n_kv_tiles)``."""
+    Hkv = Hq if Hkv is None else Hkv
     bh_n = B * Hq
     nqc = _cdiv(nq, UNIT_ROWS)
+    G = head_group(B, Hq, Hkv, nk, d)
+    order = []
+    for first in range(0, bh_n, G):
+        heads = list(range(first, min(bh_n, first + G)))
+        for pos in range(nqc):
+            for bh in heads:
+                order.append((bh, nqc - 1 - pos))
     out = []
-    for i in range(bh_n * nqc):
-        qc = nqc - 1 - i // bh_n
-        bh = i % bh_n
+    for bh, qc in order:
         kv = set()
         for t in range(2):
             kv |= _tile_kv_set(2 * qc + t, nq, nk, kind, q_offset, kv_offset,

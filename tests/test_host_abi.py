@@ -112,18 +112,30 @@ def test_chunk_schedule_balance():
 
 
 CASES = [
-    (0, 1, 2, 600, 600, 0, 0), (1, 1, 2, 600, 600, 0, 0), (1, 2, 3, 1000, 1000, 0, 0),
-    (1, 1, 4, 4096, 4096, 4096, 0), (1, 1, 4, 4096, 4096, 4096, 8192), (1, 1, 2, 300, 700, 128, 0),
-    (0, 2, 3, 129, 1, 0, 0), (1, 1, 1, 1, 1, 0, 0), (1, 1, 2, 512, 512, 0, 300),
+    (0, 1, 2, 2, 600, 600, 0, 0, 64), (1, 1, 2, 2, 600, 600, 0, 0, 128), (1, 2, 3, 3, 1000, 1000, 0, 0, 64),
+    (1, 1, 4, 4, 4096, 4096, 4096, 0, 128), (1, 1, 4, 2, 4096, 4096, 4096, 8192, 128),
+    (1, 1, 2, 1, 300, 700, 128, 0, 64), (0, 2, 3, 1, 129, 1, 0, 0, 128), (1, 1, 1, 1, 1, 1, 0, 0, 64),
+    (1, 1, 2, 2, 512, 512, 0, 300, 128),
+    # head grouping kicks in: K+V of a head is 4 MiB (16 heads per group) / 16 MiB with GQA 4
+    (1, 2, 32, 32, 8192, 8192, 0, 0, 128), (1, 1, 32, 8, 32768, 32768, 0, 0, 128),
+    (0, 3, 7, 7, 65536, 65536, 0, 0, 64),
 ]
 
 
 @pytest.mark.parametrize("case", CASES)
 def test_fwd_schedule_matches_oracle(lib, case):
-    kind, B_, H, nq, nk, qo, ko = case
-    got = api.build_schedule(kind, B_, H, nq, nk, qo, ko)
-    want = np.array(oracle.fwd_work_units(["none", "causal"][kind], B_, H, nq, nk, qo, ko), dtype=np.int32)
+    kind, B_, H, Hkv, nq, nk, qo, ko, d = case
+    got = api.build_schedule(kind, B_, H, nq, nk, qo, ko, Hkv=Hkv, d=d)
+    want = np.array(oracle.fwd_work_units(["none", "causal"][kind], B_, H, nq, nk, qo, ko, Hkv=Hkv, d=d),
+                    dtype=np.int32)
     np.testing.assert_array_equal(got, want.reshape(-1, 3))
+
+
+def test_head_groups():
+    assert oracle.schedule.head_group(2, 32, 32, 8192, 128) == 16
+    assert oracle.schedule.head_group(1, 32, 8, 32768, 128) == 16
+    assert oracle.schedule.head_group(8, 16, 16, 512, 64) == 128
+    assert oracle.schedule.head_group(1, 4, 4, 1 << 20, 128) == 1
 
 
 @pytest.mark.parametrize("cib", [False, True])
@@ -131,8 +143,8 @@ def test_fwd_schedule_block_sparse_matches_oracle(lib, cib):
     n = 1000
     nb = -(-n // 128)
     bm = inputs.block_sparse_mask(nb, nb, 0.25, seed=5)
-    got = api.build_schedule(2, 2, 3, n, n, 0, 0, host_block_mask=bm, causal_in_blocks=cib)
-    want = oracle.fwd_work_units("block_sparse", 2, 3, n, n, 0, 0, bm, cib)
+    got = api.build_schedule(2, 2, 3, n, n, 0, 0, host_block_mask=bm, causal_in_blocks=cib, d=64)
+    want = oracle.fwd_work_units("block_sparse", 2, 3, n, n, 0, 0, bm, cib, d=64)
     np.testing.assert_array_equal(got, np.array(want, dtype=np.int32).reshape(-1, 3))
 
 
