@@ -71,9 +71,8 @@ __device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint3
 // Tensor memory: S^T [0,128) (P^T bf16 overwrites [0,64)), dP^T [128,256)
 // (dS^T bf16 overwrites [128,192)), dV [256,256+d), dK [256+d,256+2d).
 // Shared memory: K, V (resident), NS-deep ring of {Q_i, dO_i, lse2_i, D_i}.
-// Order on the tensor core per query tile i: S^T_i, dP^T_i, dV_i, dK_i.
-// S^T_{i+1} waits for dV_i (P^T_i lives in its columns) and dP^T_{i+1} for
-// dK_i; each wait overlaps the other MMA still queued.
+// Order on the tensor core: S^T_0, dP^T_0, then dV_i, S^T_{i+1}, dK_i,
+// dP^T_{i+1} per query tile i (see the MMA issuer).
 // =========================================================================
 template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
@@ -184,52 +183,87 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
+      // Order: S^T_0, dP^T_0, then per query tile i: dV_i, S^T_{i+1}, dK_i,
+      // dP^T_{i+1}.  S^T_{i+1} overwrites the P^T_i columns dV_i reads and
+      // dP^T_{i+1} the dS^T_i columns dK_i reads; each is issued right after
+      // that reader (tcgen05.mma from one thread execute in issue order).
+      // Each elementwise phase has two MMAs of cover.
       const uint32_t id_s = idesc_bf16(128, 128, false, false);
       const uint32_t id_acc = idesc_bf16(128, D, false, true);
-      bool ok = wait_bar(bar_kv, 0, wc);
-      int i = 0;
-      for (int h = 0; h < g && ok; ++h) {
-        for (int qt = qt_first; qt < nqt && ok; ++qt) {
-          if (!tile_pair_visible(p, qt, kt)) continue;
-          const int s = i % NS;
-          const uint32_t st = s_base + OFF_RING + s * STAGE;
-          if (!(ok = wait_bar(bar_q(s), (i / NS) & 1, wc))) break;
-          if (i > 0 && !(ok = wait_bar(bar_dv, (i - 1) & 1, wc))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-            mma_ss(tmem + 0, sdesc_sw128(s_base + off, 16, 1024), sdesc_sw128(st + off, 16, 1024), id_s, kk > 0);
+      // (h, qt) pairs in order; returns false past the end
+      auto advance = [&](int& h, int& qt) {
+        for (;;) {
+          ++qt;
+          if (qt >= nqt) {
+            ++h;
+            qt = qt_first;
+            if (h >= g) return false;
           }
-          mma_commit(bar_s);
-          if (i > 0 && !(ok = wait_bar(bar_dk, (i - 1) & 1, wc))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-            mma_ss(tmem + 128, sdesc_sw128(s_base + OFF_V + off, 16, 1024),
-                   sdesc_sw128(st + C::TILE_BYTES + off, 16, 1024), id_s, kk > 0);
-          }
-          mma_commit(bar_dp);
-          // dV += P^T dO   (dO as an MN-major operand: N = d, K = query rows)
-          if (!(ok = wait_bar(bar_p, i & 1, wc))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < TILE / 16; ++kk)
-            mma_ts(tmem + 256, tmem + 0 + kk * 8, sdesc_sw128(st + C::TILE_BYTES + kk * 2048, C::BOX_BYTES, 1024),
-                   id_acc, (i > 0 || kk > 0));
-          mma_commit(bar_dv);
-          // dK += dS^T Q
-          if (!(ok = wait_bar(bar_ds, i & 1, wc))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < TILE / 16; ++kk)
-            mma_ts(tmem + 256 + D, tmem + 128 + kk * 8, sdesc_sw128(st + kk * 2048, C::BOX_BYTES, 1024), id_acc,
-                   (i > 0 || kk > 0));
-          mma_commit(bar_dk);
-          mma_commit(bar_qfree(s));
-          ++i;
+          if (tile_pair_visible(p, qt, kt)) return true;
         }
+      };
+      auto issue_st = [&](uint32_t st) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+          mma_ss(tmem + 0, sdesc_sw128(s_base + off, 16, 1024), sdesc_sw128(st + off, 16, 1024), id_s, kk > 0);
+        }
+        mma_commit(bar_s);
+      };
+      auto issue_dpt = [&](uint32_t st) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+          mma_ss(tmem + 128, sdesc_sw128(s_base + OFF_V + off, 16, 1024),
+                 sdesc_sw128(st + C::TILE_BYTES + off, 16, 1024), id_s, kk > 0);
+        }
+        mma_commit(bar_dp);
+      };
+      bool ok = wait_bar(bar_kv, 0, wc);
+      int h = 0, qt = qt_first - 1;
+      bool have = ok && advance(h, qt);
+      if (have) {
+        ok = wait_bar(bar_q(0), 0, wc);
+        if (ok) {
+          tc_fence_after();
+          issue_st(s_base + OFF_RING);
+          issue_dpt(s_base + OFF_RING);
+        }
+      }
+      int i = 0;
+      while (ok && have) {
+        const int s = i % NS, sn = (i + 1) % NS;
+        const uint32_t st = s_base + OFF_RING + s * STAGE;
+        const uint32_t stn = s_base + OFF_RING + sn * STAGE;
+        int h2 = h, qt2 = qt;
+        const bool more = advance(h2, qt2);
+        // dV += P^T dO   (dO as an MN-major operand: N = d, K = query rows)
+        if (!(ok = wait_bar(bar_p, i & 1, wc))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk)
+          mma_ts(tmem + 256, tmem + 0 + kk * 8, sdesc_sw128(st + C::TILE_BYTES + kk * 2048, C::BOX_BYTES, 1024),
+                 id_acc, (i > 0 || kk > 0));
+        mma_commit(bar_dv);
+        if (more) {
+          if (!(ok = wait_bar(bar_q(sn), ((i + 1) / NS) & 1, wc))) break;
+          tc_fence_after();
+          issue_st(stn);
+        }
+        // dK += dS^T Q
+        if (!(ok = wait_bar(bar_ds, i & 1, wc))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk)
+          mma_ts(tmem + 256 + D, tmem + 128 + kk * 8, sdesc_sw128(st + kk * 2048, C::BOX_BYTES, 1024), id_acc,
+                 (i > 0 || kk > 0));
+        mma_commit(bar_dk);
+        mma_commit(bar_qfree(s));
+        if (more) issue_dpt(stn);
+        h = h2;
+        qt = qt2;
+        have = more;
+        ++i;
       }
       mma_commit(bar_done);
       wait_bar(bar_done, 0, wc, false);
@@ -566,14 +600,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       {
         uint32_t sr[128];
         tmem_ld128(tmem + lane_off + T_S, sr);
+        // S has been read: the next S MMA may overwrite it while P is computed
+        tc_fence_before();
+        mbar_arrive(bar_sfree);
 #pragma unroll
-        for (int col = 0; col < 128; ++col) {
-          const float pv = ex2(fmaf(__uint_as_float(sr[col]), c, -l2));
-          pr[col] = (col < lim) ? pv : 0.f;
+        for (int col = 0; col < 128; col += 2) {
+          float x0, x1;
+          fma2(x0, x1, __uint_as_float(sr[col]), __uint_as_float(sr[col + 1]), c, c, -l2, -l2);
+          pr[col] = (col < lim) ? ex2(x0) : 0.f;
+          pr[col + 1] = (col + 1 < lim) ? ex2(x1) : 0.f;
         }
       }
-      tc_fence_before();
-      mbar_arrive(bar_sfree);
       ok = wait_bar(bar_dp, j & 1, wc) && (j == 0 || wait_bar(bar_dq, (j - 1) & 1, wc));
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();

@@ -25,9 +25,8 @@
 // thread): 128*56 + 256*224 = 384*168, the block's launch allotment.
 // Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d),
 // O_1 [256+d, 256+2d).  P_t (bf16 pairs) overwrites the first 64 columns of S_t.
-// The tensor core order is S_0, S_1, PV_0, PV_1 per key tile; S_t of the next
-// key tile is issued only after PV_t of this one has completed, because P_t
-// lives in the columns S_t overwrites.
+// The tensor core order is PV_0(n), S_0(n+1), PV_1(n), S_1(n+1): S_t of the
+// next key tile follows the PV_t that reads P_t out of the same columns.
 //
 // Online softmax per row, in units of log2: x = s * scale * log2(e),
 // m = running max, p = 2^(x - m), l = sum p.  The max used for p is only moved
@@ -164,49 +163,79 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     }
    } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Order per key tile n: PV_0(n), S_0(n+1), PV_1(n), S_1(n+1).  S_t(n+1)
+    // overwrites the columns P_t(n) occupies; it is issued right after the
+    // PV_t(n) that reads them, and tcgen05.mma from one thread execute in
+    // issue order.  Each softmax thus has two MMAs of cover (PV of the other
+    // tile and its S) before its own PV is needed.
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16(128, 128, false, false);
       const uint32_t id_pv = idesc_bf16(128, D, false, true);
-      int it[2] = {0, 0};
-      int n = 0;
-      bool ok = wait_bar(bar_q, 0, wc);
-      for (int kt = 0; kt < u.kt_end && ok; ++kt) {
-        const uint32_t use = unit_uses(u, kt);
-        if (!use) continue;
-        const int s = n % NS;
-        const uint32_t ph = (n / NS) & 1;
-        if (!(ok = wait_bar(bar_k(s), ph, wc))) break;
-        tc_fence_after();
-        const uint32_t kb = s_base + C::OFF_K + s * C::TILE_BYTES;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (!(use & (1u << t))) continue;
-          if (it[t] > 0 && !(ok = wait_bar(bar_o(t), (it[t] - 1) & 1, wc))) break;
-          tc_fence_after();
-          const uint32_t qb = s_base + t * C::TILE_BYTES;
+      auto next_kt = [&](int from) {
+        int k = from;
+        while (k < u.kt_end && !unit_uses(u, k)) ++k;
+        return k;
+      };
+      auto issue_s = [&](int t, int stage) {
+        const uint32_t kb = s_base + C::OFF_K + stage * C::TILE_BYTES;
+        const uint32_t qb = s_base + t * C::TILE_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-            mma_ss(tmem + t * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), id_s,
-                   kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+          mma_ss(tmem + t * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), id_s, kk > 0);
+        }
+        mma_commit(bar_s(t));
+      };
+      auto issue_pv = [&](int t, int stage, bool acc) {
+        const uint32_t vb = s_base + C::OFF_V + stage * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk)
+          mma_ts(tmem + C::TMEM_O + t * D, tmem + t * 128 + kk * 8, sdesc_sw128(vb + kk * 2048, C::BOX_BYTES, 1024),
+                 id_pv, (acc || kk > 0));
+        mma_commit(bar_o(t));
+      };
+      int it[2] = {0, 0};
+      bool ok = wait_bar(bar_q, 0, wc);
+      int kt = next_kt(0);
+      if (ok && kt < u.kt_end) {
+        const uint32_t use0 = unit_uses(u, kt);
+        ok = wait_bar(bar_k(0), 0, wc);
+        if (ok) {
+          tc_fence_after();
+          for (int t = 0; t < 2; ++t)
+            if (use0 & (1u << t)) issue_s(t, 0);
+          mma_commit(bar_kfree(0));
+        }
+      }
+      int n = 0;
+      while (ok && kt < u.kt_end) {
+        const uint32_t use = unit_uses(u, kt);
+        const int s = n % NS, sn = (n + 1) % NS;
+        const uint32_t ph = (n / NS) & 1, phn = ((n + 1) / NS) & 1;
+        const int ktn = next_kt(kt + 1);
+        const uint32_t usen = ktn < u.kt_end ? unit_uses(u, ktn) : 0u;
+        bool kwaited = false;
+        if (!(ok = wait_bar(bar_v(s), ph, wc))) break;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (use & (1u << t)) {
+            if (!(ok = wait_bar(bar_p(t), it[t] & 1, wc))) break;
+            tc_fence_after();
+            issue_pv(t, s, it[t] > 0);
+            ++it[t];
           }
-          mma_commit(bar_s(t));
+          if (t == 1) mma_commit(bar_vfree(s));   // both PV MMAs of this key tile issued
+          if (usen & (1u << t)) {
+            if (!kwaited) {
+              if (!(ok = wait_bar(bar_k(sn), phn, wc))) break;
+              tc_fence_after();
+              kwaited = true;
+            }
+            issue_s(t, sn);
+          }
         }
         if (!ok) break;
-        mma_commit(bar_kfree(s));   // K slot free once both S MMAs have read it
-        if (!(ok = wait_bar(bar_v(s), ph, wc))) break;
-        const uint32_t vb = s_base + C::OFF_V + s * C::TILE_BYTES;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (!(use & (1u << t))) continue;
-          if (!(ok = wait_bar(bar_p(t), it[t] & 1, wc))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < TILE / 16; ++kk)
-            mma_ts(tmem + C::TMEM_O + t * D, tmem + t * 128 + kk * 8,
-                   sdesc_sw128(vb + kk * 2048, C::BOX_BYTES, 1024), id_pv, (it[t] > 0 || kk > 0));
-          mma_commit(bar_o(t));
-          ++it[t];
-        }
-        mma_commit(bar_vfree(s));
+        if (usen) mma_commit(bar_kfree(sn));
+        kt = ktn;
         ++n;
       }
       // every commit above lands before the CTA leaves
@@ -273,14 +302,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       // Row max of the tile alongside exponentials taken against the current
       // reference max: the usual case (max moved by at most the threshold)
       // needs no second pass and the max is off the critical path.
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 128; j += 4) {
+      for (int j = 0; j < 128; j += 8) {
         mx0 = max3(mx0, s[j], s[j + 1]);
         mx1 = max3(mx1, s[j + 2], s[j + 3]);
+        mx2 = max3(mx2, s[j + 4], s[j + 5]);
+        mx3 = max3(mx3, s[j + 6], s[j + 7]);
       }
+      mx0 = max3(mx0, mx1, fmaxf(mx2, mx3));
       exponentials(s, (m == -INFINITY) ? 0.f : m);
-      const float m_new = fmaxf(m, fmaxf(mx0, mx1) * c);
+      const float m_new = fmaxf(m, mx0 * c);
       float alpha = 1.f;
       bool rescale = false;
       if (__any_sync(0xffffffffu, it == 0 || m_new > m + RESCALE_THRESHOLD)) {
@@ -298,12 +330,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       // bf16-rounded weights P.V sees, so O / lr cancels the rounding of a
       // dominant weight
       uint32_t pk[64];
-      float l0 = 0.f, l1 = 0.f;
+      float la[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // four independent packed chains
 #pragma unroll
       for (int j = 0; j < 64; ++j) {
-        pk[j] = pack_bf16(s[2 * j], s[2 * j + 1]);
-        add2(l0, l1, l0, l1, s[2 * j], s[2 * j + 1]);
+        // bf16 by truncation (one byte permute per pair); O is normalised by
+        // the sum of these same weights, so the rounding direction cancels
+        pk[j] = __byte_perm(__float_as_uint(s[2 * j]), __float_as_uint(s[2 * j + 1]), 0x7632);
+        const int a = 2 * (j & 3);
+        add2(la[a], la[a + 1], la[a], la[a + 1], s[2 * j], s[2 * j + 1]);
       }
+      const float l0 = (la[0] + la[1]) + (la[2] + la[3]), l1 = (la[4] + la[5]) + (la[6] + la[7]);
       tmem_st64(tS, pk);    // P_t (bf16 pairs) over the first 64 columns of S_t
       if (rescale) {
         // PV_t of the previous key tile must have landed in O_t first
@@ -323,10 +359,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       mbar_arrive(bar_p(t));
       ++it;
       // rounded-weight sum after P has been handed to the tensor core
-      float r0 = 0.f, r1 = 0.f;
+      float ra[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int j = 0; j < 64; ++j)
-        add2(r0, r1, r0, r1, __uint_as_float(pk[j] << 16), __uint_as_float(pk[j] & 0xffff0000u));
+      for (int j = 0; j < 64; ++j) {
+        const int a = 2 * (j & 3);
+        add2(ra[a], ra[a + 1], ra[a], ra[a + 1], __uint_as_float(pk[j] << 16), __uint_as_float(pk[j] & 0xffff0000u));
+      }
+      const float r0 = (ra[0] + ra[1]) + (ra[2] + ra[3]), r1 = (ra[4] + ra[5]) + (ra[6] + ra[7]);
       l = l * alpha + (l0 + l1);
       lr = lr * alpha + (r0 + r1);
 
