@@ -385,25 +385,36 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 // =========================================================================
 // dQ
 // Tensor memory: S [0,128), dP [128,256), dQ [256,256+d), dS bf16 [384,448).
-// Shared memory: Q, dO (resident), NS-deep ring of {K_j, V_j}.
-// Tensor-core order: S_0, dP_0, then per key tile j: S_{j+1} (once P_j has
-// been read out of S), dQ_j (once dS_j is written), dP_{j+1} (once dP_j has
-// been read).  dS has its own columns, so dP_{j+1} never waits on dQ_j.
+// Shared memory: Q, dO (resident), a KS-deep ring of K_j and a VS-deep ring of
+// V_j.  K_j is read by S_j and dQ_j, V_j only by dP_j, so the V slots come
+// free much earlier and the K ring is the deeper one.
+// Tensor-core order: S_0, dP_0, then per key tile j: S_{j+1} (as soon as S_j
+// has been read out of TMEM), dQ_j (once dS_j is written), dP_{j+1}.  dS has
+// its own columns, so dP_{j+1} never waits on dQ_j.
 // =========================================================================
+template <int D>
+struct DqCfg {
+  static constexpr int KS = (D == 128) ? 3 : 6;
+  static constexpr int VS = (D == 128) ? 2 : 4;
+  static constexpr uint32_t TILE_BYTES = BwdCfg<D>::TILE_BYTES;
+  static constexpr uint32_t OFF_DO = TILE_BYTES;
+  static constexpr uint32_t OFF_K = 2 * TILE_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + KS * TILE_BYTES;
+  static constexpr uint32_t SMEM = OFF_V + VS * TILE_BYTES + 1024;
+};
+
 template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
               const BwdParams p) {
   using C = BwdCfg<D>;
-  constexpr int NS = C::NS;
-  constexpr uint32_t OFF_DO = C::TILE_BYTES;
-  constexpr uint32_t OFF_RING = 2 * C::TILE_BYTES;
-  constexpr uint32_t STAGE = 2 * C::TILE_BYTES;  // K_j, V_j
+  using Q = DqCfg<D>;
+  constexpr int KS = Q::KS, VS = Q::VS;
   constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256, T_DS = 384;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bars[1 + 3 * NS + 7];
+  __shared__ __align__(8) uint64_t bars[1 + 2 * KS + 2 * VS + 6];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -411,14 +422,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const uint32_t s_base = smem_u32(smem);
   const uint32_t bar_qdo = smem_u32(&bars[0]);
   auto bar_k = [&](int s) { return smem_u32(&bars[1 + s]); };
-  auto bar_v = [&](int s) { return smem_u32(&bars[1 + NS + s]); };
-  auto bar_free = [&](int s) { return smem_u32(&bars[1 + 2 * NS + s]); };
-  const uint32_t bar_s = smem_u32(&bars[1 + 3 * NS + 0]);
-  const uint32_t bar_dp = smem_u32(&bars[1 + 3 * NS + 1]);
-  const uint32_t bar_sfree = smem_u32(&bars[1 + 3 * NS + 2]);
-  const uint32_t bar_ds = smem_u32(&bars[1 + 3 * NS + 3]);
-  const uint32_t bar_dq = smem_u32(&bars[1 + 3 * NS + 4]);
-  const uint32_t bar_done = smem_u32(&bars[1 + 3 * NS + 5]);
+  auto bar_kfree = [&](int s) { return smem_u32(&bars[1 + KS + s]); };
+  auto bar_v = [&](int s) { return smem_u32(&bars[1 + 2 * KS + s]); };
+  auto bar_vfree = [&](int s) { return smem_u32(&bars[1 + 2 * KS + VS + s]); };
+  const uint32_t bar_s = smem_u32(&bars[1 + 2 * KS + 2 * VS + 0]);
+  const uint32_t bar_dp = smem_u32(&bars[1 + 2 * KS + 2 * VS + 1]);
+  const uint32_t bar_sfree = smem_u32(&bars[1 + 2 * KS + 2 * VS + 2]);
+  const uint32_t bar_ds = smem_u32(&bars[1 + 2 * KS + 2 * VS + 3]);
+  const uint32_t bar_dq = smem_u32(&bars[1 + 2 * KS + 2 * VS + 4]);
+  const uint32_t bar_done = smem_u32(&bars[1 + 2 * KS + 2 * VS + 5]);
 
   const int nqt = (p.N + TILE - 1) / TILE;
   int bh = 0, qpos = 0;
@@ -433,10 +445,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(bar_qdo, 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < KS; ++s) {
       mbar_init(bar_k(s), 1);
+      mbar_init(bar_kfree(s), 1);
+    }
+    for (int s = 0; s < VS; ++s) {
       mbar_init(bar_v(s), 1);
-      mbar_init(bar_free(s), 1);
+      mbar_init(bar_vfree(s), 1);
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
@@ -468,64 +483,63 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     __syncwarp();
     if (lane < C::NBOX) tma_load_3d(s_base + lane * C::BOX_BYTES, &tq, lane * 64, qt * TILE, bh, bar_qdo);
     else if (lane < 2 * C::NBOX)
-      tma_load_3d(s_base + OFF_DO + (lane - C::NBOX) * C::BOX_BYTES, &tdo, (lane - C::NBOX) * 64, qt * TILE, bh,
+      tma_load_3d(s_base + Q::OFF_DO + (lane - C::NBOX) * C::BOX_BYTES, &tdo, (lane - C::NBOX) * 64, qt * TILE, bh,
                   bar_qdo);
     int n = 0;
     bool ok = true;
     for (int kt = 0; kt < kt_end && ok; ++kt) {
       if (!tile_pair_visible(p, qt, kt)) continue;
-      const int s = n % NS;
-      if (n >= NS) ok = wait_bar(bar_free(s), ((n / NS) - 1) & 1, wc);
+      const int sk = n % KS, sv = n % VS;
+      if (n >= KS) ok = wait_bar(bar_kfree(sk), ((n / KS) - 1) & 1, wc);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
-      const uint32_t st = s_base + OFF_RING + s * STAGE;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar_k(s), C::TILE_BYTES);
-        mbar_arrive_expect_tx(bar_v(s), C::TILE_BYTES);
-      }
+      if (lane == 0) mbar_arrive_expect_tx(bar_k(sk), C::TILE_BYTES);
       __syncwarp();
       if (lane < C::NBOX)
-        tma_load_3d(st + lane * C::BOX_BYTES, &tk, lane * 64, kt * TILE, bkv, bar_k(s));
-      else if (lane < 2 * C::NBOX)
-        tma_load_3d(st + C::TILE_BYTES + (lane - C::NBOX) * C::BOX_BYTES, &tv, (lane - C::NBOX) * 64, kt * TILE, bkv,
-                    bar_v(s));
+        tma_load_3d(s_base + Q::OFF_K + sk * C::TILE_BYTES + lane * C::BOX_BYTES, &tk, lane * 64, kt * TILE, bkv,
+                    bar_k(sk));
+      if (n >= VS) ok = wait_bar(bar_vfree(sv), ((n / VS) - 1) & 1, wc);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      if (lane == 0) mbar_arrive_expect_tx(bar_v(sv), C::TILE_BYTES);
+      __syncwarp();
+      if (lane >= C::NBOX && lane < 2 * C::NBOX)
+        tma_load_3d(s_base + Q::OFF_V + sv * C::TILE_BYTES + (lane - C::NBOX) * C::BOX_BYTES, &tv,
+                    (lane - C::NBOX) * 64, kt * TILE, bkv, bar_v(sv));
       ++n;
     }
     if ((!ok || abort_flag) && lane == 0) {
       wait_bar(bar_qdo, 0, wc, false);
-      for (int j = n - NS < 0 ? 0 : n - NS; j < n; ++j) {
-        wait_bar(bar_k(j % NS), (j / NS) & 1, wc, false);
-        wait_bar(bar_v(j % NS), (j / NS) & 1, wc, false);
-      }
+      for (int j = n - KS < 0 ? 0 : n - KS; j < n; ++j) wait_bar(bar_k(j % KS), (j / KS) & 1, wc, false);
+      for (int j = n - VS < 0 ? 0 : n - VS; j < n; ++j) wait_bar(bar_v(j % VS), (j / VS) & 1, wc, false);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       const uint32_t id_s = idesc_bf16(128, 128, false, false);
       const uint32_t id_dq = idesc_bf16(128, D, false, true);
-      // visible key tiles in order
       auto next_kt = [&](int from) {
         int kt = from;
         while (kt < kt_end && !tile_pair_visible(p, qt, kt)) ++kt;
         return kt;
       };
-      auto issue_s = [&](int stage) {
-        const uint32_t st = s_base + OFF_RING + stage * STAGE;
+      auto issue_s = [&](int n) {   // S = Q K_n^T
+        const uint32_t kb = s_base + Q::OFF_K + (n % KS) * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-          mma_ss(tmem + T_S, sdesc_sw128(s_base + off, 16, 1024), sdesc_sw128(st + off, 16, 1024), id_s, kk > 0);
+          mma_ss(tmem + T_S, sdesc_sw128(s_base + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), id_s, kk > 0);
         }
         mma_commit(bar_s);
       };
-      auto issue_dp = [&](int stage) {
-        const uint32_t st = s_base + OFF_RING + stage * STAGE + C::TILE_BYTES;
+      auto issue_dp = [&](int n) {  // dP = dO V_n^T; the V slot is free once it completes
+        const uint32_t vb = s_base + Q::OFF_V + (n % VS) * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-          mma_ss(tmem + T_DP, sdesc_sw128(s_base + OFF_DO + off, 16, 1024), sdesc_sw128(st + off, 16, 1024), id_s,
+          mma_ss(tmem + T_DP, sdesc_sw128(s_base + Q::OFF_DO + off, 16, 1024), sdesc_sw128(vb + off, 16, 1024), id_s,
                  kk > 0);
         }
         mma_commit(bar_dp);
+        mma_commit(bar_vfree(n % VS));
       };
       bool ok = wait_bar(bar_qdo, 0, wc);
       int kt = next_kt(0);
@@ -543,31 +557,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
       }
       while (ok && kt < kt_end) {
-        const int s = j % NS;
         const int kt_next = next_kt(kt + 1);
-        const int sn = (j + 1) % NS;
-        const uint32_t phn = ((j + 1) / NS) & 1;
         if (kt_next < kt_end) {
-          // S_{j+1} once P_j has been read out of the S columns
-          if (!(ok = wait_bar(bar_k(sn), phn, wc) && wait_bar(bar_sfree, j & 1, wc))) break;
+          // S_{j+1} once S_j has been read out of TMEM
+          if (!(ok = wait_bar(bar_k((j + 1) % KS), ((j + 1) / KS) & 1, wc) && wait_bar(bar_sfree, j & 1, wc))) break;
           tc_fence_after();
-          issue_s(sn);
+          issue_s(j + 1);
         }
         // dQ_j += dS_j K_j   (K_j as an MN-major operand: N = d, K = keys)
         if (!(ok = wait_bar(bar_ds, j & 1, wc))) break;
         tc_fence_after();
-        const uint32_t kb = s_base + OFF_RING + s * STAGE;
+        const uint32_t kb = s_base + Q::OFF_K + (j % KS) * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < TILE / 16; ++kk)
           mma_ts(tmem + T_DQ, tmem + T_DS + kk * 8, sdesc_sw128(kb + kk * 2048, C::BOX_BYTES, 1024), id_dq,
                  (j > 0 || kk > 0));
         mma_commit(bar_dq);
-        mma_commit(bar_free(s));
+        mma_commit(bar_kfree(j % KS));
         if (kt_next < kt_end) {
           // dP_{j+1}: dP_j has been read (dS_j written) already
-          if (!(ok = wait_bar(bar_v(sn), phn, wc))) break;
+          if (!(ok = wait_bar(bar_v((j + 1) % VS), ((j + 1) / VS) & 1, wc))) break;
           tc_fence_after();
-          issue_dp(sn);
+          issue_dp(j + 1);
         }
         kt = kt_next;
         ++j;
@@ -594,6 +605,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       // key column col is visible iff key < N and (not causal or key <= query)
+      const bool edge = (kt == nkt - 1 && (p.N % TILE) != 0) || (causal && kt == qt);
       int lim = p.N - kt * TILE;
       if (causal && kt == qt) lim = min(lim, r + 1);
       float pr[128];
@@ -607,8 +619,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         for (int col = 0; col < 128; col += 2) {
           float x0, x1;
           fma2(x0, x1, __uint_as_float(sr[col]), __uint_as_float(sr[col + 1]), c, c, -l2, -l2);
-          pr[col] = (col < lim) ? ex2(x0) : 0.f;
-          pr[col + 1] = (col + 1 < lim) ? ex2(x1) : 0.f;
+          pr[col] = ex2(x0);
+          pr[col + 1] = ex2(x1);
+        }
+        if (edge) {
+#pragma unroll
+          for (int col = 0; col < 128; ++col) pr[col] = (col < lim) ? pr[col] : 0.f;
         }
       }
       ok = wait_bar(bar_dp, j & 1, wc) && (j == 0 || wait_bar(bar_dq, (j - 1) & 1, wc));
@@ -622,8 +638,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
           const int col = hh * 64 + 2 * jj;
-          pk[jj] = pack_bf16(pr[col] * (__uint_as_float(dpr[2 * jj]) - dr),
-                             pr[col + 1] * (__uint_as_float(dpr[2 * jj + 1]) - dr));
+          // dS = P * (dP - D) = P*dP + (-P*D)
+          float a0, a1, d0, d1;
+          fma2(a0, a1, pr[col], pr[col + 1], -dr, -dr, 0.f, 0.f);
+          fma2(d0, d1, pr[col], pr[col + 1], __uint_as_float(dpr[2 * jj]), __uint_as_float(dpr[2 * jj + 1]), a0, a1);
+          pk[jj] = pack_bf16_rn_int(d0, d1);
         }
         tmem_st32(tmem + lane_off + T_DS + hh * 32, pk);
       }
@@ -664,11 +683,6 @@ constexpr uint32_t dkdv_smem() {
   return 2 * BwdCfg<D>::TILE_BYTES + BwdCfg<D>::NS * (2 * BwdCfg<D>::TILE_BYTES + 1024) + 1024;
 }
 template <int D>
-constexpr uint32_t dq_smem() {
-  return 2 * BwdCfg<D>::TILE_BYTES + BwdCfg<D>::NS * 2 * BwdCfg<D>::TILE_BYTES + 1024;
-}
-
-template <int D>
 cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const BwdParams& p, cudaStream_t s) {
   constexpr uint32_t smem = dkdv_smem<D>();
@@ -683,7 +697,7 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
 template <int D>
 cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const CUtensorMap& tdo, const BwdParams& p, cudaStream_t s) {
-  constexpr uint32_t smem = dq_smem<D>();
+  constexpr uint32_t smem = DqCfg<D>::SMEM;
   static_assert(smem <= 232448 - 256, "dQ shared memory");
   cudaError_t e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
