@@ -153,6 +153,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded)}
 
 
+def slowest_rank_ms(elapsed_ms, dist, device):
+    """Every rank's timed region ends at a barrier; the job's time is the slowest rank's."""
+    if dist is None:
+        return float(elapsed_ms)
+    import torch
+    t = torch.tensor([float(elapsed_ms)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, steps, flops_per_rank_step, elapsed_ms):
+    """Whole-job throughput: every rank processes its own batch (weak scaling)."""
+    return world * steps * flops_per_rank_step / (elapsed_ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ oracle leg
 
 def oracle_sample(seconds, rank=0):
@@ -304,14 +319,11 @@ def main():
     clocks = sampler.stop()
     recs, n_launch = api.trace_read(8 * args.steps + 64)
     status = api.get_status()
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = slowest_rank_ms(elapsed_ms, dist, "cuda")
 
     f_fwd, f_bwd = step_flops(w)
     ms_step = elapsed_ms / args.steps
-    value = world * args.steps * (f_fwd + f_bwd) / (elapsed_ms * 1e-3) / 1e12
+    value = job_tflops(world, args.steps, f_fwd + f_bwd, elapsed_ms)
     peaks, peak_src = load_peaks()
     peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     peak_burst = peaks["bf16_tflops"]
