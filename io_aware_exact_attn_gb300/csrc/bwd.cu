@@ -20,9 +20,10 @@
 //                loops over the key tiles it sees: S = Q K^T, dP = dO V^T,
 //                dS = P * (dP - D), dQ += dS K, dQ accumulated in fp32 in
 //                tensor memory and scaled / rounded once at the end.
-// Warp roles (8 warps): warp 0 TMA producer, warp 1 MMA issuer (one thread,
-// owns the TMEM allocation), warps 2-3 idle, warps 4-7 elementwise work
-// (warp w owns TMEM lanes 32*(w%4)..+31; one thread per tile row).
+// Warp roles (12 warps): warp 0 TMA producer, warp 1 MMA issuer (one thread,
+// owns the TMEM allocation), warps 2-3 idle, warps 4-11 elementwise work in
+// two warpgroups that split the 128 columns of every tile row between them
+// (warp w owns TMEM lanes 32*(w%4)..+31; one thread per row and half).
 #include "internal.h"
 #include "ptx.cuh"
 #include "schedule.h"
@@ -38,6 +39,10 @@ struct BwdCfg {
   static constexpr uint32_t TILE_BYTES = NBOX * BOX_BYTES;
   static constexpr int NS = (D == 128) ? 2 : 4;  // ring depth
   static constexpr int THREADS = 256;
+  // both kernels: 12 warps; the control warpgroup gives registers back to the
+  // two elementwise warpgroups: 128*56 + 256*224 = 384*168 (launch allotment)
+  static constexpr int SPLIT_THREADS = 384;
+  static constexpr uint32_t REGS_CTRL = 56, REGS_ELEM = 224;
 };
 
 __device__ __forceinline__ bool causal_of(const BwdParams& p) {
@@ -50,6 +55,11 @@ __device__ __forceinline__ bool tile_pair_visible(const BwdParams& p, int qt, in
   if (p.mask_kind == MASK_BLOCK_SPARSE && p.block_mask[(size_t)qt * p.nkb + kt] == 0) return false;
   return true;
 }
+
+// TMEM column of the bf16 A operand for MMA k-step kk (16 rows of K each) when
+// the operand is written in two halves: k-steps 0-3 at columns [0, 32) and
+// 4-7 at [64, 96) relative to the region start.
+__host__ __device__ constexpr uint32_t half_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
 
 // Convert 32 fp32 accumulator columns to bf16 (times `mul`) and store them as
 // 64 contiguous bytes.
@@ -75,7 +85,7 @@ __device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint3
 // dP^T_{i+1} per query tile i (see the MMA issuer).
 // =========================================================================
 template <int D>
-__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                 const BwdParams p) {
@@ -121,8 +131,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
-    mbar_init(bar_p, 128);
-    mbar_init(bar_ds, 128);
+    mbar_init(bar_p, 256);
+    mbar_init(bar_ds, 256);
     mbar_init(bar_dv, 1);
     mbar_init(bar_dk, 1);
     mbar_init(bar_done, 1);
@@ -143,7 +153,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == 0) {
+  if (warp < 4) {
+   reg_dealloc<C::REGS_CTRL>();
+   if (warp == 0) {
     // ---------------------------------------------------------- producer
     // one lane per TMA copy (copies issued by one thread are serialised)
     if (lane == 0) mbar_arrive_expect_tx(bar_kv, 2 * C::TILE_BYTES);
@@ -180,7 +192,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       wait_bar(bar_kv, 0, wc, false);
       for (int j = n - NS < 0 ? 0 : n - NS; j < n; ++j) wait_bar(bar_q(j % NS), (j / NS) & 1, wc, false);
     }
-  } else if (warp == 1) {
+   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       // Order: S^T_0, dP^T_0, then per query tile i: dV_i, S^T_{i+1}, dK_i,
@@ -242,7 +254,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < TILE / 16; ++kk)
-          mma_ts(tmem + 256, tmem + 0 + kk * 8, sdesc_sw128(st + C::TILE_BYTES + kk * 2048, C::BOX_BYTES, 1024),
+          mma_ts(tmem + 256, tmem + half_col(kk), sdesc_sw128(st + C::TILE_BYTES + kk * 2048, C::BOX_BYTES, 1024),
                  id_acc, (i > 0 || kk > 0));
         mma_commit(bar_dv);
         if (more) {
@@ -255,7 +267,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < TILE / 16; ++kk)
-          mma_ts(tmem + 256 + D, tmem + 128 + kk * 8, sdesc_sw128(st + kk * 2048, C::BOX_BYTES, 1024), id_acc,
+          mma_ts(tmem + 256 + D, tmem + 128 + half_col(kk), sdesc_sw128(st + kk * 2048, C::BOX_BYTES, 1024), id_acc,
                  (i > 0 || kk > 0));
         mma_commit(bar_dk);
         mma_commit(bar_qfree(s));
@@ -268,8 +280,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       mma_commit(bar_done);
       wait_bar(bar_done, 0, wc, false);
     }
-  } else if (warp >= 4) {
+   }
+  } else {
+    reg_alloc<C::REGS_ELEM>();
     // ------------------------------------------------------------ elementwise
+    // warpgroup hf (0: warps 4-7, 1: warps 8-11) owns query columns
+    // [64*hf, 64*hf + 64) of every row; its bf16 results go over the first 32
+    // of those columns, which only it has read
+    const int hf = (warp - 4) >> 2;
+    const int cb = 64 * hf;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;                   // key row inside the tile
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -287,21 +306,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         const bool diag = causal && qt == kt;       // key r sees query column j iff r <= j
-        const float4* l4 = reinterpret_cast<const float4*>(lse2);
-        const float4* d4 = reinterpret_cast<const float4*>(dsum);
-        // phase A: P^T = 2^(S^T c - lse2) -> bf16 pairs into the first 64 S^T columns
-        uint32_t pk[64];
+        const float4* l4 = reinterpret_cast<const float4*>(lse2) + 16 * hf;
+        const float4* d4 = reinterpret_cast<const float4*>(dsum) + 16 * hf;
+        // phase A: P^T = 2^(S^T c - lse2) for this warpgroup's 64 query columns
+        uint32_t pk[32];
         {
-          uint32_t sr[128];
-          tmem_ld128(tmem + lane_off, sr);
+          uint32_t sr[64];
+          tmem_ld64(tmem + lane_off + cb, sr);
 #pragma unroll
-          for (int j4 = 0; j4 < 32; ++j4) {
+          for (int j4 = 0; j4 < 16; ++j4) {
             const float4 L = l4[j4];
-            const int col = 4 * j4;
-            float p0 = ex2(fmaf(__uint_as_float(sr[col + 0]), c, -L.x));
-            float p1 = ex2(fmaf(__uint_as_float(sr[col + 1]), c, -L.y));
-            float p2 = ex2(fmaf(__uint_as_float(sr[col + 2]), c, -L.z));
-            float p3 = ex2(fmaf(__uint_as_float(sr[col + 3]), c, -L.w));
+            const int col = cb + 4 * j4;
+            float p0 = ex2(fmaf(__uint_as_float(sr[4 * j4 + 0]), c, -L.x));
+            float p1 = ex2(fmaf(__uint_as_float(sr[4 * j4 + 1]), c, -L.y));
+            float p2 = ex2(fmaf(__uint_as_float(sr[4 * j4 + 2]), c, -L.z));
+            float p3 = ex2(fmaf(__uint_as_float(sr[4 * j4 + 3]), c, -L.w));
             if (diag) {
               p0 = (r <= col + 0) ? p0 : 0.f;
               p1 = (r <= col + 1) ? p1 : 0.f;
@@ -312,23 +331,22 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             pk[2 * j4 + 1] = pack_bf16(p2, p3);
           }
         }
-        tmem_st64(tmem + lane_off, pk);
+        tmem_st32(tmem + lane_off + cb, pk);
         tc_fence_before();
         mbar_arrive(bar_p);
         ok = wait_bar(bar_dp, i & 1, wc);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        // phase B: dS^T = P^T * (dP^T - D), in two 64-column halves; the bf16
-        // pairs go over the dP^T columns already read
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        // phase B: dS^T = P^T * (dP^T - D) for the same 64 columns; the bf16
+        // pairs go over the first 32 dP^T columns of the half
+        {
           uint32_t dr[64];
-          tmem_ld64(tmem + lane_off + 128 + hh * 64, dr);
+          tmem_ld64(tmem + lane_off + 128 + cb, dr);
           uint32_t ds[32];
 #pragma unroll
           for (int j4 = 0; j4 < 16; ++j4) {
-            const float4 Dv = d4[hh * 16 + j4];
-            const uint32_t pa = pk[hh * 32 + 2 * j4], pb = pk[hh * 32 + 2 * j4 + 1];
+            const float4 Dv = d4[j4];
+            const uint32_t pa = pk[2 * j4], pb = pk[2 * j4 + 1];
             const float d0 = __uint_as_float(pa << 16) * (__uint_as_float(dr[4 * j4 + 0]) - Dv.x);
             const float d1 = __uint_as_float(pa & 0xffff0000u) * (__uint_as_float(dr[4 * j4 + 1]) - Dv.y);
             const float d2 = __uint_as_float(pb << 16) * (__uint_as_float(dr[4 * j4 + 2]) - Dv.z);
@@ -336,7 +354,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             ds[2 * j4] = pack_bf16(d0, d1);
             ds[2 * j4 + 1] = pack_bf16(d2, d3);
           }
-          tmem_st32(tmem + lane_off + 128 + hh * 32, ds);
+          tmem_st32(tmem + lane_off + 128 + cb, ds);
         }
         tc_fence_before();
         mbar_arrive(bar_ds);
@@ -353,22 +371,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tc_fence_after();
         const int key = kt * TILE + r;
         const size_t orow = (size_t)bkv * p.N + (size_t)key;
-        __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(p.dv) + orow * D;
-        __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(p.dk) + orow * D;
+        // warpgroup 0 writes dV, warpgroup 1 writes scale * dK
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(hf == 0 ? p.dv : p.dk) + orow * D;
+        const float mul = hf == 0 ? 1.f : p.scale;
 #pragma unroll
         for (int q4 = 0; q4 < D / 32; ++q4) {
-          uint32_t rv[32], rk[32];
+          uint32_t rv[32];
           if (i > 0) {
-            tmem_ld32(tmem + lane_off + 256 + q4 * 32, rv);
-            tmem_ld32(tmem + lane_off + 256 + D + q4 * 32, rk);
+            tmem_ld32(tmem + lane_off + 256 + hf * D + q4 * 32, rv);
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) rv[j] = rk[j] = 0u;
+            for (int j = 0; j < 32; ++j) rv[j] = 0u;
           }
-          if (key < p.N) {
-            store_row32_bf16(dv + q4 * 32, rv, 1.f);
-            store_row32_bf16(dk + q4 * 32, rk, p.scale);
-          }
+          if (key < p.N) store_row32_bf16(dst + q4 * 32, rv, mul);
         }
       }
     }
@@ -384,13 +399,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
 // =========================================================================
 // dQ
-// Tensor memory: S [0,128), dP [128,256), dQ [256,256+d), dS bf16 [384,448).
+// Tensor memory: S [0,128), dP [128,256), dQ [256,256+d), two bf16 dS buffers
+// [384,448) and [448,512): dS_j goes to buffer j % 2, so writing dS_{j+1} does
+// not wait for dQ_j (the MMA issuer queues dQ_j behind S_{j+1} and dP_{j+1}).
 // Shared memory: Q, dO (resident), a KS-deep ring of K_j and a VS-deep ring of
 // V_j.  K_j is read by S_j and dQ_j, V_j only by dP_j, so the V slots come
 // free much earlier and the K ring is the deeper one.
 // Tensor-core order: S_0, dP_0, then per key tile j: S_{j+1} (as soon as S_j
-// has been read out of TMEM), dQ_j (once dS_j is written), dP_{j+1}.  dS has
-// its own columns, so dP_{j+1} never waits on dQ_j.
+// has been read out of TMEM), dP_{j+1} (as soon as dP_j has been read), dQ_j
+// (once dS_j is written to its buffer).
 // =========================================================================
 template <int D>
 struct DqCfg {
@@ -404,17 +421,18 @@ struct DqCfg {
 };
 
 template <int D>
-__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
               const BwdParams p) {
   using C = BwdCfg<D>;
   using Q = DqCfg<D>;
   constexpr int KS = Q::KS, VS = Q::VS;
+  static_assert(KS >= 2 && VS >= 2, "the issuer's ring counters start at slot 1");
   constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256, T_DS = 384;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bars[1 + 2 * KS + 2 * VS + 6];
+  __shared__ __align__(8) uint64_t bars[1 + 2 * KS + 2 * VS + 9];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -428,9 +446,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const uint32_t bar_s = smem_u32(&bars[1 + 2 * KS + 2 * VS + 0]);
   const uint32_t bar_dp = smem_u32(&bars[1 + 2 * KS + 2 * VS + 1]);
   const uint32_t bar_sfree = smem_u32(&bars[1 + 2 * KS + 2 * VS + 2]);
-  const uint32_t bar_ds = smem_u32(&bars[1 + 2 * KS + 2 * VS + 3]);
-  const uint32_t bar_dq = smem_u32(&bars[1 + 2 * KS + 2 * VS + 4]);
-  const uint32_t bar_done = smem_u32(&bars[1 + 2 * KS + 2 * VS + 5]);
+  const uint32_t bar_done = smem_u32(&bars[1 + 2 * KS + 2 * VS + 3]);
+  const uint32_t bar_dpread = smem_u32(&bars[1 + 2 * KS + 2 * VS + 4]);
+  // per dS buffer: dS_j written (256 arrivals), dQ_j done (its buffer is free)
+  auto bar_ds = [&](int j) { return smem_u32(&bars[1 + 2 * KS + 2 * VS + 5 + (j & 1)]); };
+  auto bar_dq = [&](int j) { return smem_u32(&bars[1 + 2 * KS + 2 * VS + 7 + (j & 1)]); };
 
   const int nqt = (p.N + TILE - 1) / TILE;
   int bh = 0, qpos = 0;
@@ -455,10 +475,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
-    mbar_init(bar_sfree, 128);
-    mbar_init(bar_ds, 128);
-    mbar_init(bar_dq, 1);
+    mbar_init(bar_sfree, 256);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_ds(t), 256);
+      mbar_init(bar_dq(t), 1);
+    }
     mbar_init(bar_done, 1);
+    mbar_init(bar_dpread, 256);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -476,75 +499,87 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == 0) {
-    // ---------------------------------------------------------- producer
-    // one lane per TMA copy (copies issued by one thread are serialised)
-    if (lane == 0) mbar_arrive_expect_tx(bar_qdo, 2 * C::TILE_BYTES);
-    __syncwarp();
-    if (lane < C::NBOX) tma_load_3d(s_base + lane * C::BOX_BYTES, &tq, lane * 64, qt * TILE, bh, bar_qdo);
-    else if (lane < 2 * C::NBOX)
-      tma_load_3d(s_base + Q::OFF_DO + (lane - C::NBOX) * C::BOX_BYTES, &tdo, (lane - C::NBOX) * 64, qt * TILE, bh,
-                  bar_qdo);
+  if (warp < 4) {
+   reg_dealloc<C::REGS_CTRL>();
+   if (warp == 0 || warp == 2) {
+    // ---------------------------------------------------------- producers
+    // warp 0 streams K (and loads Q, dO once), warp 2 streams V: a K slot is
+    // only free once dQ_j has run, a V slot once dP_j has, so the V stream
+    // must not wait behind the K stream.  One lane per TMA copy (copies
+    // issued by one thread are serialised).
+    const bool is_k = warp == 0;
+    if (is_k) {
+      if (lane == 0) mbar_arrive_expect_tx(bar_qdo, 2 * C::TILE_BYTES);
+      __syncwarp();
+      if (lane < C::NBOX) tma_load_3d(s_base + lane * C::BOX_BYTES, &tq, lane * 64, qt * TILE, bh, bar_qdo);
+      else if (lane < 2 * C::NBOX)
+        tma_load_3d(s_base + Q::OFF_DO + (lane - C::NBOX) * C::BOX_BYTES, &tdo, (lane - C::NBOX) * 64, qt * TILE, bh,
+                    bar_qdo);
+    }
+    const int depth = is_k ? KS : VS;
+    const uint32_t ring = s_base + (is_k ? Q::OFF_K : Q::OFF_V);
+    const CUtensorMap* map = is_k ? &tk : &tv;
+    auto full = [&](int sl) { return is_k ? bar_k(sl) : bar_v(sl); };
+    auto freed = [&](int sl) { return is_k ? bar_kfree(sl) : bar_vfree(sl); };
     int n = 0;
     bool ok = true;
     for (int kt = 0; kt < kt_end && ok; ++kt) {
       if (!tile_pair_visible(p, qt, kt)) continue;
-      const int sk = n % KS, sv = n % VS;
-      if (n >= KS) ok = wait_bar(bar_kfree(sk), ((n / KS) - 1) & 1, wc);
+      const int sl = n % depth;
+      if (n >= depth) ok = wait_bar(freed(sl), ((n / depth) - 1) & 1, wc);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
-      if (lane == 0) mbar_arrive_expect_tx(bar_k(sk), C::TILE_BYTES);
+      if (lane == 0) mbar_arrive_expect_tx(full(sl), C::TILE_BYTES);
       __syncwarp();
       if (lane < C::NBOX)
-        tma_load_3d(s_base + Q::OFF_K + sk * C::TILE_BYTES + lane * C::BOX_BYTES, &tk, lane * 64, kt * TILE, bkv,
-                    bar_k(sk));
-      if (n >= VS) ok = wait_bar(bar_vfree(sv), ((n / VS) - 1) & 1, wc);
-      if (!(ok = __all_sync(0xffffffffu, ok))) break;
-      if (lane == 0) mbar_arrive_expect_tx(bar_v(sv), C::TILE_BYTES);
-      __syncwarp();
-      if (lane >= C::NBOX && lane < 2 * C::NBOX)
-        tma_load_3d(s_base + Q::OFF_V + sv * C::TILE_BYTES + (lane - C::NBOX) * C::BOX_BYTES, &tv,
-                    (lane - C::NBOX) * 64, kt * TILE, bkv, bar_v(sv));
+        tma_load_3d(ring + sl * C::TILE_BYTES + lane * C::BOX_BYTES, map, lane * 64, kt * TILE, bkv, full(sl));
       ++n;
     }
     if ((!ok || abort_flag) && lane == 0) {
-      wait_bar(bar_qdo, 0, wc, false);
-      for (int j = n - KS < 0 ? 0 : n - KS; j < n; ++j) wait_bar(bar_k(j % KS), (j / KS) & 1, wc, false);
-      for (int j = n - VS < 0 ? 0 : n - VS; j < n; ++j) wait_bar(bar_v(j % VS), (j / VS) & 1, wc, false);
+      if (is_k) wait_bar(bar_qdo, 0, wc, false);
+      for (int j = n - depth < 0 ? 0 : n - depth; j < n; ++j) wait_bar(full(j % depth), (j / depth) & 1, wc, false);
     }
-  } else if (warp == 1) {
+   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
+      // tcgen05.mma issue stalls once a few MMAs are queued, so this thread
+      // is held for most of each 8-MMA group; whatever it does between groups
+      // leaves the tensor pipe idle.  The loop therefore keeps no more than
+      // ring counters: descriptors are built once and each k-step adds a
+      // compile-time offset to the start-address field (shared-memory
+      // addresses stay below 256 KB, so the 14-bit field never carries).
       const uint32_t id_s = idesc_bf16(128, 128, false, false);
       const uint32_t id_dq = idesc_bf16(128, D, false, true);
-      auto next_kt = [&](int from) {
-        int kt = from;
-        while (kt < kt_end && !tile_pair_visible(p, qt, kt)) ++kt;
-        return kt;
-      };
-      auto issue_s = [&](int n) {   // S = Q K_n^T
-        const uint32_t kb = s_base + Q::OFF_K + (n % KS) * C::TILE_BYTES;
+      // the upper descriptor word (stride offset, version, swizzle) is the
+      // same for every operand here; only the lower word moves
+      constexpr uint32_t SLOT = C::TILE_BYTES >> 4;
+      const uint32_t hi = (uint32_t)(sdesc_sw128(0, 16, 1024) >> 32);
+      const uint32_t d_q = (uint32_t)sdesc_sw128(s_base, 16, 1024);
+      const uint32_t d_do = (uint32_t)sdesc_sw128(s_base + Q::OFF_DO, 16, 1024);
+      const uint32_t d_k = (uint32_t)sdesc_sw128(s_base + Q::OFF_K, 16, 1024);               // K-major (S)
+      const uint32_t d_kmn = (uint32_t)sdesc_sw128(s_base + Q::OFF_K, C::BOX_BYTES, 1024);   // MN-major (dQ)
+      const uint32_t d_v = (uint32_t)sdesc_sw128(s_base + Q::OFF_V, 16, 1024);
+      auto desc = [&](uint32_t lo) { return ((uint64_t)hi << 32) | lo; };
+      auto kstep = [](int kk) { return (uint32_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4); };
+      auto issue_s = [&](int slot) {   // S = Q K^T
+        const uint32_t kd = d_k + (uint32_t)slot * SLOT;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-          mma_ss(tmem + T_S, sdesc_sw128(s_base + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), id_s, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + T_S, desc(d_q + kstep(kk)), desc(kd + kstep(kk)), id_s, kk > 0);
         mma_commit(bar_s);
       };
-      auto issue_dp = [&](int n) {  // dP = dO V_n^T; the V slot is free once it completes
-        const uint32_t vb = s_base + Q::OFF_V + (n % VS) * C::TILE_BYTES;
+      auto issue_dp = [&](int slot) {  // dP = dO V^T; the V slot is free once it completes
+        const uint32_t vd = d_v + (uint32_t)slot * SLOT;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-          mma_ss(tmem + T_DP, sdesc_sw128(s_base + Q::OFF_DO + off, 16, 1024), sdesc_sw128(vb + off, 16, 1024), id_s,
-                 kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + T_DP, desc(d_do + kstep(kk)), desc(vd + kstep(kk)), id_s, kk > 0);
         mma_commit(bar_dp);
-        mma_commit(bar_vfree(n % VS));
+        mma_commit(bar_vfree(slot));
       };
+      int nvis = 0;
+      for (int kt = 0; kt < kt_end; ++kt) nvis += tile_pair_visible(p, qt, kt) ? 1 : 0;
+      // ring positions: K_{j+1} / V_{j+1} (next S / dP) and K_j (dQ)
+      int ks = 0, kpar = 0, vs = 0, vpar = 0, kq = 0;
       bool ok = wait_bar(bar_qdo, 0, wc);
-      int kt = next_kt(0);
-      int j = 0;
-      if (ok && kt < kt_end) {
+      if (ok && nvis > 0) {
         ok = wait_bar(bar_k(0), 0, wc);
         if (ok) {
           tc_fence_after();
@@ -555,39 +590,45 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tc_fence_after();
           issue_dp(0);
         }
+        ks = vs = 1;
       }
-      while (ok && kt < kt_end) {
-        const int kt_next = next_kt(kt + 1);
-        if (kt_next < kt_end) {
+      for (int j = 0; ok && j < nvis; ++j) {
+        const uint32_t par = (uint32_t)j & 1u;
+        if (j + 1 < nvis) {
           // S_{j+1} once S_j has been read out of TMEM
-          if (!(ok = wait_bar(bar_k((j + 1) % KS), ((j + 1) / KS) & 1, wc) && wait_bar(bar_sfree, j & 1, wc))) break;
+          if (!(ok = wait_bar(bar_k(ks), kpar, wc) && wait_bar(bar_sfree, par, wc))) break;
           tc_fence_after();
-          issue_s(j + 1);
+          issue_s(ks);
+          if (++ks == KS) { ks = 0; kpar ^= 1; }
+          // dP_{j+1} as soon as dP_j has been read out of TMEM
+          if (!(ok = wait_bar(bar_v(vs), vpar, wc) && wait_bar(bar_dpread, par, wc))) break;
+          tc_fence_after();
+          issue_dp(vs);
+          if (++vs == VS) { vs = 0; vpar ^= 1; }
         }
         // dQ_j += dS_j K_j   (K_j as an MN-major operand: N = d, K = keys)
-        if (!(ok = wait_bar(bar_ds, j & 1, wc))) break;
+        if (!(ok = wait_bar(bar_ds(j), ((uint32_t)j >> 1) & 1u, wc))) break;
         tc_fence_after();
-        const uint32_t kb = s_base + Q::OFF_K + (j % KS) * C::TILE_BYTES;
+        const uint32_t kd = d_kmn + (uint32_t)kq * SLOT;
+        const uint32_t ds = tmem + T_DS + (par << 6);
 #pragma unroll
         for (int kk = 0; kk < TILE / 16; ++kk)
-          mma_ts(tmem + T_DQ, tmem + T_DS + kk * 8, sdesc_sw128(kb + kk * 2048, C::BOX_BYTES, 1024), id_dq,
-                 (j > 0 || kk > 0));
-        mma_commit(bar_dq);
-        mma_commit(bar_kfree(j % KS));
-        if (kt_next < kt_end) {
-          // dP_{j+1}: dP_j has been read (dS_j written) already
-          if (!(ok = wait_bar(bar_v((j + 1) % VS), ((j + 1) / VS) & 1, wc))) break;
-          tc_fence_after();
-          issue_dp(j + 1);
-        }
-        kt = kt_next;
-        ++j;
+          mma_ts(tmem + T_DQ, ds + kk * 8, desc(kd + (uint32_t)kk * (2048 >> 4)), id_dq, (j > 0 || kk > 0));
+        mma_commit(bar_dq(j));
+        mma_commit(bar_kfree(kq));
+        if (++kq == KS) kq = 0;
       }
       mma_commit(bar_done);
       wait_bar(bar_done, 0, wc, false);
     }
-  } else if (warp >= 4) {
+   }
+  } else {
+    reg_alloc<C::REGS_ELEM>();
     // ------------------------------------------------------------ elementwise
+    // warpgroup hf (0: warps 4-7, 1: warps 8-11) owns key columns
+    // [64*hf, 64*hf + 64) of every query row
+    const int hf = (warp - 4) >> 2;
+    const int cb = 64 * hf;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;                   // query row inside the tile
     const int qrow = qt * TILE + r;
@@ -608,15 +649,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const bool edge = (kt == nkt - 1 && (p.N % TILE) != 0) || (causal && kt == qt);
       int lim = p.N - kt * TILE;
       if (causal && kt == qt) lim = min(lim, r + 1);
-      float pr[128];
+      float pr[64];
       {
-        uint32_t sr[128];
-        tmem_ld128(tmem + lane_off + T_S, sr);
+        uint32_t sr[64];
+        tmem_ld64(tmem + lane_off + T_S + cb, sr);
         // S has been read: the next S MMA may overwrite it while P is computed
         tc_fence_before();
         mbar_arrive(bar_sfree);
 #pragma unroll
-        for (int col = 0; col < 128; col += 2) {
+        for (int col = 0; col < 64; col += 2) {
           float x0, x1;
           fma2(x0, x1, __uint_as_float(sr[col]), __uint_as_float(sr[col + 1]), c, c, -l2, -l2);
           pr[col] = ex2(x0);
@@ -624,42 +665,48 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
         if (edge) {
 #pragma unroll
-          for (int col = 0; col < 128; ++col) pr[col] = (col < lim) ? pr[col] : 0.f;
+          for (int col = 0; col < 64; ++col) pr[col] = (cb + col < lim) ? pr[col] : 0.f;
         }
       }
-      ok = wait_bar(bar_dp, j & 1, wc) && (j == 0 || wait_bar(bar_dq, (j - 1) & 1, wc));
+      // dS_j reuses the buffer of dS_{j-2}: dQ_{j-2} must have read it
+      ok = wait_bar(bar_dp, j & 1, wc) && (j < 2 || wait_bar(bar_dq(j), ((j >> 1) - 1) & 1, wc));
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
+      {
         uint32_t dpr[64];
-        tmem_ld64(tmem + lane_off + T_DP + hh * 64, dpr);
+        tmem_ld64(tmem + lane_off + T_DP + cb, dpr);
+        // dP has been read: the next dP MMA may overwrite it while dS is computed
+        tc_fence_before();
+        mbar_arrive(bar_dpread);
         uint32_t pk[32];
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
-          const int col = hh * 64 + 2 * jj;
           // dS = P * (dP - D) = P*dP + (-P*D)
           float a0, a1, d0, d1;
-          fma2(a0, a1, pr[col], pr[col + 1], -dr, -dr, 0.f, 0.f);
-          fma2(d0, d1, pr[col], pr[col + 1], __uint_as_float(dpr[2 * jj]), __uint_as_float(dpr[2 * jj + 1]), a0, a1);
+          fma2(a0, a1, pr[2 * jj], pr[2 * jj + 1], -dr, -dr, 0.f, 0.f);
+          fma2(d0, d1, pr[2 * jj], pr[2 * jj + 1], __uint_as_float(dpr[2 * jj]), __uint_as_float(dpr[2 * jj + 1]), a0,
+               a1);
           pk[jj] = pack_bf16_rn_int(d0, d1);
         }
-        tmem_st32(tmem + lane_off + T_DS + hh * 32, pk);
+        // key columns [64 hf, 64 hf + 64) packed into columns [32 hf, 32 hf + 32) of the buffer
+        tmem_st32(tmem + lane_off + T_DS + (j & 1) * 64 + hf * 32, pk);
       }
       tc_fence_before();
-      mbar_arrive(bar_ds);
+      mbar_arrive(bar_ds(j));
       ++j;
     }
     if (ok && !abort_flag) {
-      if (j > 0) ok = __all_sync(0xffffffffu, wait_bar(bar_dq, (j - 1) & 1, wc));
+      // dQ MMAs complete in issue order: the last one covers them all
+      if (j > 0) ok = __all_sync(0xffffffffu, wait_bar(bar_dq(j - 1), ((j - 1) >> 1) & 1, wc));
       if (ok) {
         tc_fence_after();
-        __nv_bfloat16* dq = static_cast<__nv_bfloat16*>(p.dq) + ((size_t)bh * p.N + qrow) * D;
+        // each warpgroup writes its half of the dQ row
+        __nv_bfloat16* dq = static_cast<__nv_bfloat16*>(p.dq) + ((size_t)bh * p.N + qrow) * D + hf * (D / 2);
 #pragma unroll
-        for (int q4 = 0; q4 < D / 32; ++q4) {
+        for (int q4 = 0; q4 < D / 64; ++q4) {
           uint32_t rq[32];
           if (j > 0) {
-            tmem_ld32(tmem + lane_off + T_DQ + q4 * 32, rq);
+            tmem_ld32(tmem + lane_off + T_DQ + hf * (D / 2) + q4 * 32, rq);
           } else {
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) rq[jj] = 0u;
@@ -690,7 +737,7 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(p.B * p.Hkv) * (unsigned)((p.N + TILE - 1) / TILE);
-  dkdv_kernel<D><<<grid, BwdCfg<D>::THREADS, smem, s>>>(tq, tk, tv, tdo, p);
+  dkdv_kernel<D><<<grid, BwdCfg<D>::SPLIT_THREADS, smem, s>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }
 
@@ -702,7 +749,7 @@ cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   cudaError_t e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(p.B * p.Hq) * (unsigned)((p.N + TILE - 1) / TILE);
-  dq_kernel<D><<<grid, BwdCfg<D>::THREADS, smem, s>>>(tq, tk, tv, tdo, p);
+  dq_kernel<D><<<grid, BwdCfg<D>::SPLIT_THREADS, smem, s>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }
 
