@@ -200,82 +200,80 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       // dP^T_{i+1} the dS^T_i columns dK_i reads; each is issued right after
       // that reader (tcgen05.mma from one thread execute in issue order).
       // Each elementwise phase has two MMAs of cover.
+      // tcgen05.mma issue stalls once a few MMAs are queued, so this thread
+      // is held for most of each group and anything it does between groups
+      // idles the tensor pipe: it keeps ring counters only, and descriptors
+      // are built once (a k-step adds a compile-time offset to the
+      // start-address field; shared-memory addresses stay below 256 KB, so
+      // the 14-bit field never carries).
       const uint32_t id_s = idesc_bf16(128, 128, false, false);
       const uint32_t id_acc = idesc_bf16(128, D, false, true);
-      // (h, qt) pairs in order; returns false past the end
-      auto advance = [&](int& h, int& qt) {
-        for (;;) {
-          ++qt;
-          if (qt >= nqt) {
-            ++h;
-            qt = qt_first;
-            if (h >= g) return false;
-          }
-          if (tile_pair_visible(p, qt, kt)) return true;
-        }
-      };
-      auto issue_st = [&](uint32_t st) {
+      constexpr uint32_t STAGE16 = STAGE >> 4, TILE16 = C::TILE_BYTES >> 4;
+      const uint32_t hi = (uint32_t)(sdesc_sw128(0, 16, 1024) >> 32);
+      const uint32_t d_k = (uint32_t)sdesc_sw128(s_base, 16, 1024);
+      const uint32_t d_v = (uint32_t)sdesc_sw128(s_base + OFF_V, 16, 1024);
+      const uint32_t d_ring = (uint32_t)sdesc_sw128(s_base + OFF_RING, 16, 1024);              // K-major
+      const uint32_t d_ring_mn = (uint32_t)sdesc_sw128(s_base + OFF_RING, C::BOX_BYTES, 1024);  // MN-major
+      auto desc = [&](uint32_t lo) { return ((uint64_t)hi << 32) | lo; };
+      auto kstep = [](int kk) { return (uint32_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4); };
+      auto issue_st = [&](int slot) {   // S^T = K Q^T
+        const uint32_t qd = d_ring + (uint32_t)slot * STAGE16;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-          mma_ss(tmem + 0, sdesc_sw128(s_base + off, 16, 1024), sdesc_sw128(st + off, 16, 1024), id_s, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + 0, desc(d_k + kstep(kk)), desc(qd + kstep(kk)), id_s, kk > 0);
         mma_commit(bar_s);
       };
-      auto issue_dpt = [&](uint32_t st) {
+      auto issue_dpt = [&](int slot) {  // dP^T = V dO^T
+        const uint32_t dd = d_ring + (uint32_t)slot * STAGE16 + TILE16;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-          mma_ss(tmem + 128, sdesc_sw128(s_base + OFF_V + off, 16, 1024),
-                 sdesc_sw128(st + C::TILE_BYTES + off, 16, 1024), id_s, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + 128, desc(d_v + kstep(kk)), desc(dd + kstep(kk)), id_s, kk > 0);
         mma_commit(bar_dp);
       };
+      int nvis = 0;
+      for (int qt = qt_first; qt < nqt; ++qt) nvis += tile_pair_visible(p, qt, kt) ? 1 : 0;
+      const int ntile = nvis * g;   // (query head, query tile) pairs, in the producer's order
       bool ok = wait_bar(bar_kv, 0, wc);
-      int h = 0, qt = qt_first - 1;
-      bool have = ok && advance(h, qt);
-      if (have) {
+      if (ok && ntile > 0) {
         ok = wait_bar(bar_q(0), 0, wc);
         if (ok) {
           tc_fence_after();
-          issue_st(s_base + OFF_RING);
-          issue_dpt(s_base + OFF_RING);
+          issue_st(0);
+          issue_dpt(0);
         }
       }
-      int i = 0;
-      while (ok && have) {
-        const int s = i % NS, sn = (i + 1) % NS;
-        const uint32_t st = s_base + OFF_RING + s * STAGE;
-        const uint32_t stn = s_base + OFF_RING + sn * STAGE;
-        int h2 = h, qt2 = qt;
-        const bool more = advance(h2, qt2);
+      int s = 0;
+      uint32_t spar = 0;   // ring slot of tile i and the parity of its fill
+      for (int i = 0; ok && i < ntile; ++i) {
+        const bool more = i + 1 < ntile;
+        const int sn = (s + 1 == NS) ? 0 : s + 1;
+        const uint32_t snpar = (s + 1 == NS) ? spar ^ 1u : spar;
+        const uint32_t par = (uint32_t)i & 1u;
+        const uint32_t md = d_ring_mn + (uint32_t)s * STAGE16;
         // dV += P^T dO   (dO as an MN-major operand: N = d, K = query rows)
-        if (!(ok = wait_bar(bar_p, i & 1, wc))) break;
+        if (!(ok = wait_bar(bar_p, par, wc))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < TILE / 16; ++kk)
-          mma_ts(tmem + 256, tmem + half_col(kk), sdesc_sw128(st + C::TILE_BYTES + kk * 2048, C::BOX_BYTES, 1024),
-                 id_acc, (i > 0 || kk > 0));
+          mma_ts(tmem + 256, tmem + half_col(kk), desc(md + TILE16 + (uint32_t)kk * (2048 >> 4)), id_acc,
+                 (i > 0 || kk > 0));
         mma_commit(bar_dv);
         if (more) {
-          if (!(ok = wait_bar(bar_q(sn), ((i + 1) / NS) & 1, wc))) break;
+          if (!(ok = wait_bar(bar_q(sn), snpar, wc))) break;
           tc_fence_after();
-          issue_st(stn);
+          issue_st(sn);
         }
         // dK += dS^T Q
-        if (!(ok = wait_bar(bar_ds, i & 1, wc))) break;
+        if (!(ok = wait_bar(bar_ds, par, wc))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < TILE / 16; ++kk)
-          mma_ts(tmem + 256 + D, tmem + 128 + half_col(kk), sdesc_sw128(st + kk * 2048, C::BOX_BYTES, 1024), id_acc,
+          mma_ts(tmem + 256 + D, tmem + 128 + half_col(kk), desc(md + (uint32_t)kk * (2048 >> 4)), id_acc,
                  (i > 0 || kk > 0));
         mma_commit(bar_dk);
         mma_commit(bar_qfree(s));
-        if (more) issue_dpt(stn);
-        h = h2;
-        qt = qt2;
-        have = more;
-        ++i;
+        if (more) issue_dpt(sn);
+        s = sn;
+        spar = snpar;
       }
       mma_commit(bar_done);
       wait_bar(bar_done, 0, wc, false);
