@@ -168,75 +168,94 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     // PV_t(n) that reads them, and tcgen05.mma from one thread execute in
     // issue order.  Each softmax thus has two MMAs of cover (PV of the other
     // tile and its S) before its own PV is needed.
+    // tcgen05.mma issue stalls once a few MMAs are queued, so this thread is
+    // held for most of each group and anything it does between groups idles
+    // the tensor pipe: it keeps ring counters only, and descriptors are built
+    // once (a k-step adds a compile-time offset to the start-address field;
+    // shared-memory addresses stay below 256 KB, so the 14-bit field never
+    // carries).
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16(128, 128, false, false);
       const uint32_t id_pv = idesc_bf16(128, D, false, true);
+      constexpr uint32_t TILE16 = C::TILE_BYTES >> 4;
+      const uint32_t hi = (uint32_t)(sdesc_sw128(0, 16, 1024) >> 32);
+      const uint32_t d_q = (uint32_t)sdesc_sw128(s_base, 16, 1024);
+      const uint32_t d_k = (uint32_t)sdesc_sw128(s_base + C::OFF_K, 16, 1024);
+      const uint32_t d_vmn = (uint32_t)sdesc_sw128(s_base + C::OFF_V, C::BOX_BYTES, 1024);
+      auto desc = [&](uint32_t lo) { return ((uint64_t)hi << 32) | lo; };
+      auto kstep = [](int kk) { return (uint32_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4); };
       auto next_kt = [&](int from) {
         int k = from;
         while (k < u.kt_end && !unit_uses(u, k)) ++k;
         return k;
       };
-      auto issue_s = [&](int t, int stage) {
-        const uint32_t kb = s_base + C::OFF_K + stage * C::TILE_BYTES;
-        const uint32_t qb = s_base + t * C::TILE_BYTES;
+      auto issue_s = [&](int t, int slot) {
+        const uint32_t kd = d_k + (uint32_t)slot * TILE16;
+        const uint32_t qd = d_q + (uint32_t)t * TILE16;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-          mma_ss(tmem + t * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), id_s, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + t * 128, desc(qd + kstep(kk)), desc(kd + kstep(kk)), id_s, kk > 0);
         mma_commit(bar_s(t));
       };
-      auto issue_pv = [&](int t, int stage, bool acc) {
-        const uint32_t vb = s_base + C::OFF_V + stage * C::TILE_BYTES;
+      auto issue_pv = [&](int t, int slot, bool acc) {
+        const uint32_t vd = d_vmn + (uint32_t)slot * TILE16;
 #pragma unroll
         for (int kk = 0; kk < TILE / 16; ++kk)
-          mma_ts(tmem + C::TMEM_O + t * D, tmem + t * 128 + kk * 8, sdesc_sw128(vb + kk * 2048, C::BOX_BYTES, 1024),
-                 id_pv, (acc || kk > 0));
+          mma_ts(tmem + C::TMEM_O + t * D, tmem + t * 128 + kk * 8, desc(vd + (uint32_t)kk * (2048 >> 4)), id_pv,
+                 (acc || kk > 0));
         mma_commit(bar_o(t));
       };
-      int it[2] = {0, 0};
+      int it0 = 0, it1 = 0;   // PV MMAs issued per tile
       bool ok = wait_bar(bar_q, 0, wc);
       int kt = next_kt(0);
-      if (ok && kt < u.kt_end) {
-        const uint32_t use0 = unit_uses(u, kt);
+      uint32_t use = kt < u.kt_end ? unit_uses(u, kt) : 0u;
+      if (ok && use) {
         ok = wait_bar(bar_k(0), 0, wc);
         if (ok) {
           tc_fence_after();
-          for (int t = 0; t < 2; ++t)
-            if (use0 & (1u << t)) issue_s(t, 0);
+          if (use & 1u) issue_s(0, 0);
+          if (use & 2u) issue_s(1, 0);
           mma_commit(bar_kfree(0));
         }
       }
-      int n = 0;
-      while (ok && kt < u.kt_end) {
-        const uint32_t use = unit_uses(u, kt);
-        const int s = n % NS, sn = (n + 1) % NS;
-        const uint32_t ph = (n / NS) & 1, phn = ((n + 1) / NS) & 1;
+      int s = 0;
+      uint32_t ph = 0;   // ring slot of key tile n and the parity of its fill
+      while (ok && use) {
+        const int sn = (s + 1 == NS) ? 0 : s + 1;
+        const uint32_t phn = (s + 1 == NS) ? ph ^ 1u : ph;
         const int ktn = next_kt(kt + 1);
         const uint32_t usen = ktn < u.kt_end ? unit_uses(u, ktn) : 0u;
         bool kwaited = false;
         if (!(ok = wait_bar(bar_v(s), ph, wc))) break;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (use & (1u << t)) {
-            if (!(ok = wait_bar(bar_p(t), it[t] & 1, wc))) break;
-            tc_fence_after();
-            issue_pv(t, s, it[t] > 0);
-            ++it[t];
-          }
-          if (t == 1) mma_commit(bar_vfree(s));   // both PV MMAs of this key tile issued
-          if (usen & (1u << t)) {
-            if (!kwaited) {
-              if (!(ok = wait_bar(bar_k(sn), phn, wc))) break;
-              tc_fence_after();
-              kwaited = true;
-            }
-            issue_s(t, sn);
-          }
+        if (use & 1u) {
+          if (!(ok = wait_bar(bar_p(0), (uint32_t)it0 & 1u, wc))) break;
+          tc_fence_after();
+          issue_pv(0, s, it0 > 0);
+          ++it0;
         }
-        if (!ok) break;
+        if (usen & 1u) {
+          if (!(ok = wait_bar(bar_k(sn), phn, wc))) break;
+          tc_fence_after();
+          kwaited = true;
+          issue_s(0, sn);
+        }
+        if (use & 2u) {
+          if (!(ok = wait_bar(bar_p(1), (uint32_t)it1 & 1u, wc))) break;
+          tc_fence_after();
+          issue_pv(1, s, it1 > 0);
+          ++it1;
+        }
+        mma_commit(bar_vfree(s));   // both PV MMAs of this key tile issued
+        if (usen & 2u) {
+          if (!kwaited && !(ok = wait_bar(bar_k(sn), phn, wc))) break;
+          tc_fence_after();
+          issue_s(1, sn);
+        }
         if (usen) mma_commit(bar_kfree(sn));
         kt = ktn;
-        ++n;
+        use = usen;
+        s = sn;
+        ph = phn;
       }
       // every commit above lands before the CTA leaves
       mma_commit(bar_done);
