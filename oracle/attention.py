@@ -23,7 +23,11 @@ Readings where the pages are silent (each listed in the design doc):
   ``h // (Hq // Hkv)``, and dK/dV sum over the query heads of a group;
 * block-sparse: a kept ``block x block`` block is dense, a dropped one is
   masked out entirely (FlashAttention abstract; BurstAttention author
-  responses: sparse attention only changes the mask matrix).
+  responses: sparse attention only changes the mask matrix);
+* sliding window of width ``w`` (the local attention the FlashAttention-2
+  reviews mention for Mistral): key ``j`` is visible to query ``i`` iff
+  ``0 <= (q_offset + i) - (kv_offset + j) < w``, i.e. the causal rule plus
+  the ``w`` most recent positions, the query's own included.
 """
 from __future__ import annotations
 
@@ -39,23 +43,28 @@ ROW_BLOCK = 1024  # query rows per block when a head is processed in pieces
 class MaskSpec:
     """Which keys a query may see.
 
-    kind: ``"none"``, ``"causal"`` or ``"block_sparse"``.
+    kind: ``"none"``, ``"causal"``, ``"block_sparse"`` or ``"sliding_window"``.
     block_mask: for ``block_sparse``, a boolean ``[ceil(Nq/block), ceil(Nk/block)]``
         array shared by every batch and head; ``True`` keeps the block.
     causal_in_blocks: for ``block_sparse``, additionally apply the element
         causal rule inside kept blocks.
+    window: for ``sliding_window``, how many positions a query looks back,
+        its own included (``>= 1``).
     """
 
     kind: str = "none"
     block_mask: Optional[np.ndarray] = None
     block: int = 128
     causal_in_blocks: bool = False
+    window: int = 0
 
     def __post_init__(self):
-        if self.kind not in ("none", "causal", "block_sparse"):
+        if self.kind not in ("none", "causal", "block_sparse", "sliding_window"):
             raise ValueError(f"unknown mask kind {self.kind!r}")
         if self.kind == "block_sparse" and self.block_mask is None:
             raise ValueError("block_sparse needs a block_mask")
+        if self.kind == "sliding_window" and self.window < 1:
+            raise ValueError("sliding_window needs window >= 1")
 
 
 def visible(rows: np.ndarray, nk: int, mask: MaskSpec,
@@ -68,9 +77,12 @@ def visible(rows: np.ndarray, nk: int, mask: MaskSpec,
     rows = np.asarray(rows, dtype=np.int64)
     cols = np.arange(nk, dtype=np.int64)
     vis = np.ones((rows.size, nk), dtype=bool)
-    causal = mask.kind == "causal" or (mask.kind == "block_sparse" and mask.causal_in_blocks)
+    causal = mask.kind in ("causal", "sliding_window") or (mask.kind == "block_sparse" and mask.causal_in_blocks)
+    back = (q_offset + rows)[:, None] - (kv_offset + cols)[None, :]   # how far key j lies behind query i
     if causal:
-        vis &= (kv_offset + cols)[None, :] <= (q_offset + rows)[:, None]
+        vis &= back >= 0
+    if mask.kind == "sliding_window":
+        vis &= back < mask.window
     if mask.kind == "block_sparse":
         bm = np.asarray(mask.block_mask, dtype=bool)
         vis &= bm[(rows // mask.block)[:, None], (cols // mask.block)[None, :]]

@@ -50,7 +50,7 @@ def kv_tile_range_causal(r_first: int, r_last: int, nk: int,
 
 
 def _tile_kv_set(t_row: int, nq: int, nk: int, kind: str, q_offset: int,
-                 kv_offset: int, block_mask, causal_in_blocks: bool):
+                 kv_offset: int, block_mask, causal_in_blocks: bool, window: int = 0):
     """Set of key tiles visible to query tile ``t_row`` (row-block index)."""
     nkt = _cdiv(nk, TILE)
     r0 = t_row * TILE
@@ -59,6 +59,12 @@ def _tile_kv_set(t_row: int, nq: int, nk: int, kind: str, q_offset: int,
     r1 = min(nq, r0 + TILE) - 1
     if kind == "none":
         return set(range(nkt))
+    if kind == "sliding_window":
+        # brute force over the tile's rows and every key: a key tile counts
+        # when any of its keys lies 0..window-1 positions behind any row
+        back = (q_offset + np.arange(r0, r1 + 1))[:, None] - (kv_offset + np.arange(nk))[None, :]
+        seen = ((back >= 0) & (back < window)).any(axis=0)
+        return {kt for kt in range(nkt) if seen[kt * TILE:(kt + 1) * TILE].any()}
     lim = kv_tile_range_causal(r0, r1, nk, q_offset, kv_offset)
     if kind == "causal":
         return set(range(lim))
@@ -80,7 +86,8 @@ def head_group(B: int, Hq: int, Hkv: int, nk: int, d: int) -> int:
 
 def fwd_work_units(kind: str, B: int, Hq: int, nq: int, nk: int,
                    q_offset: int = 0, kv_offset: int = 0, block_mask=None,
-                   causal_in_blocks: bool = False, Hkv: int = None, d: int = 128):
+                   causal_in_blocks: bool = False, Hkv: int = None, d: int = 128,
+                   window: int = 0):
     """Forward work units in launch order: list of ``(bh, qchunk, n_kv_tiles)``."""
     Hkv = Hq if Hkv is None else Hkv
     bh_n = B * Hq
@@ -97,7 +104,7 @@ def fwd_work_units(kind: str, B: int, Hq: int, nq: int, nk: int,
         kv = set()
         for t in range(2):
             kv |= _tile_kv_set(2 * qc + t, nq, nk, kind, q_offset, kv_offset,
-                               block_mask, causal_in_blocks)
+                               block_mask, causal_in_blocks, window)
         out.append((bh, qc, len(kv)))
     return out
 

@@ -4,7 +4,8 @@ Closed forms (Q = 0, constant V, one dominant logit, a single key), hand-worked
 golden fixtures, central finite differences, a library softmax and PyTorch's
 float64 scaled-dot-product attention with autograd, and invariants (chunked
 merge == monolithic, GQA == repeated MHA, all-ones block mask == dense,
-block-triangular + causal == causal).  ``test_planted_mistakes`` shows that a
+block-triangular + causal == causal, a window wider than the sequence ==
+causal, a window of one == identity).  ``test_planted_mistakes`` shows that a
 plausible slip in the oracle (a dropped term, a sign, an off-by-one, a
 transposed operand, a missing merge weight) fails at least one pin.
 """
@@ -331,6 +332,95 @@ def test_sampled_rows_match_full():
     np.testing.assert_allclose(dqg[0], dq[1, 2:4], atol=1e-14)
 
 
+# ---------------------------------------------------------------- sliding window
+
+def _window_visible_loops(nq, nk, w, qo=0, ko=0):
+    """Visibility written out element by element: key j lies 0..w-1 positions
+    behind query i (global positions)."""
+    vis = np.zeros((nq, nk), bool)
+    for i in range(nq):
+        for j in range(nk):
+            back = (qo + i) - (ko + j)
+            vis[i, j] = 0 <= back < w
+    return vis
+
+
+def test_sliding_window_q_zero_gives_mean_of_window():
+    for nq, nk, qo, ko, w in [(9, 9, 0, 0, 1), (9, 9, 0, 0, 3), (7, 11, 4, 0, 5), (8, 6, 0, 3, 2), (6, 9, 9, 1, 4)]:
+        q = np.zeros((1, 1, nq, 3))
+        k, v = rnd(1, 1, nk, 3), rnd(1, 1, nk, 3)
+        o, lse = oracle.attention_forward(q, k, v, 0.4, MaskSpec("sliding_window", window=w), qo, ko)
+        vis = _window_visible_loops(nq, nk, w, qo, ko)
+        for i in range(nq):
+            js = np.flatnonzero(vis[i])
+            if js.size == 0:
+                assert np.all(o[0, 0, i] == 0) and lse[0, 0, i] == -np.inf
+            else:
+                np.testing.assert_allclose(o[0, 0, i], v[0, 0, js].mean(axis=0), rtol=0, atol=1e-13)
+                assert abs(lse[0, 0, i] - np.log(js.size)) < 1e-13
+
+
+def test_sliding_window_of_one_is_identity():
+    q, k, v = rnd(2, 3, 10, 8), rnd(2, 3, 10, 8), rnd(2, 3, 10, 8)
+    o, lse = oracle.attention_forward(q, k, v, 0.3, MaskSpec("sliding_window", window=1))
+    np.testing.assert_allclose(o, v, atol=1e-15)
+    np.testing.assert_allclose(lse, 0.3 * (q * k).sum(-1), atol=1e-14)
+
+
+def test_wide_sliding_window_equals_causal():
+    q, k, v, do = rnd(1, 4, 13, 5), rnd(1, 2, 13, 5), rnd(1, 2, 13, 5), rnd(1, 4, 13, 5)
+    for w in (13, 14, 100):
+        a = oracle.attention_forward(q, k, v, 0.5, MaskSpec("sliding_window", window=w))
+        b = oracle.attention_forward(q, k, v, 0.5, MaskSpec("causal"))
+        np.testing.assert_allclose(a[0], b[0], atol=1e-15)
+        np.testing.assert_allclose(a[1], b[1], atol=1e-15)
+        for x, y in zip(oracle.attention_backward(q, k, v, do, 0.5, MaskSpec("sliding_window", window=w)),
+                        oracle.attention_backward(q, k, v, do, 0.5, MaskSpec("causal"))):
+            np.testing.assert_allclose(x, y, atol=1e-14)
+
+
+def test_sliding_window_torch_sdpa_with_explicit_mask():
+    """PyTorch's float64 attention with the boolean mask written out by loops."""
+    F = torch.nn.functional
+    for nq, w, hq, hkv in [(20, 1, 2, 2), (20, 5, 4, 2), (24, 7, 2, 1), (17, 30, 2, 2)]:
+        q, k, v, do = rnd(1, hq, nq, 8), rnd(1, hkv, nq, 8), rnd(1, hkv, nq, 8), rnd(1, hq, nq, 8)
+        mask = MaskSpec("sliding_window", window=w)
+        o, _ = oracle.attention_forward(q, k, v, 0.35, mask)
+        dq, dk, dv = oracle.attention_backward(q, k, v, do, 0.35, mask)
+        tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+        g = hq // hkv
+        am = torch.tensor(_window_visible_loops(nq, nq, w))
+        to = F.scaled_dot_product_attention(tq, tk.repeat_interleave(g, 1), tv.repeat_interleave(g, 1),
+                                            attn_mask=am, scale=0.35)
+        to.backward(torch.tensor(do))
+        np.testing.assert_allclose(o, to.detach().numpy(), atol=1e-12)
+        np.testing.assert_allclose(dq, tq.grad.numpy(), atol=1e-11)
+        np.testing.assert_allclose(dk, tk.grad.numpy(), atol=1e-11)
+        np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-11)
+
+
+@pytest.mark.parametrize("w,qo,ko", [(1, 0, 0), (3, 0, 0), (4, 5, 2), (9, 0, 0)])
+def test_finite_difference_gradients_sliding_window(w, qo, ko):
+    fd_check(oracle.attention_forward, oracle.attention_backward, MaskSpec("sliding_window", window=w),
+             qo=qo, ko=ko, nq=7, nk=8)
+
+
+def test_sliding_window_chunked_merge_equals_monolithic():
+    n, d, w = 48, 8, 11
+    mask = MaskSpec("sliding_window", window=w)
+    q, k, v = rnd(1, 2, n, d), rnd(1, 1, n, d), rnd(1, 1, n, d)
+    full_o, full_l = oracle.attention_forward(q, k, v, 0.3, mask)
+    for nc in (2, 3, 4, 6, 8, 16):
+        c = n // nc
+        for qc in range(nc):
+            qs = slice(qc * c, (qc + 1) * c)
+            parts = [oracle.attention_forward(q[:, :, qs], k[:, :, kc * c:(kc + 1) * c], v[:, :, kc * c:(kc + 1) * c],
+                                              0.3, mask, qc * c, kc * c) for kc in range(qc + 1)]
+            o, l = oracle.merge_partials([p[0] for p in parts], [p[1] for p in parts])
+            np.testing.assert_allclose(o, full_o[:, :, qs], atol=1e-12)
+            np.testing.assert_allclose(l, full_l[:, :, qs], atol=1e-12)
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def _fails(fn):
@@ -387,6 +477,16 @@ def test_planted_mistakes(monkeypatch):
 
     monkeypatch.setattr(oa, "visible", vis_off_by_one)
     assert _fails(test_q_zero_gives_mean_of_visible_rows)
+    monkeypatch.setattr(oa, "visible", good_vis)
+
+    def vis_window_one_too_wide(rows, nk, mask, q_offset=0, kv_offset=0):   # back <= w
+        if mask.kind != "sliding_window":
+            return good_vis(rows, nk, mask, q_offset, kv_offset)
+        return good_vis(rows, nk, MaskSpec("sliding_window", window=mask.window + 1), q_offset, kv_offset)
+
+    monkeypatch.setattr(oa, "visible", vis_window_one_too_wide)
+    assert _fails(test_sliding_window_q_zero_gives_mean_of_window)
+    assert _fails(test_sliding_window_of_one_is_identity)
     monkeypatch.setattr(oa, "visible", good_vis)
 
     monkeypatch.setattr(oa, "head_forward", fwd_no_scale_in_lse)
