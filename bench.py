@@ -40,6 +40,7 @@ sys.path.insert(0, ROOT)
 METRIC = "attention fwd+bwd TFLOP/s (bf16, causal-adjusted) and % of GB300 dense BF16 peak"
 WORKLOAD = dict(name="gpt_causal", B=2, Hq=32, Hkv=32, N=8192, d=128, mask="causal")
 CHUNKED = dict(name="chunked_gqa", B=1, Hq=32, Hkv=8, N=32768, d=128, chunks=8)
+WINDOW = dict(name="gpt_sliding_window", B=2, Hq=32, Hkv=32, N=8192, d=128, window=4096)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
     "fwd": ["fwd.cu", "ptx.cuh", "schedule.h", "internal.h"],
@@ -389,6 +390,7 @@ def main():
     if not args.no_extras:
         out["e2e"] = e2e_leg(api, inputs, torch, w, causal, rank)
         out["chunked_gqa"] = chunked_leg(api, inputs, torch, peaks, rank)
+        out["sliding_window"] = window_leg(api, inputs, torch, peaks, rank)
         if rank == 0:
             out["cpu_baseline"] = {k_: v_ for k_, v_ in oracle_sample(args.cpu_seconds).items()
                                    if k_ in ("value", "unit", "cores", "kind", "sample")}
@@ -476,6 +478,45 @@ def chunked_leg(api, inputs, torch, peaks, rank, reps=3):
                 partial_fwd_ms=part_ms, partial_fwd_tflops=flops / (part_ms * 1e-3) / 1e12,
                 merge_ms=merge_ms, merge_bytes=merge_bytes, merge_gbs=gbs, merge_frac_of_hbm=gbs / peaks["hbm_gbs"],
                 chunked_vs_monolithic=agree)
+
+
+def window_pairs(N, w):
+    """Visible (query, key) pairs of a sliding window of width w over N positions:
+    row i sees min(i + 1, w) keys."""
+    w = min(w, N)
+    return w * (w + 1) // 2 + (N - w) * w
+
+
+def window_leg(api, inputs, torch, peaks, rank, reps=5):
+    """Sliding-window (local causal) attention at the GPT shape: B=2, H=32,
+    N=8192, d=128, each query sees itself and the 4095 positions before it.
+    FLOPs count the visible pairs: fwd 4*d per pair and head, bwd 2.5x that."""
+    c = WINDOW
+    B, Hq, Hkv, N, d, wnd = c["B"], c["Hq"], c["Hkv"], c["N"], c["d"], c["window"]
+    q, k, v, do = (t.cuda() for t in inputs.make_qkvdo(B, Hq, Hkv, N, N, d, seed=inputs.SEED + 100 * rank + 5))
+    ws = torch.empty(api.bwd_workspace_bytes(B, Hq, Hkv, N, d), device="cuda", dtype=torch.uint8)
+
+    def run():
+        o, lse = api.attn_fwd(q, k, v, window=wnd)
+        api.attn_bwd(q, k, v, o, lse, do, window=wnd, workspace=ws)
+
+    run()
+    torch.cuda.synchronize()
+    api.trace_enable(16 * reps)
+    for _ in range(reps):
+        run()
+    torch.cuda.synchronize()
+    api.trace_disable()
+    recs, _ = api.trace_read(16 * reps)
+    fwd_ms = sum(ms for n, ms in recs if n == "fwd") / reps
+    bwd_ms = sum(ms for n, ms in recs if n.startswith("bwd_")) / reps
+    f_fwd = 4.0 * B * Hq * d * window_pairs(N, wnd)
+    return dict(workload=f"B={B} Hq={Hq} Hkv={Hkv} N={N} d={d} sliding window {wnd}",
+                visible_fraction_of_causal=window_pairs(N, wnd) / (N * (N + 1) / 2),
+                fwd_ms=fwd_ms, bwd_ms=bwd_ms, fwd_tflops=f_fwd / (fwd_ms * 1e-3) / 1e12,
+                bwd_tflops=2.5 * f_fwd / (bwd_ms * 1e-3) / 1e12,
+                step_tflops=3.5 * f_fwd / ((fwd_ms + bwd_ms) * 1e-3) / 1e12,
+                fwd_frac_of_burst_peak=f_fwd / (fwd_ms * 1e-3) / 1e12 / peaks["bf16_tflops"])
 
 
 if __name__ == "__main__":

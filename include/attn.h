@@ -56,7 +56,8 @@ typedef enum {
 typedef enum {
   ATTN_MASK_NONE = 0,
   ATTN_MASK_CAUSAL = 1,
-  ATTN_MASK_BLOCK_SPARSE = 2
+  ATTN_MASK_BLOCK_SPARSE = 2,
+  ATTN_MASK_SLIDING_WINDOW = 3
 } attn_mask_kind_t;
 
 typedef enum { ATTN_DTYPE_BF16 = 0, ATTN_DTYPE_F32 = 1 } attn_dtype_t;
@@ -77,13 +78,20 @@ typedef enum { ATTN_DTYPE_BF16 = 0, ATTN_DTYPE_F32 = 1 } attn_dtype_t;
  *     FlashAttention; BurstAttention author responses: sparse attention only
  *     changes the attention mask matrix).  causal_in_blocks != 0 additionally
  *     applies the causal rule inside kept blocks.
+ *   kind = ATTN_MASK_SLIDING_WINDOW: local causal attention over the last
+ *     `window` positions, the query's own included: key j is visible to query
+ *     i iff 0 <= (q_offset + i) - (kv_offset + j) < window (window >= 1;
+ *     "FlashAttention-2" reviews: the sliding-window attention of Mistral).
+ *     Key tiles outside every row's window are skipped.
  * The descriptor is read during the call; block_mask must stay valid until the
- * launched work has completed.
+ * launched work has completed.  window is read only for
+ * ATTN_MASK_SLIDING_WINDOW.
  */
 typedef struct attn_mask {
   int32_t kind;
   int32_t causal_in_blocks;
   const uint8_t* block_mask;
+  int32_t window;
 } attn_mask_t;
 
 /*
@@ -209,12 +217,13 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
  * group the latest (heaviest) query chunk of every head comes first, then the
  * next, and so on (DISTFLASHATTN reviews, first review point 1: with causal
  * masking careless placement leaves processors idle).  host_block_mask is a
- * HOST copy of the block mask (only read for ATTN_MASK_BLOCK_SPARSE).  Writes
- * at most cap int32 values to out and the number of units to *n_out;
- * ATTN_ERR_INVALID_ARG if cap is too small (n_out still set).
+ * HOST copy of the block mask (only read for ATTN_MASK_BLOCK_SPARSE); window
+ * is read only for ATTN_MASK_SLIDING_WINDOW.  Writes at most cap int32 values
+ * to out and the number of units to *n_out; ATTN_ERR_INVALID_ARG if cap is
+ * too small (n_out still set).
  */
 int attn_build_schedule(int mask_kind, int causal_in_blocks,
-                        const uint8_t* host_block_mask, int B, int Hq, int Hkv,
+                        const uint8_t* host_block_mask, int window, int B, int Hq, int Hkv,
                         int Nq, int Nk, int d, int64_t q_offset, int64_t kv_offset,
                         int32_t* out, size_t cap, size_t* n_out);
 

@@ -24,10 +24,11 @@ KERNEL_NAMES = {1: "fwd", 2: "partial_fwd", 3: "merge", 4: "bwd_preprocess", 5: 
 
 
 class attn_mask_t(C.Structure):
-    _fields_ = [("kind", C.c_int32), ("causal_in_blocks", C.c_int32), ("block_mask", C.c_void_p)]
+    _fields_ = [("kind", C.c_int32), ("causal_in_blocks", C.c_int32), ("block_mask", C.c_void_p),
+                ("window", C.c_int32)]
 
 
-MASK_NONE, MASK_CAUSAL, MASK_BLOCK_SPARSE = 0, 1, 2
+MASK_NONE, MASK_CAUSAL, MASK_BLOCK_SPARSE, MASK_SLIDING_WINDOW = 0, 1, 2, 3
 DTYPE_BF16, DTYPE_F32 = 0, 1
 STATUS = {0: "ATTN_OK", -1: "ATTN_ERR_INVALID_ARG", -2: "ATTN_ERR_UNSUPPORTED", -3: "ATTN_ERR_MISALIGNED",
           -4: "ATTN_ERR_CUDA", -5: "ATTN_ERR_DEVICE_TIMEOUT", -6: "ATTN_ERR_WORKSPACE",
@@ -49,8 +50,8 @@ SIGNATURES = {
                                         c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float,
                                         C.POINTER(attn_mask_t), c_void_p]),
     "attn_bwd_workspace_bytes": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
-    "attn_build_schedule": (c_int, [c_int, c_int, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int64,
-                                    c_int64, C.POINTER(C.c_int32), c_size_t, C.POINTER(c_size_t)]),
+    "attn_build_schedule": (c_int, [c_int, c_int, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                    c_int64, c_int64, C.POINTER(C.c_int32), c_size_t, C.POINTER(c_size_t)]),
     "attn_build_chunk_schedule": (c_int, [c_int, c_int, C.POINTER(C.c_int32), c_size_t, C.POINTER(c_size_t)]),
     "attn_get_status": (c_int, [c_void_p]),
     "attn_set_wait_limit_ns": (None, [c_int64]),

@@ -47,8 +47,18 @@ def _contig(t: torch.Tensor, name: str, dtype=torch.bfloat16):
 
 
 def mask_desc(causal: bool = False, block_mask: Optional[torch.Tensor] = None,
-              causal_in_blocks: bool = False):
-    """Build the C mask descriptor; returns (descriptor or None, tensor to keep alive)."""
+              causal_in_blocks: bool = False, window: Optional[int] = None):
+    """Build the C mask descriptor; returns (descriptor or None, tensor to keep alive).
+
+    ``window`` selects the sliding-window mask: a query sees itself and the
+    ``window - 1`` positions before it (causal implied).
+    """
+    if window is not None:
+        if block_mask is not None:
+            raise ValueError("a sliding window and a block mask do not combine")
+        if int(window) < 1:
+            raise ValueError("window must be >= 1")
+        return attn_mask_t(_ffi.MASK_SLIDING_WINDOW, 0, None, int(window)), None
     if block_mask is not None:
         bm = block_mask
         if bm.dtype != torch.uint8:
@@ -56,10 +66,10 @@ def mask_desc(causal: bool = False, block_mask: Optional[torch.Tensor] = None,
         bm = bm.contiguous()
         if not bm.is_cuda:
             raise ValueError("block_mask must be on the GPU")
-        m = attn_mask_t(_ffi.MASK_BLOCK_SPARSE, 1 if causal_in_blocks else 0, bm.data_ptr())
+        m = attn_mask_t(_ffi.MASK_BLOCK_SPARSE, 1 if causal_in_blocks else 0, bm.data_ptr(), 0)
         return m, bm
     if causal:
-        return attn_mask_t(_ffi.MASK_CAUSAL, 0, None), None
+        return attn_mask_t(_ffi.MASK_CAUSAL, 0, None, 0), None
     return None, None
 
 
@@ -69,7 +79,8 @@ def _mp(m):
 
 def attn_fwd(q, k, v, scale: Optional[float] = None, causal: bool = False,
              block_mask: Optional[torch.Tensor] = None, causal_in_blocks: bool = False,
-             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None):
+             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+             window: Optional[int] = None):
     """Exact attention forward: returns ``(O [B,Hq,N,d] bf16, LSE [B,Hq,N] f32)``."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _contig(t, n)
@@ -82,7 +93,7 @@ def attn_fwd(q, k, v, scale: Optional[float] = None, causal: bool = False,
     l = torch.empty((B, Hq, N), device=q.device, dtype=torch.float32) if lse is None else lse
     _contig(l, "lse", torch.float32)
     sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    m, keep = mask_desc(causal, block_mask, causal_in_blocks)
+    m, keep = mask_desc(causal, block_mask, causal_in_blocks, window)
     check(_ffi.lib().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
                               B, Hq, Hkv, N, d, sc, _mp(m), _stream(q)), "attn_fwd")
     del keep
@@ -92,7 +103,7 @@ def attn_fwd(q, k, v, scale: Optional[float] = None, causal: bool = False,
 def attn_partial_fwd(q, k, v, q_offset: int = 0, kv_offset: int = 0, scale: Optional[float] = None,
                      causal: bool = False, block_mask: Optional[torch.Tensor] = None,
                      causal_in_blocks: bool = False, o_part: Optional[torch.Tensor] = None,
-                     lse_part: Optional[torch.Tensor] = None):
+                     lse_part: Optional[torch.Tensor] = None, window: Optional[int] = None):
     """Attention of one query chunk against one key/value chunk.
 
     ``q`` ``[B,Hq,Nq,d]`` and ``k``/``v`` ``[B,Hkv,Nk,d]`` may be row-slices of
@@ -112,7 +123,7 @@ def attn_partial_fwd(q, k, v, q_offset: int = 0, kv_offset: int = 0, scale: Opti
     _contig(o, "o_part", torch.float32)
     _contig(l, "lse_part", torch.float32)
     sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    m, keep = mask_desc(causal, block_mask, causal_in_blocks)
+    m, keep = mask_desc(causal, block_mask, causal_in_blocks, window)
     check(_ffi.lib().attn_partial_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
                                       B, Hq, Hkv, Nq, Nk, d, sc, _mp(m), int(q_offset), int(kv_offset),
                                       qhs, khs, _stream(q)), "attn_partial_fwd")
@@ -158,7 +169,8 @@ def bwd_workspace_bytes(B: int, Hq: int, Hkv: int, N: int, d: int) -> int:
 
 def attn_bwd(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = False,
              block_mask: Optional[torch.Tensor] = None, causal_in_blocks: bool = False,
-             workspace: Optional[torch.Tensor] = None, dq=None, dk=None, dv=None):
+             workspace: Optional[torch.Tensor] = None, dq=None, dk=None, dv=None,
+             window: Optional[int] = None):
     """Exact backward pass; returns ``(dQ, dK, dV)`` in bf16."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
         _contig(t, n)
@@ -171,7 +183,7 @@ def attn_bwd(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = 
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    m, keep = mask_desc(causal, block_mask, causal_in_blocks)
+    m, keep = mask_desc(causal, block_mask, causal_in_blocks, window)
     check(_ffi.lib().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                               do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(),
                               ws.numel() * ws.element_size(), B, Hq, Hkv, N, d, sc, _mp(m), _stream(q)),
@@ -182,7 +194,8 @@ def attn_bwd(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = 
 
 def build_schedule(mask_kind: int, B: int, Hq: int, Nq: int, Nk: int, q_offset: int = 0,
                    kv_offset: int = 0, host_block_mask: Optional[np.ndarray] = None,
-                   causal_in_blocks: bool = False, Hkv: Optional[int] = None, d: int = 128) -> np.ndarray:
+                   causal_in_blocks: bool = False, Hkv: Optional[int] = None, d: int = 128,
+                   window: int = 0) -> np.ndarray:
     """Forward work units in launch order, ``[n, 3]`` int32 (bh, query chunk, key tiles)."""
     L = _ffi.lib()
     hkv = Hq if Hkv is None else Hkv
@@ -191,11 +204,12 @@ def build_schedule(mask_kind: int, B: int, Hq: int, Nq: int, Nk: int, q_offset: 
     if host_block_mask is not None:
         bm = np.ascontiguousarray(host_block_mask, dtype=np.uint8)
     bmp = bm.ctypes.data if bm is not None else None
-    L.attn_build_schedule(mask_kind, int(causal_in_blocks), bmp, B, Hq, hkv, Nq, Nk, d, q_offset, kv_offset,
-                          None, 0, C.byref(n))
+    L.attn_build_schedule(mask_kind, int(causal_in_blocks), bmp, int(window), B, Hq, hkv, Nq, Nk, d, q_offset,
+                          kv_offset, None, 0, C.byref(n))
     out = np.zeros(3 * n.value, dtype=np.int32)
-    check(L.attn_build_schedule(mask_kind, int(causal_in_blocks), bmp, B, Hq, hkv, Nq, Nk, d, q_offset, kv_offset,
-                                out.ctypes.data_as(C.POINTER(C.c_int32)), out.size, C.byref(n)),
+    check(L.attn_build_schedule(mask_kind, int(causal_in_blocks), bmp, int(window), B, Hq, hkv, Nq, Nk, d,
+                                q_offset, kv_offset, out.ctypes.data_as(C.POINTER(C.c_int32)), out.size,
+                                C.byref(n)),
           "attn_build_schedule")
     return out.reshape(-1, 3)
 

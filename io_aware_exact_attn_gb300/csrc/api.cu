@@ -91,18 +91,24 @@ struct MaskArgs {
   int kind = MASK_NONE;
   int causal_in_blocks = 0;
   const uint8_t* block_mask = nullptr;
+  int window = 0;
 };
 
 int read_mask(const attn_mask_t* m, MaskArgs* out) {
   *out = MaskArgs();
   if (m == nullptr) return ATTN_OK;
-  if (m->kind != ATTN_MASK_NONE && m->kind != ATTN_MASK_CAUSAL && m->kind != ATTN_MASK_BLOCK_SPARSE)
+  if (m->kind != ATTN_MASK_NONE && m->kind != ATTN_MASK_CAUSAL && m->kind != ATTN_MASK_BLOCK_SPARSE &&
+      m->kind != ATTN_MASK_SLIDING_WINDOW)
     return fail(ATTN_ERR_INVALID_ARG, "unknown mask kind %d", (int)m->kind);
   out->kind = m->kind;
   out->causal_in_blocks = m->causal_in_blocks ? 1 : 0;
   if (m->kind == ATTN_MASK_BLOCK_SPARSE) {
     if (m->block_mask == nullptr) return fail(ATTN_ERR_INVALID_ARG, "block-sparse mask without block_mask");
     out->block_mask = m->block_mask;
+  }
+  if (m->kind == ATTN_MASK_SLIDING_WINDOW) {
+    if (m->window < 1) return fail(ATTN_ERR_INVALID_ARG, "sliding window %d < 1", (int)m->window);
+    out->window = m->window;
   }
   return ATTN_OK;
 }
@@ -249,6 +255,7 @@ static int fwd_common(const void* q, const void* k, const void* v, void* o, bool
   p.mask_kind = m.kind;
   p.causal_in_blocks = m.causal_in_blocks;
   p.block_mask = m.block_mask;
+  p.window = m.window;
   p.nkb = (int)cdiv(Nk, TILE);
   p.q_offset = q_off;
   p.kv_offset = kv_off;
@@ -355,6 +362,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   p.mask_kind = m.kind;
   p.causal_in_blocks = m.causal_in_blocks;
   p.block_mask = m.block_mask;
+  p.window = m.window;
   p.nkb = (int)cdiv(N, TILE);
   p.kv_group = q_stream_group(B, Hq, Hkv, N, d);
   p.q_group = kv_stream_group(B, Hq, Hkv, N, d);
@@ -373,16 +381,19 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   return ATTN_OK;
 }
 
-int attn_build_schedule(int mask_kind, int causal_in_blocks, const uint8_t* host_block_mask, int B, int Hq, int Hkv,
+int attn_build_schedule(int mask_kind, int causal_in_blocks, const uint8_t* host_block_mask, int window, int B, int Hq,
+                        int Hkv,
                         int Nq, int Nk, int d, int64_t q_offset, int64_t kv_offset, int32_t* out, size_t cap,
                         size_t* n_out) {
   if (n_out == nullptr) return fail(ATTN_ERR_INVALID_ARG, "n_out is NULL");
   *n_out = 0;
   if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || d < 1) return fail(ATTN_ERR_INVALID_ARG, "sizes must be positive");
   if (Hq % Hkv) return fail(ATTN_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
-  if (mask_kind < 0 || mask_kind > 2) return fail(ATTN_ERR_INVALID_ARG, "unknown mask kind %d", mask_kind);
+  if (mask_kind < 0 || mask_kind > 3) return fail(ATTN_ERR_INVALID_ARG, "unknown mask kind %d", mask_kind);
   if (mask_kind == ATTN_MASK_BLOCK_SPARSE && host_block_mask == nullptr)
     return fail(ATTN_ERR_INVALID_ARG, "block-sparse schedule needs host_block_mask");
+  if (mask_kind == ATTN_MASK_SLIDING_WINDOW && window < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "sliding window %d < 1", window);
   const int nqc = (int)cdiv(Nq, UNIT_ROWS);
   const int nkb = (int)cdiv(Nk, TILE);
   const int64_t units = (int64_t)B * Hq * nqc;
@@ -391,9 +402,9 @@ int attn_build_schedule(int mask_kind, int causal_in_blocks, const uint8_t* host
   if (out == nullptr || cap < (size_t)units * 3) return fail(ATTN_ERR_INVALID_ARG, "output capacity too small");
   for (int64_t i = 0; i < units; ++i) {
     const Unit u = fwd_unit(i, B, Hq, Hkv, Nq, Nk, nqc, group, mask_kind, causal_in_blocks, host_block_mask, nkb,
-                            q_offset, kv_offset);
+                            window, q_offset, kv_offset);
     int cnt = 0;
-    for (int kt = 0; kt < u.kt_end; ++kt) cnt += unit_uses(u, kt) ? 1 : 0;
+    for (int kt = u.kt_begin; kt < u.kt_end; ++kt) cnt += unit_uses(u, kt) ? 1 : 0;
     out[3 * i + 0] = u.bh;
     out[3 * i + 1] = u.row0 / UNIT_ROWS;
     out[3 * i + 2] = cnt;
@@ -604,6 +615,7 @@ extern "C" int attn_bwd_static_scratch(const void* q, const void* k, const void*
   p.mask_kind = m.kind;
   p.causal_in_blocks = m.causal_in_blocks;
   p.block_mask = m.block_mask;
+  p.window = m.window;
   p.nkb = (int)cdiv(N, TILE);
   p.kv_group = q_stream_group(B, Hq, Hkv, N, d);
   p.q_group = kv_stream_group(B, Hq, Hkv, N, d);

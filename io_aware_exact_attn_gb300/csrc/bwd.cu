@@ -24,6 +24,8 @@
 // owns the TMEM allocation), warps 2-3 idle, warps 4-11 elementwise work in
 // two warpgroups that split the 128 columns of every tile row between them
 // (warp w owns TMEM lanes 32*(w%4)..+31; one thread per row and half).
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 #include "schedule.h"
@@ -45,13 +47,22 @@ struct BwdCfg {
   static constexpr uint32_t REGS_CTRL = 56, REGS_ELEM = 224;
 };
 
+// The sliding window includes the causal rule.
 __device__ __forceinline__ bool causal_of(const BwdParams& p) {
-  return p.mask_kind == MASK_CAUSAL || (p.mask_kind == MASK_BLOCK_SPARSE && p.causal_in_blocks);
+  return p.mask_kind == MASK_CAUSAL || p.mask_kind == MASK_SLIDING_WINDOW ||
+         (p.mask_kind == MASK_BLOCK_SPARSE && p.causal_in_blocks);
 }
 
-// Query tile qt sees key tile kt (equal 128-row tiles, no offsets).
+// Width of the sliding window, or a bound no position difference reaches.
+__device__ __forceinline__ int window_of(const BwdParams& p) {
+  return p.mask_kind == MASK_SLIDING_WINDOW ? p.window : 0x7fffffff;
+}
+
+// Query tile qt sees key tile kt (equal 128-row tiles, no offsets): some query
+// of qt lies 0..window-1 positions after some key of kt.
 __device__ __forceinline__ bool tile_pair_visible(const BwdParams& p, int qt, int kt) {
   if (causal_of(p) && qt < kt) return false;
+  if ((qt - kt) * TILE - (TILE - 1) >= window_of(p)) return false;
   if (p.mask_kind == MASK_BLOCK_SPARSE && p.block_mask[(size_t)qt * p.nkb + kt] == 0) return false;
   return true;
 }
@@ -303,14 +314,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
         ok = wait_bar(bar_q(s), (i / NS) & 1, wc) && wait_bar(bar_s, i & 1, wc);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        const bool diag = causal && qt == kt;       // key r sees query column j iff r <= j
+        // key r sees query column j iff 0 <= (qt - kt) * 128 + j - r < window:
+        // j >= r on the diagonal tile, j < hi where the window's edge crosses
+        const bool diag = causal && qt == kt;
+        const bool wedge = (qt - kt) * TILE + (TILE - 1) >= window_of(p);
+        const int hi = wedge ? window_of(p) + r - (qt - kt) * TILE : TILE;
         const float4* l4 = reinterpret_cast<const float4*>(lse2) + 16 * hf;
         const float4* d4 = reinterpret_cast<const float4*>(dsum) + 16 * hf;
-        // phase A: P^T = 2^(S^T c - lse2) for this warpgroup's 64 query columns
+        // phase A: P^T = 2^(S^T c - lse2) for this warpgroup's 64 query columns.
+        // Masked tiles (the diagonal, a window's edge) take their own copy of
+        // the loop so that the others carry no mask arithmetic at all.
         uint32_t pk[32];
-        {
+        auto phase_a = [&](auto masked) {
           uint32_t sr[64];
           tmem_ld64(tmem + lane_off + cb, sr);
+          const int lo = diag ? r : 0;                // visible query columns: lo <= j < hi
 #pragma unroll
           for (int j4 = 0; j4 < 16; ++j4) {
             const float4 L = l4[j4];
@@ -319,16 +337,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
             float p1 = ex2(fmaf(__uint_as_float(sr[4 * j4 + 1]), c, -L.y));
             float p2 = ex2(fmaf(__uint_as_float(sr[4 * j4 + 2]), c, -L.z));
             float p3 = ex2(fmaf(__uint_as_float(sr[4 * j4 + 3]), c, -L.w));
-            if (diag) {
-              p0 = (r <= col + 0) ? p0 : 0.f;
-              p1 = (r <= col + 1) ? p1 : 0.f;
-              p2 = (r <= col + 2) ? p2 : 0.f;
-              p3 = (r <= col + 3) ? p3 : 0.f;
+            if constexpr (decltype(masked)::value) {
+              p0 = (col + 0 >= lo && col + 0 < hi) ? p0 : 0.f;
+              p1 = (col + 1 >= lo && col + 1 < hi) ? p1 : 0.f;
+              p2 = (col + 2 >= lo && col + 2 < hi) ? p2 : 0.f;
+              p3 = (col + 3 >= lo && col + 3 < hi) ? p3 : 0.f;
             }
             pk[2 * j4] = pack_bf16(p0, p1);
             pk[2 * j4 + 1] = pack_bf16(p2, p3);
           }
-        }
+        };
+        if (diag || wedge) phase_a(std::true_type{});
+        else phase_a(std::false_type{});
         tmem_st32(tmem + lane_off + cb, pk);
         tc_fence_before();
         mbar_arrive(bar_p);
@@ -643,10 +663,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       ok = wait_bar(bar_s, j & 1, wc);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      // key column col is visible iff key < N and (not causal or key <= query)
-      const bool edge = (kt == nkt - 1 && (p.N % TILE) != 0) || (causal && kt == qt);
+      // key column col is visible iff key < N, key <= query (causal) and
+      // query - key < window: lo <= col < lim
+      const int wnd = window_of(p);
+      const bool wedge = (qt - kt) * TILE + (TILE - 1) >= wnd;
+      const bool edge = (kt == nkt - 1 && (p.N % TILE) != 0) || (causal && kt == qt) || wedge;
       int lim = p.N - kt * TILE;
       if (causal && kt == qt) lim = min(lim, r + 1);
+      const int lo = wedge ? (qt - kt) * TILE + r - wnd + 1 : 0;
       float pr[64];
       {
         uint32_t sr[64];
@@ -663,7 +687,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
         }
         if (edge) {
 #pragma unroll
-          for (int col = 0; col < 64; ++col) pr[col] = (cb + col < lim) ? pr[col] : 0.f;
+          for (int col = 0; col < 64; ++col) pr[col] = (cb + col >= lo && cb + col < lim) ? pr[col] : 0.f;
         }
       }
       // dS_j reuses the buffer of dS_{j-2}: dQ_{j-2} must have read it

@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   const uint32_t bar_done = smem_u32(&bars[1 + 4 * NS + 6]);
 
   const Unit u = fwd_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.Nq, p.Nk, p.nqc, p.head_group, p.mask_kind, p.causal_in_blocks,
-                          p.block_mask, p.nkb, p.q_offset, p.kv_offset);
+                          p.block_mask, p.nkb, p.window, p.q_offset, p.kv_offset);
   WaitCtx wc{p.wait_limit_ns, p.status, &abort_flag};
 
   if (threadIdx.x == 0) {
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     }
     int n = 0;
     bool ok = true;
-    for (int kt = 0; kt < u.kt_end && ok; ++kt) {
+    for (int kt = u.kt_begin; kt < u.kt_end && ok; ++kt) {
       if (!unit_uses(u, kt)) continue;
       const int s = n % NS;
       const uint32_t fph = ((n / NS) - 1) & 1;
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       };
       int it0 = 0, it1 = 0;   // PV MMAs issued per tile
       bool ok = wait_bar(bar_q, 0, wc);
-      int kt = next_kt(0);
+      int kt = next_kt(u.kt_begin);
       uint32_t use = kt < u.kt_end ? unit_uses(u, kt) : 0u;
       if (ok && use) {
         ok = wait_bar(bar_k(0), 0, wc);
@@ -278,32 +278,40 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     float m = -INFINITY, l = 0.f, lr = 0.f;
     int it = 0;
     bool ok = true;
-    for (int kt = 0; kt < u.kt_end; ++kt) {
+    for (int kt = u.kt_begin; kt < u.kt_end; ++kt) {
       if (!(unit_uses(u, kt) & (1u << t))) continue;
       ok = wait_bar(bar_s(t), it & 1, wc);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      // element mask on the ragged last key tile and on causal diagonal tiles
+      // element mask on the ragged last key tile, on causal diagonal tiles
+      // and on tiles crossing the lower edge of a sliding window: column j is
+      // visible iff lo <= j < lim
       const int64_t key0 = p.kv_offset + (int64_t)kt * TILE;
       const bool tail = (kt == u.nkt - 1) && (p.Nk % TILE) != 0;
       const bool diag = causal && (key0 + TILE - 1 > row_first_pos);
-      int lim = 128;
-      if (tail || diag) {
+      const bool wedge = p.mask_kind == MASK_SLIDING_WINDOW && key0 + p.window <= row_first_pos + TILE - 1;
+      const bool edge = tail || diag || wedge;
+      int lo = 0, lim = 128;
+      if (edge) {
         int64_t l64 = p.Nk - (int64_t)kt * TILE;
         if (causal) {
           const int64_t lc = p.q_offset + qrow - key0 + 1;
           l64 = lc < l64 ? lc : l64;
         }
         lim = (int)(l64 < 0 ? 0 : (l64 > 128 ? 128 : l64));
+        if (wedge) {
+          const int64_t f64 = p.q_offset + qrow - p.window + 1 - key0;   // first key in the row's window
+          lo = (int)(f64 < 0 ? 0 : (f64 > 128 ? 128 : f64));
+        }
       }
       auto load_scores = [&](float (&sc)[128]) {
         uint32_t rr[128];
         tmem_ld128(tS, rr);   // the whole score row in one round trip
 #pragma unroll
         for (int j = 0; j < 128; ++j) sc[j] = __uint_as_float(rr[j]);
-        if (tail || diag) {
+        if (edge) {
 #pragma unroll
-          for (int j = 0; j < 128; ++j) sc[j] = (j < lim) ? sc[j] : -INFINITY;
+          for (int j = 0; j < 128; ++j) sc[j] = (j >= lo && j < lim) ? sc[j] : -INFINITY;
         }
       };
       // p = 2^(s*c - mb), two lanes per packed FMA; in place
@@ -352,9 +360,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       float la[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // four independent packed chains
 #pragma unroll
       for (int j = 0; j < 64; ++j) {
-        // bf16 by truncation (one byte permute per pair); O is normalised by
-        // the sum of these same weights, so the rounding direction cancels
-        pk[j] = __byte_perm(__float_as_uint(s[2 * j]), __float_as_uint(s[2 * j + 1]), 0x7632);
+        // bf16, rounded to nearest; O is normalised by the sum of these same
+        // weights, so a dominant weight's rounding cancels
+        pk[j] = pack_bf16(s[2 * j], s[2 * j + 1]);
         const int a = 2 * (j & 3);
         add2(la[a], la[a + 1], la[a], la[a + 1], s[2 * j], s[2 * j + 1]);
       }

@@ -11,7 +11,7 @@ namespace attn {
 constexpr int TILE = 128;       // query-tile rows, key-tile rows, block-mask granularity
 constexpr int UNIT_ROWS = 256;  // query rows per forward work unit (two query tiles)
 
-enum MaskKind : int { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_BLOCK_SPARSE = 2 };
+enum MaskKind : int { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_BLOCK_SPARSE = 2, MASK_SLIDING_WINDOW = 3 };
 
 // Everything a forward launch needs besides the three TMA descriptors.
 struct FwdParams {
@@ -26,6 +26,7 @@ struct FwdParams {
   int causal_in_blocks;
   const uint8_t* block_mask;  // [ceil(Nq/128)][ceil(Nk/128)]
   int nkb;                    // ceil(Nk/128)
+  int window;                 // sliding window width (MASK_SLIDING_WINDOW)
   int64_t q_offset, kv_offset;
   unsigned int* status;
   int64_t wait_limit_ns;
@@ -46,6 +47,7 @@ struct BwdParams {
   int causal_in_blocks;
   const uint8_t* block_mask;
   int nkb;
+  int window;               // sliding window width (MASK_SLIDING_WINDOW)
   int kv_group;             // kv heads per L2 group of the dK/dV kernel
   int q_group;              // query heads per L2 group of the dQ kernel
   unsigned int* status;

@@ -29,8 +29,8 @@ struct Unit {
   int bh, kvh;
   int row0;         // first local query row of the unit
   int nkt;          // key tiles in the call
-  int lim[2];       // per query tile t: key tiles [0, lim[t]) may be visible
-  int kt_end;       // max(lim)
+  int lo[2], lim[2];  // per query tile t: key tiles [lo[t], lim[t]) may be visible
+  int kt_begin, kt_end;  // min(lo), max(lim) over the unit's tiles
   const uint8_t* mrow[2];  // block-sparse mask row per tile, or null
 };
 
@@ -43,8 +43,18 @@ ATTN_HD int causal_tiles(int64_t last_row, int64_t q_off, int64_t kv_off, int nk
   return n < nkt ? (int)n : nkt;
 }
 
+// First key tile holding a key inside the window of local query row
+// `first_row`: the window of a row reaches back window - 1 positions, so the
+// earliest key any row of a tile starting at first_row sees is
+// q_offset + first_row - window + 1 (global position).
+ATTN_HD int window_first_tile(int64_t first_row, int64_t q_off, int64_t kv_off, int window) {
+  const int64_t first_key = q_off + first_row - window + 1 - kv_off;
+  return first_key <= 0 ? 0 : (int)(first_key / TILE);
+}
+
+// The sliding window includes the causal rule.
 ATTN_HD bool mask_is_causal(int kind, int causal_in_blocks) {
-  return kind == MASK_CAUSAL || (kind == MASK_BLOCK_SPARSE && causal_in_blocks);
+  return kind == MASK_CAUSAL || kind == MASK_SLIDING_WINDOW || (kind == MASK_BLOCK_SPARSE && causal_in_blocks);
 }
 
 // Work units are taken head-group by head-group so that the operand a group
@@ -93,7 +103,7 @@ ATTN_HD void grouped_unit(int64_t i, int heads, int per_head, int group, int* he
 
 // `block_mask` may be a host or a device pointer, matching the caller.
 ATTN_HD Unit fwd_unit(int64_t i, int B, int Hq, int Hkv, int Nq, int Nk, int nqc, int head_group, int mask_kind,
-                      int causal_in_blocks, const uint8_t* block_mask, int nkb, int64_t q_off,
+                      int causal_in_blocks, const uint8_t* block_mask, int nkb, int window, int64_t q_off,
                       int64_t kv_off) {
   Unit u;
   int pos = 0;
@@ -104,26 +114,34 @@ ATTN_HD Unit fwd_unit(int64_t i, int B, int Hq, int Hkv, int Nq, int Nk, int nqc
   u.row0 = qc * UNIT_ROWS;
   u.nkt = (Nk + TILE - 1) / TILE;
   const bool causal = mask_is_causal(mask_kind, causal_in_blocks);
+  u.kt_begin = u.nkt;
   u.kt_end = 0;
   for (int t = 0; t < 2; ++t) {
     const int r0 = u.row0 + t * TILE;
-    int lim = 0;
+    int lo = 0, lim = 0;
     if (r0 < Nq) {
       const int rl = (Nq < r0 + TILE ? Nq : r0 + TILE) - 1;
       lim = causal ? causal_tiles(rl, q_off, kv_off, u.nkt) : u.nkt;
+      if (mask_kind == MASK_SLIDING_WINDOW) lo = window_first_tile(r0, q_off, kv_off, window);
+      if (lo > lim) lo = lim;
     }
+    u.lo[t] = lo;
     u.lim[t] = lim;
-    u.kt_end = u.kt_end > lim ? u.kt_end : lim;
+    if (lo < lim) {
+      u.kt_begin = u.kt_begin < lo ? u.kt_begin : lo;
+      u.kt_end = u.kt_end > lim ? u.kt_end : lim;
+    }
     u.mrow[t] = (mask_kind == MASK_BLOCK_SPARSE && r0 < Nq) ? block_mask + (int64_t)(r0 / TILE) * nkb : nullptr;
   }
+  if (u.kt_begin > u.kt_end) u.kt_begin = u.kt_end;
   return u;
 }
 
 // Bit t set: query tile t of the unit sees key tile kt.
 ATTN_HD uint32_t unit_uses(const Unit& u, int kt) {
   uint32_t m = 0;
-  if (kt < u.lim[0] && (u.mrow[0] == nullptr || u.mrow[0][kt] != 0)) m |= 1u;
-  if (kt < u.lim[1] && (u.mrow[1] == nullptr || u.mrow[1][kt] != 0)) m |= 2u;
+  if (kt >= u.lo[0] && kt < u.lim[0] && (u.mrow[0] == nullptr || u.mrow[0][kt] != 0)) m |= 1u;
+  if (kt >= u.lo[1] && kt < u.lim[1] && (u.mrow[1] == nullptr || u.mrow[1][kt] != 0)) m |= 2u;
   return m;
 }
 

@@ -73,8 +73,9 @@ class Workload:
     Hkv: int
     N: int
     d: int
-    mask: str = "none"            # "none" | "causal" | "block_sparse"
+    mask: str = "none"            # "none" | "causal" | "block_sparse" | "sliding_window"
     density: float = 1.0
+    window: int = 0               # sliding_window: positions a query looks back, its own included
     k_mul: float = 1.0
     chunks: int = 0               # >0: chunked causal (partial fwd + merge)
     note: str = ""
@@ -102,4 +103,6 @@ WORKLOADS = {
     "gpt_noncausal": Workload("gpt_noncausal", 2, 32, 32, 8192, 128, "none"),
     "chunked_gqa": Workload("chunked_gqa", 1, 32, 8, 32768, 128, "causal", chunks=8),
     "block_sparse": Workload("block_sparse", 1, 16, 16, 16384, 64, "block_sparse", density=1.0 / 8.0),
+    # local attention over the last 4096 positions (a Mistral-style sliding window) at the GPT shape
+    "gpt_sliding_window": Workload("gpt_sliding_window", 2, 32, 32, 8192, 128, "sliding_window", window=4096),
 }

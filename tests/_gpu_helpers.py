@@ -20,9 +20,11 @@ def f64(t):
     return inputs.to_f64(t)
 
 
-def mask_spec(kind, bm=None, cib=False):
+def mask_spec(kind, bm=None, cib=False, window=0):
     if kind == "block_sparse":
         return oracle.MaskSpec("block_sparse", np.asarray(bm, bool), 128, cib)
+    if kind == "sliding_window":
+        return oracle.MaskSpec("sliding_window", window=window)
     return oracle.MaskSpec(kind)
 
 

@@ -82,3 +82,13 @@ def test_kernel_work_and_flop_convention():
     work = bench.kernel_work(w)
     assert work["fwd"] == ("tensor", f)
     assert work["bwd_dkdv"][1] + work["bwd_dq"][1] == 2.5 * f
+
+
+def test_window_pair_count_matches_brute_force():
+    import numpy as np
+    for n, w in [(1, 1), (10, 1), (10, 3), (10, 10), (10, 25), (300, 128), (1000, 999)]:
+        i = np.arange(n)[:, None]
+        j = np.arange(n)[None, :]
+        assert bench.window_pairs(n, w) == int(((i - j >= 0) & (i - j < w)).sum())
+    # the benchmark's window is three quarters of the causal pairs
+    assert abs(bench.window_pairs(8192, 4096) / (8192 * 8193 / 2) - 0.75) < 1e-3

@@ -40,8 +40,9 @@ def gpu_fwd_bwd(w, bm=None):
     q, k, v, do = (t.cuda() for t in w.tensors())
     bmt = torch.as_tensor(bm, dtype=torch.uint8).cuda() if bm is not None else None
     causal = w.mask == "causal"
-    o, lse = api.attn_fwd(q, k, v, causal=causal, block_mask=bmt)
-    dq, dk, dv = api.attn_bwd(q, k, v, o, lse, do, causal=causal, block_mask=bmt)
+    win = w.window if w.mask == "sliding_window" else None
+    o, lse = api.attn_fwd(q, k, v, causal=causal, block_mask=bmt, window=win)
+    dq, dk, dv = api.attn_bwd(q, k, v, o, lse, do, causal=causal, block_mask=bmt, window=win)
     torch.cuda.synchronize()
     return (q, k, v, do), (o, lse), (dq, dk, dv)
 
@@ -49,7 +50,7 @@ def gpu_fwd_bwd(w, bm=None):
 def check_sampled(w, bm=None, n_kv_heads_full=1):
     (q, k, v, do), (o, lse), (dq, dk, dv) = gpu_fwd_bwd(w, bm)
     scale = 1.0 / math.sqrt(w.d)
-    mask = mask_spec(w.mask, bm)
+    mask = mask_spec(w.mask, bm, window=w.window)
     heads, rows = sample_heads_rows(w.B, w.Hq, w.N)
     qf, kf, vf, dof = f64(q), f64(k), f64(v), f64(do)
     o_ref, l_ref = oracle.attention_forward(qf, kf, vf, scale, mask, heads=heads, rows=rows)
@@ -77,6 +78,10 @@ def test_gpt_causal_peaked_full_size():
 
 def test_gpt_noncausal_full_size():
     check_sampled(inputs.WORKLOADS["gpt_noncausal"], n_kv_heads_full=0)
+
+
+def test_gpt_sliding_window_full_size():
+    check_sampled(inputs.WORKLOADS["gpt_sliding_window"])
 
 
 def test_block_sparse_full_size():

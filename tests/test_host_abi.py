@@ -148,6 +148,29 @@ def test_fwd_schedule_block_sparse_matches_oracle(lib, cib):
     np.testing.assert_array_equal(got, np.array(want, dtype=np.int32).reshape(-1, 3))
 
 
+WINDOW_CASES = [
+    # (B, Hq, Hkv, Nq, Nk, q_offset, kv_offset, d, window)
+    (1, 2, 2, 1000, 1000, 0, 0, 128, 1), (1, 2, 2, 1000, 1000, 0, 0, 128, 100),
+    (2, 3, 1, 700, 700, 0, 0, 64, 128), (1, 2, 2, 1000, 1000, 0, 0, 128, 129),
+    (1, 1, 1, 1500, 1500, 0, 0, 64, 300), (1, 2, 1, 600, 900, 256, 0, 128, 333),
+    (1, 2, 2, 512, 512, 1024, 512, 128, 700), (1, 2, 2, 2048, 2048, 0, 0, 128, 100000),
+    (1, 4, 4, 8192, 8192, 0, 0, 128, 4096),
+]
+
+
+@pytest.mark.parametrize("case", WINDOW_CASES)
+def test_fwd_schedule_sliding_window_matches_oracle(lib, case):
+    B_, H, Hkv, nq, nk, qo, ko, d, w = case
+    got = api.build_schedule(3, B_, H, nq, nk, qo, ko, Hkv=Hkv, d=d, window=w)
+    want = oracle.fwd_work_units("sliding_window", B_, H, nq, nk, qo, ko, Hkv=Hkv, d=d, window=w)
+    np.testing.assert_array_equal(got, np.array(want, dtype=np.int32).reshape(-1, 3))
+
+
+def test_schedule_rejects_bad_window(lib):
+    with pytest.raises(RuntimeError):
+        api.build_schedule(3, 1, 1, 256, 256, window=0)
+
+
 def test_schedule_covers_every_visible_tile_pair_once():
     """Coverage from the visibility matrix itself: each work unit visits exactly
     the key tiles that hold at least one key visible to one of its rows."""
