@@ -35,6 +35,7 @@ from .attention import (  # noqa: F401
     attention_forward,
     attention_backward,
     attention_backward_dq_rows,
+    decode_forward,
     merge_partials,
 )
 from .schedule import (  # noqa: F401

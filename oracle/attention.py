@@ -226,6 +226,34 @@ def attention_backward_dq_rows(q, k, v, do, scale: float, b: int, h: int, rows,
     return dq
 
 
+def decode_forward(q, k_cache, v_cache, scale: float, seq_lens=None, causal: bool = True):
+    """Attention of the newest ``Nq`` positions of each sequence against its
+    key/value cache, in float64 (the decoding step of a KV-cache model;
+    FlashAttention-2 reviews: splitting the KV cache among thread blocks).
+
+    ``q`` is ``[B, Hq, Nq, d]``; ``k_cache``/``v_cache`` are ``[B, Hkv, Nk, d]``
+    of which sequence ``b`` uses the first ``seq_lens[b]`` positions (all
+    ``Nk`` when ``seq_lens`` is None).  Query ``i`` of sequence ``b`` sits at
+    position ``seq_lens[b] - Nq + i``; with ``causal`` it sees the cached keys
+    at positions up to its own, otherwise every cached key of its sequence.
+    Returns ``O [B, Hq, Nq, d]`` and ``LSE [B, Hq, Nq]``.
+    """
+    q = np.asarray(q, np.float64)
+    B, Hq, Nq, d = q.shape
+    Nk = np.asarray(k_cache).shape[2]
+    lens = [Nk] * B if seq_lens is None else [int(x) for x in seq_lens]
+    o = np.zeros((B, Hq, Nq, d))
+    lse = np.full((B, Hq, Nq), -np.inf)
+    for b in range(B):
+        n = lens[b]
+        if n <= 0:
+            continue
+        ob, lb = attention_forward(q[b:b + 1], np.asarray(k_cache)[b:b + 1, :, :n], np.asarray(v_cache)[b:b + 1, :, :n],
+                                   scale, MaskSpec("causal" if causal else "none"), q_offset=n - Nq, kv_offset=0)
+        o[b], lse[b] = ob[0], lb[0]
+    return o, lse
+
+
 def merge_partials(o_parts, lse_parts):
     """Combine partial attention results over disjoint key sets.
 

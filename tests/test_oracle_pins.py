@@ -421,6 +421,47 @@ def test_sliding_window_chunked_merge_equals_monolithic():
             np.testing.assert_allclose(l, full_l[:, :, qs], atol=1e-12)
 
 
+# ---------------------------------------------------------------- decoding against a KV cache
+
+def test_decode_equals_last_rows_of_causal_attention():
+    """The newest Nq positions attending to the cache give the last Nq rows of
+    causal attention over the whole sequence (the pinned forward)."""
+    B, Hq, Hkv, N, d = 3, 4, 2, 20, 6
+    lens = [20, 13, 5]
+    for nq in (1, 3):
+        q_all, k, v = rnd(B, Hq, N, d), rnd(B, Hkv, N, d), rnd(B, Hkv, N, d)
+        q = np.stack([q_all[b, :, lens[b] - nq:lens[b]] for b in range(B)])
+        o, lse = oracle.decode_forward(q, k, v, 0.4, lens, causal=True)
+        for b in range(B):
+            n = lens[b]
+            of, lf = oracle.attention_forward(q_all[b:b + 1, :, :n], k[b:b + 1, :, :n], v[b:b + 1, :, :n], 0.4,
+                                              MaskSpec("causal"))
+            np.testing.assert_allclose(o[b], of[0, :, n - nq:], atol=1e-14)
+            np.testing.assert_allclose(lse[b], lf[0, :, n - nq:], atol=1e-14)
+
+
+def test_decode_q_zero_gives_mean_of_cached_values():
+    B, Hq, Hkv, Nk, d, nq = 2, 4, 1, 9, 3, 2
+    lens = [9, 4]
+    k, v = rnd(B, Hkv, Nk, d), rnd(B, Hkv, Nk, d)
+    q = np.zeros((B, Hq, nq, d))
+    for causal in (False, True):
+        o, lse = oracle.decode_forward(q, k, v, 0.5, lens, causal)
+        for b in range(B):
+            for i in range(nq):
+                top = lens[b] - nq + i + 1 if causal else lens[b]     # keys 0..top-1 are visible
+                for h in range(Hq):
+                    np.testing.assert_allclose(o[b, h, i], v[b, 0, :top].mean(axis=0), atol=1e-14)
+                    assert abs(lse[b, h, i] - np.log(top)) < 1e-13
+
+
+def test_decode_empty_sequence():
+    q, k, v = rnd(2, 2, 1, 4), rnd(2, 2, 5, 4), rnd(2, 2, 5, 4)
+    o, lse = oracle.decode_forward(q, k, v, 0.5, [0, 5])
+    assert np.all(o[0] == 0) and np.all(lse[0] == -np.inf)
+    assert np.all(np.isfinite(lse[1]))
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def _fails(fn):
