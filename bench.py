@@ -41,6 +41,7 @@ METRIC = "attention fwd+bwd TFLOP/s (bf16, causal-adjusted) and % of GB300 dense
 WORKLOAD = dict(name="gpt_causal", B=2, Hq=32, Hkv=32, N=8192, d=128, mask="causal")
 CHUNKED = dict(name="chunked_gqa", B=1, Hq=32, Hkv=8, N=32768, d=128, chunks=8)
 WINDOW = dict(name="gpt_sliding_window", B=2, Hq=32, Hkv=32, N=8192, d=128, window=4096)
+DECODE = dict(name="decode_gqa", B=8, Hq=32, Hkv=8, Nq=1, Nk=32768, d=128)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
     "fwd": ["fwd.cu", "ptx.cuh", "schedule.h", "internal.h"],
@@ -391,6 +392,7 @@ def main():
         out["e2e"] = e2e_leg(api, inputs, torch, w, causal, rank)
         out["chunked_gqa"] = chunked_leg(api, inputs, torch, peaks, rank)
         out["sliding_window"] = window_leg(api, inputs, torch, peaks, rank)
+        out["decode"] = decode_leg(api, inputs, torch, peaks, rank)
         if rank == 0:
             out["cpu_baseline"] = {k_: v_ for k_, v_ in oracle_sample(args.cpu_seconds).items()
                                    if k_ in ("value", "unit", "cores", "kind", "sample")}
@@ -517,6 +519,45 @@ def window_leg(api, inputs, torch, peaks, rank, reps=5):
                 bwd_tflops=2.5 * f_fwd / (bwd_ms * 1e-3) / 1e12,
                 step_tflops=3.5 * f_fwd / ((fwd_ms + bwd_ms) * 1e-3) / 1e12,
                 fwd_frac_of_burst_peak=f_fwd / (fwd_ms * 1e-3) / 1e12 / peaks["bf16_tflops"])
+
+
+def decode_leg(api, inputs, torch, peaks, rank, reps=20, splits=(0, 8, 16, 24)):
+    """Split-KV decoding: one new token per sequence (B=8, Hq=32, Hkv=8, d=128)
+    against a full 32768-position cache.  HBM-bound: the algorithmic bytes are
+    the cache read once (K and V), the queries read and the outputs written."""
+    c = DECODE
+    B, Hq, Hkv, Nq, Nk, d = c["B"], c["Hq"], c["Hkv"], c["Nq"], c["Nk"], c["d"]
+    gen = torch.Generator().manual_seed(inputs.SEED + 100 * rank + 9)
+    q = torch.randn(B, Hq, Nq, d, generator=gen).to(torch.bfloat16).cuda()
+    k = torch.randn(B, Hkv, Nk, d, generator=gen).to(torch.bfloat16).cuda()
+    v = torch.randn(B, Hkv, Nk, d, generator=gen).to(torch.bfloat16).cuda()
+    algo_bytes = 2 * B * Hkv * Nk * d * 2 + B * Hq * Nq * (d * 2 * 2 + 4)
+    res = {}
+    for ns in splits:
+        ws = torch.empty(api.decode_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, ns), device="cuda", dtype=torch.uint8)
+        o = torch.empty_like(q)
+        lse = torch.empty(B, Hq, Nq, device="cuda")
+        for _ in range(3):
+            api.attn_decode(q, k, v, n_splits=ns, out=o, lse=lse, workspace=ws)
+        torch.cuda.synchronize()
+        api.trace_enable(4 * reps)
+        for _ in range(reps):
+            api.attn_decode(q, k, v, n_splits=ns, out=o, lse=lse, workspace=ws)
+        torch.cuda.synchronize()
+        api.trace_disable()
+        recs, _ = api.trace_read(4 * reps)
+        dec_ms = sum(ms for n, ms in recs if n == "decode") / reps
+        mrg_ms = sum(ms for n, ms in recs if n == "merge") / reps
+        res[ns] = (dec_ms, mrg_ms)
+    auto = api.decode_splits(B, Hkv, Nk)
+    dec_ms, mrg_ms = res[0]
+    gbs = algo_bytes / ((dec_ms + mrg_ms) * 1e-3) / 1e9
+    return dict(workload=f"B={B} Hq={Hq} Hkv={Hkv} Nq={Nq} Nk={Nk} d={d} causal, {auto} splits (automatic)",
+                algorithmic_bytes=algo_bytes, decode_ms=dec_ms, merge_ms=mrg_ms, gbs=gbs,
+                frac_of_hbm=gbs / peaks["hbm_gbs"],
+                by_splits={str(ns if ns else auto): dict(decode_ms=a, merge_ms=b,
+                                                         gbs=algo_bytes / ((a + b) * 1e-3) / 1e9)
+                           for ns, (a, b) in res.items()})
 
 
 if __name__ == "__main__":

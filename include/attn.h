@@ -174,6 +174,43 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o,
              int N, int d, float scale, const attn_mask_t* mask, void* stream);
 
 /*
+ * attn_decode_fwd -- one decoding step against a key/value cache, split over
+ * the cache ("FlashAttention-2" reviews: splitting the KV cache amongst thread
+ * blocks for inference).  Sequence b holds seq_lens[b] cached positions (Nk
+ * each when seq_lens is NULL); its newest Nq positions are the queries: query
+ * i sits at position seq_lens[b] - Nq + i and, with causal != 0, sees the
+ * cached keys up to its own position, otherwise all of its sequence's keys.
+ * The key range is cut into n_splits parts (0 picks a count that fills the
+ * GPU); each part's attention is computed independently into the workspace
+ * (fp32 O and LSE) and the parts are combined by the log-sum-exp merge of
+ * attn_merge_lse.  The g = Hq/Hkv query heads of a kv head share its cache
+ * reads: their g*Nq rows form one tile (g*Nq <= 256).
+ *   q          device bf16 [B, Hq, Nq, d]
+ *   k_cache    device bf16 [B, Hkv, Nk, d]   v_cache likewise
+ *   seq_lens   device int32 [B] in [0, Nk], or NULL; read by the kernels
+ *   o          device bf16 [B, Hq, Nq, d]   (written)
+ *   lse        device f32 [B, Hq, Nq]       (written; may be NULL)
+ *   workspace  device, >= attn_decode_workspace_bytes(B, Hq, Hkv, Nq, Nk, d,
+ *              n_splits) bytes, 16-byte aligned; caller-owned.
+ * Rows of a sequence with no visible key get O = 0, LSE = -inf.
+ * ATTN_ERR_INVALID_ARG for g*Nq > 256, Nq > Nk, n_splits outside [0, 64];
+ * ATTN_ERR_WORKSPACE if the workspace is too small.
+ */
+int attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* seq_lens, void* o, float* lse, int B, int Hq,
+                    int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                    int n_splits, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/* Splits attn_decode_fwd uses for n_splits = 0 (at least one key tile each). */
+int attn_decode_splits(int B, int Hkv, int Nk);
+
+/* Workspace for attn_decode_fwd: per split, fp32 O and LSE of every query row,
+ * rounded up to 256 bytes per split.  n_splits = 0 means attn_decode_splits. */
+size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                                   int n_splits);
+
+/*
  * attn_bwd_static_scratch -- the same backward pass as attn_bwd, for callers
  * that must not allocate device memory: code running where cudaMalloc is not
  * allowed or would break a memory budget fixed up front (an allocator or
@@ -276,7 +313,8 @@ typedef enum {
   ATTN_KERNEL_BWD_PREPROCESS = 4, /* attn_bwd step 1: D and LSE*log2 e */
   ATTN_KERNEL_BWD_DKDV = 5,       /* attn_bwd step 2: dK, dV */
   ATTN_KERNEL_BWD_DQ = 6,         /* attn_bwd step 3: dQ */
-  ATTN_KERNEL_SELFTEST = 7        /* attn_selftest_wait_timeout */
+  ATTN_KERNEL_SELFTEST = 7,       /* attn_selftest_wait_timeout */
+  ATTN_KERNEL_DECODE = 8          /* attn_decode_fwd split-KV partials (its merge is ATTN_KERNEL_MERGE) */
 } attn_kernel_id_t;
 
 typedef struct attn_trace_record {

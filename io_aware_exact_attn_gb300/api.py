@@ -192,6 +192,49 @@ def attn_bwd(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = 
     return dq, dk, dv
 
 
+def decode_splits(B: int, Hkv: int, Nk: int) -> int:
+    return int(_ffi.lib().attn_decode_splits(B, Hkv, Nk))
+
+
+def decode_workspace_bytes(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int, n_splits: int = 0) -> int:
+    return int(_ffi.lib().attn_decode_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, n_splits))
+
+
+def attn_decode(q, k_cache, v_cache, seq_lens: Optional[torch.Tensor] = None, causal: bool = True,
+                scale: Optional[float] = None, n_splits: int = 0, out: Optional[torch.Tensor] = None,
+                lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+    """One decoding step against a KV cache, split over the cache.
+
+    ``q`` ``[B, Hq, Nq, d]`` holds the newest ``Nq`` positions of each
+    sequence; ``k_cache``/``v_cache`` ``[B, Hkv, Nk, d]`` of which sequence ``b``
+    uses the first ``seq_lens[b]`` positions (int32 CUDA tensor, or None for
+    all ``Nk``).  Returns ``(O [B,Hq,Nq,d] bf16, LSE [B,Hq,Nq] f32)``.
+    """
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _contig(t, n)
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k_cache.shape[1], k_cache.shape[2]
+    if k_cache.shape != (B, Hkv, Nk, d) or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache must be [B, Hkv, Nk, d] matching q")
+    sl = None
+    if seq_lens is not None:
+        sl = seq_lens.to(device=q.device, dtype=torch.int32).contiguous()
+        if sl.shape != (B,):
+            raise ValueError("seq_lens must have shape [B]")
+    o = torch.empty_like(q) if out is None else out
+    _contig(o, "out")
+    l = torch.empty((B, Hq, Nq), device=q.device, dtype=torch.float32) if lse is None else lse
+    _contig(l, "lse", torch.float32)
+    need = decode_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, n_splits)
+    ws = torch.empty(need, device=q.device, dtype=torch.uint8) if workspace is None else workspace
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    check(_ffi.lib().attn_decode_fwd(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                     sl.data_ptr() if sl is not None else None, o.data_ptr(), l.data_ptr(),
+                                     B, Hq, Hkv, Nq, Nk, d, sc, 1 if causal else 0, int(n_splits),
+                                     ws.data_ptr(), ws.numel() * ws.element_size(), _stream(q)), "attn_decode_fwd")
+    return o, l
+
+
 def build_schedule(mask_kind: int, B: int, Hq: int, Nq: int, Nk: int, q_offset: int = 0,
                    kv_offset: int = 0, host_block_mask: Optional[np.ndarray] = None,
                    causal_in_blocks: bool = False, Hkv: Optional[int] = None, d: int = 128,

@@ -259,6 +259,7 @@ static int fwd_common(const void* q, const void* k, const void* v, void* o, bool
   p.nkb = (int)cdiv(Nk, TILE);
   p.q_offset = q_off;
   p.kv_offset = kv_off;
+  p.dec_nq = 1;
   p.status = status;
   p.wait_limit_ns = wait_limit();
   cudaError_t e;
@@ -281,6 +282,94 @@ int attn_partial_fwd(const void* q, const void* k, const void* v, float* o_part,
   if (lse_part == nullptr) return fail(ATTN_ERR_INVALID_ARG, "lse_part is NULL");
   return fwd_common(q, k, v, o_part, true, lse_part, B, Hq, Hkv, Nq, Nk, d, scale, mask, q_offset, kv_offset,
                     q_head_stride > 0 ? q_head_stride : Nq, kv_head_stride > 0 ? kv_head_stride : Nk, stream);
+}
+
+int attn_decode_splits(int B, int Hkv, int Nk) {
+  if (B < 1 || Hkv < 1 || Nk < 1) return 1;
+  // about six waves of CTAs on 148 SMs (measured on B=8, Hkv=8, Nk=32768:
+  // 5 splits 3.9 TB/s, 8: 4.5, 16: 4.7, 32: 4.1), at least one key tile each
+  const int64_t want = cdiv(6 * 148, (int64_t)B * Hkv);
+  const int64_t tiles = cdiv(Nk, TILE);
+  int64_t n = want < tiles ? want : tiles;
+  if (n > 64) n = 64;
+  return n < 1 ? 1 : (int)n;
+}
+
+size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d, int n_splits) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || d < 1) return 0;
+  const int ns = n_splits > 0 ? n_splits : attn_decode_splits(B, Hkv, Nk);
+  const size_t rows = (size_t)B * Hq * Nq;
+  const size_t per = ((rows * (size_t)d * 4 + 255) & ~(size_t)255) + ((rows * 4 + 255) & ~(size_t)255);
+  return per * (size_t)ns;
+}
+
+int attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens, void* o,
+                    float* lse, int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal, int n_splits,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  int rc;
+  if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k_cache, "k_cache")) || (rc = check_ptr(v_cache, "v_cache")) ||
+      (rc = check_ptr(o, "o")) || (rc = check_ptr(workspace, "workspace")))
+    return rc;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(ATTN_ERR_MISALIGNED, "lse not 4-byte aligned");
+  if (seq_lens != nullptr && (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return fail(ATTN_ERR_MISALIGNED, "seq_lens not 4-byte aligned");
+  if ((rc = check_dims(B, Hq, Hkv, Nq, Nk, d, scale))) return rc;
+  const int rows = (Hq / Hkv) * Nq;
+  if (rows > UNIT_ROWS) return fail(ATTN_ERR_INVALID_ARG, "(Hq/Hkv)*Nq = %d exceeds %d rows", rows, UNIT_ROWS);
+  if (Nq > Nk) return fail(ATTN_ERR_INVALID_ARG, "Nq=%d exceeds the cache length Nk=%d", Nq, Nk);
+  if (n_splits < 0 || n_splits > 64) return fail(ATTN_ERR_INVALID_ARG, "n_splits=%d outside [0, 64]", n_splits);
+  const int ns = n_splits > 0 ? n_splits : attn_decode_splits(B, Hkv, Nk);
+  if (workspace_bytes < attn_decode_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, ns))
+    return fail(ATTN_ERR_WORKSPACE, "decode workspace of %zu bytes is too small", workspace_bytes);
+  unsigned int* status = nullptr;
+  if ((rc = device_ready(&status))) return rc;
+  CUtensorMap tq, tk, tv;
+  // q viewed as [B*Hkv][g*Nq rows][d]: the g heads of a kv head are adjacent
+  if ((rc = encode_rows_map(&tq, q, d, rows, B * Hkv, rows)) ||
+      (rc = encode_rows_map(&tk, k_cache, d, Nk, B * Hkv, Nk)) || (rc = encode_rows_map(&tv, v_cache, d, Nk, B * Hkv, Nk)))
+    return rc;
+  // the split partials lie one after another, each laid out like o_part /
+  // lse_part of attn_partial_fwd: all O blocks first, then all LSE blocks
+  const int64_t total_rows = (int64_t)B * Hq * Nq;
+  const size_t o_bytes = ((size_t)total_rows * d * 4 + 255) & ~(size_t)255;
+  float* ws_o = static_cast<float*>(workspace);
+  float* ws_l = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes * ns);
+  FwdParams p{};
+  p.o = ws_o;
+  p.lse = ws_l;
+  p.o_head_stride = rows;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = rows; p.Nk = Nk;
+  p.nqc = 1;
+  p.head_group = 1;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.mask_kind = causal ? MASK_CAUSAL : MASK_NONE;
+  p.nkb = (int)cdiv(Nk, TILE);
+  p.seq_lens = seq_lens;
+  p.n_splits = ns;
+  p.split_tiles = (int)cdiv(cdiv(Nk, TILE), ns);
+  p.dec_nq = Nq;
+  p.split_rows = total_rows;
+  p.status = status;
+  p.wait_limit_ns = wait_limit();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  {
+    TraceScope ts(ATTN_KERNEL_DECODE, s);
+    e = launch_fwd(d, true, tq, tk, tv, p, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  const float* op[64];
+  const float* lp[64];
+  for (int c = 0; c < ns; ++c) {
+    op[c] = ws_o + (size_t)c * total_rows * d;
+    lp[c] = ws_l + (size_t)c * total_rows;
+  }
+  {
+    TraceScope ts(ATTN_KERNEL_MERGE, s);
+    e = launch_merge(op, lp, ns, o, false, lse, Nq, B * Hq, d, Nq, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "decode merge launch");
+  return ATTN_OK;
 }
 
 int attn_merge_lse(const float* const* o_parts, const float* const* lse_parts, int n_parts, void* o_out,

@@ -83,8 +83,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   auto bar_o = [&](int t) { return smem_u32(&bars[1 + 4 * NS + 4 + t]); };
   const uint32_t bar_done = smem_u32(&bars[1 + 4 * NS + 6]);
 
-  const Unit u = fwd_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.Nq, p.Nk, p.nqc, p.head_group, p.mask_kind, p.causal_in_blocks,
-                          p.block_mask, p.nkb, p.window, p.q_offset, p.kv_offset);
+  const Unit u = p.n_splits > 0
+                     ? decode_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.dec_nq, p.Nk, p.seq_lens, p.n_splits, p.split_tiles)
+                     : fwd_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.Nq, p.Nk, p.nqc, p.head_group, p.mask_kind,
+                                p.causal_in_blocks, p.block_mask, p.nkb, p.window, p.q_offset, p.kv_offset);
   WaitCtx wc{p.wait_limit_ns, p.status, &abort_flag};
 
   if (threadIdx.x == 0) {
@@ -274,7 +276,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const uint32_t tO = tmem + lane_off + C::TMEM_O + t * D;
     const float c = p.scale_log2;
     const bool causal = mask_is_causal(p.mask_kind, p.causal_in_blocks);
-    const int64_t row_first_pos = p.q_offset + u.row0 + t * TILE;  // first row of the tile
+    // positions: row i of the call sits at q_offset + i; when decoding, row r
+    // is query r % dec_nq of its head, at u.pos0 + r % dec_nq
+    const bool decoding = p.n_splits > 0;
+    const int64_t row_first_pos = decoding ? u.pos0 : p.q_offset + u.row0 + t * TILE;  // earliest row of the tile
+    const int64_t qpos = decoding ? u.pos0 + qrow % p.dec_nq : p.q_offset + qrow;
     float m = -INFINITY, l = 0.f, lr = 0.f;
     int it = 0;
     bool ok = true;
@@ -287,20 +293,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       // and on tiles crossing the lower edge of a sliding window: column j is
       // visible iff lo <= j < lim
       const int64_t key0 = p.kv_offset + (int64_t)kt * TILE;
-      const bool tail = (kt == u.nkt - 1) && (p.Nk % TILE) != 0;
+      const bool tail = (kt == u.nkt - 1) && (u.nk % TILE) != 0;
       const bool diag = causal && (key0 + TILE - 1 > row_first_pos);
       const bool wedge = p.mask_kind == MASK_SLIDING_WINDOW && key0 + p.window <= row_first_pos + TILE - 1;
       const bool edge = tail || diag || wedge;
       int lo = 0, lim = 128;
       if (edge) {
-        int64_t l64 = p.Nk - (int64_t)kt * TILE;
+        int64_t l64 = u.nk - (int64_t)kt * TILE;
         if (causal) {
-          const int64_t lc = p.q_offset + qrow - key0 + 1;
+          const int64_t lc = qpos - key0 + 1;
           l64 = lc < l64 ? lc : l64;
         }
         lim = (int)(l64 < 0 ? 0 : (l64 > 128 ? 128 : l64));
         if (wedge) {
-          const int64_t f64 = p.q_offset + qrow - p.window + 1 - key0;   // first key in the row's window
+          const int64_t f64 = qpos - p.window + 1 - key0;   // first key in the row's window
           lo = (int)(f64 < 0 ? 0 : (f64 > 128 ? 128 : f64));
         }
       }
@@ -408,7 +414,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         tc_fence_after();
         const bool valid_row = qrow < p.Nq;
         const float inv_l = (lr > 0.f) ? 1.f / lr : 0.f;
-        const size_t orow = (size_t)u.bh * (size_t)p.o_head_stride + (size_t)qrow;
+        const size_t orow = (size_t)u.split * (size_t)p.split_rows + (size_t)u.bh * (size_t)p.o_head_stride +
+                            (size_t)qrow;
 #pragma unroll
         for (int h64 = 0; h64 < D / 64; ++h64) {
           uint32_t rr[64];
@@ -461,7 +468,8 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   auto kern = fwd_kernel<D, F32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(p.B * p.Hq) * (unsigned)p.nqc;
+  const unsigned grid = p.n_splits > 0 ? (unsigned)(p.B * p.Hkv) * (unsigned)p.n_splits
+                                       : (unsigned)(p.B * p.Hq) * (unsigned)p.nqc;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

@@ -28,6 +28,14 @@ struct FwdParams {
   int nkb;                    // ceil(Nk/128)
   int window;                 // sliding window width (MASK_SLIDING_WINDOW)
   int64_t q_offset, kv_offset;
+  // split-KV decoding (n_splits > 0): a unit is one (b * Hkv + kv head, split);
+  // its query rows are the Hq/Hkv heads x dec_nq positions of that kv head
+  // (contiguous in q), and it covers split_tiles key tiles of the cache
+  const int* seq_lens;        // device [B] keys per sequence, or null (Nk each)
+  int n_splits;
+  int split_tiles;
+  int dec_nq;                 // query positions per head
+  int64_t split_rows;         // output rows between consecutive splits' partials
   unsigned int* status;
   int64_t wait_limit_ns;
 };

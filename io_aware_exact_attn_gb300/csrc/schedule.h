@@ -28,7 +28,10 @@ namespace attn {
 struct Unit {
   int bh, kvh;
   int row0;         // first local query row of the unit
-  int nkt;          // key tiles in the call
+  int nk;           // keys the unit's rows may see (Nk, or a cached sequence's length)
+  int nkt;          // ceil(nk / 128)
+  int split;        // decoding: which split of the key range (0 otherwise)
+  int64_t pos0;     // decoding: position of query 0 (nk - dec_nq)
   int lo[2], lim[2];  // per query tile t: key tiles [lo[t], lim[t]) may be visible
   int kt_begin, kt_end;  // min(lo), max(lim) over the unit's tiles
   const uint8_t* mrow[2];  // block-sparse mask row per tile, or null
@@ -112,7 +115,10 @@ ATTN_HD Unit fwd_unit(int64_t i, int B, int Hq, int Hkv, int Nq, int Nk, int nqc
   const int b = u.bh / Hq, h = u.bh % Hq;
   u.kvh = b * Hkv + h / (Hq / Hkv);
   u.row0 = qc * UNIT_ROWS;
+  u.nk = Nk;
   u.nkt = (Nk + TILE - 1) / TILE;
+  u.split = 0;
+  u.pos0 = 0;
   const bool causal = mask_is_causal(mask_kind, causal_in_blocks);
   u.kt_begin = u.nkt;
   u.kt_end = 0;
@@ -134,6 +140,40 @@ ATTN_HD Unit fwd_unit(int64_t i, int B, int Hq, int Hkv, int Nq, int Nk, int nqc
     u.mrow[t] = (mask_kind == MASK_BLOCK_SPARSE && r0 < Nq) ? block_mask + (int64_t)(r0 / TILE) * nkb : nullptr;
   }
   if (u.kt_begin > u.kt_end) u.kt_begin = u.kt_end;
+  return u;
+}
+
+// Split-KV decoding unit i of B * Hkv * n_splits: splits of one kv head are
+// adjacent.  The rows are the g = Hq/Hkv heads x nq positions of kv head
+// (b, hk), packed in q's own order (head-major), so row r is query position
+// r % nq of head hk * g + r / nq.  Key tiles [split * split_tiles, ...) of the
+// sequence's len = seq_lens[b] cached keys; a split past the end is empty.
+ATTN_HD Unit decode_unit(int64_t i, int B, int Hq, int Hkv, int nq, int Nk, const int* seq_lens, int n_splits,
+                         int split_tiles) {
+  Unit u;
+  u.split = (int)(i % n_splits);
+  const int bkv = (int)(i / n_splits);
+  const int b = bkv / Hkv;
+  u.bh = bkv;
+  u.kvh = bkv;
+  u.row0 = 0;
+  int len = seq_lens != nullptr ? seq_lens[b] : Nk;
+  len = len < 0 ? 0 : (len > Nk ? Nk : len);
+  u.nk = len;
+  u.nkt = (len + TILE - 1) / TILE;
+  u.pos0 = (int64_t)len - nq;
+  const int rows = (Hq / Hkv) * nq;
+  int lo = u.split * split_tiles, lim = lo + split_tiles;
+  if (lim > u.nkt) lim = u.nkt;
+  if (lo > lim) lo = lim;
+  u.kt_begin = lo;
+  u.kt_end = lim;
+  for (int t = 0; t < 2; ++t) {
+    const bool has_rows = t * TILE < rows;
+    u.lo[t] = has_rows ? lo : 0;
+    u.lim[t] = has_rows ? lim : 0;
+    u.mrow[t] = nullptr;
+  }
   return u;
 }
 

@@ -64,10 +64,10 @@ def test_argument_validation_without_gpu(lib):
                         None) == -1
     assert lib.attn_fwd(_ptr(good), _ptr(good), _ptr(good), _ptr(good), None, 1, 2, 2, 128, 64, -1.0, m,
                         None) == -1
-    bad = _ffi.attn_mask_t(7, 0, None)
+    bad = _ffi.attn_mask_t(7, 0, None, 0)
     assert lib.attn_fwd(_ptr(good), _ptr(good), _ptr(good), _ptr(good), None, 1, 2, 2, 128, 64, 0.125,
                         C.byref(bad), None) == -1
-    sparse_no_mask = _ffi.attn_mask_t(2, 0, None)
+    sparse_no_mask = _ffi.attn_mask_t(2, 0, None, 0)
     assert lib.attn_fwd(_ptr(good), _ptr(good), _ptr(good), _ptr(good), None, 1, 2, 2, 128, 64, 0.125,
                         C.byref(sparse_no_mask), None) == -1
     assert "multiple" in lib.attn_last_error_message().decode() or lib.attn_last_error_message()
@@ -80,6 +80,26 @@ def test_argument_validation_without_gpu(lib):
     assert need == ((2 * 2 * 4 * 128 * 4 + 255) // 256) * 256
     p = [_ptr(good)] * 10
     assert lib.attn_bwd(*p, need - 256, 2, 4, 2, 100, 64, 0.125, None, None) == -6
+    # sliding window needs a width of at least one
+    no_width = _ffi.attn_mask_t(3, 0, None, 0)
+    assert lib.attn_fwd(_ptr(good), _ptr(good), _ptr(good), _ptr(good), None, 1, 2, 2, 128, 64, 0.125,
+                        C.byref(no_width), None) == -1
+    # decode: workspace size, split count, row and length limits
+    assert lib.attn_decode_splits(8, 8, 32768) == 14           # ceil(6 * 148 / 64) splits
+    assert lib.attn_decode_splits(1, 1, 100) == 1              # never more splits than key tiles
+    assert lib.attn_decode_splits(1, 1, 1 << 20) == 64
+    wsb = lib.attn_decode_workspace_bytes(2, 8, 2, 3, 1000, 64, 4)
+    rows = 2 * 8 * 3
+    assert wsb == 4 * (((rows * 64 * 4 + 255) // 256) * 256 + ((rows * 4 + 255) // 256) * 256)
+    q = [_ptr(good)] * 3
+    assert lib.attn_decode_fwd(*q, None, _ptr(good), None, 2, 8, 2, 3, 1000, 64, 0.125, 1, 4, _ptr(good),
+                               wsb - 1, None) == -6
+    assert lib.attn_decode_fwd(*q, None, _ptr(good), None, 2, 64, 1, 8, 1000, 64, 0.125, 1, 4, _ptr(good),
+                               1 << 30, None) == -1                                       # 64 * 8 rows > 256
+    assert lib.attn_decode_fwd(*q, None, _ptr(good), None, 2, 8, 2, 3, 2, 64, 0.125, 1, 4, _ptr(good),
+                               1 << 30, None) == -1                                       # Nq > Nk
+    assert lib.attn_decode_fwd(*q, None, _ptr(good), None, 2, 8, 2, 3, 1000, 64, 0.125, 1, 65, _ptr(good),
+                               1 << 30, None) == -1                                       # too many splits
     # partial fwd: head stride smaller than the rows is rejected
     assert lib.attn_partial_fwd(_ptr(good), _ptr(good), _ptr(good), _ptr(good), _ptr(good), 1, 2, 2, 256, 256,
                                 64, 0.125, None, 0, 0, 100, 0, None) == -1
