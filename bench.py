@@ -42,6 +42,7 @@ WORKLOAD = dict(name="gpt_causal", B=2, Hq=32, Hkv=32, N=8192, d=128, mask="caus
 CHUNKED = dict(name="chunked_gqa", B=1, Hq=32, Hkv=8, N=32768, d=128, chunks=8)
 WINDOW = dict(name="gpt_sliding_window", B=2, Hq=32, Hkv=32, N=8192, d=128, window=4096)
 DECODE = dict(name="decode_gqa", B=8, Hq=32, Hkv=8, Nq=1, Nk=32768, d=128)
+VARLEN = dict(name="varlen_causal", B=16, Hq=32, Hkv=32, d=128, min_len=512, max_len=8192)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
     "fwd": ["fwd.cu", "ptx.cuh", "schedule.h", "internal.h"],
@@ -393,6 +394,7 @@ def main():
         out["chunked_gqa"] = chunked_leg(api, inputs, torch, peaks, rank)
         out["sliding_window"] = window_leg(api, inputs, torch, peaks, rank)
         out["decode"] = decode_leg(api, inputs, torch, peaks, rank)
+        out["varlen"] = varlen_leg(api, inputs, torch, peaks, rank)
         if rank == 0:
             out["cpu_baseline"] = {k_: v_ for k_, v_ in oracle_sample(args.cpu_seconds).items()
                                    if k_ in ("value", "unit", "cores", "kind", "sample")}
@@ -558,6 +560,48 @@ def decode_leg(api, inputs, torch, peaks, rank, reps=20, splits=(0, 8, 16, 24)):
                 by_splits={str(ns if ns else auto): dict(decode_ms=a, merge_ms=b,
                                                          gbs=algo_bytes / ((a + b) * 1e-3) / 1e9)
                            for ns, (a, b) in res.items()})
+
+
+def varlen_lengths(seed):
+    """Seeded ragged lengths: uniform in [min_len, max_len] (the longest forced to max_len)."""
+    import numpy as np
+    c = VARLEN
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(c["min_len"], c["max_len"] + 1, c["B"])
+    lens[0] = c["max_len"]
+    return [int(x) for x in lens]
+
+
+def varlen_leg(api, inputs, torch, peaks, rank, reps=10):
+    """Causal forward over 16 packed sequences of 512..8192 tokens (H=32, d=128),
+    token-major [total, H, d].  FLOPs: 4*H*d*len^2/2 per sequence (the causal
+    convention of the main metric)."""
+    import numpy as np
+    c = VARLEN
+    lens = varlen_lengths(inputs.SEED + 100 * rank + 11)
+    total = sum(lens)
+    g = torch.Generator().manual_seed(inputs.SEED + 100 * rank + 12)
+    q = torch.randn(total, c["Hq"], c["d"], generator=g).to(torch.bfloat16).cuda()
+    k = torch.randn(total, c["Hkv"], c["d"], generator=g).to(torch.bfloat16).cuda()
+    v = torch.randn(total, c["Hkv"], c["d"], generator=g).to(torch.bfloat16).cuda()
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32).cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty(c["Hq"], total, device="cuda")
+    for _ in range(3):
+        api.attn_varlen_fwd(q, k, v, cu, max(lens), causal=True, out=o, lse=lse)
+    torch.cuda.synchronize()
+    api.trace_enable(2 * reps)
+    for _ in range(reps):
+        api.attn_varlen_fwd(q, k, v, cu, max(lens), causal=True, out=o, lse=lse)
+    torch.cuda.synchronize()
+    api.trace_disable()
+    recs, _ = api.trace_read(2 * reps)
+    ms = sum(t for n, t in recs if n == "varlen_fwd") / reps
+    flops = sum(4.0 * c["Hq"] * c["d"] * n * n * 0.5 for n in lens)
+    tf = flops / (ms * 1e-3) / 1e12
+    return dict(workload=f"{c['B']} sequences, {c['min_len']}..{c['max_len']} tokens (total {total}), "
+                         f"Hq={c['Hq']} Hkv={c['Hkv']} d={c['d']} causal, packed [total, H, d]",
+                fwd_ms=ms, fwd_tflops=tf, fwd_frac_of_burst_peak=tf / peaks["bf16_tflops"])
 
 
 if __name__ == "__main__":

@@ -174,6 +174,26 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o,
              int N, int d, float scale, const attn_mask_t* mask, void* stream);
 
 /*
+ * attn_varlen_fwd -- attn_fwd over a batch of sequences of different lengths
+ * packed back to back ("FlashAttention-2" reviews: variable-length inputs
+ * without padding).  Sequence b holds tokens [cu_seqlens[b], cu_seqlens[b+1])
+ * of the packed token-major tensors; positions, the causal rule and the
+ * sliding window are local to each sequence, and no key of one sequence is
+ * visible to a query of another.
+ *   q           device bf16 [total, Hq,  d]   k, v device bf16 [total, Hkv, d]
+ *   o           device bf16 [total, Hq,  d]   (written)
+ *   lse         device f32  [Hq, total]       (written; may be NULL)
+ *   cu_seqlens  device int32 [B + 1], non-decreasing, cu_seqlens[0] = 0 and
+ *               cu_seqlens[B] = total; read by the kernel
+ *   max_len     >= the longest sequence (work beyond it is not launched)
+ *   mask        NULL, causal or sliding window (block-sparse: UNSUPPORTED)
+ */
+int attn_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int32_t* cu_seqlens, int B, int max_len, int64_t total,
+                    int Hq, int Hkv, int d, float scale, const attn_mask_t* mask,
+                    void* stream);
+
+/*
  * attn_decode_fwd -- one decoding step against a key/value cache, split over
  * the cache ("FlashAttention-2" reviews: splitting the KV cache amongst thread
  * blocks for inference).  Sequence b holds seq_lens[b] cached positions (Nk
@@ -314,7 +334,8 @@ typedef enum {
   ATTN_KERNEL_BWD_DKDV = 5,       /* attn_bwd step 2: dK, dV */
   ATTN_KERNEL_BWD_DQ = 6,         /* attn_bwd step 3: dQ */
   ATTN_KERNEL_SELFTEST = 7,       /* attn_selftest_wait_timeout */
-  ATTN_KERNEL_DECODE = 8          /* attn_decode_fwd split-KV partials (its merge is ATTN_KERNEL_MERGE) */
+  ATTN_KERNEL_DECODE = 8,         /* attn_decode_fwd split-KV partials (its merge is ATTN_KERNEL_MERGE) */
+  ATTN_KERNEL_VARLEN_FWD = 9      /* attn_varlen_fwd forward kernel */
 } attn_kernel_id_t;
 
 typedef struct attn_trace_record {

@@ -192,6 +192,41 @@ def attn_bwd(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = 
     return dq, dk, dv
 
 
+def attn_varlen_fwd(q, k, v, cu_seqlens: torch.Tensor, max_len: Optional[int] = None,
+                    scale: Optional[float] = None, causal: bool = False, window: Optional[int] = None,
+                    out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None):
+    """Forward over sequences of different lengths packed back to back.
+
+    ``q`` ``[total, Hq, d]``, ``k``/``v`` ``[total, Hkv, d]`` (token-major);
+    ``cu_seqlens`` int32 ``[B + 1]`` token offsets (on the GPU).  Returns
+    ``(O [total, Hq, d] bf16, LSE [Hq, total] f32)``.
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 3):
+            raise ValueError(f"{n} must be a contiguous CUDA bf16 [total, heads, d] tensor")
+    total, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (total, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [total, Hkv, d] matching q")
+    cu = cu_seqlens.to(device=q.device, dtype=torch.int32).contiguous()
+    B = cu.numel() - 1
+    if B < 1:
+        raise ValueError("cu_seqlens needs at least two entries")
+    if max_len is None:
+        max_len = int((cu[1:] - cu[:-1]).max().item())
+    o = torch.empty_like(q) if out is None else out
+    _contig(o, "out")
+    l = torch.empty((Hq, total), device=q.device, dtype=torch.float32) if lse is None else lse
+    _contig(l, "lse", torch.float32)
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    m, keep = mask_desc(causal, None, False, window)
+    check(_ffi.lib().attn_varlen_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
+                                     cu.data_ptr(), B, int(max_len), int(total), Hq, Hkv, d, sc, _mp(m), _stream(q)),
+          "attn_varlen_fwd")
+    del keep
+    return o, l
+
+
 def decode_splits(B: int, Hkv: int, Nk: int) -> int:
     return int(_ffi.lib().attn_decode_splits(B, Hkv, Nk))
 

@@ -192,6 +192,22 @@ int encode_rows_map(CUtensorMap* map, const void* base, int d, int rows, int hea
   return ATTN_OK;
 }
 
+// Token-major [total][heads][d] bf16 as the same 3-D view (columns, rows =
+// tokens, heads): consecutive tokens of one head are heads*d elements apart.
+int encode_tokens_map(CUtensorMap* map, const void* base, int d, int64_t total, int heads) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)total, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {(cuuint64_t)heads * d * 2, (cuuint64_t)d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_INVALID_ARG, "cuTensorMapEncodeTiled (token-major) failed (%d)", (int)r);
+  return ATTN_OK;
+}
+
 }  // namespace attn
 
 // ====================================================================== C ABI
@@ -247,7 +263,10 @@ static int fwd_common(const void* q, const void* k, const void* v, void* o, bool
   FwdParams p{};
   p.o = o;
   p.lse = lse;
-  p.o_head_stride = Nq;
+  p.o_hs = (int64_t)Nq * d;
+  p.o_rs = d;
+  p.l_hs = Nq;
+  p.l_rs = 1;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = Nq; p.Nk = Nk;
   p.nqc = (int)cdiv(Nq, UNIT_ROWS);
   p.head_group = kv_stream_group(B, Hq, Hkv, Nk, d);
@@ -282,6 +301,55 @@ int attn_partial_fwd(const void* q, const void* k, const void* v, float* o_part,
   if (lse_part == nullptr) return fail(ATTN_ERR_INVALID_ARG, "lse_part is NULL");
   return fwd_common(q, k, v, o_part, true, lse_part, B, Hq, Hkv, Nq, Nk, d, scale, mask, q_offset, kv_offset,
                     q_head_stride > 0 ? q_head_stride : Nq, kv_head_stride > 0 ? kv_head_stride : Nk, stream);
+}
+
+int attn_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens, int B,
+                    int max_len, int64_t total, int Hq, int Hkv, int d, float scale, const attn_mask_t* mask,
+                    void* stream) {
+  int rc;
+  if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k, "k")) || (rc = check_ptr(v, "v")) || (rc = check_ptr(o, "o")))
+    return rc;
+  if (cu_seqlens == nullptr) return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens is NULL");
+  if (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) return fail(ATTN_ERR_MISALIGNED, "cu_seqlens not 4-byte aligned");
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(ATTN_ERR_MISALIGNED, "lse not 4-byte aligned");
+  if (total < 1 || total > ((int64_t)1 << 31) - 1) return fail(ATTN_ERR_INVALID_ARG, "total=%lld", (long long)total);
+  if (max_len < 1) return fail(ATTN_ERR_INVALID_ARG, "max_len=%d", max_len);
+  if ((rc = check_dims(B, Hq, Hkv, max_len, max_len, d, scale))) return rc;
+  MaskArgs m;
+  if ((rc = read_mask(mask, &m))) return rc;
+  if (m.kind == MASK_BLOCK_SPARSE) return fail(ATTN_ERR_UNSUPPORTED, "block-sparse masks are not built for ragged batches");
+  unsigned int* status = nullptr;
+  if ((rc = device_ready(&status))) return rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = encode_tokens_map(&tq, q, d, total, Hq)) || (rc = encode_tokens_map(&tk, k, d, total, Hkv)) ||
+      (rc = encode_tokens_map(&tv, v, d, total, Hkv)))
+    return rc;
+  FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.o_hs = d;
+  p.o_rs = (int64_t)Hq * d;
+  p.l_hs = total;
+  p.l_rs = 1;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = max_len; p.Nk = max_len;
+  p.nqc = (int)cdiv(max_len, UNIT_ROWS);
+  p.head_group = 1;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.mask_kind = m.kind;
+  p.window = m.window;
+  p.nkb = (int)cdiv(max_len, TILE);
+  p.dec_nq = 1;
+  p.cu_seqlens = cu_seqlens;
+  p.varlen_nqc = p.nqc;
+  p.status = status;
+  p.wait_limit_ns = wait_limit();
+  cudaError_t e;
+  {
+    TraceScope ts(ATTN_KERNEL_VARLEN_FWD, static_cast<cudaStream_t>(stream));
+    e = launch_fwd(d, false, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "variable-length forward launch");
+  return ATTN_OK;
 }
 
 int attn_decode_splits(int B, int Hkv, int Nk) {
@@ -337,7 +405,10 @@ int attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, con
   FwdParams p{};
   p.o = ws_o;
   p.lse = ws_l;
-  p.o_head_stride = rows;
+  p.o_hs = (int64_t)rows * d;
+  p.o_rs = d;
+  p.l_hs = rows;
+  p.l_rs = 1;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = rows; p.Nk = Nk;
   p.nqc = 1;
   p.head_group = 1;

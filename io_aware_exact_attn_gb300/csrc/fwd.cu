@@ -83,10 +83,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   auto bar_o = [&](int t) { return smem_u32(&bars[1 + 4 * NS + 4 + t]); };
   const uint32_t bar_done = smem_u32(&bars[1 + 4 * NS + 6]);
 
-  const Unit u = p.n_splits > 0
-                     ? decode_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.dec_nq, p.Nk, p.seq_lens, p.n_splits, p.split_tiles)
-                     : fwd_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.Nq, p.Nk, p.nqc, p.head_group, p.mask_kind,
-                                p.causal_in_blocks, p.block_mask, p.nkb, p.window, p.q_offset, p.kv_offset);
+  const Unit u =
+      p.n_splits > 0 ? decode_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.dec_nq, p.Nk, p.seq_lens, p.n_splits, p.split_tiles)
+      : p.cu_seqlens != nullptr
+          ? varlen_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.varlen_nqc, p.cu_seqlens, p.mask_kind, p.window)
+          : fwd_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.Nq, p.Nk, p.nqc, p.head_group, p.mask_kind, p.causal_in_blocks,
+                     p.block_mask, p.nkb, p.window, p.q_offset, p.kv_offset);
+  if (u.empty) return;   // a chunk past the end of its sequence: nothing to do, nothing set up yet
   WaitCtx wc{p.wait_limit_ns, p.status, &abort_flag};
 
   if (threadIdx.x == 0) {
@@ -131,7 +134,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     __syncwarp();
     if (lane < 2 * C::NBOX) {
       const int t = lane / C::NBOX, bx = lane % C::NBOX;
-      tma_load_3d(s_base + t * C::TILE_BYTES + bx * C::BOX_BYTES, &tq, bx * 64, u.row0 + t * TILE, u.bh, bar_q);
+      tma_load_3d(s_base + t * C::TILE_BYTES + bx * C::BOX_BYTES, &tq, bx * 64, (int)(u.seq0 + u.row0 + t * TILE), u.bh,
+                  bar_q);
     }
     int n = 0;
     bool ok = true;
@@ -144,7 +148,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       if (lane == 0) mbar_arrive_expect_tx(bar_k(s), C::TILE_BYTES);
       __syncwarp();
       if (lane < C::NBOX)
-        tma_load_3d(s_base + C::OFF_K + s * C::TILE_BYTES + lane * C::BOX_BYTES, &tk, lane * 64, kt * TILE, u.kvh,
+        tma_load_3d(s_base + C::OFF_K + s * C::TILE_BYTES + lane * C::BOX_BYTES, &tk, lane * 64,
+                    (int)(u.seq0 + kt * TILE), u.kvh,
                     bar_k(s));
       if (n >= NS) ok = wait_bar(bar_vfree(s), fph, wc);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
@@ -152,7 +157,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       __syncwarp();
       if (lane >= C::NBOX && lane < 2 * C::NBOX)
         tma_load_3d(s_base + C::OFF_V + s * C::TILE_BYTES + (lane - C::NBOX) * C::BOX_BYTES, &tv,
-                    (lane - C::NBOX) * 64, kt * TILE, u.kvh, bar_v(s));
+                    (lane - C::NBOX) * 64, (int)(u.seq0 + kt * TILE), u.kvh, bar_v(s));
       ++n;
     }
     if ((!ok || abort_flag) && lane == 0) {
@@ -412,10 +417,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
       if (ok) {
         tc_fence_after();
-        const bool valid_row = qrow < p.Nq;
+        const bool valid_row = qrow < u.nq;
         const float inv_l = (lr > 0.f) ? 1.f / lr : 0.f;
-        const size_t orow = (size_t)u.split * (size_t)p.split_rows + (size_t)u.bh * (size_t)p.o_head_stride +
-                            (size_t)qrow;
+        const int64_t grow = u.seq0 + qrow;   // row within the head (token index when batches are ragged)
+        const int64_t split_off = (int64_t)u.split * p.split_rows;
+        const size_t o_off = (size_t)(split_off * D + (int64_t)u.bh * p.o_hs + grow * p.o_rs);
+        const size_t l_off = (size_t)(split_off + (int64_t)u.bh * p.l_hs + grow * p.l_rs);
 #pragma unroll
         for (int h64 = 0; h64 < D / 64; ++h64) {
           uint32_t rr[64];
@@ -427,14 +434,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           }
           if (valid_row) {
             if constexpr (OUT_F32) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + h64 * 64);
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + o_off + h64 * 64);
 #pragma unroll
               for (int j = 0; j < 16; ++j)
                 dst[j] = make_float4(__uint_as_float(rr[4 * j]) * inv_l, __uint_as_float(rr[4 * j + 1]) * inv_l,
                                      __uint_as_float(rr[4 * j + 2]) * inv_l,
                                      __uint_as_float(rr[4 * j + 3]) * inv_l);
             } else {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + h64 * 64);
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + o_off + h64 * 64);
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
                 uint4 v4;
@@ -448,7 +455,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           }
         }
         if (valid_row && p.lse != nullptr)
-          p.lse[orow] = (l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+          p.lse[l_off] = (l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
     }
   }
@@ -468,8 +475,9 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   auto kern = fwd_kernel<D, F32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const unsigned grid = p.n_splits > 0 ? (unsigned)(p.B * p.Hkv) * (unsigned)p.n_splits
-                                       : (unsigned)(p.B * p.Hq) * (unsigned)p.nqc;
+  const unsigned grid = p.n_splits > 0           ? (unsigned)(p.B * p.Hkv) * (unsigned)p.n_splits
+                        : p.cu_seqlens != nullptr ? (unsigned)(p.B * p.Hq) * (unsigned)p.varlen_nqc
+                                                  : (unsigned)(p.B * p.Hq) * (unsigned)p.nqc;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

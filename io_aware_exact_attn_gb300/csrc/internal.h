@@ -17,7 +17,6 @@ enum MaskKind : int { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_BLOCK_SPARSE = 2, MAS
 struct FwdParams {
   void* o;                  // bf16 or f32 output rows, row stride d
   float* lse;               // may be null
-  int64_t o_head_stride;    // rows between consecutive (b, h) heads of o / lse
   int B, Hq, Hkv, Nq, Nk;
   int nqc;                  // number of 256-row query chunks
   int head_group;           // heads per L2 group (schedule.h)
@@ -36,6 +35,13 @@ struct FwdParams {
   int split_tiles;
   int dec_nq;                 // query positions per head
   int64_t split_rows;         // output rows between consecutive splits' partials
+  // variable-length batches (cu_seqlens != null): q, k, v, o are token-major
+  // [total, heads, d]; sequence b holds tokens [cu_seqlens[b], cu_seqlens[b+1])
+  const int* cu_seqlens;      // device [B + 1]
+  int varlen_nqc;             // 256-row chunks of the longest sequence
+  // output element strides: O[head h, row r] at h * o_hs + r * o_rs (plus the
+  // split offset when decoding), LSE at h * l_hs + r * l_rs
+  int64_t o_hs, o_rs, l_hs, l_rs;
   unsigned int* status;
   int64_t wait_limit_ns;
 };

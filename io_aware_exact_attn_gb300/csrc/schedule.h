@@ -32,6 +32,9 @@ struct Unit {
   int nkt;          // ceil(nk / 128)
   int split;        // decoding: which split of the key range (0 otherwise)
   int64_t pos0;     // decoding: position of query 0 (nk - dec_nq)
+  int nq;           // query rows of the unit's sequence (rows at or past it are not written)
+  int64_t seq0;     // variable-length batches: first token of the sequence (0 otherwise)
+  bool empty;       // variable-length batches: no rows of this sequence in the unit
   int lo[2], lim[2];  // per query tile t: key tiles [lo[t], lim[t]) may be visible
   int kt_begin, kt_end;  // min(lo), max(lim) over the unit's tiles
   const uint8_t* mrow[2];  // block-sparse mask row per tile, or null
@@ -119,6 +122,9 @@ ATTN_HD Unit fwd_unit(int64_t i, int B, int Hq, int Hkv, int Nq, int Nk, int nqc
   u.nkt = (Nk + TILE - 1) / TILE;
   u.split = 0;
   u.pos0 = 0;
+  u.nq = Nq;
+  u.seq0 = 0;
+  u.empty = false;
   const bool causal = mask_is_causal(mask_kind, causal_in_blocks);
   u.kt_begin = u.nkt;
   u.kt_end = 0;
@@ -163,6 +169,9 @@ ATTN_HD Unit decode_unit(int64_t i, int B, int Hq, int Hkv, int nq, int Nk, cons
   u.nkt = (len + TILE - 1) / TILE;
   u.pos0 = (int64_t)len - nq;
   const int rows = (Hq / Hkv) * nq;
+  u.nq = rows;
+  u.seq0 = 0;
+  u.empty = false;
   int lo = u.split * split_tiles, lim = lo + split_tiles;
   if (lim > u.nkt) lim = u.nkt;
   if (lo > lim) lo = lim;
@@ -174,6 +183,32 @@ ATTN_HD Unit decode_unit(int64_t i, int B, int Hq, int Hkv, int nq, int Nk, cons
     u.lim[t] = has_rows ? lim : 0;
     u.mrow[t] = nullptr;
   }
+  return u;
+}
+
+// Variable-length unit i of B * Hq * nqc_max: position-major with the
+// (batch, head) pairs inner, so every sequence's latest (heaviest) chunk comes
+// first; chunks past a sequence's end are empty.  Inside its sequence a unit
+// is an ordinary forward unit (local positions, the same masks).
+ATTN_HD Unit varlen_unit(int64_t i, int B, int Hq, int Hkv, int nqc_max, const int* cu_seqlens, int mask_kind,
+                         int window) {
+  const int64_t bh = i % ((int64_t)B * Hq);
+  const int pos = (int)(i / ((int64_t)B * Hq));
+  const int b = (int)(bh / Hq), h = (int)(bh % Hq);
+  const int64_t seq0 = cu_seqlens[b];
+  int len = (int)(cu_seqlens[b + 1] - seq0);
+  len = len < 0 ? 0 : len;
+  const int qc = nqc_max - 1 - pos;
+  const int nqc = (len + UNIT_ROWS - 1) / UNIT_ROWS;
+  Unit u;
+  if (qc >= nqc) {
+    u.empty = true;
+    return u;
+  }
+  u = fwd_unit(nqc - 1 - qc, 1, 1, 1, len, len, nqc, 1, mask_kind, 0, nullptr, 0, window, 0, 0);
+  u.bh = h;
+  u.kvh = h / (Hq / Hkv);
+  u.seq0 = seq0;
   return u;
 }
 

@@ -36,6 +36,7 @@ from .attention import (  # noqa: F401
     attention_backward,
     attention_backward_dq_rows,
     decode_forward,
+    varlen_forward,
     merge_partials,
 )
 from .schedule import (  # noqa: F401

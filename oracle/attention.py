@@ -226,6 +226,31 @@ def attention_backward_dq_rows(q, k, v, do, scale: float, b: int, h: int, rows,
     return dq
 
 
+def varlen_forward(q, k, v, cu_seqlens, scale: float, mask: MaskSpec = MaskSpec()):
+    """Exact attention over sequences packed back to back, in float64.
+
+    ``q`` is ``[total, Hq, d]`` and ``k``/``v`` ``[total, Hkv, d]`` (token-major);
+    sequence ``b`` is tokens ``cu_seqlens[b]:cu_seqlens[b+1]``.  Each sequence
+    is attended on its own with local positions (no key of one sequence is
+    visible to another's queries).  Returns ``O [total, Hq, d]`` and
+    ``LSE [Hq, total]``.
+    """
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
+    total, Hq, d = q.shape
+    o = np.zeros((total, Hq, d))
+    lse = np.full((Hq, total), -np.inf)
+    cu = [int(x) for x in cu_seqlens]
+    for b in range(len(cu) - 1):
+        s0, s1 = cu[b], cu[b + 1]
+        if s1 <= s0:
+            continue
+        ob, lb = attention_forward(q[s0:s1].transpose(1, 0, 2)[None], k[s0:s1].transpose(1, 0, 2)[None],
+                                   v[s0:s1].transpose(1, 0, 2)[None], scale, mask)
+        o[s0:s1] = ob[0].transpose(1, 0, 2)
+        lse[:, s0:s1] = lb[0]
+    return o, lse
+
+
 def decode_forward(q, k_cache, v_cache, scale: float, seq_lens=None, causal: bool = True):
     """Attention of the newest ``Nq`` positions of each sequence against its
     key/value cache, in float64 (the decoding step of a KV-cache model;

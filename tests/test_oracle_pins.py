@@ -462,6 +462,37 @@ def test_decode_empty_sequence():
     assert np.all(np.isfinite(lse[1]))
 
 
+# ---------------------------------------------------------------- ragged (packed) batches
+
+def test_varlen_equal_lengths_equal_batched_forward():
+    B, Hq, Hkv, n, d = 3, 4, 2, 11, 5
+    q, k, v = rnd(B, Hq, n, d), rnd(B, Hkv, n, d), rnd(B, Hkv, n, d)
+    pack = lambda x: x.transpose(0, 2, 1, 3).reshape(B * n, x.shape[1], d)
+    cu = [0, n, 2 * n, 3 * n]
+    for mask in (MaskSpec("none"), MaskSpec("causal"), MaskSpec("sliding_window", window=4)):
+        o, lse = oracle.varlen_forward(pack(q), pack(k), pack(v), cu, 0.45, mask)
+        ob, lb = oracle.attention_forward(q, k, v, 0.45, mask)
+        np.testing.assert_allclose(o, pack(ob), atol=1e-15)
+        np.testing.assert_allclose(lse, lb.transpose(1, 0, 2).reshape(Hq, B * n), atol=1e-15)
+
+
+def test_varlen_q_zero_sees_only_its_own_sequence():
+    lens = [5, 1, 0, 9]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    total = int(cu[-1])
+    k, v = rnd(total, 2, 3), rnd(total, 2, 3)
+    q = np.zeros((total, 4, 3))
+    for causal in (False, True):
+        o, lse = oracle.varlen_forward(q, k, v, cu, 0.7, MaskSpec("causal" if causal else "none"))
+        for b, n in enumerate(lens):
+            for i in range(n):
+                t = cu[b] + i
+                top = i + 1 if causal else n                 # keys cu[b] .. cu[b] + top - 1 are visible
+                for h in range(4):
+                    np.testing.assert_allclose(o[t, h], v[cu[b]:cu[b] + top, h // 2].mean(axis=0), atol=1e-14)
+                    assert abs(lse[h, t] - np.log(top)) < 1e-13
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def _fails(fn):
