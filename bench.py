@@ -573,35 +573,45 @@ def varlen_lengths(seed):
 
 
 def varlen_leg(api, inputs, torch, peaks, rank, reps=10):
-    """Causal forward over 16 packed sequences of 512..8192 tokens (H=32, d=128),
-    token-major [total, H, d].  FLOPs: 4*H*d*len^2/2 per sequence (the causal
-    convention of the main metric)."""
+    """Causal forward and backward over 16 packed sequences of 512..8192 tokens
+    (H=32, d=128), token-major [total, H, d].  FLOPs: 4*H*d*len^2/2 per
+    sequence forward (the causal convention of the main metric), 2.5x that
+    backward."""
     import numpy as np
     c = VARLEN
     lens = varlen_lengths(inputs.SEED + 100 * rank + 11)
     total = sum(lens)
     g = torch.Generator().manual_seed(inputs.SEED + 100 * rank + 12)
-    q = torch.randn(total, c["Hq"], c["d"], generator=g).to(torch.bfloat16).cuda()
-    k = torch.randn(total, c["Hkv"], c["d"], generator=g).to(torch.bfloat16).cuda()
-    v = torch.randn(total, c["Hkv"], c["d"], generator=g).to(torch.bfloat16).cuda()
+    q, k, v, do = (torch.randn(total, h, c["d"], generator=g).to(torch.bfloat16).cuda()
+                   for h in (c["Hq"], c["Hkv"], c["Hkv"], c["Hq"]))
     cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32).cuda()
     o = torch.empty_like(q)
     lse = torch.empty(c["Hq"], total, device="cuda")
+    ws = torch.empty(api.varlen_bwd_workspace_bytes(len(lens), total, c["Hq"]), device="cuda", dtype=torch.uint8)
+    grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+
+    def run():
+        api.attn_varlen_fwd(q, k, v, cu, max(lens), causal=True, out=o, lse=lse)
+        api.attn_varlen_bwd(q, k, v, o, lse, do, cu, max(lens), causal=True, workspace=ws, dq=grads[0],
+                            dk=grads[1], dv=grads[2])
+
     for _ in range(3):
-        api.attn_varlen_fwd(q, k, v, cu, max(lens), causal=True, out=o, lse=lse)
+        run()
     torch.cuda.synchronize()
-    api.trace_enable(2 * reps)
+    api.trace_enable(8 * reps)
     for _ in range(reps):
-        api.attn_varlen_fwd(q, k, v, cu, max(lens), causal=True, out=o, lse=lse)
+        run()
     torch.cuda.synchronize()
     api.trace_disable()
-    recs, _ = api.trace_read(2 * reps)
-    ms = sum(t for n, t in recs if n == "varlen_fwd") / reps
+    recs, _ = api.trace_read(8 * reps)
+    fwd_ms = sum(t for n, t in recs if n == "varlen_fwd") / reps
+    bwd_ms = sum(t for n, t in recs if n.startswith("bwd_")) / reps
     flops = sum(4.0 * c["Hq"] * c["d"] * n * n * 0.5 for n in lens)
-    tf = flops / (ms * 1e-3) / 1e12
     return dict(workload=f"{c['B']} sequences, {c['min_len']}..{c['max_len']} tokens (total {total}), "
                          f"Hq={c['Hq']} Hkv={c['Hkv']} d={c['d']} causal, packed [total, H, d]",
-                fwd_ms=ms, fwd_tflops=tf, fwd_frac_of_burst_peak=tf / peaks["bf16_tflops"])
+                fwd_ms=fwd_ms, fwd_tflops=flops / (fwd_ms * 1e-3) / 1e12,
+                bwd_ms=bwd_ms, bwd_tflops=2.5 * flops / (bwd_ms * 1e-3) / 1e12,
+                fwd_frac_of_burst_peak=flops / (fwd_ms * 1e-3) / 1e12 / peaks["bf16_tflops"])
 
 
 if __name__ == "__main__":

@@ -194,6 +194,26 @@ int attn_varlen_fwd(const void* q, const void* k, const void* v, void* o, float*
                     void* stream);
 
 /*
+ * attn_varlen_bwd -- attn_bwd for the packed batches of attn_varlen_fwd
+ * (same layouts, cu_seqlens, max_len and mask; lse from attn_varlen_fwd).
+ *   dout        device bf16 [total, Hq, d]
+ *   dq          device bf16 [total, Hq, d]    dk, dv device bf16 [total, Hkv, d]
+ *   workspace   device, >= attn_varlen_bwd_workspace_bytes(B, total, Hq)
+ *               bytes, 256-byte aligned; caller-owned.  It holds the
+ *               per-sequence tile-padded offsets and D, LSE*log2 e per row.
+ * GQA: dK / dV sum over the query heads of a group, as in attn_bwd.
+ */
+int attn_varlen_bwd(const void* q, const void* k, const void* v, const void* o,
+                    const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                    const int32_t* cu_seqlens, int B, int max_len, int64_t total,
+                    int Hq, int Hkv, int d, float scale, const attn_mask_t* mask,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes for attn_varlen_bwd: (B+1) ints, then two float arrays of
+ * Hq * (total + 127*B) rows, each rounded up to 256 bytes. */
+size_t attn_varlen_bwd_workspace_bytes(int B, int64_t total, int Hq);
+
+/*
  * attn_decode_fwd -- one decoding step against a key/value cache, split over
  * the cache ("FlashAttention-2" reviews: splitting the KV cache amongst thread
  * blocks for inference).  Sequence b holds seq_lens[b] cached positions (Nk

@@ -52,6 +52,10 @@ SIGNATURES = {
     "attn_bwd_workspace_bytes": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
     "attn_varlen_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int64,
                                 c_int, c_int, c_int, c_float, C.POINTER(attn_mask_t), c_void_p]),
+    "attn_varlen_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                c_void_p, c_void_p, c_int, c_int, c_int64, c_int, c_int, c_int, c_float,
+                                C.POINTER(attn_mask_t), c_void_p, c_size_t, c_void_p]),
+    "attn_varlen_bwd_workspace_bytes": (c_size_t, [c_int, c_int64, c_int]),
     "attn_decode_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                                 c_int, c_int, c_int, c_float, c_int, c_int, c_void_p, c_size_t, c_void_p]),
     "attn_decode_splits": (c_int, [c_int, c_int, c_int]),

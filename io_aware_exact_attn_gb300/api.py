@@ -227,6 +227,39 @@ def attn_varlen_fwd(q, k, v, cu_seqlens: torch.Tensor, max_len: Optional[int] = 
     return o, l
 
 
+def varlen_bwd_workspace_bytes(B: int, total: int, Hq: int) -> int:
+    return int(_ffi.lib().attn_varlen_bwd_workspace_bytes(B, int(total), Hq))
+
+
+def attn_varlen_bwd(q, k, v, o, lse, do, cu_seqlens: torch.Tensor, max_len: Optional[int] = None,
+                    scale: Optional[float] = None, causal: bool = False, window: Optional[int] = None,
+                    workspace: Optional[torch.Tensor] = None, dq=None, dk=None, dv=None):
+    """Backward of ``attn_varlen_fwd``: returns ``(dQ [total,Hq,d], dK, dV [total,Hkv,d])`` in bf16."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 3):
+            raise ValueError(f"{n} must be a contiguous CUDA bf16 [total, heads, d] tensor")
+    _contig(lse, "lse", torch.float32)
+    total, Hq, d = q.shape
+    Hkv = k.shape[1]
+    cu = cu_seqlens.to(device=q.device, dtype=torch.int32).contiguous()
+    B = cu.numel() - 1
+    if max_len is None:
+        max_len = int((cu[1:] - cu[:-1]).max().item())
+    need = varlen_bwd_workspace_bytes(B, total, Hq)
+    ws = torch.empty(need, device=q.device, dtype=torch.uint8) if workspace is None else workspace
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    m, keep = mask_desc(causal, None, False, window)
+    check(_ffi.lib().attn_varlen_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                     do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), cu.data_ptr(), B,
+                                     int(max_len), int(total), Hq, Hkv, d, sc, _mp(m), ws.data_ptr(),
+                                     ws.numel() * ws.element_size(), _stream(q)), "attn_varlen_bwd")
+    del keep
+    return dq, dk, dv
+
+
 def decode_splits(B: int, Hkv: int, Nk: int) -> int:
     return int(_ffi.lib().attn_decode_splits(B, Hkv, Nk))
 

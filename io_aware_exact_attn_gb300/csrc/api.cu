@@ -541,6 +541,85 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   return ATTN_OK;
 }
 
+size_t attn_varlen_bwd_workspace_bytes(int B, int64_t total, int Hq) {
+  if (B < 1 || total < 1 || Hq < 1) return 0;
+  const size_t pcu = ((size_t)(B + 1) * sizeof(int) + 255) & ~(size_t)255;
+  // each sequence padded to whole tiles: at most total + 127 B rows per head
+  const size_t rows = (size_t)Hq * (size_t)(total + (int64_t)(TILE - 1) * B);
+  const size_t arr = (rows * sizeof(float) + 255) & ~(size_t)255;
+  return pcu + 2 * arr;
+}
+
+int attn_varlen_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                    void* dq, void* dk, void* dv, const int32_t* cu_seqlens, int B, int max_len, int64_t total, int Hq,
+                    int Hkv, int d, float scale, const attn_mask_t* mask, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  int rc;
+  if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k, "k")) || (rc = check_ptr(v, "v")) ||
+      (rc = check_ptr(o, "o")) || (rc = check_ptr(lse, "lse")) || (rc = check_ptr(dout, "dout")) ||
+      (rc = check_ptr(dq, "dq")) || (rc = check_ptr(dk, "dk")) || (rc = check_ptr(dv, "dv")) ||
+      (rc = check_ptr(workspace, "workspace")))
+    return rc;
+  if (cu_seqlens == nullptr) return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens is NULL");
+  if (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) return fail(ATTN_ERR_MISALIGNED, "cu_seqlens not 4-byte aligned");
+  if (total < 1 || total > ((int64_t)1 << 31) - 1) return fail(ATTN_ERR_INVALID_ARG, "total=%lld", (long long)total);
+  if (max_len < 1) return fail(ATTN_ERR_INVALID_ARG, "max_len=%d", max_len);
+  if ((rc = check_dims(B, Hq, Hkv, max_len, max_len, d, scale))) return rc;
+  if (workspace_bytes < attn_varlen_bwd_workspace_bytes(B, total, Hq))
+    return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes, need %zu", workspace_bytes,
+                attn_varlen_bwd_workspace_bytes(B, total, Hq));
+  MaskArgs m;
+  if ((rc = read_mask(mask, &m))) return rc;
+  if (m.kind == MASK_BLOCK_SPARSE) return fail(ATTN_ERR_UNSUPPORTED, "block-sparse masks are not built for ragged batches");
+  unsigned int* status = nullptr;
+  if ((rc = device_ready(&status))) return rc;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((rc = encode_tokens_map(&tq, q, d, total, Hq)) || (rc = encode_tokens_map(&tk, k, d, total, Hkv)) ||
+      (rc = encode_tokens_map(&tv, v, d, total, Hkv)) || (rc = encode_tokens_map(&tdo, dout, d, total, Hq)))
+    return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* pcu = static_cast<int*>(workspace);
+  const size_t pcu_bytes = ((size_t)(B + 1) * sizeof(int) + 255) & ~(size_t)255;
+  const int64_t bound = total + (int64_t)(TILE - 1) * B;   // padded rows per head, at most
+  float* dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) + pcu_bytes);
+  float* lse2 = dsum + (((size_t)Hq * bound * sizeof(float) + 255) & ~(size_t)255) / sizeof(float);
+  cudaError_t e;
+  {
+    TraceScope ts(ATTN_KERNEL_BWD_PREPROCESS, s);
+    e = launch_varlen_pad(cu_seqlens, B, pcu, s);
+    if (e == cudaSuccess)
+      e = launch_bwd_preprocess_varlen(o, dout, lse, dsum, lse2, Hq, total, cu_seqlens, pcu, B, bound, d, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "ragged backward preprocess launch");
+  BwdParams p{};
+  p.lse2 = lse2;
+  p.dsum = dsum;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = max_len;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.mask_kind = m.kind;
+  p.window = m.window;
+  p.nkb = (int)cdiv(max_len, TILE);
+  p.cu_seqlens = cu_seqlens;
+  p.pcu = pcu;
+  p.kv_group = 1;
+  p.q_group = 1;
+  p.status = status;
+  p.wait_limit_ns = wait_limit();
+  {
+    TraceScope ts(ATTN_KERNEL_BWD_DKDV, s);
+    e = launch_bwd_dkdv(d, tq, tk, tv, tdo, p, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "ragged backward dK/dV launch");
+  {
+    TraceScope ts(ATTN_KERNEL_BWD_DQ, s);
+    e = launch_bwd_dq(d, tq, tk, tv, tdo, p, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "ragged backward dQ launch");
+  return ATTN_OK;
+}
+
 int attn_build_schedule(int mask_kind, int causal_in_blocks, const uint8_t* host_block_mask, int window, int B, int Hq,
                         int Hkv,
                         int Nq, int Nk, int d, int64_t q_offset, int64_t kv_offset, int32_t* out, size_t cap,

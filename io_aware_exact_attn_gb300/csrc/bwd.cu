@@ -125,11 +125,25 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
   const uint32_t bar_done = smem_u32(&bars[1 + 2 * NS + 6]);
 
   const int nkt_all = (p.N + TILE - 1) / TILE;
+  const bool ragged = p.cu_seqlens != nullptr;
   int kt = 0, bkv = 0;
-  grouped_unit(blockIdx.x, p.B * p.Hkv, nkt_all, p.kv_group, &bkv, &kt);  // key tiles ascending: heaviest first
+  if (ragged) {   // key tiles ascending (heaviest first), every sequence and kv head inner
+    kt = (int)(blockIdx.x / ((unsigned)p.B * p.Hkv));
+    bkv = (int)(blockIdx.x % ((unsigned)p.B * p.Hkv));
+  } else {
+    grouped_unit(blockIdx.x, p.B * p.Hkv, nkt_all, p.kv_group, &bkv, &kt);  // key tiles ascending: heaviest first
+  }
   const int b = bkv / p.Hkv, hkv = bkv % p.Hkv;
   const int g = p.Hq / p.Hkv;
-  const int nqt = (p.N + TILE - 1) / TILE;
+  // the unit's sequence: its first token's row in the maps, its length, and
+  // where its rows start in lse2 / dsum (head 0) and between query heads
+  const int tok0 = ragged ? p.cu_seqlens[b] : 0;    // packed tensors hold fewer than 2^31 tokens
+  const int n_seq = ragged ? p.cu_seqlens[b + 1] - tok0 : p.N;
+  if (kt * TILE >= n_seq) return;   // past the end of a shorter sequence; nothing is set up yet
+  const int64_t lrow_hs = ragged ? (int64_t)p.pcu[p.B] : (int64_t)p.Np;
+  const int64_t lrow_b = ragged ? (int64_t)p.pcu[b] : (int64_t)b * p.Hq * p.Np;
+  const int kv_head = ragged ? hkv : bkv;   // head coordinate in the K / V maps
+  const int nqt = (n_seq + TILE - 1) / TILE;
   const int qt_first = causal_of(p) ? kt : 0;
   WaitCtx wc{p.wait_limit_ns, p.status, &abort_flag};
 
@@ -171,13 +185,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
     // one lane per TMA copy (copies issued by one thread are serialised)
     if (lane == 0) mbar_arrive_expect_tx(bar_kv, 2 * C::TILE_BYTES);
     __syncwarp();
-    if (lane < C::NBOX) tma_load_3d(s_base + lane * C::BOX_BYTES, &tk, lane * 64, kt * TILE, bkv, bar_kv);
+    const int krow = tok0 + kt * TILE;
+    if (lane < C::NBOX) tma_load_3d(s_base + lane * C::BOX_BYTES, &tk, lane * 64, krow, kv_head, bar_kv);
     else if (lane < 2 * C::NBOX)
-      tma_load_3d(s_base + OFF_V + (lane - C::NBOX) * C::BOX_BYTES, &tv, (lane - C::NBOX) * 64, kt * TILE, bkv, bar_kv);
+      tma_load_3d(s_base + OFF_V + (lane - C::NBOX) * C::BOX_BYTES, &tv, (lane - C::NBOX) * 64, krow, kv_head, bar_kv);
     int n = 0;
     bool ok = true;
     for (int h = 0; h < g && ok; ++h) {
-      const int bh = b * p.Hq + hkv * g + h;
+      const int hq = hkv * g + h;                 // query head within the batch
+      const int q_head = ragged ? hq : b * p.Hq + hq;
       for (int qt = qt_first; qt < nqt && ok; ++qt) {
         if (!tile_pair_visible(p, qt, kt)) continue;
         const int s = n % NS;
@@ -186,11 +202,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
         const uint32_t st = s_base + OFF_RING + s * STAGE;
         if (lane == 0) mbar_arrive_expect_tx(bar_q(s), 2 * C::TILE_BYTES + 1024);
         __syncwarp();
-        const size_t roff = (size_t)bh * p.Np + (size_t)qt * TILE;
+        const size_t roff = (size_t)(lrow_b + hq * lrow_hs) + (size_t)qt * TILE;
+        const int qrow0 = tok0 + qt * TILE;
         if (lane < C::NBOX)
-          tma_load_3d(st + lane * C::BOX_BYTES, &tq, lane * 64, qt * TILE, bh, bar_q(s));
+          tma_load_3d(st + lane * C::BOX_BYTES, &tq, lane * 64, qrow0, q_head, bar_q(s));
         else if (lane < 2 * C::NBOX)
-          tma_load_3d(st + C::TILE_BYTES + (lane - C::NBOX) * C::BOX_BYTES, &tdo, (lane - C::NBOX) * 64, qt * TILE, bh,
+          tma_load_3d(st + C::TILE_BYTES + (lane - C::NBOX) * C::BOX_BYTES, &tdo, (lane - C::NBOX) * 64, qrow0, q_head,
                       bar_q(s));
         else if (lane == 2 * C::NBOX)
           bulk_load(st + 2 * C::TILE_BYTES, p.lse2 + roff, 512, bar_q(s));
@@ -388,7 +405,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       if (ok) {
         tc_fence_after();
         const int key = kt * TILE + r;
-        const size_t orow = (size_t)bkv * p.N + (size_t)key;
+        const size_t orow = ragged ? (size_t)(tok0 + key) * p.Hkv + hkv : (size_t)bkv * p.N + key;
         // warpgroup 0 writes dV, warpgroup 1 writes scale * dK
         __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(hf == 0 ? p.dv : p.dk) + orow * D;
         const float mul = hf == 0 ? 1.f : p.scale;
@@ -401,7 +418,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) rv[j] = 0u;
           }
-          if (key < p.N) store_row32_bf16(dst + q4 * 32, rv, mul);
+          if (key < n_seq) store_row32_bf16(dst + q4 * 32, rv, mul);
         }
       }
     }
@@ -436,6 +453,9 @@ struct DqCfg {
   static constexpr uint32_t OFF_K = 2 * TILE_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + KS * TILE_BYTES;
   static constexpr uint32_t SMEM = OFF_V + VS * TILE_BYTES + 1024;
+  // two producers and the ragged-batch bookkeeping need more than 56 registers
+  // in the control warps: 128*72 + 256*216 <= 384*168
+  static constexpr uint32_t REGS_CTRL = 72, REGS_ELEM = 216;
 };
 
 template <int D>
@@ -470,13 +490,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
   auto bar_ds = [&](int j) { return smem_u32(&bars[1 + 2 * KS + 2 * VS + 5 + (j & 1)]); };
   auto bar_dq = [&](int j) { return smem_u32(&bars[1 + 2 * KS + 2 * VS + 7 + (j & 1)]); };
 
-  const int nqt = (p.N + TILE - 1) / TILE;
+  const int nqt_all = (p.N + TILE - 1) / TILE;
+  const bool ragged = p.cu_seqlens != nullptr;
   int bh = 0, qpos = 0;
-  grouped_unit(blockIdx.x, p.B * p.Hq, nqt, p.q_group, &bh, &qpos);
-  const int qt = nqt - 1 - qpos;  // latest query tile first: heaviest under a causal mask
+  if (ragged) {   // latest query tiles first, every sequence and head inner
+    qpos = (int)(blockIdx.x / ((unsigned)p.B * p.Hq));
+    bh = (int)(blockIdx.x % ((unsigned)p.B * p.Hq));
+  } else {
+    grouped_unit(blockIdx.x, p.B * p.Hq, nqt_all, p.q_group, &bh, &qpos);
+  }
+  const int qt = nqt_all - 1 - qpos;  // latest query tile first: heaviest under a causal mask
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int bkv = b * p.Hkv + h / (p.Hq / p.Hkv);
-  const int nkt = (p.N + TILE - 1) / TILE;
+  const int tok0 = ragged ? p.cu_seqlens[b] : 0;    // packed tensors hold fewer than 2^31 tokens
+  const int n_seq = ragged ? p.cu_seqlens[b + 1] - tok0 : p.N;
+  if (qt * TILE >= n_seq) return;   // past the end of a shorter sequence; nothing is set up yet
+  const int q_head = ragged ? h : bh, kv_head = ragged ? h / (p.Hq / p.Hkv) : bkv;   // heads in the maps
+  const int nkt = (n_seq + TILE - 1) / TILE;
   const int kt_end = causal_of(p) ? qt + 1 : nkt;
   WaitCtx wc{p.wait_limit_ns, p.status, &abort_flag};
 
@@ -518,7 +548,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
   const uint32_t tmem = tmem_slot;
 
   if (warp < 4) {
-   reg_dealloc<C::REGS_CTRL>();
+   reg_dealloc<Q::REGS_CTRL>();
    if (warp == 0 || warp == 2) {
     // ---------------------------------------------------------- producers
     // warp 0 streams K (and loads Q, dO once), warp 2 streams V: a K slot is
@@ -529,9 +559,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
     if (is_k) {
       if (lane == 0) mbar_arrive_expect_tx(bar_qdo, 2 * C::TILE_BYTES);
       __syncwarp();
-      if (lane < C::NBOX) tma_load_3d(s_base + lane * C::BOX_BYTES, &tq, lane * 64, qt * TILE, bh, bar_qdo);
+      const int qrow0 = tok0 + qt * TILE;
+      if (lane < C::NBOX) tma_load_3d(s_base + lane * C::BOX_BYTES, &tq, lane * 64, qrow0, q_head, bar_qdo);
       else if (lane < 2 * C::NBOX)
-        tma_load_3d(s_base + Q::OFF_DO + (lane - C::NBOX) * C::BOX_BYTES, &tdo, (lane - C::NBOX) * 64, qt * TILE, bh,
+        tma_load_3d(s_base + Q::OFF_DO + (lane - C::NBOX) * C::BOX_BYTES, &tdo, (lane - C::NBOX) * 64, qrow0, q_head,
                     bar_qdo);
     }
     const int depth = is_k ? KS : VS;
@@ -549,7 +580,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       if (lane == 0) mbar_arrive_expect_tx(full(sl), C::TILE_BYTES);
       __syncwarp();
       if (lane < C::NBOX)
-        tma_load_3d(ring + sl * C::TILE_BYTES + lane * C::BOX_BYTES, map, lane * 64, kt * TILE, bkv, full(sl));
+        tma_load_3d(ring + sl * C::TILE_BYTES + lane * C::BOX_BYTES, map, lane * 64, tok0 + kt * TILE, kv_head,
+                    full(sl));
       ++n;
     }
     if ((!ok || abort_flag) && lane == 0) {
@@ -641,7 +673,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
     }
    }
   } else {
-    reg_alloc<C::REGS_ELEM>();
+    reg_alloc<Q::REGS_ELEM>();
     // ------------------------------------------------------------ elementwise
     // warpgroup hf (0: warps 4-7, 1: warps 8-11) owns key columns
     // [64*hf, 64*hf + 64) of every query row
@@ -653,7 +685,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const float c = p.scale_log2;
     const bool causal = causal_of(p);
-    const size_t prow = (size_t)bh * p.Np + (size_t)qrow;
+    const size_t prow = ragged ? (size_t)h * p.pcu[p.B] + p.pcu[b] + qrow : (size_t)bh * p.Np + qrow;
     const float l2 = p.lse2[prow];
     const float dr = p.dsum[prow];
     int j = 0;
@@ -667,8 +699,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       // query - key < window: lo <= col < lim
       const int wnd = window_of(p);
       const bool wedge = (qt - kt) * TILE + (TILE - 1) >= wnd;
-      const bool edge = (kt == nkt - 1 && (p.N % TILE) != 0) || (causal && kt == qt) || wedge;
-      int lim = p.N - kt * TILE;
+      const bool edge = (kt == nkt - 1 && (n_seq % TILE) != 0) || (causal && kt == qt) || wedge;
+      int lim = n_seq - kt * TILE;
       if (causal && kt == qt) lim = min(lim, r + 1);
       const int lo = wedge ? (qt - kt) * TILE + r - wnd + 1 : 0;
       float pr[64];
@@ -723,7 +755,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       if (ok) {
         tc_fence_after();
         // each warpgroup writes its half of the dQ row
-        __nv_bfloat16* dq = static_cast<__nv_bfloat16*>(p.dq) + ((size_t)bh * p.N + qrow) * D + hf * (D / 2);
+        const size_t qo = ragged ? (size_t)(tok0 + qrow) * p.Hq + h : (size_t)bh * p.N + qrow;
+        __nv_bfloat16* dq = static_cast<__nv_bfloat16*>(p.dq) + qo * D + hf * (D / 2);
 #pragma unroll
         for (int q4 = 0; q4 < D / 64; ++q4) {
           uint32_t rq[32];
@@ -733,7 +766,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) rq[jj] = 0u;
           }
-          if (qrow < p.N) store_row32_bf16(dq + q4 * 32, rq, p.scale);
+          if (qrow < n_seq) store_row32_bf16(dq + q4 * 32, rq, p.scale);
         }
       }
     }

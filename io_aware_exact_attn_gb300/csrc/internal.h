@@ -62,6 +62,12 @@ struct BwdParams {
   const uint8_t* block_mask;
   int nkb;
   int window;               // sliding window width (MASK_SLIDING_WINDOW)
+  // variable-length batches (cu_seqlens != null): tensors are token-major
+  // [total, heads, d], sequence b holds tokens [cu_seqlens[b], cu_seqlens[b+1])
+  // and N is the longest sequence; lse2 / dsum rows of query head h and
+  // sequence b start at h * pcu[B] + pcu[b] (sequences padded to whole tiles)
+  const int* cu_seqlens;
+  const int* pcu;
   int kv_group;             // kv heads per L2 group of the dK/dV kernel
   int q_group;              // query heads per L2 group of the dQ kernel
   unsigned int* status;
@@ -86,6 +92,10 @@ cudaError_t launch_merge(const float* const* o_parts, const float* const* lse_pa
 
 cudaError_t launch_bwd_preprocess(const void* o, const void* dout, const float* lse, float* dsum, float* lse2,
                                   int64_t heads, int N, int Np, int d, cudaStream_t s);
+cudaError_t launch_varlen_pad(const int* cu_seqlens, int B, int* pcu, cudaStream_t s);
+cudaError_t launch_bwd_preprocess_varlen(const void* o, const void* dout, const float* lse, float* dsum, float* lse2,
+                                         int heads, int64_t total, const int* cu_seqlens, const int* pcu, int B,
+                                         int64_t padded_rows_bound, int d, cudaStream_t s);
 
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,

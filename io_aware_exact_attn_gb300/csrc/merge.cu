@@ -88,30 +88,75 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
   }
 }
 
+// Ragged backward passes pad every sequence to whole 128-row tiles in the
+// D / lse2 arrays: pcu[b] = sum over b' < b of len(b') rounded up to a tile,
+// pcu[B] their total.  One warp, 32 sequences per step.
+__global__ void __launch_bounds__(32) varlen_pad_kernel(const int* __restrict__ cu, int B, int* __restrict__ pcu) {
+  const int lane = threadIdx.x;
+  int carry = 0;
+  for (int base = 0; base <= B; base += 32) {
+    const int b = base + lane;
+    int v = 0;
+    if (b < B) {
+      const int len = cu[b + 1] - cu[b];
+      v = len > 0 ? (len + TILE - 1) / TILE * TILE : 0;
+    }
+    int x = v;   // inclusive scan over the warp
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (b <= B) pcu[b] = carry + x - v;
+    carry += __shfl_sync(0xffffffffu, x, 31);
+  }
+}
+
 // D_i = sum_k dO_ik * O_ik and lse2_i = LSE_i * log2(e) for the backward
 // kernels; groups of d/8 lanes per row, 8 bf16 per lane.  Both outputs are
 // [heads][Np] with Np = N rounded up to a whole tile; rows past N (and rows
 // whose LSE is -inf, i.e. that saw no key) get D = 0 and lse2 = +inf, which
-// makes every recomputed probability of such a row exactly 0.
-template <int D>
+// makes every recomputed probability of such a row exactly 0.  Ragged
+// batches (RAGGED): O, dO token-major [total][heads][d], LSE [heads][total],
+// outputs [heads][pcu[B]] with sequence b's rows from pcu[b] (see above).
+template <int D, bool RAGGED>
 __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ dout,
                                                          const float* __restrict__ lse,
                                                          float* __restrict__ dsum, float* __restrict__ lse2,
-                                                         int64_t heads, int N, int Np) {
+                                                         int64_t heads, int N, int Np, const int* __restrict__ cu,
+                                                         const int* __restrict__ pcu, int B, int64_t total) {
   constexpr int LPR = D / 8;
   constexpr int RPW = 32 / LPR;
   const int lane = threadIdx.x & 31;
   const int sub = lane / LPR, col = (lane % LPR) * 8;
-  const int64_t rows = heads * Np;
+  const int64_t per_head = RAGGED ? (int64_t)pcu[B] : (int64_t)Np;   // padded rows per head
+  const int64_t rows = heads * per_head;
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x / 32);
   for (int64_t wrow = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; wrow * RPW < rows;
        wrow += warps_total) {
     const int64_t prow = wrow * RPW + sub;        // padded row index
-    const int64_t head = prow / Np;
-    const int r = (int)(prow - head * Np);
-    const bool valid = prow < rows && r < N;
-    const int64_t row = head * N + r;             // dense row index
+    const int64_t head = prow / per_head;
+    const int64_t pr = prow - head * per_head;
+    bool valid;
+    int64_t row, lrow;                            // row of O / dO (in d-element units), index of LSE
+    if constexpr (RAGGED) {
+      int lo = 0, hi = B;                         // the sequence: largest b with pcu[b] <= pr
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pcu[mid] <= pr) lo = mid;
+        else hi = mid;
+      }
+      const int64_t i = pr - pcu[lo];
+      valid = prow < rows && i < (int64_t)(cu[lo + 1] - cu[lo]);
+      const int64_t t = cu[lo] + i;               // token
+      row = t * heads + head;
+      lrow = head * total + t;
+    } else {
+      valid = prow < rows && pr < N;
+      row = head * N + pr;                        // dense row index
+      lrow = row;
+    }
     float acc = 0.f;
     if (valid) {
       const uint4 a = __ldcs(reinterpret_cast<const uint4*>(o + row * D + col));
@@ -131,7 +176,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
     if (prow < rows && (lane % LPR) == 0) {
       float l2 = INFINITY;
       if (valid) {
-        const float L = lse[row];
+        const float L = lse[lrow];
         l2 = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
       }
       dsum[prow] = valid ? acc : 0.f;
@@ -192,14 +237,31 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dout, const float* 
                                   int64_t heads, int N, int Np, int d, cudaStream_t s) {
   const int rpw = 32 / (d / 8);
   const int grid = grid_for((heads * Np + rpw - 1) / rpw);
+  const auto* po = static_cast<const __nv_bfloat16*>(o);
+  const auto* pd = static_cast<const __nv_bfloat16*>(dout);
   if (d == 128)
-    preprocess_kernel<128><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
-                                                static_cast<const __nv_bfloat16*>(dout), lse, dsum, lse2, heads,
-                                                N, Np);
+    preprocess_kernel<128, false><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, N, Np, nullptr, nullptr, 0, 0);
   else
-    preprocess_kernel<64><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
-                                               static_cast<const __nv_bfloat16*>(dout), lse, dsum, lse2, heads,
-                                               N, Np);
+    preprocess_kernel<64, false><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, N, Np, nullptr, nullptr, 0, 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_varlen_pad(const int* cu_seqlens, int B, int* pcu, cudaStream_t s) {
+  varlen_pad_kernel<<<1, 32, 0, s>>>(cu_seqlens, B, pcu);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_preprocess_varlen(const void* o, const void* dout, const float* lse, float* dsum, float* lse2,
+                                         int heads, int64_t total, const int* cu_seqlens, const int* pcu, int B,
+                                         int64_t padded_rows_bound, int d, cudaStream_t s) {
+  const int rpw = 32 / (d / 8);
+  const int grid = grid_for((heads * padded_rows_bound + rpw - 1) / rpw);
+  const auto* po = static_cast<const __nv_bfloat16*>(o);
+  const auto* pd = static_cast<const __nv_bfloat16*>(dout);
+  if (d == 128)
+    preprocess_kernel<128, true><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, 0, 0, cu_seqlens, pcu, B, total);
+  else
+    preprocess_kernel<64, true><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, 0, 0, cu_seqlens, pcu, B, total);
   return cudaGetLastError();
 }
 

@@ -37,6 +37,7 @@ from .attention import (  # noqa: F401
     attention_backward_dq_rows,
     decode_forward,
     varlen_forward,
+    varlen_backward,
     merge_partials,
 )
 from .schedule import (  # noqa: F401

@@ -251,6 +251,24 @@ def varlen_forward(q, k, v, cu_seqlens, scale: float, mask: MaskSpec = MaskSpec(
     return o, lse
 
 
+def varlen_backward(q, k, v, do, cu_seqlens, scale: float, mask: MaskSpec = MaskSpec()):
+    """Exact gradient of ``<O, dO>`` for sequences packed back to back (the
+    layouts of ``varlen_forward``): each sequence on its own.  Returns
+    ``dQ [total, Hq, d]``, ``dK``/``dV`` ``[total, Hkv, d]``."""
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64); do = np.asarray(do, np.float64)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    cu = [int(x) for x in cu_seqlens]
+    t = lambda x: x.transpose(1, 0, 2)[None]
+    for b in range(len(cu) - 1):
+        s0, s1 = cu[b], cu[b + 1]
+        if s1 <= s0:
+            continue
+        a, bk, bv = attention_backward(t(q[s0:s1]), t(k[s0:s1]), t(v[s0:s1]), t(do[s0:s1]), scale, mask)
+        dq[s0:s1], dk[s0:s1], dv[s0:s1] = (x[0].transpose(1, 0, 2) for x in (a, bk, bv))
+    return dq, dk, dv
+
+
 def decode_forward(q, k_cache, v_cache, scale: float, seq_lens=None, causal: bool = True):
     """Attention of the newest ``Nq`` positions of each sequence against its
     key/value cache, in float64 (the decoding step of a KV-cache model;

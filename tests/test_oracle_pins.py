@@ -493,6 +493,39 @@ def test_varlen_q_zero_sees_only_its_own_sequence():
                     assert abs(lse[h, t] - np.log(top)) < 1e-13
 
 
+def test_varlen_backward_equal_lengths_and_finite_differences():
+    B, Hq, Hkv, n, d = 2, 4, 2, 7, 3
+    q, k, v, do = rnd(B, Hq, n, d), rnd(B, Hkv, n, d), rnd(B, Hkv, n, d), rnd(B, Hq, n, d)
+    pack = lambda x: x.transpose(0, 2, 1, 3).reshape(B * n, x.shape[1], d)
+    cu = [0, n, 2 * n]
+    for mask in (MaskSpec("causal"), MaskSpec("sliding_window", window=3)):
+        got = oracle.varlen_backward(pack(q), pack(k), pack(v), pack(do), cu, 0.5, mask)
+        want = oracle.attention_backward(q, k, v, do, 0.5, mask)
+        for a, b in zip(got, want):
+            np.testing.assert_allclose(a, pack(b), atol=1e-14)
+    # ragged: central differences of <O, dO> through varlen_forward
+    lens = [3, 1, 4]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    rng = np.random.default_rng(5)
+    qq, kk, vv, dd = (rng.standard_normal((8, h, 3)) for h in (2, 1, 1, 2))
+    mask = MaskSpec("causal")
+    gq, gk, gv = oracle.varlen_backward(qq, kk, vv, dd, cu, 0.6, mask)
+    h = 1e-6
+    for x, gx in ((qq, gq), (kk, gk), (vv, gv)):
+        num = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = x[idx]
+            x[idx] = old + h
+            fp = float((oracle.varlen_forward(qq, kk, vv, cu, 0.6, mask)[0] * dd).sum())
+            x[idx] = old - h
+            fm = float((oracle.varlen_forward(qq, kk, vv, cu, 0.6, mask)[0] * dd).sum())
+            x[idx] = old
+            num[idx] = (fp - fm) / (2 * h)
+        assert np.abs(num - gx).max() / max(1.0, np.abs(num).max()) < 1e-7
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def _fails(fn):
