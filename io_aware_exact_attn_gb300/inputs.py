@@ -41,6 +41,26 @@ def make_qkvdo(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int,
     return q, k, v, do
 
 
+def make_qkv_e4m3(B: int, Hq: int, Hkv: int, N: int, d: int, seed: int = SEED):
+    """E4M3 Q ``[B,Hq,N,d]``, K/V ``[B,Hkv,N,d]`` as uint8 CPU code tensors, with
+    per-tensor dequantisation factors ``(qd, kd, vd)``.
+
+    Each tensor is the float32 N(0,1) draw of ``randn_bf16``'s generator (same
+    seeds) divided by ``amax / 448`` (its largest magnitude mapped to the
+    largest finite E4M3 value) and rounded to E4M3 by torch's conversion; the
+    factor is ``amax / 448``.
+    """
+    out, desc = [], []
+    for shape, name in (((B, Hq, N, d), "q"), ((B, Hkv, N, d), "k"), ((B, Hkv, N, d), "v")):
+        g = torch.Generator(device="cpu")
+        g.manual_seed(int(seed + OFFSET[name]))
+        x = torch.randn(*shape, generator=g, dtype=torch.float32)
+        f = float(x.abs().max()) / 448.0
+        out.append((x / f).to(torch.float8_e4m3fn).view(torch.uint8))
+        desc.append(f)
+    return out[0], out[1], out[2], tuple(desc)
+
+
 def block_sparse_mask(nqb: int, nkb: int, density: float = 1.0 / 8.0,
                       seed: int = SEED) -> np.ndarray:
     """Boolean ``[nqb, nkb]`` block mask: every diagonal block kept, plus exactly
@@ -105,4 +125,6 @@ WORKLOADS = {
     "block_sparse": Workload("block_sparse", 1, 16, 16, 16384, 64, "block_sparse", density=1.0 / 8.0),
     # local attention over the last 4096 positions (a Mistral-style sliding window) at the GPT shape
     "gpt_sliding_window": Workload("gpt_sliding_window", 2, 32, 32, 8192, 128, "sliding_window", window=4096),
+    # the GPT shape with e4m3 Q, K, V and per-tensor scales (make_qkv_e4m3)
+    "gpt_causal_fp8": Workload("gpt_causal_fp8", 2, 32, 32, 8192, 128, "causal"),
 }

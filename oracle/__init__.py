@@ -22,6 +22,8 @@ Sources, by page and section:
 * BurstAttention author responses: local attention results are combined
   across devices with online-softmax statistics (the merge); sparse attention
   only changes the attention mask matrix.
+* FlashAttention (IO-Awareness) page, related papers, FlashAttention-3:
+  attention on FP8 operands (``fp8.py``: E4M3 codes with per-tensor scales).
 
 Every function here is pinned by tests in ``tests/test_oracle_pins.py`` to
 something other than itself (closed forms, finite differences, library
@@ -39,6 +41,12 @@ from .attention import (  # noqa: F401
     varlen_forward,
     varlen_backward,
     merge_partials,
+)
+from .fp8 import (  # noqa: F401
+    E4M3_MAX,
+    e4m3_decode,
+    fp8_forward,
+    fp8_row_error_bound,
 )
 from .schedule import (  # noqa: F401
     chunk_pair_schedule,

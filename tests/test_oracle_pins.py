@@ -7,7 +7,8 @@ merge == monolithic, GQA == repeated MHA, all-ones block mask == dense,
 block-triangular + causal == causal, a window wider than the sequence ==
 causal, a window of one == identity).  ``test_planted_mistakes`` shows that a
 plausible slip in the oracle (a dropped term, a sign, an off-by-one, a
-transposed operand, a missing merge weight) fails at least one pin.
+transposed operand, a missing merge weight, a wrong E4M3 exponent bias, a lost
+scale factor) fails at least one pin.
 """
 import glob
 import json
@@ -526,6 +527,102 @@ def test_varlen_backward_equal_lengths_and_finite_differences():
         assert np.abs(num - gx).max() / max(1.0, np.abs(num).max()) < 1e-7
 
 
+# ---------------------------------------------------------------- e4m3 operands
+
+def test_e4m3_decode_matches_torch_float8():
+    """All 256 codes against torch's own float8_e4m3fn -> float64 conversion."""
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.e4m3_decode(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(ref[ok]))
+
+
+def test_e4m3_decode_closed_forms():
+    d = oracle.e4m3_decode
+    assert d(0x38) == 1.0 and d(0xB8) == -1.0 and d(0x40) == 2.0 and d(0x3C) == 1.5
+    assert d(0x7E) == 448.0 == oracle.E4M3_MAX
+    assert d(0x01) == 2.0 ** -9 and d(0x07) == 7 * 2.0 ** -9 and d(0x08) == 2.0 ** -6
+    assert d(0x00) == 0.0 and np.signbit(d(0x80))
+    assert np.isnan(d(0x7F)) and np.isnan(d(0xFF))
+    assert np.nanmax(d(np.arange(256, dtype=np.uint8))) == 448.0
+
+
+def _codes(*shape, rng, lo=-60.0, hi=60.0):
+    x = torch.from_numpy(rng.uniform(lo, hi, shape).astype(np.float32))
+    return x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_fp8_forward_descale_invariances():
+    """Only the product of the Q and K factors matters; O is linear in the V
+    factor and the LSE does not see it."""
+    rng = np.random.default_rng(11)
+    q8, k8, v8 = _codes(1, 2, 9, 4, rng=rng), _codes(1, 1, 9, 4, rng=rng), _codes(1, 1, 9, 4, rng=rng)
+    for mask in (MaskSpec("none"), MaskSpec("causal"), MaskSpec("sliding_window", window=3)):
+        o1, l1 = oracle.fp8_forward(q8, k8, v8, 0.02, 0.015, 0.1, 0.5, mask)
+        o2, l2 = oracle.fp8_forward(q8, k8, v8, 0.04, 0.0075, 0.1, 0.5, mask)
+        o3, l3 = oracle.fp8_forward(q8, k8, v8, 0.02, 0.015, 0.3, 0.5, mask)
+        np.testing.assert_allclose(o1, o2, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(l1, l2, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(o3, 3.0 * o1, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(l3, l1, rtol=1e-12, atol=1e-14)
+
+
+def test_fp8_forward_q_zero_gives_mean_of_visible_values():
+    rng = np.random.default_rng(12)
+    q8 = np.zeros((1, 1, 6, 4), np.uint8)
+    k8, v8 = _codes(1, 1, 6, 4, rng=rng), _codes(1, 1, 6, 4, rng=rng)
+    vv = 0.25 * oracle.e4m3_decode(v8)[0, 0]
+    o, lse = oracle.fp8_forward(q8, k8, v8, 1.0, 1.0, 0.25, 0.7, MaskSpec("causal"))
+    for i in range(6):
+        np.testing.assert_allclose(o[0, 0, i], vv[:i + 1].mean(axis=0), rtol=0, atol=1e-13)
+        assert abs(lse[0, 0, i] - np.log(i + 1)) < 1e-13
+
+
+def _simulated_rounding_error(q8, k8, v8, qd, kd, vd, scale, t):
+    """max_d |O_sim - O_exact| per row, O_sim from weights w * 2^t rounded to
+    E4M3 by torch (round to nearest), normalised by the exact sum."""
+    q = qd * oracle.e4m3_decode(q8)[0, 0]
+    k = kd * oracle.e4m3_decode(k8)[0, 0]
+    v = vd * oracle.e4m3_decode(v8)[0, 0]
+    s = scale * q @ k.T
+    w = np.exp(s - s.max(axis=1, keepdims=True))
+    p = torch.from_numpy(w * 2.0 ** t).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    o_sim = (p @ v) / (w * 2.0 ** t).sum(axis=1, keepdims=True)
+    o_ex = (w @ v) / w.sum(axis=1, keepdims=True)
+    return np.abs(o_sim - o_ex).max(axis=1)
+
+
+def test_fp8_row_error_bound_holds_for_simulated_rounding():
+    rng = np.random.default_rng(13)
+    for n, krange in ((40, 60.0), (300, 200.0)):
+        q8, k8, v8 = _codes(1, 1, n, 8, rng=rng), _codes(1, 1, n, 8, rng=rng, lo=-krange, hi=krange), \
+            _codes(1, 1, n, 8, rng=rng)
+        bound = oracle.fp8_row_error_bound(q8, k8, v8, 0.01, 0.01, 0.02, 0.3)[0, 0]
+        for t in (7.0, 7.5, 8.0):
+            err = _simulated_rounding_error(q8, k8, v8, 0.01, 0.01, 0.02, 0.3, t)
+            assert np.all(err <= bound), (n, t)
+
+
+def test_fp8_row_error_bound_subnormal_term():
+    """One key at the row max and 16384 keys whose weights (2.45 * 2^-16 of it)
+    land on the subnormal grid at t = 7, all rounded the same way: the error
+    exceeds 2^-4 max|v| and the bound still covers it."""
+    n = 16384
+    q8 = np.full((1, 1, 1, 1), 0x38, np.uint8)               # q = 1
+    k8 = np.full((1, 1, n + 1, 1), 0xB8, np.uint8)           # k = -1 ...
+    k8[0, 0, 0, 0] = 0x00                                    # ... but key 0 at score 0
+    v8 = np.full((1, 1, n + 1, 1), 0x38, np.uint8)           # v = 1 ...
+    v8[0, 0, 0, 0] = 0x00                                    # ... but 0 for the max key
+    scale = -np.log(2.45 * 2.0 ** -16)
+    err = _simulated_rounding_error(q8, k8, v8, 1.0, 1.0, 1.0, scale, 7.0)[0]
+    bound = oracle.fp8_row_error_bound(q8, k8, v8, 1.0, 1.0, 1.0, scale)[0, 0, 0]
+    assert err > 2.0 ** -4
+    assert err <= bound
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def _fails(fn):
@@ -597,6 +694,50 @@ def test_planted_mistakes(monkeypatch):
     monkeypatch.setattr(oa, "head_forward", fwd_no_scale_in_lse)
     assert _fails(test_library_softmax_scipy)
     monkeypatch.setattr(oa, "head_forward", good_fwd)
+
+    from oracle import fp8 as of
+    good_dec = of.e4m3_decode
+
+    def dec_bias_8(codes):                               # exponent bias off by one
+        return 0.5 * good_dec(codes)
+
+    def dec_no_subnormals(codes):                        # exponent field 0 read as normal
+        c = np.asarray(codes, np.uint8)
+        x = good_dec(codes)
+        sub = ((c >> 3) & 0xF) == 0
+        return np.where(sub & ((c & 7) != 0), np.sign(x) * (1 + (c & 7) / 8.0) * 2.0 ** -7, x)
+
+    for bad in (dec_bias_8, dec_no_subnormals):
+        monkeypatch.setattr(of, "e4m3_decode", bad)
+        monkeypatch.setattr(oracle, "e4m3_decode", bad)
+        assert _fails(test_e4m3_decode_matches_torch_float8) and _fails(test_e4m3_decode_closed_forms), bad.__name__
+        monkeypatch.setattr(of, "e4m3_decode", good_dec)
+        monkeypatch.setattr(oracle, "e4m3_decode", good_dec)
+
+    good_fp8 = of.fp8_forward
+
+    def fwd_k_descale_dropped(q8, k8, v8, qd, kd, vd, scale, mask=MaskSpec(), heads=None, rows=None):
+        return good_fp8(q8, k8, v8, qd, 1.0, vd, scale, mask, heads=heads, rows=rows)
+
+    monkeypatch.setattr(oracle, "fp8_forward", fwd_k_descale_dropped)
+    assert _fails(test_fp8_forward_descale_invariances)
+    monkeypatch.setattr(oracle, "fp8_forward", good_fp8)
+
+    def bound_normal_only(q8, k8, v8, qd, kd, vd, scale, mask=MaskSpec(), heads=None, rows=None):
+        q = qd * of.e4m3_decode(q8)
+        k = kd * of.e4m3_decode(k8)
+        v = vd * of.e4m3_decode(v8)
+        out = np.zeros(q.shape[:3])
+        for b in range(q.shape[0]):
+            for h in range(q.shape[1]):
+                vis = oracle.visible(np.arange(q.shape[2]), k.shape[2], mask)
+                vmax = np.where(vis, np.abs(v[b, h // (q.shape[1] // k.shape[1])]).max(axis=1)[None, :], 0).max(1)
+                out[b, h] = vmax * 2.0 ** -4
+        return out
+
+    monkeypatch.setattr(oracle, "fp8_row_error_bound", bound_normal_only)
+    assert _fails(test_fp8_row_error_bound_subnormal_term)
+    monkeypatch.setattr(oracle, "fp8_row_error_bound", of.fp8_row_error_bound)
 
     monkeypatch.setattr(oa, "merge_partials", merge_no_weights)
     monkeypatch.setattr(oracle, "merge_partials", merge_no_weights)
