@@ -43,6 +43,7 @@ CHUNKED = dict(name="chunked_gqa", B=1, Hq=32, Hkv=8, N=32768, d=128, chunks=8)
 WINDOW = dict(name="gpt_sliding_window", B=2, Hq=32, Hkv=32, N=8192, d=128, window=4096)
 DECODE = dict(name="decode_gqa", B=8, Hq=32, Hkv=8, Nq=1, Nk=32768, d=128)
 VARLEN = dict(name="varlen_causal", B=16, Hq=32, Hkv=32, d=128, min_len=512, max_len=8192)
+FP8 = dict(name="gpt_causal_fp8", B=2, Hq=32, Hkv=32, N=8192, d=128)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
     "fwd": ["fwd.cu", "ptx.cuh", "schedule.h", "internal.h"],
@@ -51,6 +52,7 @@ KERNEL_SOURCES = {
     "bwd_dq": ["bwd.cu", "ptx.cuh", "internal.h"],
     "bwd_preprocess": ["merge.cu", "ptx.cuh", "internal.h"],
     "merge": ["merge.cu", "ptx.cuh", "internal.h"],
+    "fwd_fp8": ["fwd_fp8.cu", "ptx.cuh", "schedule.h", "internal.h"],
 }
 
 
@@ -395,6 +397,7 @@ def main():
         out["sliding_window"] = window_leg(api, inputs, torch, peaks, rank)
         out["decode"] = decode_leg(api, inputs, torch, peaks, rank)
         out["varlen"] = varlen_leg(api, inputs, torch, peaks, rank)
+        out["fp8_fwd"] = fp8_leg(api, inputs, torch, peaks, rank)
         if rank == 0:
             out["cpu_baseline"] = {k_: v_ for k_, v_ in oracle_sample(args.cpu_seconds).items()
                                    if k_ in ("value", "unit", "cores", "kind", "sample")}
@@ -613,6 +616,43 @@ def varlen_leg(api, inputs, torch, peaks, rank, reps=10):
                 bwd_ms=bwd_ms, bwd_tflops=2.5 * flops / (bwd_ms * 1e-3) / 1e12,
                 fwd_frac_of_burst_peak=flops / (fwd_ms * 1e-3) / 1e12 / peaks["bf16_tflops"])
 
+
+
+def fp8_leg(api, inputs, torch, peaks, rank, reps=10):
+    """Causal forward on E4M3 Q, K, V (per-tensor scales) at the GPT shape:
+    B=2, H=32, N=8192, d=128.  Both products run on the fp8 tensor core; its
+    peak is taken as twice the measured bf16 burst peak (the nominal fp8:bf16
+    ratio).  The V transpose the kernel needs is timed separately."""
+    c = FP8
+    B, Hq, Hkv, N, d = c["B"], c["Hq"], c["Hkv"], c["N"], c["d"]
+    q8, k8, v8, (qd, kd, vd) = inputs.make_qkv_e4m3(B, Hq, Hkv, N, d, seed=inputs.SEED + 100 * rank + 7)
+    q8, k8, v8 = q8.cuda(), k8.cuda(), v8.cuda()
+    ws = torch.empty(api.fwd_fp8_workspace_bytes(B, Hkv, N, d), device="cuda", dtype=torch.uint8)
+    o = torch.empty((B, Hq, N, d), device="cuda", dtype=torch.bfloat16)
+    lse = torch.empty((B, Hq, N), device="cuda", dtype=torch.float32)
+
+    def run():
+        api.attn_fwd_fp8(q8, k8, v8, qd, kd, vd, causal=True, out=o, lse=lse, workspace=ws)
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    api.trace_enable(4 * reps)
+    for _ in range(reps):
+        run()
+    torch.cuda.synchronize()
+    api.trace_disable()
+    recs, _ = api.trace_read(4 * reps)
+    fwd_ms = sum(ms for n, ms in recs if n == "fwd_fp8") / reps
+    tr_ms = sum(ms for n, ms in recs if n == "fp8_transpose_v") / reps
+    flops = fwd_flops(B, Hq, N, d, True)
+    peak8 = 2.0 * peaks["bf16_tflops"]
+    tr_bytes = 2.0 * B * Hkv * N * d
+    return dict(workload=f"B={B} Hq={Hq} Hkv={Hkv} N={N} d={d} causal, e4m3 Q/K/V",
+                fwd_ms=fwd_ms, transpose_v_ms=tr_ms, fwd_tflops=flops / (fwd_ms * 1e-3) / 1e12,
+                with_transpose_tflops=flops / ((fwd_ms + tr_ms) * 1e-3) / 1e12,
+                fp8_peak_tflops=peak8, fwd_frac_of_fp8_peak=flops / (fwd_ms * 1e-3) / 1e12 / peak8,
+                transpose_v_gbs=tr_bytes / (tr_ms * 1e-3) / 1e9)
 
 if __name__ == "__main__":
     sys.exit(main())

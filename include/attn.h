@@ -214,6 +214,33 @@ int attn_varlen_bwd(const void* q, const void* k, const void* v, const void* o,
 size_t attn_varlen_bwd_workspace_bytes(int B, int64_t total, int Hq);
 
 /*
+ * attn_fwd_fp8 -- attn_fwd with e4m3 (fp8) Q, K and V, both products on the
+ * fp8 tensor core ("FlashAttention: Fast and Memory-Efficient Exact Attention
+ * with IO-Awareness", related papers, FlashAttention-3: FP8 attention).  The
+ * stored codes are dequantised by per-tensor factors: the operation is
+ *   O = softmax(scale * (q_descale Q8)(k_descale K8)^T) (v_descale V8)
+ * with the mask of attn_fwd; O is bf16, LSE natural-log f32 as in attn_fwd.
+ * The probabilities enter the second product as e4m3 (relative rounding
+ * 2^-4 for weights above 2^-13 of the row max, absolute 2^-17 of it below),
+ * so |O - O_exact| <= max|v| (2^-4 + 2^-17 n_small / sum of the relative
+ * weights) plus the bf16 rounding of O, max|v| over the row's visible values;
+ * the row sums and the LSE stay fp32.
+ *   q8          device e4m3 [B, Hq,  N, 128]   k8, v8 device e4m3 [B, Hkv, N, 128]
+ *   o           device bf16 [B, Hq,  N, 128]   (written)
+ *   lse         device f32  [B, Hq,  N]        (written; may be NULL)
+ *   workspace   device, >= attn_fwd_fp8_workspace_bytes(B, Hkv, N, d) bytes,
+ *               16-byte aligned; caller-owned.  It receives V^T.
+ * d must be 128 (ATTN_ERR_UNSUPPORTED otherwise); descales finite and > 0.
+ */
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, float q_descale, float k_descale,
+                 float v_descale, void* o, float* lse, int B, int Hq, int Hkv, int N, int d,
+                 float scale, const attn_mask_t* mask, void* workspace, size_t workspace_bytes,
+                 void* stream);
+
+/* Workspace bytes for attn_fwd_fp8: V^T, B*Hkv*d*ceil(N/128)*128 bytes. */
+size_t attn_fwd_fp8_workspace_bytes(int B, int Hkv, int N, int d);
+
+/*
  * attn_decode_fwd -- one decoding step against a key/value cache, split over
  * the cache ("FlashAttention-2" reviews: splitting the KV cache amongst thread
  * blocks for inference).  Sequence b holds seq_lens[b] cached positions (Nk
@@ -355,7 +382,9 @@ typedef enum {
   ATTN_KERNEL_BWD_DQ = 6,         /* attn_bwd step 3: dQ */
   ATTN_KERNEL_SELFTEST = 7,       /* attn_selftest_wait_timeout */
   ATTN_KERNEL_DECODE = 8,         /* attn_decode_fwd split-KV partials (its merge is ATTN_KERNEL_MERGE) */
-  ATTN_KERNEL_VARLEN_FWD = 9      /* attn_varlen_fwd forward kernel */
+  ATTN_KERNEL_VARLEN_FWD = 9,     /* attn_varlen_fwd forward kernel */
+  ATTN_KERNEL_FP8_TRANSPOSE_V = 10, /* attn_fwd_fp8 step 1: V -> V^T */
+  ATTN_KERNEL_FP8_FWD = 11        /* attn_fwd_fp8 step 2: forward kernel */
 } attn_kernel_id_t;
 
 typedef struct attn_trace_record {

@@ -6,6 +6,8 @@ entry point raises.
 """
 from .api import (  # noqa: F401
     attn_fwd,
+    attn_fwd_fp8,
+    fwd_fp8_workspace_bytes,
     attn_partial_fwd,
     attn_merge_lse,
     attn_bwd,

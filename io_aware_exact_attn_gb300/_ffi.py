@@ -20,7 +20,7 @@ class attn_trace_record_t(C.Structure):
 
 
 KERNEL_NAMES = {1: "fwd", 2: "partial_fwd", 3: "merge", 4: "bwd_preprocess", 5: "bwd_dkdv", 6: "bwd_dq",
-                7: "selftest", 8: "decode", 9: "varlen_fwd"}
+                7: "selftest", 8: "decode", 9: "varlen_fwd", 10: "fp8_transpose_v", 11: "fwd_fp8"}
 
 
 class attn_mask_t(C.Structure):
@@ -56,6 +56,10 @@ SIGNATURES = {
                                 c_void_p, c_void_p, c_int, c_int, c_int64, c_int, c_int, c_int, c_float,
                                 C.POINTER(attn_mask_t), c_void_p, c_size_t, c_void_p]),
     "attn_varlen_bwd_workspace_bytes": (c_size_t, [c_int, c_int64, c_int]),
+    "attn_fwd_fp8": (c_int, [c_void_p, c_void_p, c_void_p, c_float, c_float, c_float, c_void_p, c_void_p, c_int,
+                             c_int, c_int, c_int, c_int, c_float, C.POINTER(attn_mask_t), c_void_p, c_size_t,
+                             c_void_p]),
+    "attn_fwd_fp8_workspace_bytes": (c_size_t, [c_int, c_int, c_int, c_int]),
     "attn_decode_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                                 c_int, c_int, c_int, c_float, c_int, c_int, c_void_p, c_size_t, c_void_p]),
     "attn_decode_splits": (c_int, [c_int, c_int, c_int]),

@@ -16,7 +16,7 @@ import torch
 from . import _ffi
 from ._ffi import attn_mask_t, check
 
-__all__ = ["attn_fwd", "attn_partial_fwd", "attn_merge_lse", "attn_bwd", "bwd_workspace_bytes",
+__all__ = ["attn_fwd", "attn_fwd_fp8", "fwd_fp8_workspace_bytes", "attn_partial_fwd", "attn_merge_lse", "attn_bwd", "bwd_workspace_bytes",
            "build_schedule", "build_chunk_schedule", "get_status", "set_wait_limit_ns",
            "selftest_wait_timeout", "mask_desc", "trace_enable", "trace_disable", "trace_read"]
 
@@ -96,6 +96,47 @@ def attn_fwd(q, k, v, scale: Optional[float] = None, causal: bool = False,
     m, keep = mask_desc(causal, block_mask, causal_in_blocks, window)
     check(_ffi.lib().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
                               B, Hq, Hkv, N, d, sc, _mp(m), _stream(q)), "attn_fwd")
+    del keep
+    return o, l
+
+
+def fwd_fp8_workspace_bytes(B: int, Hkv: int, N: int, d: int = 128) -> int:
+    return int(_ffi.lib().attn_fwd_fp8_workspace_bytes(B, Hkv, N, d))
+
+
+def _e4m3(t: torch.Tensor, name: str):
+    """Accept float8_e4m3fn or uint8 (raw E4M3 codes) contiguous CUDA tensors."""
+    if not (t.is_cuda and t.dtype in (torch.float8_e4m3fn, torch.uint8) and t.is_contiguous() and t.dim() == 4):
+        raise ValueError(f"{name} must be a contiguous CUDA float8_e4m3fn (or uint8 code) [B, H, N, d] tensor")
+
+
+def attn_fwd_fp8(q8, k8, v8, q_descale: float = 1.0, k_descale: float = 1.0, v_descale: float = 1.0,
+                 scale: Optional[float] = None, causal: bool = False, block_mask: Optional[torch.Tensor] = None,
+                 causal_in_blocks: bool = False, window: Optional[int] = None,
+                 out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                 workspace: Optional[torch.Tensor] = None):
+    """Forward on E4M3 operands: ``O = softmax(scale (qd Q8)(kd K8)^T) (vd V8)``.
+
+    Returns ``(O [B,Hq,N,d] bf16, LSE [B,Hq,N] f32)``; ``d`` must be 128.
+    ``workspace`` (uint8, >= ``fwd_fp8_workspace_bytes``) receives V^T.
+    """
+    for t, n in ((q8, "q8"), (k8, "k8"), (v8, "v8")):
+        _e4m3(t, n)
+    B, Hq, N, d = q8.shape
+    Hkv = k8.shape[1]
+    if k8.shape != (B, Hkv, N, d) or v8.shape != k8.shape:
+        raise ValueError("k8 and v8 must be [B, Hkv, N, d] matching q8")
+    o = torch.empty((B, Hq, N, d), device=q8.device, dtype=torch.bfloat16) if out is None else out
+    _contig(o, "out")
+    l = torch.empty((B, Hq, N), device=q8.device, dtype=torch.float32) if lse is None else lse
+    _contig(l, "lse", torch.float32)
+    need = fwd_fp8_workspace_bytes(B, Hkv, N, d)
+    ws = torch.empty(max(need, 16), device=q8.device, dtype=torch.uint8) if workspace is None else workspace
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    m, keep = mask_desc(causal, block_mask, causal_in_blocks, window)
+    check(_ffi.lib().attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), float(q_descale), float(k_descale),
+                                  float(v_descale), o.data_ptr(), l.data_ptr(), B, Hq, Hkv, N, d, sc, _mp(m),
+                                  ws.data_ptr(), ws.numel() * ws.element_size(), _stream(q8)), "attn_fwd_fp8")
     del keep
     return o, l
 

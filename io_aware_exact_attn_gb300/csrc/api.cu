@@ -352,6 +352,83 @@ int attn_varlen_fwd(const void* q, const void* k, const void* v, void* o, float*
   return ATTN_OK;
 }
 
+size_t attn_fwd_fp8_workspace_bytes(int B, int Hkv, int N, int d) {
+  if (B < 1 || Hkv < 1 || N < 1 || d < 1) return 0;
+  return (size_t)B * Hkv * d * (size_t)(cdiv(N, TILE) * TILE);
+}
+
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, float q_descale, float k_descale, float v_descale,
+                 void* o, float* lse, int B, int Hq, int Hkv, int N, int d, float scale, const attn_mask_t* mask,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+  int rc;
+  if ((rc = check_ptr(q8, "q8")) || (rc = check_ptr(k8, "k8")) || (rc = check_ptr(v8, "v8")) ||
+      (rc = check_ptr(o, "o")) || (rc = check_ptr(workspace, "workspace")))
+    return rc;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(ATTN_ERR_MISALIGNED, "lse not 4-byte aligned");
+  if ((rc = check_dims(B, Hq, Hkv, N, N, d, scale))) return rc;
+  if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the e4m3 forward is built for d = 128 only (d=%d)", d);
+  for (float f : {q_descale, k_descale, v_descale})
+    if (!(f > 0.f) || !std::isfinite(f)) return fail(ATTN_ERR_INVALID_ARG, "descale factors must be finite and > 0");
+  if (workspace_bytes < attn_fwd_fp8_workspace_bytes(B, Hkv, N, d))
+    return fail(ATTN_ERR_WORKSPACE, "workspace %zu < %zu bytes", workspace_bytes,
+                attn_fwd_fp8_workspace_bytes(B, Hkv, N, d));
+  MaskArgs m;
+  if ((rc = read_mask(mask, &m))) return rc;
+  unsigned int* status = nullptr;
+  if ((rc = device_ready(&status))) return rc;
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const int Np = (int)(cdiv(N, TILE) * TILE);
+  // byte maps, 128 x 128 boxes (128 e4m3 values = one 128-byte swizzle row)
+  auto encode = [&](CUtensorMap* map, const void* base, int64_t cols, int64_t rows, int64_t heads) {
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)cols, (cuuint64_t)(cols * rows)};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_INVALID_ARG, "cuTensorMapEncodeTiled (e4m3) failed (%d)", (int)r);
+    return (int)ATTN_OK;
+  };
+  CUtensorMap tq, tk, tvt;
+  if ((rc = encode(&tq, q8, d, N, (int64_t)B * Hq)) || (rc = encode(&tk, k8, d, N, (int64_t)B * Hkv)) ||
+      (rc = encode(&tvt, workspace, Np, d, (int64_t)B * Hkv)))
+    return rc;
+  FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.o_hs = (int64_t)N * d;
+  p.o_rs = d;
+  p.l_hs = N;
+  p.l_rs = 1;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = N; p.Nk = N;
+  p.nqc = (int)cdiv(N, UNIT_ROWS);
+  p.head_group = kv_stream_group(B, Hq, Hkv, N, d / 2);   // K + V are half the bf16 bytes
+  p.scale_log2 = scale * q_descale * k_descale * 1.4426950408889634f;
+  p.mask_kind = m.kind;
+  p.causal_in_blocks = m.causal_in_blocks;
+  p.block_mask = m.block_mask;
+  p.window = m.window;
+  p.nkb = (int)cdiv(N, TILE);
+  p.dec_nq = 1;
+  p.status = status;
+  p.wait_limit_ns = wait_limit();
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  {
+    TraceScope ts(ATTN_KERNEL_FP8_TRANSPOSE_V, st);
+    e = launch_transpose_v_fp8(v8, workspace, B * Hkv, N, Np, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "e4m3 V transpose launch");
+  {
+    TraceScope ts(ATTN_KERNEL_FP8_FWD, st);
+    e = launch_fwd_fp8(tq, tk, tvt, p, v_descale, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "e4m3 forward launch");
+  return ATTN_OK;
+}
+
 int attn_decode_splits(int B, int Hkv, int Nk) {
   if (B < 1 || Hkv < 1 || Nk < 1) return 1;
   // about six waves of CTAs on 148 SMs (measured on B=8, Hkv=8, Nk=32768:

@@ -86,6 +86,12 @@ int encode_rows_map(CUtensorMap* map, const void* base, int d, int rows, int hea
 cudaError_t launch_fwd(int d, bool out_f32, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const FwdParams& p, cudaStream_t s);
 
+// e4m3 forward (d = 128): Q, K as [heads][rows][128] and V^T as
+// [heads][128][Np] byte maps with a 128 x 128 box and 128-byte swizzle.
+cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt, const FwdParams& p,
+                           float v_descale, cudaStream_t s);
+cudaError_t launch_transpose_v_fp8(const void* v, void* vt, int heads, int N, int Np, cudaStream_t s);
+
 cudaError_t launch_merge(const float* const* o_parts, const float* const* lse_parts, int n_parts,
                          void* o_out, bool out_f32, float* lse_out, int rows_per_head, int heads,
                          int d, int64_t out_head_stride, cudaStream_t s);

@@ -100,6 +100,20 @@ def test_argument_validation_without_gpu(lib):
                                1 << 30, None) == -1                                       # Nq > Nk
     assert lib.attn_decode_fwd(*q, None, _ptr(good), None, 2, 8, 2, 3, 1000, 64, 0.125, 1, 65, _ptr(good),
                                1 << 30, None) == -1                                       # too many splits
+    # e4m3 forward: d = 128 only, positive finite scale factors, workspace for V^T
+    assert lib.attn_fwd_fp8_workspace_bytes(2, 4, 300, 128) == 2 * 4 * 128 * 384
+    f8 = [_ptr(good)] * 3
+    fws = lib.attn_fwd_fp8_workspace_bytes(1, 2, 128, 128)
+    assert lib.attn_fwd_fp8(*f8, 1.0, 1.0, 1.0, _ptr(good), None, 1, 2, 2, 128, 64, 0.125, None, _ptr(good),
+                            1 << 30, None) == -2
+    assert lib.attn_fwd_fp8(*f8, 1.0, 0.0, 1.0, _ptr(good), None, 1, 2, 2, 128, 128, 0.125, None, _ptr(good),
+                            1 << 30, None) == -1
+    assert lib.attn_fwd_fp8(*f8, 1.0, 1.0, float("inf"), _ptr(good), None, 1, 2, 2, 128, 128, 0.125, None,
+                            _ptr(good), 1 << 30, None) == -1
+    assert lib.attn_fwd_fp8(*f8, 1.0, 1.0, 1.0, _ptr(good), None, 1, 2, 2, 128, 128, 0.125, None, _ptr(good),
+                            fws - 1, None) == -6
+    assert lib.attn_fwd_fp8(*f8, 1.0, 1.0, 1.0, _ptr(good), None, 1, 2, 2, 128, 128, 0.125, None, None,
+                            fws, None) == -1
     # partial fwd: head stride smaller than the rows is rejected
     assert lib.attn_partial_fwd(_ptr(good), _ptr(good), _ptr(good), _ptr(good), _ptr(good), 1, 2, 2, 256, 256,
                                 64, 0.125, None, 0, 0, 100, 0, None) == -1
