@@ -248,7 +248,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extras", action="store_true", help="skip the e2e, chunked and CPU legs")
     ap.add_argument("--profile-pass", action="store_true",
-                    help="one untimed step only (for profiler launch lists); prints nothing")
+                    help="one untimed step and one E4M3 forward only (for profiler captures); prints nothing")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -292,6 +292,10 @@ def main():
 
     if args.profile_pass:
         step()
+        # and one E4M3 forward on the same shape (the fp8_fwd leg's workload)
+        f = FP8
+        q8, k8, v8, (qd, kd, vd) = inputs.make_qkv_e4m3(f["B"], f["Hq"], f["Hkv"], f["N"], f["d"])
+        api.attn_fwd_fp8(q8.cuda(), k8.cuda(), v8.cuda(), qd, kd, vd, causal=True)
         torch.cuda.synchronize()
         return 0
 
@@ -648,7 +652,11 @@ def fp8_leg(api, inputs, torch, peaks, rank, reps=10):
     flops = fwd_flops(B, Hq, N, d, True)
     peak8 = 2.0 * peaks["bf16_tflops"]
     tr_bytes = 2.0 * B * Hkv * N * d
-    return dict(workload=f"B={B} Hq={Hq} Hkv={Hkv} N={N} d={d} causal, e4m3 Q/K/V",
+    ach = flops / (fwd_ms * 1e-3) / 1e12
+    roof = dict(bound="tensor", achieved=ach, peak=peak8, unit="TFLOP/s", frac=ach / peak8,
+                traffic=profile_traffic("fwd_fp8", c["name"]), kernel="fwd_fp8",
+                peak_source="2 x measured bf16_tflops (burst; kernel timed alone), the nominal fp8:bf16 ratio")
+    return dict(workload=f"B={B} Hq={Hq} Hkv={Hkv} N={N} d={d} causal, e4m3 Q/K/V", roofline=roof,
                 fwd_ms=fwd_ms, transpose_v_ms=tr_ms, fwd_tflops=flops / (fwd_ms * 1e-3) / 1e12,
                 with_transpose_tflops=flops / ((fwd_ms + tr_ms) * 1e-3) / 1e12,
                 fp8_peak_tflops=peak8, fwd_frac_of_fp8_peak=flops / (fwd_ms * 1e-3) / 1e12 / peak8,
