@@ -20,7 +20,7 @@
 //                loops over the key tiles it sees: S = Q K^T, dP = dO V^T,
 //                dS = P * (dP - D), dQ += dS K, dQ accumulated in fp32 in
 //                tensor memory and scaled / rounded once at the end.
-// Warp roles (12 warps): warp 0 TMA producer, warp 1 MMA issuer (one thread,
+// Warp roles (12 warps): warp 0 TMA producer, warp 1 MMA issuer (one elected lane,
 // owns the TMEM allocation), warps 2-3 idle, warps 4-11 elementwise work in
 // two warpgroups that split the 128 columns of every tile row between them
 // (warp w owns TMEM lanes 32*(w%4)..+31; one thread per row and half).
@@ -42,9 +42,10 @@ struct BwdCfg {
   static constexpr int NS = (D == 128) ? 2 : 4;  // ring depth
   static constexpr int THREADS = 256;
   // both kernels: 12 warps; the control warpgroup gives registers back to the
-  // two elementwise warpgroups: 128*56 + 256*224 = 384*168 (launch allotment)
+  // two elementwise warpgroups: 128*64 + 256*216 = 63488 <= 384*168 (launch
+  // allotment); at this split neither role spills
   static constexpr int SPLIT_THREADS = 384;
-  static constexpr uint32_t REGS_CTRL = 56, REGS_ELEM = 224;
+  static constexpr uint32_t REGS_CTRL = 64, REGS_ELEM = 216;
 };
 
 // The sliding window includes the causal rule.
@@ -221,19 +222,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       for (int j = n - NS < 0 ? 0 : n - NS; j < n; ++j) wait_bar(bar_q(j % NS), (j / NS) & 1, wc, false);
     }
    } else if (warp == 1) {
-    if (lane == 0) {
+    {
+      // every lane waits, so the warp leaves a wait together
+      auto wt = [&](uint32_t bar, uint32_t par) { return __all_sync(0xffffffffu, wait_bar(bar, par, wc)); };
       // ---------------------------------------------------------- MMA issuer
       // Order: S^T_0, dP^T_0, then per query tile i: dV_i, S^T_{i+1}, dK_i,
       // dP^T_{i+1}.  S^T_{i+1} overwrites the P^T_i columns dV_i reads and
       // dP^T_{i+1} the dS^T_i columns dK_i reads; each is issued right after
       // that reader (tcgen05.mma from one thread execute in issue order).
       // Each elementwise phase has two MMAs of cover.
-      // tcgen05.mma issue stalls once a few MMAs are queued, so this thread
+      // tcgen05.mma issue stalls once a few MMAs are queued, so the issuer
       // is held for most of each group and anything it does between groups
       // idles the tensor pipe: it keeps ring counters only, and descriptors
       // are built once (a k-step adds a compile-time offset to the
       // start-address field; shared-memory addresses stay below 256 KB, so
-      // the 14-bit field never carries).
+      // the 14-bit field never carries).  The whole warp runs the loop and
+      // elect.sync picks the issuing lane (always the same one while the warp
+      // is converged), which feeds the pipe faster than a one-lane loop.
       const uint32_t id_s = idesc_bf16(128, 128, false, false);
       const uint32_t id_acc = idesc_bf16(128, D, false, true);
       constexpr uint32_t STAGE16 = STAGE >> 4, TILE16 = C::TILE_BYTES >> 4;
@@ -247,22 +252,22 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       auto issue_st = [&](int slot) {   // S^T = K Q^T
         const uint32_t qd = d_ring + (uint32_t)slot * STAGE16;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + 0, desc(d_k + kstep(kk)), desc(qd + kstep(kk)), id_s, kk > 0);
-        mma_commit(bar_s);
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss_e(tmem + 0, desc(d_k + kstep(kk)), desc(qd + kstep(kk)), id_s, kk > 0);
+        mma_commit_e(bar_s);
       };
       auto issue_dpt = [&](int slot) {  // dP^T = V dO^T
         const uint32_t dd = d_ring + (uint32_t)slot * STAGE16 + TILE16;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + 128, desc(d_v + kstep(kk)), desc(dd + kstep(kk)), id_s, kk > 0);
-        mma_commit(bar_dp);
+          mma_ss_e(tmem + 128, desc(d_v + kstep(kk)), desc(dd + kstep(kk)), id_s, kk > 0);
+        mma_commit_e(bar_dp);
       };
       int nvis = 0;
       for (int qt = qt_first; qt < nqt; ++qt) nvis += tile_pair_visible(p, qt, kt) ? 1 : 0;
       const int ntile = nvis * g;   // (query head, query tile) pairs, in the producer's order
-      bool ok = wait_bar(bar_kv, 0, wc);
+      bool ok = wt(bar_kv, 0);
       if (ok && ntile > 0) {
-        ok = wait_bar(bar_q(0), 0, wc);
+        ok = wt(bar_q(0), 0);
         if (ok) {
           tc_fence_after();
           issue_st(0);
@@ -278,32 +283,32 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
         const uint32_t par = (uint32_t)i & 1u;
         const uint32_t md = d_ring_mn + (uint32_t)s * STAGE16;
         // dV += P^T dO   (dO as an MN-major operand: N = d, K = query rows)
-        if (!(ok = wait_bar(bar_p, par, wc))) break;
+        if (!(ok = wt(bar_p, par))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < TILE / 16; ++kk)
-          mma_ts(tmem + 256, tmem + half_col(kk), desc(md + TILE16 + (uint32_t)kk * (2048 >> 4)), id_acc,
+          mma_ts_e(tmem + 256, tmem + half_col(kk), desc(md + TILE16 + (uint32_t)kk * (2048 >> 4)), id_acc,
                  (i > 0 || kk > 0));
-        mma_commit(bar_dv);
+        mma_commit_e(bar_dv);
         if (more) {
-          if (!(ok = wait_bar(bar_q(sn), snpar, wc))) break;
+          if (!(ok = wt(bar_q(sn), snpar))) break;
           tc_fence_after();
           issue_st(sn);
         }
         // dK += dS^T Q
-        if (!(ok = wait_bar(bar_ds, par, wc))) break;
+        if (!(ok = wt(bar_ds, par))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < TILE / 16; ++kk)
-          mma_ts(tmem + 256 + D, tmem + 128 + half_col(kk), desc(md + (uint32_t)kk * (2048 >> 4)), id_acc,
+          mma_ts_e(tmem + 256 + D, tmem + 128 + half_col(kk), desc(md + (uint32_t)kk * (2048 >> 4)), id_acc,
                  (i > 0 || kk > 0));
-        mma_commit(bar_dk);
-        mma_commit(bar_qfree(s));
+        mma_commit_e(bar_dk);
+        mma_commit_e(bar_qfree(s));
         if (more) issue_dpt(sn);
         s = sn;
         spar = snpar;
       }
-      mma_commit(bar_done);
+      mma_commit_e(bar_done);
       wait_bar(bar_done, 0, wc, false);
     }
    }
@@ -589,14 +594,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       for (int j = n - depth < 0 ? 0 : n - depth; j < n; ++j) wait_bar(full(j % depth), (j / depth) & 1, wc, false);
     }
    } else if (warp == 1) {
-    if (lane == 0) {
+    {
+      // every lane waits, so the warp leaves a wait together
+      auto wt = [&](uint32_t bar, uint32_t par) { return __all_sync(0xffffffffu, wait_bar(bar, par, wc)); };
       // ---------------------------------------------------------- MMA issuer
-      // tcgen05.mma issue stalls once a few MMAs are queued, so this thread
+      // tcgen05.mma issue stalls once a few MMAs are queued, so the issuer
       // is held for most of each 8-MMA group; whatever it does between groups
       // leaves the tensor pipe idle.  The loop therefore keeps no more than
       // ring counters: descriptors are built once and each k-step adds a
       // compile-time offset to the start-address field (shared-memory
       // addresses stay below 256 KB, so the 14-bit field never carries).
+      // The whole warp runs the loop and elect.sync picks the issuing lane
+      // (always the same one while the warp is converged).
       const uint32_t id_s = idesc_bf16(128, 128, false, false);
       const uint32_t id_dq = idesc_bf16(128, D, false, true);
       // the upper descriptor word (stride offset, version, swizzle) is the
@@ -613,28 +622,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       auto issue_s = [&](int slot) {   // S = Q K^T
         const uint32_t kd = d_k + (uint32_t)slot * SLOT;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + T_S, desc(d_q + kstep(kk)), desc(kd + kstep(kk)), id_s, kk > 0);
-        mma_commit(bar_s);
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss_e(tmem + T_S, desc(d_q + kstep(kk)), desc(kd + kstep(kk)), id_s, kk > 0);
+        mma_commit_e(bar_s);
       };
       auto issue_dp = [&](int slot) {  // dP = dO V^T; the V slot is free once it completes
         const uint32_t vd = d_v + (uint32_t)slot * SLOT;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + T_DP, desc(d_do + kstep(kk)), desc(vd + kstep(kk)), id_s, kk > 0);
-        mma_commit(bar_dp);
-        mma_commit(bar_vfree(slot));
+          mma_ss_e(tmem + T_DP, desc(d_do + kstep(kk)), desc(vd + kstep(kk)), id_s, kk > 0);
+        mma_commit_e(bar_dp);
+        mma_commit_e(bar_vfree(slot));
       };
       int nvis = 0;
       for (int kt = 0; kt < kt_end; ++kt) nvis += tile_pair_visible(p, qt, kt) ? 1 : 0;
       // ring positions: K_{j+1} / V_{j+1} (next S / dP) and K_j (dQ)
       int ks = 0, kpar = 0, vs = 0, vpar = 0, kq = 0;
-      bool ok = wait_bar(bar_qdo, 0, wc);
+      bool ok = wt(bar_qdo, 0);
       if (ok && nvis > 0) {
-        ok = wait_bar(bar_k(0), 0, wc);
+        ok = wt(bar_k(0), 0);
         if (ok) {
           tc_fence_after();
           issue_s(0);
-          ok = wait_bar(bar_v(0), 0, wc);
+          ok = wt(bar_v(0), 0);
         }
         if (ok) {
           tc_fence_after();
@@ -646,29 +655,29 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
         const uint32_t par = (uint32_t)j & 1u;
         if (j + 1 < nvis) {
           // S_{j+1} once S_j has been read out of TMEM
-          if (!(ok = wait_bar(bar_k(ks), kpar, wc) && wait_bar(bar_sfree, par, wc))) break;
+          if (!(ok = wt(bar_k(ks), kpar) && wt(bar_sfree, par))) break;
           tc_fence_after();
           issue_s(ks);
           if (++ks == KS) { ks = 0; kpar ^= 1; }
           // dP_{j+1} as soon as dP_j has been read out of TMEM
-          if (!(ok = wait_bar(bar_v(vs), vpar, wc) && wait_bar(bar_dpread, par, wc))) break;
+          if (!(ok = wt(bar_v(vs), vpar) && wt(bar_dpread, par))) break;
           tc_fence_after();
           issue_dp(vs);
           if (++vs == VS) { vs = 0; vpar ^= 1; }
         }
         // dQ_j += dS_j K_j   (K_j as an MN-major operand: N = d, K = keys)
-        if (!(ok = wait_bar(bar_ds(j), ((uint32_t)j >> 1) & 1u, wc))) break;
+        if (!(ok = wt(bar_ds(j), ((uint32_t)j >> 1) & 1u))) break;
         tc_fence_after();
         const uint32_t kd = d_kmn + (uint32_t)kq * SLOT;
         const uint32_t ds = tmem + T_DS + (par << 6);
 #pragma unroll
         for (int kk = 0; kk < TILE / 16; ++kk)
-          mma_ts(tmem + T_DQ, ds + kk * 8, desc(kd + (uint32_t)kk * (2048 >> 4)), id_dq, (j > 0 || kk > 0));
-        mma_commit(bar_dq(j));
-        mma_commit(bar_kfree(kq));
+          mma_ts_e(tmem + T_DQ, ds + kk * 8, desc(kd + (uint32_t)kk * (2048 >> 4)), id_dq, (j > 0 || kk > 0));
+        mma_commit_e(bar_dq(j));
+        mma_commit_e(bar_kfree(kq));
         if (++kq == KS) kq = 0;
       }
-      mma_commit(bar_done);
+      mma_commit_e(bar_done);
       wait_bar(bar_done, 0, wc, false);
     }
    }

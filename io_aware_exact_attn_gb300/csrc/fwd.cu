@@ -15,7 +15,8 @@
 // Warp roles (12 warps, three warpgroups):
 //   warp 0      TMA producer: Q0/Q1 once, then K_j and V_j into NS-deep rings;
 //               one lane per 16 KB box, K slots released after the S MMAs
-//   warp 1      MMA issuer (one thread): S_t = Q_t K_j^T, then O_t += P_t V_j
+//   warp 1      MMA issuer (the whole warp runs the loop, one elected lane
+//               issues): S_t = Q_t K_j^T, then O_t += P_t V_j
 //               with P_t read from tensor memory; owns the TMEM allocation
 //   warps 2-3   idle (they complete the control warpgroup)
 //   warps 4-7   softmax for tile 0 (warp w owns TMEM lanes 32*(w%4)..+31)
@@ -175,13 +176,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     // PV_t(n) that reads them, and tcgen05.mma from one thread execute in
     // issue order.  Each softmax thus has two MMAs of cover (PV of the other
     // tile and its S) before its own PV is needed.
-    // tcgen05.mma issue stalls once a few MMAs are queued, so this thread is
+    // tcgen05.mma issue stalls once a few MMAs are queued, so the issuer is
     // held for most of each group and anything it does between groups idles
     // the tensor pipe: it keeps ring counters only, and descriptors are built
     // once (a k-step adds a compile-time offset to the start-address field;
     // shared-memory addresses stay below 256 KB, so the 14-bit field never
-    // carries).
-    if (lane == 0) {
+    // carries).  The whole warp runs the loop converged and elect.sync picks
+    // the issuing lane for each MMA and commit (the lowest active lane, so
+    // always the same thread, as in-order execution and commit tracking
+    // need): the same loop run by one lane of a diverged warp issued about
+    // one MMA per 90-110 cycles here, slower than the pipe's 64.
+    {
+      // every lane waits, so the warp leaves a wait together
+      auto wt = [&](uint32_t bar, uint32_t par) { return __all_sync(0xffffffffu, wait_bar(bar, par, wc)); };
       const uint32_t id_s = idesc_bf16(128, 128, false, false);
       const uint32_t id_pv = idesc_bf16(128, D, false, true);
       constexpr uint32_t TILE16 = C::TILE_BYTES >> 4;
@@ -201,28 +208,28 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const uint32_t qd = d_q + (uint32_t)t * TILE16;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + t * 128, desc(qd + kstep(kk)), desc(kd + kstep(kk)), id_s, kk > 0);
-        mma_commit(bar_s(t));
+          mma_ss_e(tmem + t * 128, desc(qd + kstep(kk)), desc(kd + kstep(kk)), id_s, kk > 0);
+        mma_commit_e(bar_s(t));
       };
       auto issue_pv = [&](int t, int slot, bool acc) {
         const uint32_t vd = d_vmn + (uint32_t)slot * TILE16;
 #pragma unroll
         for (int kk = 0; kk < TILE / 16; ++kk)
-          mma_ts(tmem + C::TMEM_O + t * D, tmem + t * 128 + kk * 8, desc(vd + (uint32_t)kk * (2048 >> 4)), id_pv,
+          mma_ts_e(tmem + C::TMEM_O + t * D, tmem + t * 128 + kk * 8, desc(vd + (uint32_t)kk * (2048 >> 4)), id_pv,
                  (acc || kk > 0));
-        mma_commit(bar_o(t));
+        mma_commit_e(bar_o(t));
       };
       int it0 = 0, it1 = 0;   // PV MMAs issued per tile
-      bool ok = wait_bar(bar_q, 0, wc);
+      bool ok = wt(bar_q, 0);
       int kt = next_kt(u.kt_begin);
       uint32_t use = kt < u.kt_end ? unit_uses(u, kt) : 0u;
       if (ok && use) {
-        ok = wait_bar(bar_k(0), 0, wc);
+        ok = wt(bar_k(0), 0);
         if (ok) {
           tc_fence_after();
           if (use & 1u) issue_s(0, 0);
           if (use & 2u) issue_s(1, 0);
-          mma_commit(bar_kfree(0));
+          mma_commit_e(bar_kfree(0));
         }
       }
       int s = 0;
@@ -233,39 +240,39 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const int ktn = next_kt(kt + 1);
         const uint32_t usen = ktn < u.kt_end ? unit_uses(u, ktn) : 0u;
         bool kwaited = false;
-        if (!(ok = wait_bar(bar_v(s), ph, wc))) break;
+        if (!(ok = wt(bar_v(s), ph))) break;
         if (use & 1u) {
-          if (!(ok = wait_bar(bar_p(0), (uint32_t)it0 & 1u, wc))) break;
+          if (!(ok = wt(bar_p(0), (uint32_t)it0 & 1u))) break;
           tc_fence_after();
           issue_pv(0, s, it0 > 0);
           ++it0;
         }
         if (usen & 1u) {
-          if (!(ok = wait_bar(bar_k(sn), phn, wc))) break;
+          if (!(ok = wt(bar_k(sn), phn))) break;
           tc_fence_after();
           kwaited = true;
           issue_s(0, sn);
         }
         if (use & 2u) {
-          if (!(ok = wait_bar(bar_p(1), (uint32_t)it1 & 1u, wc))) break;
+          if (!(ok = wt(bar_p(1), (uint32_t)it1 & 1u))) break;
           tc_fence_after();
           issue_pv(1, s, it1 > 0);
           ++it1;
         }
-        mma_commit(bar_vfree(s));   // both PV MMAs of this key tile issued
+        mma_commit_e(bar_vfree(s));   // both PV MMAs of this key tile issued
         if (usen & 2u) {
-          if (!kwaited && !(ok = wait_bar(bar_k(sn), phn, wc))) break;
+          if (!kwaited && !(ok = wt(bar_k(sn), phn))) break;
           tc_fence_after();
           issue_s(1, sn);
         }
-        if (usen) mma_commit(bar_kfree(sn));
+        if (usen) mma_commit_e(bar_kfree(sn));
         kt = ktn;
         use = usen;
         s = sn;
         ph = phn;
       }
       // every commit above lands before the CTA leaves
-      mma_commit(bar_done);
+      mma_commit_e(bar_done);
       wait_bar(bar_done, 0, wc, false);
     }
    }

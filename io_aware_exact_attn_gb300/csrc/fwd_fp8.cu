@@ -156,8 +156,12 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
     // memory.  Each product is four MMAs of K = 32; a k-step adds 32 bytes (2
     // in the descriptor's 16-byte units) inside the 128-byte swizzled rows.
     // The loop keeps ring counters only, with the descriptors' upper words
-    // fixed and the lower words built once.
-    if (lane == 0) {
+    // fixed and the lower words built once; the whole warp runs it and
+    // elect.sync picks the issuing lane (always the same one while the warp
+    // is converged).
+    {
+      // every lane waits, so the warp leaves a wait together
+      auto wt = [&](uint32_t bar, uint32_t par) { return __all_sync(0xffffffffu, wait_bar(bar, par, wc)); };
       constexpr uint32_t ID = idesc_e4m3(128, 128);
       constexpr uint32_t TILE16 = C::TILE_BYTES >> 4;
       const uint32_t HI = (uint32_t)(sdesc_sw128(0, 16, 1024) >> 32);
@@ -175,28 +179,28 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
         const uint32_t kd = d_k + (uint32_t)slot * TILE16, qd = d_q + (uint32_t)t * TILE16;
 #pragma unroll
         for (int kk = 0; kk < D / 32; ++kk)
-          mma_ss_f8(tmem + t * 128, desc(qd + kk * 2), desc(kd + kk * 2), ID, kk > 0);
-        mma_commit(bar_s(t));
+          mma_ss_f8_e(tmem + t * 128, desc(qd + kk * 2), desc(kd + kk * 2), ID, kk > 0);
+        mma_commit_e(bar_s(t));
       };
       auto issue_pv = [&](int t, int slot, bool acc) {   // O_t += P_t (V^T)^T
         const uint32_t vd = d_v + (uint32_t)slot * TILE16, pd = d_p + (uint32_t)t * TILE16;
 #pragma unroll
         for (int kk = 0; kk < TILE / 32; ++kk)
-          mma_ss_f8(tmem + C::TMEM_O + t * D, desc(pd + kk * 2), desc(vd + kk * 2), ID, acc || kk > 0);
-        mma_commit(bar_o(t));
+          mma_ss_f8_e(tmem + C::TMEM_O + t * D, desc(pd + kk * 2), desc(vd + kk * 2), ID, acc || kk > 0);
+        mma_commit_e(bar_o(t));
       };
       int cs0 = 0, cs1 = 0;   // S MMAs issued per query tile
       int cp0 = 0, cp1 = 0;   // PV MMAs issued per query tile
-      bool ok = wait_bar(bar_q, 0, wc);
+      bool ok = wt(bar_q, 0);
       int kt = next_kt(u.kt_begin);
       uint32_t use = kt < u.kt_end ? unit_uses(u, kt) : 0u;
       if (ok && use) {
-        ok = wait_bar(bar_k(0), 0, wc);
+        ok = wt(bar_k(0), 0);
         if (ok) {
           tc_fence_after();
           if (use & 1u) { issue_s(0, 0); ++cs0; }
           if (use & 2u) { issue_s(1, 0); ++cs1; }
-          mma_commit(bar_kfree(0));
+          mma_commit_e(bar_kfree(0));
         }
       }
       int s = 0;
@@ -208,43 +212,43 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
         const uint32_t usen = ktn < u.kt_end ? unit_uses(u, ktn) : 0u;
         if (usen) {
           // the next scores, each as soon as its softmax has read the current ones
-          if (!(ok = wait_bar(bar_k(sn), phn, wc))) break;
+          if (!(ok = wt(bar_k(sn), phn))) break;
           if (usen & 1u) {
-            if (cs0 > 0 && !(ok = wait_bar(bar_sread(0), (uint32_t)(cs0 - 1) & 1u, wc))) break;
+            if (cs0 > 0 && !(ok = wt(bar_sread(0), (uint32_t)(cs0 - 1) & 1u))) break;
             tc_fence_after();
             issue_s(0, sn);
             ++cs0;
           }
           if (usen & 2u) {
-            if (cs1 > 0 && !(ok = wait_bar(bar_sread(1), (uint32_t)(cs1 - 1) & 1u, wc))) break;
+            if (cs1 > 0 && !(ok = wt(bar_sread(1), (uint32_t)(cs1 - 1) & 1u))) break;
             tc_fence_after();
             issue_s(1, sn);
             ++cs1;
           }
-          mma_commit(bar_kfree(sn));
+          mma_commit_e(bar_kfree(sn));
         }
         // this key tile's P.V products
-        if (!(ok = wait_bar(bar_v(s), ph, wc))) break;
+        if (!(ok = wt(bar_v(s), ph))) break;
         if (use & 1u) {
-          if (!(ok = wait_bar(bar_p(0), (uint32_t)cp0 & 1u, wc))) break;
+          if (!(ok = wt(bar_p(0), (uint32_t)cp0 & 1u))) break;
           tc_fence_after();
           issue_pv(0, s, cp0 > 0);
           ++cp0;
         }
         if (use & 2u) {
-          if (!(ok = wait_bar(bar_p(1), (uint32_t)cp1 & 1u, wc))) break;
+          if (!(ok = wt(bar_p(1), (uint32_t)cp1 & 1u))) break;
           tc_fence_after();
           issue_pv(1, s, cp1 > 0);
           ++cp1;
         }
-        mma_commit(bar_vfree(s));
+        mma_commit_e(bar_vfree(s));
         kt = ktn;
         use = usen;
         s = sn;
         ph = phn;
       }
       // every commit above lands before the CTA leaves
-      mma_commit(bar_done);
+      mma_commit_e(bar_done);
       wait_bar(bar_done, 0, wc, false);
     }
    }
