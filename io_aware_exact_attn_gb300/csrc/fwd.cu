@@ -30,10 +30,12 @@
 // next key tile follows the PV_t that reads P_t out of the same columns.
 //
 // Online softmax per row, in units of log2: x = s * scale * log2(e),
-// m = running max, p = 2^(x - m), l = sum p.  The max used for p is only moved
-// when the true max exceeds it by more than 8 (p <= 256 in between); when it
-// moves, O_t is rescaled in tensor memory by 2^(m_old - m_new).  This keeps the
-// result exact: O and l always share the same reference max and the final
+// m = reference max, p = 2^(x - m), l = sum p.  The weights of a tile are
+// first taken against the current m; only when they sum past 2^8 (which any
+// weight above 2^8 would cause) is the tile's row max found and m moved to it,
+// so p <= 256 always and the max costs nothing in the usual case.  When m
+// moves, O_t is rescaled in tensor memory by 2^(m_old - m_new).  This keeps
+// the result exact: O and l always share the same reference max and the final
 // O / l cancels it.
 #include "internal.h"
 #include "ptx.cuh"
@@ -43,7 +45,9 @@ namespace attn {
 
 namespace {
 
-constexpr float RESCALE_THRESHOLD = 8.0f;
+// the reference max moves once a tile's weights (relative to it) sum past
+// 2^8, which any single weight above 2^8 implies
+constexpr float RESCALE_LIMIT = 256.0f;
 
 template <int D>
 struct FwdCfg {
@@ -342,49 +346,54 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           sc[j + 1] = ex2(x1);
         }
       };
+      // l sums the fp32 weights (for the log-sum-exp); lr, below, sums the
+      // bf16-rounded weights P.V sees, so O / lr cancels the rounding of a
+      // dominant weight
+      uint32_t pk[64];
+      auto pack_sum = [&](const float (&sc)[128]) {
+        float la[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // four independent packed chains
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          // bf16, rounded to nearest; O is normalised by the sum of these same
+          // weights, so a dominant weight's rounding cancels
+          pk[j] = pack_bf16(sc[2 * j], sc[2 * j + 1]);
+          const int a = 2 * (j & 3);
+          add2(la[a], la[a + 1], la[a], la[a + 1], sc[2 * j], sc[2 * j + 1]);
+        }
+        return ((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7]));
+      };
+      // Exponentials against the current reference max first.  Every weight
+      // stays within 2^THRESHOLD unless the row's sum of them exceeds that, so
+      // in the usual case the tile's row max is never needed; otherwise (and
+      // for a row's first visible tile) the max is found from the scores
+      // still in TMEM, the reference moves to it, and the weights are redone.
       float s[128];
       load_scores(s);
-      // Row max of the tile alongside exponentials taken against the current
-      // reference max: the usual case (max moved by at most the threshold)
-      // needs no second pass and the max is off the critical path.
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < 128; j += 8) {
-        mx0 = max3(mx0, s[j], s[j + 1]);
-        mx1 = max3(mx1, s[j + 2], s[j + 3]);
-        mx2 = max3(mx2, s[j + 4], s[j + 5]);
-        mx3 = max3(mx3, s[j + 6], s[j + 7]);
-      }
-      mx0 = max3(mx0, mx1, fmaxf(mx2, mx3));
       exponentials(s, (m == -INFINITY) ? 0.f : m);
-      const float m_new = fmaxf(m, mx0 * c);
+      float lt = pack_sum(s);
       float alpha = 1.f;
       bool rescale = false;
-      if (__any_sync(0xffffffffu, it == 0 || m_new > m + RESCALE_THRESHOLD)) {
-        // the reference max moves: O_t (if any) is rescaled by 2^(m_old - m_new)
-        // below, and the exponentials are redone from the scores still in TMEM
+      if (__any_sync(0xffffffffu, m == -INFINITY || !(lt <= RESCALE_LIMIT))) {
+        load_scores(s);
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 128; j += 8) {
+          mx0 = max3(mx0, s[j], s[j + 1]);
+          mx1 = max3(mx1, s[j + 2], s[j + 3]);
+          mx2 = max3(mx2, s[j + 4], s[j + 5]);
+          mx3 = max3(mx3, s[j + 6], s[j + 7]);
+        }
+        mx0 = max3(mx0, mx1, fmaxf(mx2, mx3));
+        const float m_new = fmaxf(m, mx0 * c);
+        // O_t (if any) is rescaled by 2^(m_old - m_new) below
         if (it > 0) {
           alpha = (m_new == -INFINITY) ? 1.f : ex2(m - m_new);
           rescale = true;
         }
         m = m_new;
-        load_scores(s);
         exponentials(s, (m == -INFINITY) ? 0.f : m);
+        lt = pack_sum(s);
       }
-      // l sums the fp32 weights (for the log-sum-exp); lr, below, sums the
-      // bf16-rounded weights P.V sees, so O / lr cancels the rounding of a
-      // dominant weight
-      uint32_t pk[64];
-      float la[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // four independent packed chains
-#pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        // bf16, rounded to nearest; O is normalised by the sum of these same
-        // weights, so a dominant weight's rounding cancels
-        pk[j] = pack_bf16(s[2 * j], s[2 * j + 1]);
-        const int a = 2 * (j & 3);
-        add2(la[a], la[a + 1], la[a], la[a + 1], s[2 * j], s[2 * j + 1]);
-      }
-      const float l0 = (la[0] + la[1]) + (la[2] + la[3]), l1 = (la[4] + la[5]) + (la[6] + la[7]);
       tmem_st64(tS, pk);    // P_t (bf16 pairs) over the first 64 columns of S_t
       if (rescale) {
         // PV_t of the previous key tile must have landed in O_t first
@@ -408,10 +417,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #pragma unroll
       for (int j = 0; j < 64; ++j) {
         const int a = 2 * (j & 3);
-        add2(ra[a], ra[a + 1], ra[a], ra[a + 1], __uint_as_float(pk[j] << 16), __uint_as_float(pk[j] & 0xffff0000u));
+        add_bf16x2_to_f32(ra[a], ra[a + 1], pk[j]);
       }
       const float r0 = (ra[0] + ra[1]) + (ra[2] + ra[3]), r1 = (ra[4] + ra[5]) + (ra[6] + ra[7]);
-      l = l * alpha + (l0 + l1);
+      l = l * alpha + lt;
       lr = lr * alpha + (r0 + r1);
 
     }

@@ -349,6 +349,16 @@ __device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, f
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// (acc_lo, acc_hi) += the two bf16 halves of `pk` (low half into acc_lo), each
+// converted exactly to fp32 inside a mixed-precision add: one instruction per
+// element instead of an unpack and a packed add per pair.
+__device__ __forceinline__ void add_bf16x2_to_f32(float& acc_lo, float& acc_hi, uint32_t pk) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(acc_lo), "+f"(acc_hi)
+      : "r"(pk));
+}
+
 // bf16 pair rounded to nearest with plain integer ops (half an ulp added to
 // each fp32 bit pattern, top halves kept by one byte permute): ties round away
 // from zero instead of to even, everything else matches round-to-nearest.
