@@ -343,10 +343,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
         const int hi = wedge ? window_of(p) + r - (qt - kt) * TILE : TILE;
         const float4* l4 = reinterpret_cast<const float4*>(lse2) + 16 * hf;
         const float4* d4 = reinterpret_cast<const float4*>(dsum) + 16 * hf;
-        // phase A: P^T = 2^(S^T c - lse2) for this warpgroup's 64 query columns.
+        // phase A: P^T = 2^(S^T c - lse2) for this warpgroup's 64 query columns,
+        // kept in fp32 for phase B and rounded to bf16 pairs for dV = P^T dO.
         // Masked tiles (the diagonal, a window's edge) take their own copy of
         // the loop so that the others carry no mask arithmetic at all.
-        uint32_t pk[32];
+        float pf[64];
         auto phase_a = [&](auto masked) {
           uint32_t sr[64];
           tmem_ld64(tmem + lane_off + cb, sr);
@@ -355,23 +356,30 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
           for (int j4 = 0; j4 < 16; ++j4) {
             const float4 L = l4[j4];
             const int col = cb + 4 * j4;
-            float p0 = ex2(fmaf(__uint_as_float(sr[4 * j4 + 0]), c, -L.x));
-            float p1 = ex2(fmaf(__uint_as_float(sr[4 * j4 + 1]), c, -L.y));
-            float p2 = ex2(fmaf(__uint_as_float(sr[4 * j4 + 2]), c, -L.z));
-            float p3 = ex2(fmaf(__uint_as_float(sr[4 * j4 + 3]), c, -L.w));
+            float x0, x1, x2, x3;
+            fma2(x0, x1, __uint_as_float(sr[4 * j4 + 0]), __uint_as_float(sr[4 * j4 + 1]), c, c, -L.x, -L.y);
+            fma2(x2, x3, __uint_as_float(sr[4 * j4 + 2]), __uint_as_float(sr[4 * j4 + 3]), c, c, -L.z, -L.w);
+            float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
             if constexpr (decltype(masked)::value) {
               p0 = (col + 0 >= lo && col + 0 < hi) ? p0 : 0.f;
               p1 = (col + 1 >= lo && col + 1 < hi) ? p1 : 0.f;
               p2 = (col + 2 >= lo && col + 2 < hi) ? p2 : 0.f;
               p3 = (col + 3 >= lo && col + 3 < hi) ? p3 : 0.f;
             }
-            pk[2 * j4] = pack_bf16(p0, p1);
-            pk[2 * j4 + 1] = pack_bf16(p2, p3);
+            pf[4 * j4 + 0] = p0;
+            pf[4 * j4 + 1] = p1;
+            pf[4 * j4 + 2] = p2;
+            pf[4 * j4 + 3] = p3;
           }
         };
         if (diag || wedge) phase_a(std::true_type{});
         else phase_a(std::false_type{});
-        tmem_st32(tmem + lane_off + cb, pk);
+        {
+          uint32_t pk[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) pk[j] = pack_bf16(pf[2 * j], pf[2 * j + 1]);
+          tmem_st32(tmem + lane_off + cb, pk);
+        }
         tc_fence_before();
         mbar_arrive(bar_p);
         ok = wait_bar(bar_dp, i & 1, wc);
@@ -386,11 +394,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
 #pragma unroll
           for (int j4 = 0; j4 < 16; ++j4) {
             const float4 Dv = d4[j4];
-            const uint32_t pa = pk[2 * j4], pb = pk[2 * j4 + 1];
-            const float d0 = __uint_as_float(pa << 16) * (__uint_as_float(dr[4 * j4 + 0]) - Dv.x);
-            const float d1 = __uint_as_float(pa & 0xffff0000u) * (__uint_as_float(dr[4 * j4 + 1]) - Dv.y);
-            const float d2 = __uint_as_float(pb << 16) * (__uint_as_float(dr[4 * j4 + 2]) - Dv.z);
-            const float d3 = __uint_as_float(pb & 0xffff0000u) * (__uint_as_float(dr[4 * j4 + 3]) - Dv.w);
+            float t0, t1, t2, t3, d0, d1, d2, d3;
+            add2(t0, t1, __uint_as_float(dr[4 * j4 + 0]), __uint_as_float(dr[4 * j4 + 1]), -Dv.x, -Dv.y);
+            add2(t2, t3, __uint_as_float(dr[4 * j4 + 2]), __uint_as_float(dr[4 * j4 + 3]), -Dv.z, -Dv.w);
+            mul2(d0, d1, pf[4 * j4 + 0], pf[4 * j4 + 1], t0, t1);
+            mul2(d2, d3, pf[4 * j4 + 2], pf[4 * j4 + 3], t2, t3);
             ds[2 * j4] = pack_bf16(d0, d1);
             ds[2 * j4 + 1] = pack_bf16(d2, d3);
           }
@@ -749,7 +757,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
           fma2(a0, a1, pr[2 * jj], pr[2 * jj + 1], -dr, -dr, 0.f, 0.f);
           fma2(d0, d1, pr[2 * jj], pr[2 * jj + 1], __uint_as_float(dpr[2 * jj]), __uint_as_float(dpr[2 * jj + 1]), a0,
                a1);
-          pk[jj] = pack_bf16_rn_int(d0, d1);
+          pk[jj] = pack_bf16(d0, d1);
         }
         // key columns [64 hf, 64 hf + 64) packed into columns [32 hf, 32 hf + 32) of the buffer
         tmem_st32(tmem + lane_off + T_DS + (j & 1) * 64 + hf * 32, pk);

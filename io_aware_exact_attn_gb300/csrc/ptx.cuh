@@ -340,6 +340,15 @@ __device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, f
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
+// (d0, d1) = (a0 * b0, a1 * b1)
+__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2,%3};\n\tmov.b64 rb, {%4,%5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0,%1}, rd;}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // (d0, d1) = (a0 + b0, a1 + b1)
 __device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
   asm("{.reg .b64 ra, rb, rd;\n\t"
