@@ -296,6 +296,8 @@ def main():
         f = FP8
         q8, k8, v8, (qd, kd, vd) = inputs.make_qkv_e4m3(f["B"], f["Hq"], f["Hkv"], f["N"], f["d"])
         api.attn_fwd_fp8(q8.cuda(), k8.cuda(), v8.cuda(), qd, kd, vd, causal=True)
+        # and one pass of the chunked workload (36 partial forwards, 8 merges)
+        chunked_setup(api, inputs, torch, rank)[-1]()
         torch.cuda.synchronize()
         return 0
 
@@ -402,6 +404,7 @@ def main():
         out["decode"] = decode_leg(api, inputs, torch, peaks, rank)
         out["varlen"] = varlen_leg(api, inputs, torch, peaks, rank)
         out["fp8_fwd"] = fp8_leg(api, inputs, torch, peaks, rank)
+        out["configs"] = configs_leg(api, inputs, torch, peaks, rank)
         if rank == 0:
             out["cpu_baseline"] = {k_: v_ for k_, v_ in oracle_sample(args.cpu_seconds).items()
                                    if k_ in ("value", "unit", "cores", "kind", "sample")}
@@ -445,9 +448,10 @@ def e2e_leg(api, inputs, torch, w, causal, rank, steps=6):
                 d2h_bytes_per_step=d2h, steps=steps, ms_per_step=1e3 * el / steps)
 
 
-def chunked_leg(api, inputs, torch, peaks, rank, reps=3):
-    """Chunked causal GQA (B=1, Hq=32, Hkv=8, N=32768, d=128, 8 chunks): the 36
-    partial forwards in load-balanced order, then one LSE merge per query chunk."""
+def chunked_setup(api, inputs, torch, rank):
+    """Inputs, partial buffers and one pass of the chunked causal GQA workload
+    (B=1, Hq=32, Hkv=8, N=32768, d=128, 8 chunks): the 36 partial forwards in
+    load-balanced order, then one LSE merge per query chunk."""
     c = CHUNKED
     B, Hq, Hkv, N, d, nc = c["B"], c["Hq"], c["Hkv"], c["N"], c["d"], c["chunks"]
     L = N // nc
@@ -467,6 +471,16 @@ def chunked_leg(api, inputs, torch, peaks, rank, reps=3):
                                [parts[(qc, kc)][1] for kc in range(qc + 1)],
                                out=o[:, :, qc * L:(qc + 1) * L], lse_out=lse[:, :, qc * L:(qc + 1) * L])
 
+    return q, k, v, o, lse, run
+
+
+def chunked_leg(api, inputs, torch, peaks, rank, reps=3):
+    """The chunked causal GQA workload: partial forwards and merges timed from
+    the library's launch trace, and the merged result against monolithic attn_fwd."""
+    c = CHUNKED
+    B, Hq, Hkv, N, d, nc = c["B"], c["Hq"], c["Hkv"], c["N"], c["d"], c["chunks"]
+    L = N // nc
+    q, k, v, o, lse, run = chunked_setup(api, inputs, torch, rank)
     run()
     torch.cuda.synchronize()
     api.trace_enable(64 * reps)
@@ -485,9 +499,16 @@ def chunked_leg(api, inputs, torch, peaks, rank, reps=3):
     agree = dict(o_max_abs=float((o.float() - o_m.float()).abs().max()),
                  lse_max_abs=float((lse - l_m).abs().max()))
     gbs = merge_bytes / (merge_ms * 1e-3) / 1e9
-    return dict(workload=f"B={B} Hq={Hq} Hkv={Hkv} N={N} d={d} causal, {nc} chunks, {len(sched)} pairs",
+    # DRAM bytes of the last query chunk's merge (8 parts) from the committed ncu
+    # summary, beside that launch's algorithmic bytes
+    last_alg = nc * (B * Hq * L * (d * 4 + 4)) + B * Hq * L * (d * 2 + 4)
+    return dict(workload=f"B={B} Hq={Hq} Hkv={Hkv} N={N} d={d} causal, {nc} chunks, {nc * (nc + 1) // 2} pairs",
                 partial_fwd_ms=part_ms, partial_fwd_tflops=flops / (part_ms * 1e-3) / 1e12,
                 merge_ms=merge_ms, merge_bytes=merge_bytes, merge_gbs=gbs, merge_frac_of_hbm=gbs / peaks["hbm_gbs"],
+                merge_roofline=dict(bound="hbm", achieved=gbs, peak=peaks["hbm_gbs"], unit="GB/s",
+                                    frac=gbs / peaks["hbm_gbs"], peak_source="measured hbm_gbs",
+                                    traffic_last_merge=profile_traffic("merge", "chunked_gqa"),
+                                    algorithmic_bytes_last_merge=last_alg),
                 chunked_vs_monolithic=agree)
 
 
@@ -496,6 +517,44 @@ def window_pairs(N, w):
     row i sees min(i + 1, w) keys."""
     w = min(w, N)
     return w * (w + 1) // 2 + (N - w) * w
+
+
+def configs_leg(api, inputs, torch, peaks, rank, reps=10):
+    """The BERT-large-shaped (B=8, H=16, N=512, d=64, non-causal) and the
+    block-sparse (B=1, H=16, N=16384, d=64, 128 x 128 blocks, diagonal plus
+    1/8 of the rest) workloads: forward and backward kernel times from the
+    library's launch trace, FLOPs by the metric's convention (4 B H N^2 d for
+    the forward, 2.5x for the backward, times the kept-block fraction)."""
+    res = {}
+    for name in ("bert_large", "block_sparse"):
+        w = inputs.WORKLOADS[name]
+        q, k, v, do = (t.cuda() for t in w.tensors(seed=inputs.SEED + 100 * rank + 9))
+        bm_np = w.block_mask()
+        bm = None if bm_np is None else torch.as_tensor(bm_np, dtype=torch.uint8).cuda()
+        ws = torch.empty(api.bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.N, w.d), device="cuda", dtype=torch.uint8)
+        kept = 1.0 if bm_np is None else float(bm_np.mean())
+
+        def run():
+            o, lse = api.attn_fwd(q, k, v, block_mask=bm)
+            api.attn_bwd(q, k, v, o, lse, do, block_mask=bm, workspace=ws)
+
+        run()
+        torch.cuda.synchronize()
+        api.trace_enable(16 * reps)
+        for _ in range(reps):
+            run()
+        torch.cuda.synchronize()
+        api.trace_disable()
+        recs, _ = api.trace_read(16 * reps)
+        fwd_ms = sum(ms for n, ms in recs if n == "fwd") / reps
+        bwd_ms = sum(ms for n, ms in recs if n.startswith("bwd_")) / reps
+        f_fwd = 4.0 * w.B * w.Hq * w.N * w.N * w.d * kept
+        res[name] = dict(workload=f"B={w.B} H={w.Hq} N={w.N} d={w.d} {w.mask}" +
+                         ("" if bm_np is None else f" (kept block fraction {kept:.4f})"),
+                         fwd_ms=fwd_ms, bwd_ms=bwd_ms, fwd_tflops=f_fwd / (fwd_ms * 1e-3) / 1e12,
+                         bwd_tflops=2.5 * f_fwd / (bwd_ms * 1e-3) / 1e12,
+                         step_tflops=3.5 * f_fwd / ((fwd_ms + bwd_ms) * 1e-3) / 1e12)
+    return res
 
 
 def window_leg(api, inputs, torch, peaks, rank, reps=5):
