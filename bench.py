@@ -415,37 +415,87 @@ def main():
     return 0
 
 
-def e2e_leg(api, inputs, torch, w, causal, rank, steps=6):
+def e2e_leg(api, inputs, torch, w, causal, rank, steps=6, chunks_per_batch=2):
     """Same metric through the public API with pinned HOST buffers: every step copies
-    Q, K, V, dO to the device and O, LSE, dQ, dK, dV back."""
-    hq, hk, hv, hdo = (t.pin_memory() for t in inputs.make_qkvdo(w["B"], w["Hq"], w["Hkv"], w["N"], w["N"],
-                                                                  w["d"], seed=inputs.SEED + 100 * rank + 7))
-    outs = [torch.empty(w["B"], w["Hq"], w["N"], w["d"], dtype=torch.bfloat16).pin_memory(),
-            torch.empty(w["B"], w["Hq"], w["N"], dtype=torch.float32).pin_memory(),
-            torch.empty(w["B"], w["Hq"], w["N"], w["d"], dtype=torch.bfloat16).pin_memory(),
-            torch.empty(w["B"], w["Hkv"], w["N"], w["d"], dtype=torch.bfloat16).pin_memory(),
-            torch.empty(w["B"], w["Hkv"], w["N"], w["d"], dtype=torch.bfloat16).pin_memory()]
+    Q, K, V, dO to the device and O, LSE, dQ, dK, dV back.  The step is cut into
+    (batch, head-block) chunks that are independent problems; each chunk's copies
+    in, forward + backward, and copies out run on three streams, so one chunk's
+    transfers overlap another's kernels.  The same step run as one chunk on one
+    stream is reported beside it."""
+    B, Hq, Hkv, N, d = w["B"], w["Hq"], w["Hkv"], w["N"], w["d"]
+    hq, hk, hv, hdo = (t.pin_memory() for t in inputs.make_qkvdo(B, Hq, Hkv, N, N, d,
+                                                                  seed=inputs.SEED + 100 * rank + 7))
+    outs = [torch.empty(B, Hq, N, d, dtype=torch.bfloat16).pin_memory(),
+            torch.empty(B, Hq, N, dtype=torch.float32).pin_memory(),
+            torch.empty(B, Hq, N, d, dtype=torch.bfloat16).pin_memory(),
+            torch.empty(B, Hkv, N, d, dtype=torch.bfloat16).pin_memory(),
+            torch.empty(B, Hkv, N, d, dtype=torch.bfloat16).pin_memory()]
+    dev_in = [torch.empty(t.shape, dtype=t.dtype, device="cuda") for t in (hq, hk, hv, hdo)]
+    dev_out = [torch.empty(t.shape, dtype=t.dtype, device="cuda") for t in outs]
+    g = Hq // Hkv
+    kvc = Hkv // chunks_per_batch if Hkv % chunks_per_batch == 0 else Hkv   # kv heads per chunk
+    pieces = [(b, h0) for b in range(B) for h0 in range(0, Hkv, kvc)]
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_done = [torch.cuda.Event() for _ in pieces]   # a chunk's kernels finished (its inputs are free)
+    ev_in = [torch.cuda.Event() for _ in pieces]
+    ev_out = [torch.cuda.Event() for _ in pieces]    # a chunk's results copied out (its outputs are free)
 
-    def one():
+    def sl(b, h0, per):   # the chunk's [1, heads, ...] view: q-side tensors per = g, kv-side per = 1
+        return (slice(b, b + 1), slice(h0 * per, (h0 + kvc) * per))
+
+    def pipelined(first):
+        for c, (b, h0) in enumerate(pieces):
+            with torch.cuda.stream(s_in):
+                if not first:
+                    s_in.wait_event(ev_done[c])
+                for i, (dst, src) in enumerate(zip(dev_in, (hq, hk, hv, hdo))):
+                    idx = sl(b, h0, g if i in (0, 3) else 1)
+                    dst[idx].copy_(src[idx], non_blocking=True)
+                ev_in[c].record(s_in)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(ev_in[c])
+                if not first:
+                    s_cmp.wait_event(ev_out[c])
+                qi, ki, vi, doi = (t[sl(b, h0, g if i in (0, 3) else 1)] for i, t in enumerate(dev_in))
+                o_, l_, dq_, dk_, dv_ = (t[sl(b, h0, g if i < 3 else 1)] for i, t in enumerate(dev_out))
+                api.attn_fwd(qi, ki, vi, causal=causal, out=o_, lse=l_)
+                api.attn_bwd(qi, ki, vi, o_, l_, doi, causal=causal, dq=dq_, dk=dk_, dv=dv_)
+                ev_done[c].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[c])
+                for i, (dst, src) in enumerate(zip(outs, dev_out)):
+                    idx = sl(b, h0, g if i < 3 else 1)
+                    dst[idx].copy_(src[idx], non_blocking=True)
+                ev_out[c].record(s_out)
+
+    def sequential():
         q, k, v, do = (t.to("cuda", non_blocking=True) for t in (hq, hk, hv, hdo))
         o, lse = api.attn_fwd(q, k, v, causal=causal)
         dq, dk, dv = api.attn_bwd(q, k, v, o, lse, do, causal=causal)
         for dst, src in zip(outs, (o, lse, dq, dk, dv)):
             dst.copy_(src, non_blocking=True)
 
-    for _ in range(2):
-        one()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        one()
-    torch.cuda.synchronize()
-    el = time.perf_counter() - t0
+    def timed(fn):
+        for i in range(2):
+            fn(i == 0) if fn is pipelined else fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            fn(False) if fn is pipelined else fn()
+        torch.cuda.synchronize()
+        return time.perf_counter() - t0
+
+    el = timed(pipelined)
+    piped = [t.clone() for t in outs]
+    el_seq = timed(sequential)
+    # both schedules compute every (batch, head) problem with the same kernels
+    same = max(float((a.float() - b_.float()).abs().max()) for a, b_ in zip(piped, outs))
     f_fwd, f_bwd = step_flops(w)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
     d2h = sum(t.numel() * t.element_size() for t in outs)
     return dict(value=steps * (f_fwd + f_bwd) / el / 1e12, unit="TFLOP/s", h2d_bytes_per_step=h2d,
-                d2h_bytes_per_step=d2h, steps=steps, ms_per_step=1e3 * el / steps)
+                d2h_bytes_per_step=d2h, steps=steps, ms_per_step=1e3 * el / steps, chunks=len(pieces),
+                one_chunk_one_stream_ms_per_step=1e3 * el_seq / steps, chunked_vs_one_chunk_max_abs=same)
 
 
 def chunked_setup(api, inputs, torch, rank):
