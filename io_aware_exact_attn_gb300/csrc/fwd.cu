@@ -57,9 +57,18 @@ struct FwdCfg {
   static constexpr uint32_t TILE_BYTES = NBOX * BOX_BYTES;
   static constexpr uint32_t OFF_K = 2 * TILE_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + NS * TILE_BYTES;
-  static constexpr uint32_t SMEM_TILES = OFF_V + NS * TILE_BYTES;
+  // d = 64: the P.V product also sums the rounded weights.  Its B operand is
+  // V followed by a 64-column block of ones (N = 80: 64 columns of V, then 16
+  // of ones), so column 64 of O_t accumulates the sum of the bf16 weights,
+  // rescaled with O.  At d = 128 tensor memory has no room for those columns
+  // and the softmax sums the weights itself.
+  static constexpr bool ROWSUM_MMA = (D == 64);
+  static constexpr uint32_t OFF_ONES = OFF_V + NS * TILE_BYTES;   // 128 rows x 128 bytes of bf16 1.0
+  static constexpr uint32_t SMEM_TILES = OFF_ONES + (ROWSUM_MMA ? BOX_BYTES : 0u);
   static constexpr uint32_t SMEM_BYTES = SMEM_TILES + 1024;  // + alignment slack
   static constexpr uint32_t TMEM_O = 256;
+  static constexpr uint32_t O_STRIDE = ROWSUM_MMA ? 128 : D;     // TMEM columns between O_0 and O_1
+  static constexpr int PV_N = ROWSUM_MMA ? D + 16 : D;
   static constexpr int THREADS = 384;
   static constexpr uint32_t REGS_CTRL = 56, REGS_SOFTMAX = 224;
 };
@@ -118,6 +127,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     prefetch_tmap(&tq);
     prefetch_tmap(&tk);
     prefetch_tmap(&tv);
+  }
+  if constexpr (C::ROWSUM_MMA) {
+    // the block of ones the P.V product reads after V; the tensor core reads it
+    // through the async proxy
+    uint32_t* ones = reinterpret_cast<uint32_t*>(smem + C::OFF_ONES);
+    for (int i = threadIdx.x; i < (int)(C::BOX_BYTES / 4); i += C::THREADS) ones[i] = 0x3F803F80u;
+    fence_proxy_async_smem();
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_slot), 512);
@@ -194,12 +210,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       // every lane waits, so the warp leaves a wait together
       auto wt = [&](uint32_t bar, uint32_t par) { return __all_sync(0xffffffffu, wait_bar(bar, par, wc)); };
       const uint32_t id_s = idesc_bf16(128, 128, false, false);
-      const uint32_t id_pv = idesc_bf16(128, D, false, true);
+      const uint32_t id_pv = idesc_bf16(128, C::PV_N, false, true);
       constexpr uint32_t TILE16 = C::TILE_BYTES >> 4;
       const uint32_t hi = (uint32_t)(sdesc_sw128(0, 16, 1024) >> 32);
       const uint32_t d_q = (uint32_t)sdesc_sw128(s_base, 16, 1024);
       const uint32_t d_k = (uint32_t)sdesc_sw128(s_base + C::OFF_K, 16, 1024);
-      const uint32_t d_vmn = (uint32_t)sdesc_sw128(s_base + C::OFF_V, C::BOX_BYTES, 1024);
+      // MN-major V: at d = 128 the leading offset is the distance between its two
+      // 64-column boxes; with the row-sum columns (d = 64) it is the distance
+      // from the slot to the block of ones, which shrinks by a tile per slot
+      const uint32_t d_vmn = (uint32_t)sdesc_sw128(s_base + C::OFF_V, C::ROWSUM_MMA ? C::OFF_ONES - C::OFF_V : C::BOX_BYTES, 1024);
+      constexpr uint32_t V_SLOT_STEP = C::ROWSUM_MMA ? (C::TILE_BYTES >> 4) - ((C::TILE_BYTES >> 4) << 16) : (C::TILE_BYTES >> 4);
       auto desc = [&](uint32_t lo) { return ((uint64_t)hi << 32) | lo; };
       auto kstep = [](int kk) { return (uint32_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4); };
       auto next_kt = [&](int from) {
@@ -216,10 +236,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         mma_commit_e(bar_s(t));
       };
       auto issue_pv = [&](int t, int slot, bool acc) {
-        const uint32_t vd = d_vmn + (uint32_t)slot * TILE16;
+        const uint32_t vd = d_vmn + (uint32_t)slot * V_SLOT_STEP;
 #pragma unroll
         for (int kk = 0; kk < TILE / 16; ++kk)
-          mma_ts_e(tmem + C::TMEM_O + t * D, tmem + t * 128 + kk * 8, desc(vd + (uint32_t)kk * (2048 >> 4)), id_pv,
+          mma_ts_e(tmem + C::TMEM_O + t * C::O_STRIDE, tmem + t * 128 + kk * 8, desc(vd + (uint32_t)kk * (2048 >> 4)), id_pv,
                  (acc || kk > 0));
         mma_commit_e(bar_o(t));
       };
@@ -289,7 +309,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const int qrow = u.row0 + t * TILE + r;        // local query row
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + t * 128;
-    const uint32_t tO = tmem + lane_off + C::TMEM_O + t * D;
+    const uint32_t tO = tmem + lane_off + C::TMEM_O + t * C::O_STRIDE;
     const float c = p.scale_log2;
     const bool causal = mask_is_causal(p.mask_kind, p.causal_in_blocks);
     // positions: row i of the call sits at q_offset + i; when decoding, row r
@@ -408,20 +428,29 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           for (int j = 0; j < 64; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
           tmem_st64(tO + h64 * 64, rr);
         }
+        if constexpr (C::ROWSUM_MMA) {   // the row-sum columns scale with O
+          uint32_t rr[16];
+          tmem_ld16(tO + D, rr);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
+          tmem_st16(tO + D, rr);
+        }
       }
       tc_fence_before();
       mbar_arrive(bar_p(t));
       ++it;
-      // rounded-weight sum after P has been handed to the tensor core
-      float ra[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const int a = 2 * (j & 3);
-        add_bf16x2_to_f32(ra[a], ra[a + 1], pk[j]);
-      }
-      const float r0 = (ra[0] + ra[1]) + (ra[2] + ra[3]), r1 = (ra[4] + ra[5]) + (ra[6] + ra[7]);
       l = l * alpha + lt;
-      lr = lr * alpha + (r0 + r1);
+      if constexpr (!C::ROWSUM_MMA) {
+        // rounded-weight sum after P has been handed to the tensor core
+        float ra[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const int a = 2 * (j & 3);
+          add_bf16x2_to_f32(ra[a], ra[a + 1], pk[j]);
+        }
+        const float r0 = (ra[0] + ra[1]) + (ra[2] + ra[3]), r1 = (ra[4] + ra[5]) + (ra[6] + ra[7]);
+        lr = lr * alpha + (r0 + r1);
+      }
 
     }
     // ---------------------------------------------------------- epilogue
@@ -434,6 +463,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       if (ok) {
         tc_fence_after();
         const bool valid_row = qrow < u.nq;
+        if constexpr (C::ROWSUM_MMA) {   // the sum of the rounded weights, from the P.V product
+          uint32_t rr[16];
+          if (have) tmem_ld16(tO + D, rr);
+          lr = have ? __uint_as_float(rr[0]) : 0.f;
+        }
         const float inv_l = (lr > 0.f) ? 1.f / lr : 0.f;
         const int64_t grow = u.seq0 + qrow;   // row within the head (token index when batches are ragged)
         const int64_t split_off = (int64_t)u.split * p.split_rows;
