@@ -388,13 +388,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       // for a row's first visible tile) the max is found from the scores
       // still in TMEM, the reference moves to it, and the weights are redone.
       float s[128];
+      float lt = 0.f;
       load_scores(s);
-      exponentials(s, (m == -INFINITY) ? 0.f : m);
-      float lt = pack_sum(s);
+      if (it > 0) {   // a tile's first key tile always needs its row max: no speculative pass
+        exponentials(s, (m == -INFINITY) ? 0.f : m);
+        lt = pack_sum(s);
+      }
       float alpha = 1.f;
       bool rescale = false;
       if (__any_sync(0xffffffffu, m == -INFINITY || !(lt <= RESCALE_LIMIT))) {
-        load_scores(s);
+        if (it > 0) load_scores(s);
         float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
         for (int j = 0; j < 128; j += 8) {
