@@ -403,4 +403,38 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
+// A warp writes 32 rows of NCHUNK 16-byte chunks to global memory: row r is
+// held by lane r (chunk c in words 4c..4c+3 of w) and starts at
+// base + r * stride_bytes.  The rows pass through `stage`, this warp's
+// 32 * NCHUNK * 16 bytes of shared memory (chunks XOR-swizzled by row), so
+// that every global store instruction covers 32 / NCHUNK whole rows of
+// contiguous bytes instead of one 16-byte piece of 32 different rows.  Rows at
+// or past `nrows` are not written.  The whole warp calls it.
+template <int NCHUNK>
+__device__ __forceinline__ void warp_store_rows(uint32_t stage, const uint32_t* w, char* base, size_t stride_bytes,
+                                                int nrows) {
+  static_assert(NCHUNK >= 1 && NCHUNK <= 32 && (NCHUNK & (NCHUNK - 1)) == 0, "NCHUNK: a power of two up to 32");
+  constexpr uint32_t ROWB = NCHUNK * 16;
+  constexpr int RPI = 32 / NCHUNK;   // rows per store instruction
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = 0; c < NCHUNK; ++c)
+    st_shared_v4(stage + lane * ROWB + ((uint32_t)(c ^ (lane & (NCHUNK - 1))) << 4), w[4 * c], w[4 * c + 1],
+                 w[4 * c + 2], w[4 * c + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < NCHUNK; ++it) {
+    const int row = it * RPI + lane / NCHUNK, c = lane % NCHUNK;
+    const uint4 v = ld_shared_v4(stage + row * ROWB + ((uint32_t)(c ^ (row & (NCHUNK - 1))) << 4));
+    if (row < nrows) *reinterpret_cast<uint4*>(base + (size_t)row * stride_bytes + c * 16) = v;
+  }
+  __syncwarp();   // the stage may be written again
+}
+
 }  // namespace attn
