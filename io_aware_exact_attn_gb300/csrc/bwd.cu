@@ -417,11 +417,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       }
       if (ok) {
         tc_fence_after();
-        const int key = kt * TILE + r;
-        const size_t orow = ragged ? (size_t)(tok0 + key) * p.Hkv + hkv : (size_t)bkv * p.N + key;
-        // warpgroup 0 writes dV, warpgroup 1 writes scale * dK
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(hf == 0 ? p.dv : p.dk) + orow * D;
+        // warpgroup 0 writes dV, warpgroup 1 writes scale * dK; the rows are
+        // staged through shared memory no MMA or copy uses any more (the K and
+        // V tiles') so that each store instruction covers whole rows
         const float mul = hf == 0 ? 1.f : p.scale;
+        uint32_t w[D / 2];
 #pragma unroll
         for (int q4 = 0; q4 < D / 32; ++q4) {
           uint32_t rv[32];
@@ -431,8 +431,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) rv[j] = 0u;
           }
-          if (key < n_seq) store_row32_bf16(dst + q4 * 32, rv, mul);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            w[q4 * 16 + j] = pack_bf16(__uint_as_float(rv[2 * j]) * mul, __uint_as_float(rv[2 * j + 1]) * mul);
         }
+        const int wkey0 = kt * TILE + wq * 32;   // this warp's first key
+        const size_t orow0 = ragged ? (size_t)(tok0 + wkey0) * p.Hkv + hkv : (size_t)bkv * p.N + wkey0;
+        char* base = reinterpret_cast<char*>(static_cast<__nv_bfloat16*>(hf == 0 ? p.dv : p.dk) + orow0 * D);
+        const size_t stride = (ragged ? (size_t)p.Hkv : (size_t)1) * D * sizeof(__nv_bfloat16);
+        warp_store_rows<D / 8>(s_base + (uint32_t)(warp - 4) * (32u * D * 2), w, base, stride, n_seq - wkey0);
       }
     }
   }

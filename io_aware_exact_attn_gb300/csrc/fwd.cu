@@ -476,6 +476,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const int64_t split_off = (int64_t)u.split * p.split_rows;
         const size_t o_off = (size_t)(split_off * D + (int64_t)u.bh * p.o_hs + grow * p.o_rs);
         const size_t l_off = (size_t)(split_off + (int64_t)u.bh * p.l_hs + grow * p.l_rs);
+        uint32_t ob[OUT_F32 ? 1 : D / 2];   // the bf16 row (OUT_F32 writes fp32 rows directly)
 #pragma unroll
         for (int h64 = 0; h64 < D / 64; ++h64) {
           uint32_t rr[64];
@@ -493,19 +494,23 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                 dst[j] = make_float4(__uint_as_float(rr[4 * j]) * inv_l, __uint_as_float(rr[4 * j + 1]) * inv_l,
                                      __uint_as_float(rr[4 * j + 2]) * inv_l,
                                      __uint_as_float(rr[4 * j + 3]) * inv_l);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + o_off + h64 * 64);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                uint4 v4;
-                v4.x = pack_bf16(__uint_as_float(rr[8 * j + 0]) * inv_l, __uint_as_float(rr[8 * j + 1]) * inv_l);
-                v4.y = pack_bf16(__uint_as_float(rr[8 * j + 2]) * inv_l, __uint_as_float(rr[8 * j + 3]) * inv_l);
-                v4.z = pack_bf16(__uint_as_float(rr[8 * j + 4]) * inv_l, __uint_as_float(rr[8 * j + 5]) * inv_l);
-                v4.w = pack_bf16(__uint_as_float(rr[8 * j + 6]) * inv_l, __uint_as_float(rr[8 * j + 7]) * inv_l);
-                dst[j] = v4;
-              }
             }
           }
+          if constexpr (!OUT_F32) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              ob[h64 * 32 + j] = pack_bf16(__uint_as_float(rr[2 * j]) * inv_l, __uint_as_float(rr[2 * j + 1]) * inv_l);
+          }
+        }
+        if constexpr (!OUT_F32) {
+          // bf16 rows staged through the Q tiles (no MMA reads them once this
+          // tile's last P.V has completed), so each store covers whole rows
+          const int wrow = u.row0 + t * TILE + wq * 32;   // this warp's first local row
+          char* base = reinterpret_cast<char*>(static_cast<__nv_bfloat16*>(p.o) +
+                                               (size_t)(split_off * D + (int64_t)u.bh * p.o_hs +
+                                                        (u.seq0 + wrow) * p.o_rs));
+          warp_store_rows<D / 8>(s_base + (uint32_t)(warp - 4) * (32u * D * 2), ob, base,
+                                 (size_t)p.o_rs * sizeof(__nv_bfloat16), u.nq - wrow);
         }
         if (valid_row && p.lse != nullptr)
           p.lse[l_off] = (l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
