@@ -73,21 +73,6 @@ __device__ __forceinline__ bool tile_pair_visible(const BwdParams& p, int qt, in
 // 4-7 at [64, 96) relative to the region start.
 __host__ __device__ constexpr uint32_t half_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
 
-// Convert 32 fp32 accumulator columns to bf16 (times `mul`) and store them as
-// 64 contiguous bytes.
-__device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint32_t (&r)[32], float mul) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint4 v;
-    v.x = pack_bf16(__uint_as_float(r[8 * j + 0]) * mul, __uint_as_float(r[8 * j + 1]) * mul);
-    v.y = pack_bf16(__uint_as_float(r[8 * j + 2]) * mul, __uint_as_float(r[8 * j + 3]) * mul);
-    v.z = pack_bf16(__uint_as_float(r[8 * j + 4]) * mul, __uint_as_float(r[8 * j + 5]) * mul);
-    v.w = pack_bf16(__uint_as_float(r[8 * j + 6]) * mul, __uint_as_float(r[8 * j + 7]) * mul);
-    d4[j] = v;
-  }
-}
-
 // =========================================================================
 // dK / dV
 // Tensor memory: S^T [0,128) (P^T bf16 overwrites [0,64)), dP^T [128,256)
