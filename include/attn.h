@@ -360,6 +360,38 @@ int attn_get_status(void* stream);
 void attn_set_wait_limit_ns(int64_t limit_ns);
 
 /*
+ * attn_debug_set_tile_counts -- debug record of the work each CTA did, for
+ * checking the kernels against the schedule (which key tiles each query tile
+ * visits: the causal and block-sparse tile skipping of the "FlashAttention-2"
+ * reviews, fourth review, and the heaviest-first unit order).  From this call
+ * on, every forward launch (attn_fwd, attn_partial_fwd, attn_varlen_fwd,
+ * attn_decode_fwd) and every backward call (attn_bwd, attn_varlen_bwd,
+ * attn_bwd_static_scratch) writes 8 int32 per CTA, CTA c at counts[8 * c], into
+ * `counts`, a DEVICE array of `capacity` int32 that the caller owns and keeps
+ * alive while recording is on.  Each launch writes from counts[0]; a backward
+ * call writes its dK/dV kernel's records first and its dQ kernel's records
+ * right after them.  CTAs that have no work (a chunk past the end of a shorter
+ * sequence) write nothing.  Fields, per kernel:
+ *   forward: [0] head index of the unit (b*Hq + h; decoding: b*Hkv + kv head;
+ *            ragged batches: h), [1] first query row of the unit, [2] decode
+ *            split, [3] first token of the unit's sequence (ragged batches),
+ *            [4] key tiles loaded, [5] 0 (not recorded), [6] and [7] key
+ *            tiles processed for query tile 0 and 1 of the unit.
+ *   dK/dV:   [0] b*Hkv + kv head, [1] key tile, [2] 0, [3] first token of the
+ *            sequence, [4] (query head, query tile) stages loaded, [5] query
+ *            tiles whose dV and dK products were issued, [6] and [7] query
+ *            tiles processed by each of the two elementwise warpgroups.
+ *   dQ:      [0] b*Hq + h, [1] query tile, [2] 0, [3] first token of the
+ *            sequence, [4] key tiles loaded, [5] dQ products issued, [6] and
+ *            [7] key tiles processed by each elementwise warpgroup.
+ * Launches whose records do not fit return ATTN_ERR_INVALID_ARG before that
+ * kernel is launched.  counts == NULL turns recording off.  The e4m3 forward
+ * writes no records.  Returns ATTN_ERR_MISALIGNED for a pointer that is not
+ * 4-byte aligned.
+ */
+int attn_debug_set_tile_counts(int32_t* counts, int64_t capacity);
+
+/*
  * attn_selftest_wait_timeout -- launches one small kernel that waits, with the
  * given limit, on a barrier that nothing signals, so that the bounded-wait
  * error path can be tested without faulting or hanging the GPU.  The wait

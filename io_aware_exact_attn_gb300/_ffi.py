@@ -69,6 +69,7 @@ SIGNATURES = {
     "attn_build_chunk_schedule": (c_int, [c_int, c_int, C.POINTER(C.c_int32), c_size_t, C.POINTER(c_size_t)]),
     "attn_get_status": (c_int, [c_void_p]),
     "attn_set_wait_limit_ns": (None, [c_int64]),
+    "attn_debug_set_tile_counts": (c_int, [c_void_p, c_int64]),
     "attn_selftest_wait_timeout": (c_int, [c_int64, c_void_p]),
     "attn_trace_enable": (c_int, [c_int]),
     "attn_trace_disable": (c_int, []),

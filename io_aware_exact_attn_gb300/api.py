@@ -387,6 +387,19 @@ def set_wait_limit_ns(limit_ns: int) -> None:
     _ffi.lib().attn_set_wait_limit_ns(int(limit_ns))
 
 
+def debug_set_tile_counts(counts=None) -> None:
+    """Record, per CTA of every later launch, the work it did (8 int32 per CTA,
+    fields as attn.h lists them) into ``counts``, a contiguous int32 CUDA
+    tensor; ``None`` turns recording off.  The caller keeps ``counts`` alive
+    while recording is on."""
+    if counts is None:
+        check(_ffi.lib().attn_debug_set_tile_counts(None, 0), "attn_debug_set_tile_counts")
+        return
+    if counts.dtype != torch.int32 or not counts.is_cuda or not counts.is_contiguous():
+        raise ValueError("counts must be a contiguous int32 CUDA tensor")
+    check(_ffi.lib().attn_debug_set_tile_counts(counts.data_ptr(), counts.numel()), "attn_debug_set_tile_counts")
+
+
 def selftest_wait_timeout(limit_ns: int, device=None) -> None:
     s = torch.cuda.current_stream(device).cuda_stream
     check(_ffi.lib().attn_selftest_wait_timeout(int(limit_ns), s), "attn_selftest_wait_timeout")

@@ -23,6 +23,8 @@ namespace {
 thread_local std::string g_msg;
 std::mutex g_mu;
 int64_t g_wait_limit_ns = 2000000000ll;
+int32_t* g_debug_counts = nullptr;   // attn_debug_set_tile_counts
+int64_t g_debug_capacity = 0;
 
 constexpr int MAX_DEVICES = 64;
 unsigned int* g_status[MAX_DEVICES] = {};
@@ -242,6 +244,28 @@ static int64_t wait_limit() {
   return g_wait_limit_ns;
 }
 
+int attn_debug_set_tile_counts(int32_t* counts, int64_t capacity) {
+  if (counts != nullptr && capacity < 0) return fail(ATTN_ERR_INVALID_ARG, "negative debug record capacity");
+  if (reinterpret_cast<uintptr_t>(counts) & 3u) return fail(ATTN_ERR_MISALIGNED, "debug records not 4-byte aligned");
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_debug_counts = counts;
+  g_debug_capacity = counts != nullptr ? capacity : 0;
+  return ATTN_OK;
+}
+
+// The debug record array for a launch of `ctas` CTAs (after `skip` records
+// of an earlier kernel of the same call), or null when recording is off.
+static int debug_records(int64_t skip, int64_t ctas, int32_t** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  *out = nullptr;
+  if (g_debug_counts == nullptr) return ATTN_OK;
+  if ((skip + ctas) * DEBUG_FIELDS > g_debug_capacity)
+    return fail(ATTN_ERR_INVALID_ARG, "debug record array holds %lld int32, the launch needs %lld",
+                (long long)g_debug_capacity, (long long)((skip + ctas) * DEBUG_FIELDS));
+  *out = g_debug_counts + skip * DEBUG_FIELDS;
+  return ATTN_OK;
+}
+
 static int fwd_common(const void* q, const void* k, const void* v, void* o, bool out_f32, float* lse, int B,
                       int Hq, int Hkv, int Nq, int Nk, int d, float scale, const attn_mask_t* mask,
                       int64_t q_off, int64_t kv_off, int64_t q_hs, int64_t kv_hs, void* stream) {
@@ -281,6 +305,7 @@ static int fwd_common(const void* q, const void* k, const void* v, void* o, bool
   p.dec_nq = 1;
   p.status = status;
   p.wait_limit_ns = wait_limit();
+  if ((rc = debug_records(0, fwd_grid(p), &p.tile_counts))) return rc;
   cudaError_t e;
   {
     TraceScope ts(out_f32 ? ATTN_KERNEL_PARTIAL_FWD : ATTN_KERNEL_FWD, static_cast<cudaStream_t>(stream));
@@ -343,6 +368,7 @@ int attn_varlen_fwd(const void* q, const void* k, const void* v, void* o, float*
   p.varlen_nqc = p.nqc;
   p.status = status;
   p.wait_limit_ns = wait_limit();
+  if ((rc = debug_records(0, fwd_grid(p), &p.tile_counts))) return rc;
   cudaError_t e;
   {
     TraceScope ts(ATTN_KERNEL_VARLEN_FWD, static_cast<cudaStream_t>(stream));
@@ -499,6 +525,7 @@ int attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, con
   p.split_rows = total_rows;
   p.status = status;
   p.wait_limit_ns = wait_limit();
+  if ((rc = debug_records(0, fwd_grid(p), &p.tile_counts))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   {
@@ -605,6 +632,9 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   p.q_group = kv_stream_group(B, Hq, Hkv, N, d);
   p.status = status;
   p.wait_limit_ns = wait_limit();
+  if ((rc = debug_records(0, dkdv_grid(p), &p.dkdv_counts)) ||
+      (rc = debug_records(dkdv_grid(p), dq_grid(p), &p.dq_counts)))
+    return rc;
   {
     TraceScope ts(ATTN_KERNEL_BWD_DKDV, s);
     e = launch_bwd_dkdv(d, tq, tk, tv, tdo, p, s);
@@ -684,6 +714,9 @@ int attn_varlen_bwd(const void* q, const void* k, const void* v, const void* o, 
   p.q_group = 1;
   p.status = status;
   p.wait_limit_ns = wait_limit();
+  if ((rc = debug_records(0, dkdv_grid(p), &p.dkdv_counts)) ||
+      (rc = debug_records(dkdv_grid(p), dq_grid(p), &p.dq_counts)))
+    return rc;
   {
     TraceScope ts(ATTN_KERNEL_BWD_DKDV, s);
     e = launch_bwd_dkdv(d, tq, tk, tv, tdo, p, s);
@@ -937,6 +970,9 @@ extern "C" int attn_bwd_static_scratch(const void* q, const void* k, const void*
   p.q_group = kv_stream_group(B, Hq, Hkv, N, d);
   p.status = st.status;
   p.wait_limit_ns = wait_limit();
+  if ((rc = debug_records(0, dkdv_grid(p), &p.dkdv_counts)) ||
+      (rc = debug_records(dkdv_grid(p), dq_grid(p), &p.dq_counts)))
+    return rc;
   e = launch_bwd_dkdv(d, tq, tk, tv, tdo, p, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward dK/dV launch");
   e = launch_bwd_dq(d, tq, tk, tv, tdo, p, s);

@@ -175,6 +175,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
     if (lane < C::NBOX) tma_load_3d(s_base + lane * C::BOX_BYTES, &tk, lane * 64, krow, kv_head, bar_kv);
     else if (lane < 2 * C::NBOX)
       tma_load_3d(s_base + OFF_V + (lane - C::NBOX) * C::BOX_BYTES, &tv, (lane - C::NBOX) * 64, krow, kv_head, bar_kv);
+    if (p.dkdv_counts != nullptr && lane == 0) {   // the unit's identity in the debug record
+      int32_t* rec = p.dkdv_counts + (size_t)DEBUG_FIELDS * blockIdx.x;
+      rec[0] = bkv;
+      rec[1] = kt;
+      rec[2] = 0;
+      rec[3] = tok0;
+    }
     int n = 0;
     bool ok = true;
     for (int h = 0; h < g && ok; ++h) {
@@ -202,6 +209,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
         ++n;
       }
     }
+    if (p.dkdv_counts != nullptr && lane == 0) p.dkdv_counts[(size_t)DEBUG_FIELDS * blockIdx.x + 4] = n;   // stages loaded
     if ((!ok || abort_flag) && lane == 0) {
       wait_bar(bar_kv, 0, wc, false);
       for (int j = n - NS < 0 ? 0 : n - NS; j < n; ++j) wait_bar(bar_q(j % NS), (j / NS) & 1, wc, false);
@@ -261,7 +269,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       }
       int s = 0;
       uint32_t spar = 0;   // ring slot of tile i and the parity of its fill
-      for (int i = 0; ok && i < ntile; ++i) {
+      int i = 0;           // after the loop: query tiles whose dV and dK products were issued
+      for (; ok && i < ntile; ++i) {
         const bool more = i + 1 < ntile;
         const int sn = (s + 1 == NS) ? 0 : s + 1;
         const uint32_t snpar = (s + 1 == NS) ? spar ^ 1u : spar;
@@ -293,6 +302,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
         s = sn;
         spar = snpar;
       }
+      if (p.dkdv_counts != nullptr && lane == 0) p.dkdv_counts[(size_t)DEBUG_FIELDS * blockIdx.x + 5] = i;
       mma_commit_e(bar_done);
       wait_bar(bar_done, 0, wc, false);
     }
@@ -394,6 +404,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
         ++i;
       }
     }
+    if (p.dkdv_counts != nullptr && r == 0) p.dkdv_counts[(size_t)DEBUG_FIELDS * blockIdx.x + 6 + hf] = i;
     // ---------------------------------------------------------- epilogue
     if (ok && !abort_flag) {
       if (i > 0) {
@@ -589,6 +600,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
                     full(sl));
       ++n;
     }
+    if (is_k && p.dq_counts != nullptr && lane == 0) p.dq_counts[(size_t)DEBUG_FIELDS * blockIdx.x + 4] = n;   // key tiles loaded
     if ((!ok || abort_flag) && lane == 0) {
       if (is_k) wait_bar(bar_qdo, 0, wc, false);
       for (int j = n - depth < 0 ? 0 : n - depth; j < n; ++j) wait_bar(full(j % depth), (j / depth) & 1, wc, false);
@@ -651,7 +663,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
         }
         ks = vs = 1;
       }
-      for (int j = 0; ok && j < nvis; ++j) {
+      int j = 0;   // after the loop: key tiles whose dQ product was issued
+      for (; ok && j < nvis; ++j) {
         const uint32_t par = (uint32_t)j & 1u;
         if (j + 1 < nvis) {
           // S_{j+1} once S_j has been read out of TMEM
@@ -677,6 +690,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
         mma_commit_e(bar_kfree(kq));
         if (++kq == KS) kq = 0;
       }
+      if (p.dq_counts != nullptr && lane == 0) p.dq_counts[(size_t)DEBUG_FIELDS * blockIdx.x + 5] = j;
       mma_commit_e(bar_done);
       wait_bar(bar_done, 0, wc, false);
     }
@@ -758,6 +772,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       mbar_arrive(bar_ds(j));
       ++j;
     }
+    if (p.dq_counts != nullptr && r == 0) {
+      int32_t* rec = p.dq_counts + (size_t)DEBUG_FIELDS * blockIdx.x;
+      rec[6 + hf] = j;
+      if (hf == 0) {   // the unit's identity
+        rec[0] = bh;
+        rec[1] = qt;
+        rec[2] = 0;
+        rec[3] = tok0;
+      }
+    }
     if (ok && !abort_flag) {
       // dQ MMAs complete in issue order: the last one covers them all
       if (j > 0) ok = __all_sync(0xffffffffu, wait_bar(bar_dq(j - 1), ((j - 1) >> 1) & 1, wc));
@@ -817,7 +841,7 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   static_assert(smem <= 232448 - 256, "dK/dV shared memory");
   cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(p.B * p.Hkv) * (unsigned)((p.N + TILE - 1) / TILE);
+  const unsigned grid = dkdv_grid(p);
   dkdv_kernel<D><<<grid, BwdCfg<D>::SPLIT_THREADS, smem, s>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }
@@ -829,7 +853,7 @@ cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   static_assert(smem <= 232448 - 256, "dQ shared memory");
   cudaError_t e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(p.B * p.Hq) * (unsigned)((p.N + TILE - 1) / TILE);
+  const unsigned grid = dq_grid(p);
   dq_kernel<D><<<grid, BwdCfg<D>::SPLIT_THREADS, smem, s>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }

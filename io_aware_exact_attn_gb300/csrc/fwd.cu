@@ -158,6 +158,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       tma_load_3d(s_base + t * C::TILE_BYTES + bx * C::BOX_BYTES, &tq, bx * 64, (int)(u.seq0 + u.row0 + t * TILE), u.bh,
                   bar_q);
     }
+    if (p.tile_counts != nullptr && lane == 0) {   // the unit's identity in the debug record
+      int32_t* rec = p.tile_counts + (size_t)DEBUG_FIELDS * blockIdx.x;
+      rec[0] = u.bh;
+      rec[1] = u.row0;
+      rec[2] = u.split;
+      rec[3] = (int32_t)u.seq0;
+      rec[5] = 0;   // not recorded by the forward kernel
+    }
     int n = 0;
     bool ok = true;
     for (int kt = u.kt_begin; kt < u.kt_end && ok; ++kt) {
@@ -181,6 +189,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                     (lane - C::NBOX) * 64, (int)(u.seq0 + kt * TILE), u.kvh, bar_v(s));
       ++n;
     }
+    if (p.tile_counts != nullptr && lane == 0) p.tile_counts[(size_t)DEBUG_FIELDS * blockIdx.x + 4] = n;   // key tiles loaded
     if ((!ok || abort_flag) && lane == 0) {
       // drain: every issued copy must land before the CTA's shared memory is released
       wait_bar(bar_q, 0, wc, false);
@@ -456,6 +465,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
 
     }
+    if (p.tile_counts != nullptr && r == 0) p.tile_counts[(size_t)DEBUG_FIELDS * blockIdx.x + 6 + t] = it;
     // ---------------------------------------------------------- epilogue
     if (ok && !abort_flag) {
       const bool have = it > 0;
@@ -533,9 +543,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   auto kern = fwd_kernel<D, F32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const unsigned grid = p.n_splits > 0           ? (unsigned)(p.B * p.Hkv) * (unsigned)p.n_splits
-                        : p.cu_seqlens != nullptr ? (unsigned)(p.B * p.Hq) * (unsigned)p.varlen_nqc
-                                                  : (unsigned)(p.B * p.Hq) * (unsigned)p.nqc;
+  const unsigned grid = fwd_grid(p);
   kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

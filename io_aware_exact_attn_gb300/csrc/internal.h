@@ -44,6 +44,7 @@ struct FwdParams {
   int64_t o_hs, o_rs, l_hs, l_rs;
   unsigned int* status;
   int64_t wait_limit_ns;
+  int32_t* tile_counts;       // per-CTA debug record (DEBUG_FIELDS int32 each), or null
 };
 
 // Backward parameter block (kernels 2 and 3 of attn_bwd).
@@ -72,7 +73,24 @@ struct BwdParams {
   int q_group;              // query heads per L2 group of the dQ kernel
   unsigned int* status;
   int64_t wait_limit_ns;
+  int32_t* dkdv_counts;     // per-CTA debug records of the two kernels, or null
+  int32_t* dq_counts;
 };
+
+// Per-CTA debug record: DEBUG_FIELDS int32 at [DEBUG_FIELDS * blockIdx.x] of
+// the launch's record array; the fields of each kernel are listed with
+// attn_debug_set_tile_counts in attn.h.
+constexpr int DEBUG_FIELDS = 8;
+
+// Grid sizes (one CTA per work unit), shared by the launchers and by the
+// front end's check of the debug record's capacity.
+inline unsigned fwd_grid(const FwdParams& p) {
+  return p.n_splits > 0           ? (unsigned)(p.B * p.Hkv) * (unsigned)p.n_splits
+         : p.cu_seqlens != nullptr ? (unsigned)(p.B * p.Hq) * (unsigned)p.varlen_nqc
+                                   : (unsigned)(p.B * p.Hq) * (unsigned)p.nqc;
+}
+inline unsigned dkdv_grid(const BwdParams& p) { return (unsigned)(p.B * p.Hkv) * (unsigned)((p.N + TILE - 1) / TILE); }
+inline unsigned dq_grid(const BwdParams& p) { return (unsigned)(p.B * p.Hq) * (unsigned)((p.N + TILE - 1) / TILE); }
 
 struct TensorMaps {
   CUtensorMap a, b, c, d;

@@ -71,6 +71,10 @@ def test_argument_validation_without_gpu(lib):
     assert lib.attn_fwd(_ptr(good), _ptr(good), _ptr(good), _ptr(good), None, 1, 2, 2, 128, 64, 0.125,
                         C.byref(sparse_no_mask), None) == -1
     assert "multiple" in lib.attn_last_error_message().decode() or lib.attn_last_error_message()
+    # debug records: the setter checks its arguments and touches no device
+    assert lib.attn_debug_set_tile_counts(_ptr(good + 2), 64) == -3
+    assert lib.attn_debug_set_tile_counts(_ptr(good), -1) == -1
+    assert lib.attn_debug_set_tile_counts(None, -1) == 0   # off; the capacity is ignored
     # merge: part count limits
     arr = (C.c_void_p * 1)(good)
     assert lib.attn_merge_lse(arr, arr, 0, _ptr(good), 0, None, 1, 1, 4, 64, 0, None) == -1
