@@ -66,7 +66,10 @@ def step_flops(w):
 
 
 def kernel_work(w):
-    """Algorithmic work per launch of each kernel of one step."""
+    """Algorithmic work per launch of each kernel of one step: counted GEMM
+    FLOPs (one N x N x d product = 2*B*H*N^2*d, halved under the causal mask)
+    for the tensor-bound kernels, bytes read once plus written once for the
+    HBM-bound preprocessing kernel."""
     B, H, N, d = w["B"], w["Hq"], w["N"], w["d"]
     cf = 0.5 if w["mask"] == "causal" else 1.0
     gemm = 2.0 * B * H * N * N * d * cf          # one N x N x d product over all heads

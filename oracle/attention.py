@@ -12,7 +12,7 @@ loss ``<O, dO>``: ``dV = P^T dO``, ``dP = dO V^T``,
 ``dS = P * (dP - rowsum(P * dP))`` (the softmax Jacobian applied row by row),
 ``dQ = scale * dS K``, ``dK = scale * dS^T Q``.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 * scale is an explicit argument (the DISTFLASHATTN review writes
   ``softmax(QK^T)V`` with no scale);
 * causal visibility uses global positions: key ``j`` is visible to query ``i``
