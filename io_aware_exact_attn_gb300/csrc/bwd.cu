@@ -40,7 +40,6 @@ struct BwdCfg {
   static constexpr uint32_t BOX_BYTES = 128 * 128;
   static constexpr uint32_t TILE_BYTES = NBOX * BOX_BYTES;
   static constexpr int NS = (D == 128) ? 2 : 4;  // ring depth
-  static constexpr int THREADS = 256;
   // both kernels: 12 warps; the control warpgroup gives registers back to the
   // two elementwise warpgroups: 128*64 + 256*216 = 63488 <= 384*168 (launch
   // allotment); at this split neither role spills

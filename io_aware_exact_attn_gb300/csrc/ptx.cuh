@@ -377,14 +377,6 @@ __device__ __forceinline__ void add_bf16x2_to_f32(float& acc_lo, float& acc_hi, 
       : "r"(pk));
 }
 
-// bf16 pair rounded to nearest with plain integer ops (half an ulp added to
-// each fp32 bit pattern, top halves kept by one byte permute): ties round away
-// from zero instead of to even, everything else matches round-to-nearest.
-// Cheaper than the conversion instruction, which runs on a narrow pipe.
-__device__ __forceinline__ uint32_t pack_bf16_rn_int(float lo, float hi) {
-  return __byte_perm(__float_as_uint(lo) + 0x8000u, __float_as_uint(hi) + 0x8000u, 0x7632);
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
