@@ -46,6 +46,8 @@ SHAPES = [
     (1, 3, 1, 129, 64, "causal"), (1, 1, 1, 1, 128, "none"), (1, 1, 1, 1, 64, "causal"),
     (1, 2, 2, 1000, 64, "none"), (1, 2, 1, 777, 128, "causal"), (1, 4, 1, 256, 64, "none"),
     (2, 2, 2, 384, 128, "none"), (1, 2, 2, 17, 128, "causal"),
+    (1, 8, 1, 300, 128, "causal"),   # dK/dV sum over eight query heads
+    (2, 12, 3, 200, 64, "none"),
 ]
 
 

@@ -41,6 +41,8 @@ SHAPES = [
     (1, 3, 1, 129, 64, "causal"), (1, 1, 1, 1, 128, "none"), (1, 1, 1, 1, 64, "causal"),
     (1, 2, 2, 1000, 64, "none"), (2, 2, 2, 384, 128, "none"), (1, 2, 1, 777, 128, "causal"),
     (1, 4, 4, 256, 64, "causal"), (1, 2, 2, 17, 128, "none"),
+    (1, 8, 1, 300, 128, "causal"),   # one kv head for eight query heads
+    (2, 12, 3, 200, 64, "none"),     # groups of four, a head count that is not a power of two
 ]
 
 
