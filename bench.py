@@ -418,7 +418,7 @@ def main():
     return 0
 
 
-def e2e_leg(api, inputs, torch, w, causal, rank, steps=6, chunks_per_batch=2):
+def e2e_leg(api, inputs, torch, w, causal, rank, steps=30, chunks_per_batch=2):
     """Same metric through the public API with pinned HOST buffers: every step copies
     Q, K, V, dO to the device and O, LSE, dQ, dK, dV back.  The step is cut into
     (batch, head-block) chunks that are independent problems; each chunk's copies
