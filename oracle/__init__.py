@@ -37,6 +37,7 @@ from .attention import (  # noqa: F401
     attention_forward,
     attention_backward,
     attention_backward_dq_rows,
+    partial_backward,
     decode_forward,
     varlen_forward,
     varlen_backward,

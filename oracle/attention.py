@@ -226,6 +226,56 @@ def attention_backward_dq_rows(q, k, v, do, scale: float, b: int, h: int, rows,
     return dq
 
 
+def partial_backward(q, k, v, do, lse, dsum, scale: float, mask: MaskSpec = MaskSpec(),
+                     q_offset: int = 0, kv_offset: int = 0):
+    """One (query chunk, key/value chunk) term of the gradient of ``<O, dO>``.
+
+    Attention over a sequence cut into chunks is a sum over key chunks, so its
+    gradient is too, once every row's softmax normaliser is the one over ALL
+    of the row's keys (DISTFLASHATTN reviews, first review summary: forward and
+    backward computed chunk by chunk over workers; BurstAttention author
+    responses: local results tied together by the online-softmax statistics).
+    Given the merged ``lse [B, Hq, Nq]`` (natural log, over every key of the
+    row) and ``dsum = rowsum(dO * O) [B, Hq, Nq]`` of the merged output ``O``,
+    the chunk's probabilities are ``P_ij = exp(S_ij - lse_i)`` on its visible
+    keys (0 elsewhere and on rows with ``lse = -inf``), and its terms are
+    ``dV = P^T dO``, ``dP = dO V^T``, ``dS = P * (dP - dsum)``,
+    ``dQ = scale dS K``, ``dK = scale dS^T Q``; dK and dV sum over the query
+    heads of a GQA group.  Summed over the key chunks (dQ) and the query chunks
+    (dK, dV) these terms give ``attention_backward`` of the whole sequence.
+
+    ``q``, ``do`` ``[B, Hq, Nq, d]``; ``k``, ``v`` ``[B, Hkv, Nk, d]``; positions
+    ``q_offset + i`` and ``kv_offset + j`` as in ``visible``.  Returns
+    ``dQ [B,Hq,Nq,d]``, ``dK``, ``dV [B,Hkv,Nk,d]``.
+    """
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64); do = np.asarray(do, np.float64)
+    lse = np.asarray(lse, np.float64); dsum = np.asarray(dsum, np.float64)
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    g = _group(Hq, Hkv)
+    dq = np.zeros((B, Hq, Nq, d))
+    dk = np.zeros((B, Hkv, Nk, d))
+    dv = np.zeros((B, Hkv, Nk, d))
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // g
+            for s0 in range(0, Nq, ROW_BLOCK):
+                r = np.arange(s0, min(Nq, s0 + ROW_BLOCK))
+                vis = visible(r, Nk, mask, q_offset, kv_offset)
+                s = scale * (q[b, h, r] @ k[b, hk].T)
+                l = lse[b, h, r]
+                fin = np.isfinite(l)
+                with np.errstate(invalid="ignore", over="ignore"):
+                    p = np.where(vis & fin[:, None], np.exp(s - np.where(fin, l, 0.0)[:, None]), 0.0)
+                dp = do[b, h, r] @ v[b, hk].T
+                ds = p * (dp - dsum[b, h, r][:, None])
+                dq[b, h, r] = scale * (ds @ k[b, hk])
+                dk[b, hk] += scale * (ds.T @ q[b, h, r])
+                dv[b, hk] += p.T @ do[b, h, r]
+    return dq, dk, dv
+
+
 def varlen_forward(q, k, v, cu_seqlens, scale: float, mask: MaskSpec = MaskSpec()):
     """Exact attention over sequences packed back to back, in float64.
 

@@ -422,6 +422,70 @@ def test_sliding_window_chunked_merge_equals_monolithic():
             np.testing.assert_allclose(l, full_l[:, :, qs], atol=1e-12)
 
 
+# ---------------------------------------------------------------- chunked backward
+
+def chunked_backward(q, k, v, do, scale, mask, nc, bm=None, block=4):
+    """Gradient of the whole sequence assembled from oracle.partial_backward
+    over every (query chunk, key chunk) pair, with the merged LSE and
+    D = rowsum(dO * O) of the whole forward pass."""
+    n = q.shape[2]
+    c = n // nc
+    o, lse = oracle.attention_forward(q, k, v, scale, mask)
+    dsum = (do * o).sum(-1)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for qc in range(nc):
+        qs = slice(qc * c, (qc + 1) * c)
+        for kc in range(nc):
+            ks = slice(kc * c, (kc + 1) * c)
+            m = mask
+            if mask.kind == "block_sparse":   # the pair's own tiles of the block mask
+                m = MaskSpec("block_sparse", bm[qc * c // block:(qc + 1) * c // block,
+                                                kc * c // block:(kc + 1) * c // block], block,
+                             mask.causal_in_blocks)
+            a, bk, bv = oracle.partial_backward(q[:, :, qs], k[:, :, ks], v[:, :, ks], do[:, :, qs],
+                                                lse[:, :, qs], dsum[:, :, qs], scale, m, qc * c, kc * c)
+            dq[:, :, qs] += a
+            dk[:, :, ks] += bk
+            dv[:, :, ks] += bv
+    return dq, dk, dv
+
+
+def test_chunked_backward_equals_monolithic():
+    """Summed over every chunk pair, the chunk terms give the gradient of the
+    whole sequence (itself pinned by finite differences and torch autograd),
+    for every mask kind, GQA, and chunk counts down to one row per chunk."""
+    n, d = 24, 4
+    rng = np.random.default_rng(11)
+    q, k, v, do = rnd(2, 4, n, d, rng=rng), rnd(2, 2, n, d, rng=rng), rnd(2, 2, n, d, rng=rng), \
+        rnd(2, 4, n, d, rng=rng)
+    bm = rng.random((6, 6)) < 0.5
+    bm[np.arange(6), np.arange(6)] = True
+    masks = [MaskSpec("none"), MaskSpec("causal"), MaskSpec("sliding_window", window=5),
+             MaskSpec("block_sparse", bm, 4), MaskSpec("block_sparse", bm, 4, causal_in_blocks=True)]
+    for mask in masks:
+        want = oracle.attention_backward(q, k, v, do, 0.45, mask)
+        for nc in (1, 2, 3, 6) if mask.kind == "block_sparse" else (1, 2, 3, 4, 6, 8, 24):
+            got = chunked_backward(q, k, v, do, 0.45, mask, nc, bm)
+            for x, y in zip(got, want):
+                np.testing.assert_allclose(x, y, atol=1e-12, err_msg=f"{mask.kind} nc={nc}")
+
+
+def test_partial_backward_of_an_invisible_chunk_is_zero():
+    """A key chunk entirely after the query chunk (causal) contributes nothing,
+    and a row with LSE = -inf (it sees no key anywhere) has zero terms."""
+    q, k, v, do = rnd(1, 2, 6, 3), rnd(1, 1, 6, 3), rnd(1, 1, 6, 3), rnd(1, 2, 6, 3)
+    lse, dsum = rnd(1, 2, 6), rnd(1, 2, 6)
+    for x in oracle.partial_backward(q, k, v, do, lse, dsum, 0.5, MaskSpec("causal"), 0, 6):
+        assert np.all(x == 0)
+    lse[0, 1] = -np.inf
+    dq, dk, dv = oracle.partial_backward(q, k, v, do, lse, dsum, 0.5, MaskSpec("none"))
+    assert np.all(dq[0, 1] == 0)
+    dq0, dk0, dv0 = oracle.partial_backward(q[:, :1], k, v, do[:, :1], lse[:, :1], dsum[:, :1], 0.5,
+                                            MaskSpec("none"))
+    np.testing.assert_allclose(dk, dk0, atol=1e-14)
+    np.testing.assert_allclose(dv, dv0, atol=1e-14)
+
+
 # ---------------------------------------------------------------- decoding against a KV cache
 
 def test_decode_equals_last_rows_of_causal_attention():
@@ -742,3 +806,25 @@ def test_planted_mistakes(monkeypatch):
     monkeypatch.setattr(oa, "merge_partials", merge_no_weights)
     monkeypatch.setattr(oracle, "merge_partials", merge_no_weights)
     assert _fails(test_chunked_merge_equals_monolithic)
+
+    good_pb = oa.partial_backward
+
+    def pb_local_normaliser(q, k, v, do, lse, dsum, scale, mask=MaskSpec(), q_offset=0, kv_offset=0):
+        # each chunk normalised over its own keys instead of the merged LSE
+        _, lse_c = oracle.attention_forward(q, k, v, scale, mask, q_offset, kv_offset)
+        return good_pb(q, k, v, do, lse_c, dsum, scale, mask, q_offset, kv_offset)
+
+    def pb_no_dsum(q, k, v, do, lse, dsum, scale, mask=MaskSpec(), q_offset=0, kv_offset=0):
+        return good_pb(q, k, v, do, lse, np.zeros_like(dsum), scale, mask, q_offset, kv_offset)
+
+    def pb_dk_unscaled(q, k, v, do, lse, dsum, scale, mask=MaskSpec(), q_offset=0, kv_offset=0):
+        dq, dk, dv = good_pb(q, k, v, do, lse, dsum, scale, mask, q_offset, kv_offset)
+        return dq, dk / scale, dv
+
+    def pb_offsets_swapped(q, k, v, do, lse, dsum, scale, mask=MaskSpec(), q_offset=0, kv_offset=0):
+        return good_pb(q, k, v, do, lse, dsum, scale, mask, kv_offset, q_offset)
+
+    for bad in (pb_local_normaliser, pb_no_dsum, pb_dk_unscaled, pb_offsets_swapped):
+        monkeypatch.setattr(oracle, "partial_backward", bad)
+        assert _fails(test_chunked_backward_equals_monolithic), bad.__name__
+        monkeypatch.setattr(oracle, "partial_backward", good_pb)
