@@ -22,8 +22,10 @@
  *   - Every device pointer must be 16-byte aligned; head strides in bytes must
  *     be multiples of 16.
  *   - Pointers named "device" are CUDA device pointers owned by the caller; the
- *     library never frees them.  The library allocates only a one-word device
- *     status register per device (on first use).
+ *     library never frees them.  The library allocates no device memory: its
+ *     status word is a static device variable, whose address on a device is
+ *     looked up by that device's first call (make it before any stream
+ *     capture).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
  *     launches are asynchronous on it.  The return value reports host-side
  *     validation and launch errors only; errors seen by a kernel (a bounded
@@ -174,6 +176,58 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o,
              int N, int d, float scale, const attn_mask_t* mask, void* stream);
 
 /*
+ * attn_bwd_preprocess -- step 1 of the backward pass on its own, for the
+ * chunked backward of attn_partial_bwd: per query row, D = rowsum(dO * O) and
+ * LSE * log2(e), both float32, into the workspace ("FlashAttention-2"
+ * reviews, second review items 2-3: the saved log-sum-exp is what the
+ * backward pass recomputes P from).  Run it once per query chunk with the
+ * MERGED O and LSE of that chunk (the output of attn_merge_lse over all of
+ * the chunk's key chunks), so that every attn_partial_bwd of the chunk uses
+ * the softmax normaliser over all of each row's keys.
+ *   o, dout    device bf16, Nq rows per head, heads head_stride rows apart
+ *              (0 means Nq): [B, Hq, *, d] row slices of longer tensors work.
+ *   lse        device f32, Nq entries per head, heads head_stride apart.
+ *   workspace  device, >= attn_bwd_workspace_bytes(B, Hq, Hq, Nq, d) bytes,
+ *              16-byte aligned, caller-owned: D then LSE*log2 e, each
+ *              [B*Hq][ceil(Nq/128)*128] (rows past Nq hold 0 and +inf).
+ */
+int attn_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, int Hq, int Nq, int d,
+                        int64_t head_stride, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_partial_bwd -- the gradient terms of one (query chunk, key/value
+ * chunk) pair of chunked attention, steps 2 and 3 of attn_bwd on the pair
+ * ("DISTFLASHATTN" reviews, first review summary: attention and its backward
+ * pass computed chunk by chunk over workers; BurstAttention author responses:
+ * local results tied together by online-softmax statistics).  With the
+ * merged statistics of attn_bwd_preprocess, P_ij = exp(S_ij - LSE_i) on the
+ * pair's visible keys, and the pair contributes
+ *   dV += P^T dO,  dK += scale (P * (dO V^T - D))^T Q,  dQ += scale (P * (dO V^T - D)) K;
+ * summed over every pair these are the gradients of the whole sequence.
+ *   q, dout    device bf16, Nq rows per head, heads q_head_stride rows apart
+ *              (0 means Nq).
+ *   k, v       device bf16, Nk rows per head, heads kv_head_stride rows apart
+ *              (0 means Nk).
+ *   workspace  the query chunk's attn_bwd_preprocess output (read only).
+ *   dq         device f32 with q's layout (Nq rows per head, q_head_stride);
+ *   dk, dv     device f32 with k's layout (Nk rows per head, kv_head_stride);
+ *              dK, dV sum over the query heads of each GQA group.
+ *   accumulate != 0: the terms are ADDED to dq, dk, dv (vector float
+ *              reductions in global memory, so pairs that share an output may
+ *              run concurrently on several streams; the summation order, and
+ *              so the last bits, then varies).  accumulate == 0: the terms
+ *              are stored (rows the pair does not reach get 0).
+ *   q_offset, kv_offset: global positions of local query row 0 and key 0 for
+ *              the causal and sliding-window rules, as in attn_partial_fwd
+ *              (>= 0, |q_offset - kv_offset| <= 2^30, Nq + Nk <= 2^30); a
+ *              block-sparse mask is indexed by the pair's local tiles.
+ */
+int attn_partial_bwd(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
+                     size_t workspace_bytes, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int Nq, int Nk,
+                     int d, float scale, const attn_mask_t* mask, int64_t q_offset, int64_t kv_offset,
+                     int64_t q_head_stride, int64_t kv_head_stride, int accumulate, void* stream);
+
+/*
  * attn_varlen_fwd -- attn_fwd over a batch of sequences of different lengths
  * packed back to back ("FlashAttention-2" reviews: variable-length inputs
  * without padding).  Sequence b holds tokens [cu_seqlens[b], cu_seqlens[b+1])
@@ -292,15 +346,14 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d
  *   B*Hq*ceil(N/128)*128 <= 2^21 query rows; larger calls return
  *   ATTN_ERR_WORKSPACE and launch nothing.
  *   The first call on each device looks up the array's device address (and
- *   the device status word next to it) with cudaGetSymbolAddress while that
- *   device is current; make that first call before any stream capture.
+ *   the status word's) with cudaGetSymbolAddress while that device is
+ *   current; make that first call before any stream capture.
  *   All calls on a device share the one array: calls that may overlap on the
  *   GPU (other streams, other host threads) race and must be serialised by
  *   the caller.  Nothing in the array needs clearing: each call overwrites
  *   every entry it later reads.
- *   A kernel wait that runs out during this call is recorded in the static
- *   status word, not in the one attn_get_status() reads; dQ, dK and dV are
- *   then incomplete.
+ *   A kernel wait that runs out is reported by attn_get_status(), as for
+ *   every other entry point (one status word per device serves them all).
  */
 #define ATTN_STATIC_SCRATCH_BYTES (16u << 20)
 int attn_bwd_static_scratch(const void* q, const void* k, const void* v, const void* o,
@@ -345,7 +398,7 @@ int attn_build_chunk_schedule(int n_chunks, int n_lanes, int32_t* pairs_out,
 
 /*
  * attn_get_status -- synchronises `stream`, then reads and clears the current
- * device's status register.  Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT if a
+ * device's status word.  Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT if a
  * kernel's bounded wait ran out since the last call, or ATTN_ERR_CUDA if the
  * synchronisation itself failed.
  */
@@ -365,8 +418,8 @@ void attn_set_wait_limit_ns(int64_t limit_ns);
  * visits: the causal and block-sparse tile skipping of the "FlashAttention-2"
  * reviews, fourth review, and the heaviest-first unit order).  From this call
  * on, every forward launch (attn_fwd, attn_partial_fwd, attn_varlen_fwd,
- * attn_decode_fwd) and every backward call (attn_bwd, attn_varlen_bwd,
- * attn_bwd_static_scratch) writes 8 int32 per CTA, CTA c at counts[8 * c], into
+ * attn_decode_fwd) and every backward call (attn_bwd, attn_partial_bwd,
+ * attn_varlen_bwd, attn_bwd_static_scratch) writes 8 int32 per CTA, CTA c at counts[8 * c], into
  * `counts`, a DEVICE array of `capacity` int32 that the caller owns and keeps
  * alive while recording is on.  Each launch writes from counts[0]; a backward
  * call writes its dK/dV kernel's records first and its dQ kernel's records
@@ -409,9 +462,9 @@ typedef enum {
   ATTN_KERNEL_FWD = 1,            /* attn_fwd forward kernel */
   ATTN_KERNEL_PARTIAL_FWD = 2,    /* attn_partial_fwd forward kernel (f32 output) */
   ATTN_KERNEL_MERGE = 3,          /* attn_merge_lse */
-  ATTN_KERNEL_BWD_PREPROCESS = 4, /* attn_bwd step 1: D and LSE*log2 e */
-  ATTN_KERNEL_BWD_DKDV = 5,       /* attn_bwd step 2: dK, dV */
-  ATTN_KERNEL_BWD_DQ = 6,         /* attn_bwd step 3: dQ */
+  ATTN_KERNEL_BWD_PREPROCESS = 4, /* attn_bwd step 1: D and LSE*log2 e (also attn_bwd_preprocess) */
+  ATTN_KERNEL_BWD_DKDV = 5,       /* attn_bwd step 2: dK, dV (also attn_partial_bwd) */
+  ATTN_KERNEL_BWD_DQ = 6,         /* attn_bwd step 3: dQ (also attn_partial_bwd) */
   ATTN_KERNEL_SELFTEST = 7,       /* attn_selftest_wait_timeout */
   ATTN_KERNEL_DECODE = 8,         /* attn_decode_fwd split-KV partials (its merge is ATTN_KERNEL_MERGE) */
   ATTN_KERNEL_VARLEN_FWD = 9,     /* attn_varlen_fwd forward kernel */

@@ -50,6 +50,11 @@ SIGNATURES = {
                                         c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float,
                                         C.POINTER(attn_mask_t), c_void_p]),
     "attn_bwd_workspace_bytes": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "attn_bwd_preprocess": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int64, c_void_p,
+                                    c_size_t, c_void_p]),
+    "attn_partial_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p,
+                                 c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_float,
+                                 C.POINTER(attn_mask_t), c_int64, c_int64, c_int64, c_int64, c_int, c_void_p]),
     "attn_varlen_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int64,
                                 c_int, c_int, c_int, c_float, C.POINTER(attn_mask_t), c_void_p]),
     "attn_varlen_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,

@@ -16,7 +16,8 @@ import torch
 from . import _ffi
 from ._ffi import attn_mask_t, check
 
-__all__ = ["attn_fwd", "attn_fwd_fp8", "fwd_fp8_workspace_bytes", "attn_partial_fwd", "attn_merge_lse", "attn_bwd", "bwd_workspace_bytes",
+__all__ = ["attn_fwd", "attn_fwd_fp8", "fwd_fp8_workspace_bytes", "attn_partial_fwd", "attn_merge_lse", "attn_bwd",
+           "bwd_workspace_bytes", "attn_bwd_preprocess", "attn_partial_bwd", "chunked_fwd", "chunked_bwd",
            "build_schedule", "build_chunk_schedule", "get_status", "set_wait_limit_ns",
            "selftest_wait_timeout", "mask_desc", "trace_enable", "trace_disable", "trace_read"]
 
@@ -36,6 +37,8 @@ def _rows_view(t: torch.Tensor, name: str, dtype=torch.bfloat16):
     B, H, N, d = t.shape
     if t.stride(3) != 1 or (N > 1 and t.stride(2) != d):
         raise ValueError(f"{name}: rows must be contiguous with stride d")
+    if B * H == 1:
+        return N          # one head: no stride between heads to honour
     if t.stride(1) % d or t.stride(1) // d < N or (B > 1 and t.stride(0) != H * t.stride(1)):
         raise ValueError(f"{name}: heads must be evenly strided")
     return t.stride(1) // d
@@ -230,6 +233,137 @@ def attn_bwd(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = 
                               ws.numel() * ws.element_size(), B, Hq, Hkv, N, d, sc, _mp(m), _stream(q)),
           "attn_bwd")
     del keep
+    return dq, dk, dv
+
+
+def attn_bwd_preprocess(o, lse, do, workspace: Optional[torch.Tensor] = None):
+    """Backward step 1 for one query chunk: ``D = rowsum(dO * O)`` and ``LSE * log2 e``.
+
+    ``o``, ``do`` ``[B,Hq,Nq,d]`` bf16 and ``lse`` ``[B,Hq,Nq]`` f32 may be
+    row-slices of longer tensors (rows contiguous, one head stride for all
+    three).  Pass the MERGED O and LSE of the chunk.  Returns the workspace
+    (uint8) that ``attn_partial_bwd`` reads.
+    """
+    hs = _rows_view(o, "o")
+    if _rows_view(do, "do") != hs or do.shape != o.shape:
+        raise ValueError("do must match o's shape and head stride")
+    B, Hq, Nq, d = o.shape
+    if (lse.dtype != torch.float32 or not lse.is_cuda or lse.shape != (B, Hq, Nq) or lse.stride(-1) != 1
+            or (Hq > 1 and lse.stride(1) != hs) or (B > 1 and lse.stride(0) != Hq * hs)):
+        raise ValueError("lse must be f32 [B, Hq, Nq] with o's head stride (in rows)")
+    need = bwd_workspace_bytes(B, Hq, Hq, Nq, d)
+    ws = torch.empty(need, device=o.device, dtype=torch.uint8) if workspace is None else workspace
+    check(_ffi.lib().attn_bwd_preprocess(o.data_ptr(), do.data_ptr(), lse.data_ptr(), B, Hq, Nq, d, hs,
+                                         ws.data_ptr(), ws.numel() * ws.element_size(), _stream(o)),
+          "attn_bwd_preprocess")
+    return ws
+
+
+def attn_partial_bwd(q, k, v, do, workspace, dq, dk, dv, q_offset: int = 0, kv_offset: int = 0,
+                     scale: Optional[float] = None, causal: bool = False,
+                     block_mask: Optional[torch.Tensor] = None, causal_in_blocks: bool = False,
+                     window: Optional[int] = None, accumulate: bool = True):
+    """Gradient terms of one (query chunk, key/value chunk) pair, added to
+    (``accumulate``) or stored in the float32 ``dq`` (q's shape and head
+    stride) and ``dk``/``dv`` (k's).  ``workspace`` is the query chunk's
+    ``attn_bwd_preprocess`` output.  ``q``/``do`` and ``k``/``v`` may be
+    row-slices of longer tensors."""
+    qhs = _rows_view(q, "q")
+    khs = _rows_view(k, "k")
+    if _rows_view(v, "v") != khs or v.shape != k.shape or _rows_view(do, "do") != qhs or do.shape != q.shape:
+        raise ValueError("v must match k, do must match q (shape and head stride)")
+    if _rows_view(dq, "dq", torch.float32) != qhs or dq.shape != q.shape:
+        raise ValueError("dq must be f32 with q's shape and head stride")
+    for t, n in ((dk, "dk"), (dv, "dv")):
+        if _rows_view(t, n, torch.float32) != khs or t.shape != k.shape:
+            raise ValueError(f"{n} must be f32 with k's shape and head stride")
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    m, keep = mask_desc(causal, block_mask, causal_in_blocks, window)
+    check(_ffi.lib().attn_partial_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), workspace.data_ptr(),
+                                      workspace.numel() * workspace.element_size(), dq.data_ptr(), dk.data_ptr(),
+                                      dv.data_ptr(), B, Hq, Hkv, Nq, Nk, d, sc, _mp(m), int(q_offset),
+                                      int(kv_offset), qhs, khs, 1 if accumulate else 0, _stream(q)),
+          "attn_partial_bwd")
+    del keep
+    return dq, dk, dv
+
+
+def _chunk_pairs(n_chunks: int, causal: bool):
+    if causal:
+        return build_chunk_schedule(n_chunks)
+    return [(a, b) for a in range(n_chunks) for b in range(n_chunks)]
+
+
+def chunked_fwd(q, k, v, n_chunks: int, scale: Optional[float] = None, causal: bool = True,
+                window: Optional[int] = None):
+    """Attention of ``q``, ``k``, ``v`` ``[B,H,N,d]`` cut into ``n_chunks`` equal
+    sequence chunks, the way chunked (sequence-parallel) attention runs it on
+    one GPU: every visible (query chunk, key chunk) pair with
+    ``attn_partial_fwd`` (under a causal or sliding-window mask the pairs with
+    key chunk <= query chunk, in the load-balanced order of
+    ``build_chunk_schedule``), then one ``attn_merge_lse`` per query chunk.
+    Returns ``(O bf16, LSE f32)`` of the whole sequence."""
+    B, Hq, N, d = q.shape
+    if N % n_chunks:
+        raise ValueError("N must be a multiple of n_chunks")
+    L = N // n_chunks
+    local = causal or window is not None
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), device=q.device, dtype=torch.float32)
+    parts = {}
+    for qc, kc in _chunk_pairs(n_chunks, local):
+        parts[(qc, kc)] = attn_partial_fwd(q[:, :, qc * L:(qc + 1) * L], k[:, :, kc * L:(kc + 1) * L],
+                                           v[:, :, kc * L:(kc + 1) * L], qc * L, kc * L, scale=scale,
+                                           causal=causal and window is None, window=window)
+    for qc in range(n_chunks):
+        kcs = [kc for kc in range(n_chunks) if (qc, kc) in parts]
+        attn_merge_lse([parts[(qc, kc)][0] for kc in kcs], [parts[(qc, kc)][1] for kc in kcs],
+                       out=o[:, :, qc * L:(qc + 1) * L], lse_out=lse[:, :, qc * L:(qc + 1) * L])
+    return o, lse
+
+
+def chunked_bwd(q, k, v, o, lse, do, n_chunks: int, scale: Optional[float] = None, causal: bool = True,
+                window: Optional[int] = None, n_streams: int = 1, dq=None, dk=None, dv=None):
+    """Backward pass of ``chunked_fwd``: one ``attn_bwd_preprocess`` per query
+    chunk (with the merged ``o`` and ``lse``), then ``attn_partial_bwd`` of
+    every visible chunk pair, in the load-balanced order, adding into float32
+    ``dq``, ``dk``, ``dv`` (zeroed here unless given).  With ``n_streams`` > 1
+    the pairs are dealt round-robin to that many side streams (the float32
+    reductions make concurrent pairs safe); the current stream waits for all
+    of them.  Returns ``(dQ, dK, dV)`` in float32."""
+    B, Hq, N, d = q.shape
+    if N % n_chunks:
+        raise ValueError("N must be a multiple of n_chunks")
+    L = N // n_chunks
+    local = causal or window is not None
+    dq = torch.zeros(q.shape, device=q.device, dtype=torch.float32) if dq is None else dq
+    dk = torch.zeros(k.shape, device=q.device, dtype=torch.float32) if dk is None else dk
+    dv = torch.zeros(v.shape, device=q.device, dtype=torch.float32) if dv is None else dv
+    ws = [attn_bwd_preprocess(o[:, :, c * L:(c + 1) * L], lse[:, :, c * L:(c + 1) * L], do[:, :, c * L:(c + 1) * L])
+          for c in range(n_chunks)]
+    main = torch.cuda.current_stream(q.device)
+    streams = [main] if n_streams <= 1 else [torch.cuda.Stream(q.device) for _ in range(n_streams)]
+    if n_streams > 1:
+        ready = torch.cuda.Event()
+        ready.record(main)
+        for st in streams:
+            st.wait_event(ready)
+    for i, (qc, kc) in enumerate(_chunk_pairs(n_chunks, local)):
+        qs, ks = slice(qc * L, (qc + 1) * L), slice(kc * L, (kc + 1) * L)
+        with torch.cuda.stream(streams[i % len(streams)]):
+            attn_partial_bwd(q[:, :, qs], k[:, :, ks], v[:, :, ks], do[:, :, qs], ws[qc], dq[:, :, qs],
+                             dk[:, :, ks], dv[:, :, ks], qc * L, kc * L, scale=scale,
+                             causal=causal and window is None, window=window, accumulate=True)
+    if n_streams > 1:
+        for st in streams:
+            ev = torch.cuda.Event()
+            ev.record(st)
+            main.wait_event(ev)
+        for t in ws + [dq, dk, dv, q, k, v, do]:
+            for st in streams:
+                t.record_stream(st)
     return dq, dk, dv
 
 

@@ -1,7 +1,9 @@
 // api.cu -- the C ABI (include/attn.h): argument validation, TMA descriptor
-// encoding, launches, the per-device status register, and the host-only
-// schedule builders.  Every compute step runs in the kernels of fwd.cu,
-// bwd.cu and merge.cu; nothing here computes attention.
+// encoding, launches, the per-device status word, and the host-only schedule
+// builders.  Every compute step runs in the kernels of fwd.cu, bwd.cu and
+// merge.cu; nothing here computes attention.  The library allocates no device
+// memory: the status word and the scratch of attn_bwd_static_scratch are
+// static device variables of this file.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -27,8 +29,14 @@ int32_t* g_debug_counts = nullptr;   // attn_debug_set_tile_counts
 int64_t g_debug_capacity = 0;
 
 constexpr int MAX_DEVICES = 64;
-unsigned int* g_status[MAX_DEVICES] = {};
+unsigned int* g_status[MAX_DEVICES] = {};   // device address of g_status_word, per device
 int g_dev_ok[MAX_DEVICES] = {};  // 0 unknown, 1 ok, -1 unsupported
+
+// The device status word every kernel reports to (ATTN_DEV_TIMEOUT when a
+// bounded wait runs out) and attn_get_status reads and clears: a static
+// device variable, so no call allocates for it.  Host code passes kernels its
+// device address (looked up per device), never the host-side name.
+__device__ unsigned int g_status_word;
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -44,7 +52,8 @@ int cuda_fail(cudaError_t e, const char* what) {
   return fail(ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-// Current device, checked to be sm_103; its status word allocated on first use.
+// Current device, checked to be sm_103; the device address of its status word
+// looked up on first use (make a device's first call before any stream capture).
 int device_ready(unsigned int** status) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -59,12 +68,10 @@ int device_ready(unsigned int** status) {
   }
   if (g_dev_ok[dev] < 0) return fail(ATTN_ERR_NO_DEVICE, "device %d is not sm_103 (GB300)", dev);
   if (g_status[dev] == nullptr) {
-    unsigned int* p = nullptr;
-    e = cudaMalloc(&p, sizeof(unsigned int));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(status)");
-    e = cudaMemset(p, 0, sizeof(unsigned int));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
-    g_status[dev] = p;
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+    g_status[dev] = static_cast<unsigned int*>(p);
   }
   *status = g_status[dev];
   return ATTN_OK;
@@ -612,7 +619,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   cudaError_t e;
   {
     TraceScope ts(ATTN_KERNEL_BWD_PREPROCESS, s);
-    e = launch_bwd_preprocess(o, dout, lse, dsum, lse2, (int64_t)B * Hq, N, Np, d, s);
+    e = launch_bwd_preprocess(o, dout, lse, dsum, lse2, (int64_t)B * Hq, N, Np, N, d, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
   BwdParams p{};
@@ -620,7 +627,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   p.dsum = dsum;
   p.Np = Np;
   p.dq = dq; p.dk = dk; p.dv = dv;
-  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = N; p.Nk = N;
+  p.dq_hs = N; p.dkv_hs = N;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.mask_kind = m.kind;
@@ -637,14 +645,110 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
     return rc;
   {
     TraceScope ts(ATTN_KERNEL_BWD_DKDV, s);
-    e = launch_bwd_dkdv(d, tq, tk, tv, tdo, p, s);
+    e = launch_bwd_dkdv(d, false, tq, tk, tv, tdo, p, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "backward dK/dV launch");
   {
     TraceScope ts(ATTN_KERNEL_BWD_DQ, s);
-    e = launch_bwd_dq(d, tq, tk, tv, tdo, p, s);
+    e = launch_bwd_dq(d, false, tq, tk, tv, tdo, p, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "backward dQ launch");
+  return ATTN_OK;
+}
+
+int attn_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, int Hq, int Nq, int d,
+                        int64_t head_stride, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc;
+  if ((rc = check_ptr(o, "o")) || (rc = check_ptr(dout, "dout")) || (rc = check_ptr(workspace, "workspace")))
+    return rc;
+  if (lse == nullptr) return fail(ATTN_ERR_INVALID_ARG, "lse is NULL");
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return fail(ATTN_ERR_MISALIGNED, "lse not 4-byte aligned");
+  if ((rc = check_dims(B, Hq, Hq, Nq, Nq, d, 1.f))) return rc;
+  const int64_t hs = head_stride > 0 ? head_stride : Nq;
+  if (hs < Nq) return fail(ATTN_ERR_INVALID_ARG, "head_stride %lld smaller than Nq=%d", (long long)hs, Nq);
+  if (workspace_bytes < attn_bwd_workspace_bytes(B, Hq, Hq, Nq, d))
+    return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes, need %zu", workspace_bytes,
+                attn_bwd_workspace_bytes(B, Hq, Hq, Nq, d));
+  unsigned int* status = nullptr;
+  if ((rc = device_ready(&status))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int Np = (int)(cdiv(Nq, TILE) * TILE);
+  float* dsum = static_cast<float*>(workspace);
+  float* lse2 = dsum + (size_t)B * Hq * Np;
+  cudaError_t e;
+  {
+    TraceScope ts(ATTN_KERNEL_BWD_PREPROCESS, s);
+    e = launch_bwd_preprocess(o, dout, lse, dsum, lse2, (int64_t)B * Hq, Nq, Np, hs, d, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
+  return ATTN_OK;
+}
+
+int attn_partial_bwd(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
+                     size_t workspace_bytes, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int Nq, int Nk,
+                     int d, float scale, const attn_mask_t* mask, int64_t q_offset, int64_t kv_offset,
+                     int64_t q_head_stride, int64_t kv_head_stride, int accumulate, void* stream) {
+  int rc;
+  if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k, "k")) || (rc = check_ptr(v, "v")) ||
+      (rc = check_ptr(dout, "dout")) || (rc = check_ptr(workspace, "workspace")) || (rc = check_ptr(dq, "dq")) ||
+      (rc = check_ptr(dk, "dk")) || (rc = check_ptr(dv, "dv")))
+    return rc;
+  if ((rc = check_dims(B, Hq, Hkv, Nq, Nk, d, scale))) return rc;
+  const int64_t qhs = q_head_stride > 0 ? q_head_stride : Nq;
+  const int64_t khs = kv_head_stride > 0 ? kv_head_stride : Nk;
+  if (qhs < Nq || khs < Nk) return fail(ATTN_ERR_INVALID_ARG, "head stride smaller than the rows per head");
+  // the kernels compare position differences in 32-bit integers
+  const int64_t delta = q_offset - kv_offset;
+  if (q_offset < 0 || kv_offset < 0 || delta > ((int64_t)1 << 30) || delta < -((int64_t)1 << 30) ||
+      (int64_t)Nq + Nk > ((int64_t)1 << 30))
+    return fail(ATTN_ERR_INVALID_ARG, "offsets must be >= 0, |q_offset - kv_offset| <= 2^30 and Nq + Nk <= 2^30");
+  if (workspace_bytes < attn_bwd_workspace_bytes(B, Hq, Hkv, Nq, d))
+    return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes, need %zu", workspace_bytes,
+                attn_bwd_workspace_bytes(B, Hq, Hkv, Nq, d));
+  MaskArgs m;
+  if ((rc = read_mask(mask, &m))) return rc;
+  unsigned int* status = nullptr;
+  if ((rc = device_ready(&status))) return rc;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((rc = encode_rows_map(&tq, q, d, Nq, B * Hq, qhs)) || (rc = encode_rows_map(&tk, k, d, Nk, B * Hkv, khs)) ||
+      (rc = encode_rows_map(&tv, v, d, Nk, B * Hkv, khs)) || (rc = encode_rows_map(&tdo, dout, d, Nq, B * Hq, qhs)))
+    return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int Np = (int)(cdiv(Nq, TILE) * TILE);
+  BwdParams p{};
+  p.dsum = static_cast<const float*>(workspace);
+  p.lse2 = p.dsum + (size_t)B * Hq * Np;
+  p.Np = Np;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = Nq; p.Nk = Nk;
+  p.delta = (int)delta;
+  p.dq_hs = qhs; p.dkv_hs = khs;
+  p.accumulate = accumulate ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.mask_kind = m.kind;
+  p.causal_in_blocks = m.causal_in_blocks;
+  p.block_mask = m.block_mask;
+  p.window = m.window;
+  p.nkb = (int)cdiv(Nk, TILE);
+  p.kv_group = q_stream_group(B, Hq, Hkv, Nq, d);
+  p.q_group = kv_stream_group(B, Hq, Hkv, Nk, d);
+  p.status = status;
+  p.wait_limit_ns = wait_limit();
+  if ((rc = debug_records(0, dkdv_grid(p), &p.dkdv_counts)) ||
+      (rc = debug_records(dkdv_grid(p), dq_grid(p), &p.dq_counts)))
+    return rc;
+  cudaError_t e;
+  {
+    TraceScope ts(ATTN_KERNEL_BWD_DKDV, s);
+    e = launch_bwd_dkdv(d, true, tq, tk, tv, tdo, p, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "partial backward dK/dV launch");
+  {
+    TraceScope ts(ATTN_KERNEL_BWD_DQ, s);
+    e = launch_bwd_dq(d, true, tq, tk, tv, tdo, p, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "partial backward dQ launch");
   return ATTN_OK;
 }
 
@@ -702,7 +806,7 @@ int attn_varlen_bwd(const void* q, const void* k, const void* v, const void* o, 
   p.lse2 = lse2;
   p.dsum = dsum;
   p.dq = dq; p.dk = dk; p.dv = dv;
-  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = max_len;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = max_len; p.Nk = max_len;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.mask_kind = m.kind;
@@ -719,12 +823,12 @@ int attn_varlen_bwd(const void* q, const void* k, const void* v, const void* o, 
     return rc;
   {
     TraceScope ts(ATTN_KERNEL_BWD_DKDV, s);
-    e = launch_bwd_dkdv(d, tq, tk, tv, tdo, p, s);
+    e = launch_bwd_dkdv(d, false, tq, tk, tv, tdo, p, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "ragged backward dK/dV launch");
   {
     TraceScope ts(ATTN_KERNEL_BWD_DQ, s);
-    e = launch_bwd_dq(d, tq, tk, tv, tdo, p, s);
+    e = launch_bwd_dq(d, false, tq, tk, tv, tdo, p, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "ragged backward dQ launch");
   return ATTN_OK;
@@ -887,38 +991,25 @@ int attn_trace_read(attn_trace_record_t* out, int cap, int* n_out) {
 namespace {
 
 static __device__ __align__(256) float g_static_scratch[ATTN_STATIC_SCRATCH_BYTES / sizeof(float)];
-static __device__ unsigned int g_static_status;
 
-struct StaticScratch {
-  float* scratch = nullptr;
-  unsigned int* status = nullptr;
-};
-StaticScratch g_static_dev[MAX_DEVICES];
+float* g_static_dev[MAX_DEVICES] = {};
 std::mutex g_static_mu;
 
-// Device addresses of the static scratch and status word on the current device.
-int static_scratch_for_current_device(StaticScratch* out) {
+// Device address of the static scratch on the current device (device_ready
+// has checked the device and looked up its status word).
+int static_scratch_for_current_device(float** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(ATTN_ERR_NO_DEVICE, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= MAX_DEVICES) return fail(ATTN_ERR_NO_DEVICE, "device index %d out of range", dev);
-  int major = 0, minor = 0;
-  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (!(major == 10 && minor == 3)) return fail(ATTN_ERR_NO_DEVICE, "device %d is not sm_103 (GB300)", dev);
   std::lock_guard<std::mutex> lk(g_static_mu);
-  StaticScratch& st = g_static_dev[dev];
-  if (st.scratch == nullptr) {
+  if (g_static_dev[dev] == nullptr) {
     void* ps = nullptr;
-    void* pw = nullptr;
     e = cudaGetSymbolAddress(&ps, g_static_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
-    e = cudaGetSymbolAddress(&pw, g_static_status);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static status)");
-    st.scratch = static_cast<float*>(ps);
-    st.status = static_cast<unsigned int*>(pw);
+    g_static_dev[dev] = static_cast<float*>(ps);
   }
-  *out = st;
+  *out = g_static_dev[dev];
   return ATTN_OK;
 }
 
@@ -942,23 +1033,30 @@ extern "C" int attn_bwd_static_scratch(const void* q, const void* k, const void*
                 (long long)rows, (long long)(ATTN_STATIC_SCRATCH_BYTES / (2 * sizeof(float))));
   MaskArgs m;
   if ((rc = read_mask(mask, &m))) return rc;
-  StaticScratch st;
-  if ((rc = static_scratch_for_current_device(&st))) return rc;
+  unsigned int* status = nullptr;
+  if ((rc = device_ready(&status))) return rc;
+  float* scratch = nullptr;
+  if ((rc = static_scratch_for_current_device(&scratch))) return rc;
   CUtensorMap tq, tk, tv, tdo;
   if ((rc = encode_rows_map(&tq, q, d, N, B * Hq, N)) || (rc = encode_rows_map(&tk, k, d, N, B * Hkv, N)) ||
       (rc = encode_rows_map(&tv, v, d, N, B * Hkv, N)) || (rc = encode_rows_map(&tdo, dout, d, N, B * Hq, N)))
     return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float* dsum = st.scratch;
-  float* lse2 = st.scratch + rows;
-  cudaError_t e = launch_bwd_preprocess(o, dout, lse, dsum, lse2, (int64_t)B * Hq, N, (int)Np, d, s);
+  float* dsum = scratch;
+  float* lse2 = scratch + rows;
+  cudaError_t e;
+  {
+    TraceScope ts(ATTN_KERNEL_BWD_PREPROCESS, s);
+    e = launch_bwd_preprocess(o, dout, lse, dsum, lse2, (int64_t)B * Hq, N, (int)Np, N, d, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
   BwdParams p{};
   p.lse2 = lse2;
   p.dsum = dsum;
   p.Np = (int)Np;
   p.dq = dq; p.dk = dk; p.dv = dv;
-  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = N; p.Nk = N;
+  p.dq_hs = N; p.dkv_hs = N;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.mask_kind = m.kind;
@@ -968,14 +1066,20 @@ extern "C" int attn_bwd_static_scratch(const void* q, const void* k, const void*
   p.nkb = (int)cdiv(N, TILE);
   p.kv_group = q_stream_group(B, Hq, Hkv, N, d);
   p.q_group = kv_stream_group(B, Hq, Hkv, N, d);
-  p.status = st.status;
+  p.status = status;
   p.wait_limit_ns = wait_limit();
   if ((rc = debug_records(0, dkdv_grid(p), &p.dkdv_counts)) ||
       (rc = debug_records(dkdv_grid(p), dq_grid(p), &p.dq_counts)))
     return rc;
-  e = launch_bwd_dkdv(d, tq, tk, tv, tdo, p, s);
+  {
+    TraceScope ts(ATTN_KERNEL_BWD_DKDV, s);
+    e = launch_bwd_dkdv(d, false, tq, tk, tv, tdo, p, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "backward dK/dV launch");
-  e = launch_bwd_dq(d, tq, tk, tv, tdo, p, s);
+  {
+    TraceScope ts(ATTN_KERNEL_BWD_DQ, s);
+    e = launch_bwd_dq(d, false, tq, tk, tv, tdo, p, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "backward dQ launch");
   return ATTN_OK;
 }

@@ -58,13 +58,34 @@ __device__ __forceinline__ int window_of(const BwdParams& p) {
   return p.mask_kind == MASK_SLIDING_WINDOW ? p.window : 0x7fffffff;
 }
 
-// Query tile qt sees key tile kt (equal 128-row tiles, no offsets): some query
-// of qt lies 0..window-1 positions after some key of kt.
+// Positions from the first key of key tile kt to the first query of query
+// tile qt: query row r of qt and key column c of kt are base + r - c apart
+// (delta = q_offset - kv_offset, 0 unless the call is one chunk pair).
+__device__ __forceinline__ int tile_base(const BwdParams& p, int qt, int kt) { return p.delta + (qt - kt) * TILE; }
+
+// Query tile qt sees key tile kt: some query of qt lies 0..window-1 positions
+// after some key of kt (the largest distance in the pair is base + 127, the
+// smallest base - 127), and the block mask keeps the pair.
 __device__ __forceinline__ bool tile_pair_visible(const BwdParams& p, int qt, int kt) {
-  if (causal_of(p) && qt < kt) return false;
-  if ((qt - kt) * TILE - (TILE - 1) >= window_of(p)) return false;
+  const int base = tile_base(p, qt, kt);
+  if (causal_of(p) && base + (TILE - 1) < 0) return false;
+  if (base - (TILE - 1) >= window_of(p)) return false;
   if (p.mask_kind == MASK_BLOCK_SPARSE && p.block_mask[(size_t)qt * p.nkb + kt] == 0) return false;
   return true;
+}
+
+// Causal masks: the first query tile with a query at or after the first key
+// of key tile kt (base + 127 >= 0).
+__device__ __forceinline__ int first_query_tile(const BwdParams& p, int kt) {
+  const int y = kt * TILE - p.delta - (TILE - 1);
+  return y <= 0 ? 0 : (y + TILE - 1) / TILE;
+}
+
+// Causal masks: one past the last key tile with a key at or before the last
+// query of query tile qt, capped at nkt.
+__device__ __forceinline__ int key_tile_end(const BwdParams& p, int qt, int nkt) {
+  const int z = p.delta + qt * TILE + (TILE - 1);
+  return z < 0 ? 0 : min(nkt, z / TILE + 1);
 }
 
 // TMEM column of the bf16 A operand for MMA k-step kk (16 rows of K each) when
@@ -80,7 +101,7 @@ __host__ __device__ constexpr uint32_t half_col(int kk) { return kk < 4 ? kk * 8
 // Order on the tensor core: S^T_0, dP^T_0, then dV_i, S^T_{i+1}, dK_i,
 // dP^T_{i+1} per query tile i (see the MMA issuer).
 // =========================================================================
-template <int D>
+template <int D, bool F32>
 __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -109,7 +130,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
   const uint32_t bar_dk = smem_u32(&bars[1 + 2 * NS + 5]);
   const uint32_t bar_done = smem_u32(&bars[1 + 2 * NS + 6]);
 
-  const int nkt_all = (p.N + TILE - 1) / TILE;
+  const int nkt_all = (p.Nk + TILE - 1) / TILE;
   const bool ragged = p.cu_seqlens != nullptr;
   int kt = 0, bkv = 0;
   if (ragged) {   // key tiles ascending (heaviest first), every sequence and kv head inner
@@ -120,16 +141,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
   }
   const int b = bkv / p.Hkv, hkv = bkv % p.Hkv;
   const int g = p.Hq / p.Hkv;
-  // the unit's sequence: its first token's row in the maps, its length, and
-  // where its rows start in lse2 / dsum (head 0) and between query heads
+  // the unit's sequence: its first token's row in the maps, its keys and
+  // query rows, and where its rows start in lse2 / dsum (head 0) and between
+  // query heads
   const int tok0 = ragged ? p.cu_seqlens[b] : 0;    // packed tensors hold fewer than 2^31 tokens
-  const int n_seq = ragged ? p.cu_seqlens[b + 1] - tok0 : p.N;
+  const int n_seq = ragged ? p.cu_seqlens[b + 1] - tok0 : p.Nk;
+  const int nq_seq = ragged ? n_seq : p.Nq;
   if (kt * TILE >= n_seq) return;   // past the end of a shorter sequence; nothing is set up yet
   const int64_t lrow_hs = ragged ? (int64_t)p.pcu[p.B] : (int64_t)p.Np;
   const int64_t lrow_b = ragged ? (int64_t)p.pcu[b] : (int64_t)b * p.Hq * p.Np;
   const int kv_head = ragged ? hkv : bkv;   // head coordinate in the K / V maps
-  const int nqt = (n_seq + TILE - 1) / TILE;
-  const int qt_first = causal_of(p) ? kt : 0;
+  const int nqt = (nq_seq + TILE - 1) / TILE;
+  const int qt_first = causal_of(p) ? first_query_tile(p, kt) : 0;
   WaitCtx wc{p.wait_limit_ns, p.status, &abort_flag};
 
   if (threadIdx.x == 0) {
@@ -330,11 +353,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
         ok = wait_bar(bar_q(s), (i / NS) & 1, wc) && wait_bar(bar_s, i & 1, wc);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        // key r sees query column j iff 0 <= (qt - kt) * 128 + j - r < window:
-        // j >= r on the diagonal tile, j < hi where the window's edge crosses
-        const bool diag = causal && qt == kt;
-        const bool wedge = (qt - kt) * TILE + (TILE - 1) >= window_of(p);
-        const int hi = wedge ? window_of(p) + r - (qt - kt) * TILE : TILE;
+        // key r sees query column j iff 0 <= base + j - r < window: j >= lo
+        // where the causal edge crosses the tile, j < hi where the window's
+        // edge does
+        const int base = tile_base(p, qt, kt);
+        const bool cedge = causal && base < TILE - 1;
+        const bool wedge = base + (TILE - 1) >= window_of(p);
+        const int hi = wedge ? window_of(p) + r - base : TILE;
         const float4* l4 = reinterpret_cast<const float4*>(lse2) + 16 * hf;
         const float4* d4 = reinterpret_cast<const float4*>(dsum) + 16 * hf;
         // phase A: P^T = 2^(S^T c - lse2) for this warpgroup's 64 query columns,
@@ -345,7 +370,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
         auto phase_a = [&](auto masked) {
           uint32_t sr[64];
           tmem_ld64(tmem + lane_off + cb, sr);
-          const int lo = diag ? r : 0;                // visible query columns: lo <= j < hi
+          const int lo = cedge ? r - base : 0;        // visible query columns: lo <= j < hi
 #pragma unroll
           for (int j4 = 0; j4 < 16; ++j4) {
             const float4 L = l4[j4];
@@ -366,7 +391,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
             pf[4 * j4 + 3] = p3;
           }
         };
-        if (diag || wedge) phase_a(std::true_type{});
+        if (cedge || wedge) phase_a(std::true_type{});
         else phase_a(std::false_type{});
         {
           uint32_t pk[32];
@@ -416,6 +441,31 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
         // staged through shared memory no MMA or copy uses any more (the K and
         // V tiles') so that each store instruction covers whole rows
         const float mul = hf == 0 ? 1.f : p.scale;
+        const int wkey0 = kt * TILE + wq * 32;   // this warp's first key
+        if constexpr (F32) {
+          // float32 rows, 32 columns at a time through this warp's 4 KB of
+          // staging; added (p.accumulate) or stored.  With no visible query
+          // tile an add has nothing to contribute and a store writes zeros.
+          float* base = static_cast<float*>(hf == 0 ? p.dv : p.dk) + ((size_t)bkv * p.dkv_hs + wkey0) * D;
+          const uint32_t stage = s_base + (uint32_t)(warp - 4) * (32u * 32u * 4u);
+          if (i > 0 || !p.accumulate) {
+#pragma unroll
+            for (int q4 = 0; q4 < D / 32; ++q4) {
+              uint32_t rv[32];
+              if (i > 0) {
+                tmem_ld32(tmem + lane_off + 256 + hf * D + q4 * 32, rv);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) rv[j] = 0u;
+              }
+#pragma unroll
+              for (int j = 0; j < 32; ++j) rv[j] = __float_as_uint(__uint_as_float(rv[j]) * mul);
+              char* dst = reinterpret_cast<char*>(base + q4 * 32);
+              if (p.accumulate) warp_store_rows<8, true>(stage, rv, dst, (size_t)D * 4, n_seq - wkey0);
+              else warp_store_rows<8>(stage, rv, dst, (size_t)D * 4, n_seq - wkey0);
+            }
+          }
+        } else {
         uint32_t w[D / 2];
 #pragma unroll
         for (int q4 = 0; q4 < D / 32; ++q4) {
@@ -430,11 +480,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
           for (int j = 0; j < 16; ++j)
             w[q4 * 16 + j] = pack_bf16(__uint_as_float(rv[2 * j]) * mul, __uint_as_float(rv[2 * j + 1]) * mul);
         }
-        const int wkey0 = kt * TILE + wq * 32;   // this warp's first key
-        const size_t orow0 = ragged ? (size_t)(tok0 + wkey0) * p.Hkv + hkv : (size_t)bkv * p.N + wkey0;
+        const size_t orow0 = ragged ? (size_t)(tok0 + wkey0) * p.Hkv + hkv : (size_t)bkv * p.dkv_hs + wkey0;
         char* base = reinterpret_cast<char*>(static_cast<__nv_bfloat16*>(hf == 0 ? p.dv : p.dk) + orow0 * D);
         const size_t stride = (ragged ? (size_t)p.Hkv : (size_t)1) * D * sizeof(__nv_bfloat16);
         warp_store_rows<D / 8>(s_base + (uint32_t)(warp - 4) * (32u * D * 2), w, base, stride, n_seq - wkey0);
+        }
       }
     }
   }
@@ -473,7 +523,7 @@ struct DqCfg {
   static constexpr uint32_t REGS_CTRL = 72, REGS_ELEM = 216;
 };
 
-template <int D>
+template <int D, bool F32>
 __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -505,7 +555,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
   auto bar_ds = [&](int j) { return smem_u32(&bars[1 + 2 * KS + 2 * VS + 5 + (j & 1)]); };
   auto bar_dq = [&](int j) { return smem_u32(&bars[1 + 2 * KS + 2 * VS + 7 + (j & 1)]); };
 
-  const int nqt_all = (p.N + TILE - 1) / TILE;
+  const int nqt_all = (p.Nq + TILE - 1) / TILE;
   const bool ragged = p.cu_seqlens != nullptr;
   int bh = 0, qpos = 0;
   if (ragged) {   // latest query tiles first, every sequence and head inner
@@ -518,11 +568,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int bkv = b * p.Hkv + h / (p.Hq / p.Hkv);
   const int tok0 = ragged ? p.cu_seqlens[b] : 0;    // packed tensors hold fewer than 2^31 tokens
-  const int n_seq = ragged ? p.cu_seqlens[b + 1] - tok0 : p.N;
+  const int n_seq = ragged ? p.cu_seqlens[b + 1] - tok0 : p.Nq;   // query rows of the unit's sequence
+  const int nk_seq = ragged ? n_seq : p.Nk;                       // and its keys
   if (qt * TILE >= n_seq) return;   // past the end of a shorter sequence; nothing is set up yet
   const int q_head = ragged ? h : bh, kv_head = ragged ? h / (p.Hq / p.Hkv) : bkv;   // heads in the maps
-  const int nkt = (n_seq + TILE - 1) / TILE;
-  const int kt_end = causal_of(p) ? qt + 1 : nkt;
+  const int nkt = (nk_seq + TILE - 1) / TILE;
+  const int kt_end = causal_of(p) ? key_tile_end(p, qt, nkt) : nkt;
   WaitCtx wc{p.wait_limit_ns, p.status, &abort_flag};
 
   if (threadIdx.x == 0) {
@@ -717,14 +768,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       ok = wait_bar(bar_s, j & 1, wc);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      // key column col is visible iff key < N, key <= query (causal) and
-      // query - key < window: lo <= col < lim
+      // key column col is visible iff the key exists, key <= query (causal:
+      // base + r - col >= 0) and query - key < window: lo <= col < lim
       const int wnd = window_of(p);
-      const bool wedge = (qt - kt) * TILE + (TILE - 1) >= wnd;
-      const bool edge = (kt == nkt - 1 && (n_seq % TILE) != 0) || (causal && kt == qt) || wedge;
-      int lim = n_seq - kt * TILE;
-      if (causal && kt == qt) lim = min(lim, r + 1);
-      const int lo = wedge ? (qt - kt) * TILE + r - wnd + 1 : 0;
+      const int base = tile_base(p, qt, kt);
+      const bool cedge = causal && base < TILE - 1;
+      const bool wedge = base + (TILE - 1) >= wnd;
+      const bool edge = (kt == nkt - 1 && (nk_seq % TILE) != 0) || cedge || wedge;
+      int lim = nk_seq - kt * TILE;
+      if (cedge) lim = min(lim, base + r + 1);
+      const int lo = wedge ? base + r - wnd + 1 : 0;
       float pr[64];
       {
         uint32_t sr[64];
@@ -791,6 +844,30 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
         // memory that no MMA or copy uses any more (the Q tile's), so that the
         // stores cover whole rows (measured 1 % faster there; at d = 64 the
         // direct stores were faster)
+        if constexpr (F32) {
+          // float32 rows, 32 columns at a time through this warp's 4 KB of
+          // staging (the Q and dO tiles' memory); added or stored
+          const int wrow0 = qt * TILE + wq * 32;
+          float* base = static_cast<float*>(p.dq) + ((size_t)bh * p.dq_hs + wrow0) * D + hf * (D / 2);
+          const uint32_t stage = s_base + (uint32_t)(warp - 4) * (32u * 32u * 4u);
+          if (j > 0 || !p.accumulate) {
+#pragma unroll
+            for (int q4 = 0; q4 < D / 64; ++q4) {
+              uint32_t rq[32];
+              if (j > 0) {
+                tmem_ld32(tmem + lane_off + T_DQ + hf * (D / 2) + q4 * 32, rq);
+              } else {
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) rq[jj] = 0u;
+              }
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj) rq[jj] = __float_as_uint(__uint_as_float(rq[jj]) * p.scale);
+              char* dst = reinterpret_cast<char*>(base + q4 * 32);
+              if (p.accumulate) warp_store_rows<8, true>(stage, rq, dst, (size_t)D * 4, n_seq - wrow0);
+              else warp_store_rows<8>(stage, rq, dst, (size_t)D * 4, n_seq - wrow0);
+            }
+          }
+        } else {
         uint32_t w[D / 4];
 #pragma unroll
         for (int q4 = 0; q4 < D / 64; ++q4) {
@@ -808,14 +885,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
         const size_t stride = (ragged ? (size_t)p.Hq : (size_t)1) * D * sizeof(__nv_bfloat16);
         if constexpr (D == 128) {
           const int wrow0 = qt * TILE + wq * 32;   // this warp's first query row
-          const size_t qo0 = ragged ? (size_t)(tok0 + wrow0) * p.Hq + h : (size_t)bh * p.N + wrow0;
+          const size_t qo0 = ragged ? (size_t)(tok0 + wrow0) * p.Hq + h : (size_t)bh * p.dq_hs + wrow0;
           char* base = reinterpret_cast<char*>(static_cast<__nv_bfloat16*>(p.dq) + qo0 * D + hf * (D / 2));
           warp_store_rows<D / 16>(s_base + (uint32_t)(warp - 4) * (32u * D), w, base, stride, n_seq - wrow0);
         } else if (qrow < n_seq) {
-          const size_t qo = ragged ? (size_t)(tok0 + qrow) * p.Hq + h : (size_t)bh * p.N + qrow;
+          const size_t qo = ragged ? (size_t)(tok0 + qrow) * p.Hq + h : (size_t)bh * p.dq_hs + qrow;
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq) + qo * D + hf * (D / 2));
 #pragma unroll
           for (int c = 0; c < D / 16; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        }
         }
       }
     }
@@ -833,40 +911,46 @@ template <int D>
 constexpr uint32_t dkdv_smem() {
   return 2 * BwdCfg<D>::TILE_BYTES + BwdCfg<D>::NS * (2 * BwdCfg<D>::TILE_BYTES + 1024) + 1024;
 }
-template <int D>
+template <int D, bool F32>
 cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const BwdParams& p, cudaStream_t s) {
   constexpr uint32_t smem = dkdv_smem<D>();
   static_assert(smem <= 232448 - 256, "dK/dV shared memory");
-  cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static_assert(8 * 32 * 32 * 4 <= 2 * BwdCfg<D>::TILE_BYTES, "f32 epilogue staging fits in the K and V tiles");
+  cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = dkdv_grid(p);
-  dkdv_kernel<D><<<grid, BwdCfg<D>::SPLIT_THREADS, smem, s>>>(tq, tk, tv, tdo, p);
+  dkdv_kernel<D, F32><<<grid, BwdCfg<D>::SPLIT_THREADS, smem, s>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool F32>
 cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const CUtensorMap& tdo, const BwdParams& p, cudaStream_t s) {
   constexpr uint32_t smem = DqCfg<D>::SMEM;
   static_assert(smem <= 232448 - 256, "dQ shared memory");
-  cudaError_t e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static_assert(8 * 32 * 32 * 4 <= 2 * BwdCfg<D>::TILE_BYTES, "f32 epilogue staging fits in the Q and dO tiles");
+  cudaError_t e = cudaFuncSetAttribute(dq_kernel<D, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = dq_grid(p);
-  dq_kernel<D><<<grid, BwdCfg<D>::SPLIT_THREADS, smem, s>>>(tq, tk, tv, tdo, p);
+  dq_kernel<D, F32><<<grid, BwdCfg<D>::SPLIT_THREADS, smem, s>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_bwd_dkdv(int d, bool out_f32, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdParams& p, cudaStream_t s) {
-  return d == 128 ? launch_dkdv_t<128>(tq, tk, tv, tdo, p, s) : launch_dkdv_t<64>(tq, tk, tv, tdo, p, s);
+  if (d == 128)
+    return out_f32 ? launch_dkdv_t<128, true>(tq, tk, tv, tdo, p, s) : launch_dkdv_t<128, false>(tq, tk, tv, tdo, p, s);
+  return out_f32 ? launch_dkdv_t<64, true>(tq, tk, tv, tdo, p, s) : launch_dkdv_t<64, false>(tq, tk, tv, tdo, p, s);
 }
 
-cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_bwd_dq(int d, bool out_f32, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const BwdParams& p, cudaStream_t s) {
-  return d == 128 ? launch_dq_t<128>(tq, tk, tv, tdo, p, s) : launch_dq_t<64>(tq, tk, tv, tdo, p, s);
+  if (d == 128)
+    return out_f32 ? launch_dq_t<128, true>(tq, tk, tv, tdo, p, s) : launch_dq_t<128, false>(tq, tk, tv, tdo, p, s);
+  return out_f32 ? launch_dq_t<64, true>(tq, tk, tv, tdo, p, s) : launch_dq_t<64, false>(tq, tk, tv, tdo, p, s);
 }
 
 }  // namespace attn

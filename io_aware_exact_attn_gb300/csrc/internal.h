@@ -47,15 +47,21 @@ struct FwdParams {
   int32_t* tile_counts;       // per-CTA debug record (DEBUG_FIELDS int32 each), or null
 };
 
-// Backward parameter block (kernels 2 and 3 of attn_bwd).
+// Backward parameter block (kernels 2 and 3 of attn_bwd and attn_partial_bwd).
 struct BwdParams {
   const float* lse2;        // LSE * log2(e), [B*Hq][Np], +inf on padding rows
   const float* dsum;        // D = rowsum(dO*O), [B*Hq][Np], 0 on padding rows
-  int Np;                   // N rounded up to a multiple of 128
-  void* dq;                 // bf16 [B,Hq,N,d]
-  void* dk;                 // bf16 [B,Hkv,N,d]
-  void* dv;                 // bf16 [B,Hkv,N,d]
-  int B, Hq, Hkv, N;
+  int Np;                   // Nq rounded up to a multiple of 128
+  void* dq;                 // bf16 (or f32) [B,Hq,*,d], heads dq_hs rows apart
+  void* dk;                 // bf16 (or f32) [B,Hkv,*,d], heads dkv_hs rows apart
+  void* dv;                 // likewise
+  int B, Hq, Hkv;
+  int Nq, Nk;               // query rows and keys per head (both the longest
+                            // sequence for ragged batches)
+  int delta;                // q_offset - kv_offset: query i and key j are
+                            // delta + i - j positions apart
+  int64_t dq_hs, dkv_hs;    // rows between heads of dq and of dk / dv
+  int accumulate;           // f32 outputs: add into them instead of storing
   float scale;
   float scale_log2;
   int mask_kind;
@@ -89,8 +95,8 @@ inline unsigned fwd_grid(const FwdParams& p) {
          : p.cu_seqlens != nullptr ? (unsigned)(p.B * p.Hq) * (unsigned)p.varlen_nqc
                                    : (unsigned)(p.B * p.Hq) * (unsigned)p.nqc;
 }
-inline unsigned dkdv_grid(const BwdParams& p) { return (unsigned)(p.B * p.Hkv) * (unsigned)((p.N + TILE - 1) / TILE); }
-inline unsigned dq_grid(const BwdParams& p) { return (unsigned)(p.B * p.Hq) * (unsigned)((p.N + TILE - 1) / TILE); }
+inline unsigned dkdv_grid(const BwdParams& p) { return (unsigned)(p.B * p.Hkv) * (unsigned)((p.Nk + TILE - 1) / TILE); }
+inline unsigned dq_grid(const BwdParams& p) { return (unsigned)(p.B * p.Hq) * (unsigned)((p.Nq + TILE - 1) / TILE); }
 
 struct TensorMaps {
   CUtensorMap a, b, c, d;
@@ -114,18 +120,20 @@ cudaError_t launch_merge(const float* const* o_parts, const float* const* lse_pa
                          void* o_out, bool out_f32, float* lse_out, int rows_per_head, int heads,
                          int d, int64_t out_head_stride, cudaStream_t s);
 
+// Rows of head h of o / dout start at h * in_hs (in rows of d), of lse at h * in_hs.
 cudaError_t launch_bwd_preprocess(const void* o, const void* dout, const float* lse, float* dsum, float* lse2,
-                                  int64_t heads, int N, int Np, int d, cudaStream_t s);
+                                  int64_t heads, int N, int Np, int64_t in_hs, int d, cudaStream_t s);
 cudaError_t launch_varlen_pad(const int* cu_seqlens, int B, int* pcu, cudaStream_t s);
 cudaError_t launch_bwd_preprocess_varlen(const void* o, const void* dout, const float* lse, float* dsum, float* lse2,
                                          int heads, int64_t total, const int* cu_seqlens, const int* pcu, int B,
                                          int64_t padded_rows_bound, int d, cudaStream_t s);
 
-cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+// out_f32: dq / dk / dv are float32 (stored, or added with p.accumulate).
+cudaError_t launch_bwd_dkdv(int d, bool out_f32, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
                             cudaStream_t s);
 
-cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+cudaError_t launch_bwd_dq(int d, bool out_f32, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
                           cudaStream_t s);
 

@@ -116,7 +116,9 @@ __global__ void __launch_bounds__(32) varlen_pad_kernel(const int* __restrict__ 
 // kernels; groups of d/8 lanes per row, 8 bf16 per lane.  Both outputs are
 // [heads][Np] with Np = N rounded up to a whole tile; rows past N (and rows
 // whose LSE is -inf, i.e. that saw no key) get D = 0 and lse2 = +inf, which
-// makes every recomputed probability of such a row exactly 0.  Ragged
+// makes every recomputed probability of such a row exactly 0.  Head h's rows
+// of O, dO and LSE start in_hs rows apart (a chunk of a longer sequence when
+// in_hs > N).  Ragged
 // batches (RAGGED): O, dO token-major [total][heads][d], LSE [heads][total],
 // outputs [heads][pcu[B]] with sequence b's rows from pcu[b] (see above).
 template <int D, bool RAGGED>
@@ -124,7 +126,8 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
                                                          const __nv_bfloat16* __restrict__ dout,
                                                          const float* __restrict__ lse,
                                                          float* __restrict__ dsum, float* __restrict__ lse2,
-                                                         int64_t heads, int N, int Np, const int* __restrict__ cu,
+                                                         int64_t heads, int N, int Np, int64_t in_hs,
+                                                         const int* __restrict__ cu,
                                                          const int* __restrict__ pcu, int B, int64_t total) {
   constexpr int LPR = D / 8;
   constexpr int RPW = 32 / LPR;
@@ -154,7 +157,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
       lrow = head * total + t;
     } else {
       valid = prow < rows && pr < N;
-      row = head * N + pr;                        // dense row index
+      row = head * in_hs + pr;                    // dense row index
       lrow = row;
     }
     float acc = 0.f;
@@ -234,15 +237,17 @@ cudaError_t launch_merge(const float* const* o_parts, const float* const* lse_pa
 }
 
 cudaError_t launch_bwd_preprocess(const void* o, const void* dout, const float* lse, float* dsum, float* lse2,
-                                  int64_t heads, int N, int Np, int d, cudaStream_t s) {
+                                  int64_t heads, int N, int Np, int64_t in_hs, int d, cudaStream_t s) {
   const int rpw = 32 / (d / 8);
   const int grid = grid_for((heads * Np + rpw - 1) / rpw);
   const auto* po = static_cast<const __nv_bfloat16*>(o);
   const auto* pd = static_cast<const __nv_bfloat16*>(dout);
   if (d == 128)
-    preprocess_kernel<128, false><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, N, Np, nullptr, nullptr, 0, 0);
+    preprocess_kernel<128, false><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, N, Np, in_hs, nullptr, nullptr,
+                                                       0, 0);
   else
-    preprocess_kernel<64, false><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, N, Np, nullptr, nullptr, 0, 0);
+    preprocess_kernel<64, false><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, N, Np, in_hs, nullptr, nullptr,
+                                                      0, 0);
   return cudaGetLastError();
 }
 
@@ -259,9 +264,11 @@ cudaError_t launch_bwd_preprocess_varlen(const void* o, const void* dout, const 
   const auto* po = static_cast<const __nv_bfloat16*>(o);
   const auto* pd = static_cast<const __nv_bfloat16*>(dout);
   if (d == 128)
-    preprocess_kernel<128, true><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, 0, 0, cu_seqlens, pcu, B, total);
+    preprocess_kernel<128, true><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, 0, 0, 0, cu_seqlens, pcu, B,
+                                                      total);
   else
-    preprocess_kernel<64, true><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, 0, 0, cu_seqlens, pcu, B, total);
+    preprocess_kernel<64, true><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, 0, 0, 0, cu_seqlens, pcu, B,
+                                                     total);
   return cudaGetLastError();
 }
 

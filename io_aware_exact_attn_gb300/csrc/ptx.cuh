@@ -408,7 +408,18 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 // that every global store instruction covers 32 / NCHUNK whole rows of
 // contiguous bytes instead of one 16-byte piece of 32 different rows.  Rows at
 // or past `nrows` are not written.  The whole warp calls it.
-template <int NCHUNK>
+//
+// ADD_F32: the chunks are four float32 each and are added to global memory
+// (red.global.add.v4.f32, one vector reduction per chunk) instead of stored,
+// so that several launches, possibly running at the same time, can sum into
+// one float32 buffer.
+__device__ __forceinline__ void red_add_f32x4(void* p, uint4 v) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(__uint_as_float(v.x)),
+               "f"(__uint_as_float(v.y)), "f"(__uint_as_float(v.z)), "f"(__uint_as_float(v.w))
+               : "memory");
+}
+
+template <int NCHUNK, bool ADD_F32 = false>
 __device__ __forceinline__ void warp_store_rows(uint32_t stage, const uint32_t* w, char* base, size_t stride_bytes,
                                                 int nrows) {
   static_assert(NCHUNK >= 1 && NCHUNK <= 32 && (NCHUNK & (NCHUNK - 1)) == 0, "NCHUNK: a power of two up to 32");
@@ -424,7 +435,10 @@ __device__ __forceinline__ void warp_store_rows(uint32_t stage, const uint32_t* 
   for (int it = 0; it < NCHUNK; ++it) {
     const int row = it * RPI + lane / NCHUNK, c = lane % NCHUNK;
     const uint4 v = ld_shared_v4(stage + row * ROWB + ((uint32_t)(c ^ (row & (NCHUNK - 1))) << 4));
-    if (row < nrows) *reinterpret_cast<uint4*>(base + (size_t)row * stride_bytes + c * 16) = v;
+    if (row < nrows) {
+      if constexpr (ADD_F32) red_add_f32x4(base + (size_t)row * stride_bytes + c * 16, v);
+      else *reinterpret_cast<uint4*>(base + (size_t)row * stride_bytes + c * 16) = v;
+    }
   }
   __syncwarp();   // the stage may be written again
 }

@@ -65,7 +65,16 @@ def test_reference_arm_prints_one_line():
     assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
     assert d["value"] > 0 and d["higher_is_better"] is True
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["full_config_s_extrapolated"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_cpu_baseline_extrapolates_from_full_length_rows():
+    r = bench.oracle_sample(0.0, block=64)
+    assert r["sampled_rows"] == 64 and r["full_config_rows"] == 2 * 32 * 8192
+    assert abs(r["full_config_s_extrapolated"] - r["measured_sample_s"] * 2 * 32 * 8192 / 64) < 1e-9
+    f, b = bench.step_flops(bench.WORKLOAD)
+    assert abs(r["value"] - (f + b) / r["full_config_s_extrapolated"] / 1e12) < 1e-12
 
 
 def test_reference_arm_other_ranks_do_no_work():

@@ -6,7 +6,7 @@ import torch
 
 import oracle
 from io_aware_exact_attn_gb300 import api, inputs
-from _gpu_helpers import assert_grad, f64, make, mask_spec
+from _gpu_helpers import assert_grad, assert_o_lse, f64, make, mask_spec
 
 pytestmark = pytest.mark.gpu
 
@@ -85,8 +85,20 @@ def test_bwd_empty_block_row_and_column():
 
 
 def test_bwd_bert_large_shape():
-    """B=8, H=16, N=512, d=64 non-causal: full oracle over all heads."""
-    check_full(8, 16, 16, 512, 64, "none")
+    """B=8, H=16, N=512, d=64 non-causal: the forward's O and LSE and the
+    three gradients against the full oracle over all heads."""
+    B, H, N, d = 8, 16, 512, 64
+    q, k, v, do = make(B, H, H, N, d)
+    o, lse = api.attn_fwd(q, k, v)
+    dq, dk, dv = api.attn_bwd(q, k, v, o, lse, do)
+    torch.cuda.synchronize()
+    scale = 1 / np.sqrt(d)
+    o_ref, l_ref = oracle.attention_forward(f64(q), f64(k), f64(v), scale)
+    assert_o_lse(f64(o), f64(lse), o_ref, l_ref, "BERT-shaped forward")
+    gq, gk, gv = oracle.attention_backward(f64(q), f64(k), f64(v), f64(do), scale)
+    assert_grad(f64(dq), gq, "dQ BERT-shaped")
+    assert_grad(f64(dk), gk, "dK BERT-shaped")
+    assert_grad(f64(dv), gv, "dV BERT-shaped")
 
 
 def test_bwd_is_deterministic():

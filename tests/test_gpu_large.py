@@ -77,7 +77,7 @@ def test_gpt_causal_peaked_full_size():
 
 
 def test_gpt_noncausal_full_size():
-    check_sampled(inputs.WORKLOADS["gpt_noncausal"], n_kv_heads_full=0)
+    check_sampled(inputs.WORKLOADS["gpt_noncausal"], n_kv_heads_full=1)
 
 
 def test_gpt_sliding_window_full_size():
@@ -125,14 +125,36 @@ def test_chunked_gqa_full_size():
     o_gpu = np.stack([f64(o[b, h, rows]) for b, h in heads])
     l_gpu = np.stack([f64(lse[b, h, rows]) for b, h in heads])
     assert_o_lse(o_gpu, l_gpu, o_ref, l_ref, "chunked")
-    # backward on the merged result: dQ rows against the oracle
-    dq, dk, dv = api.attn_bwd(q, k, v, o, lse, do, causal=True)
+    # chunked backward on the merged result: one preprocess per query chunk,
+    # the 36 pairs in the load-balanced order on two streams, into float32
+    dq, dk, dv = api.chunked_bwd(q, k, v, o, lse, do, w.chunks, n_streams=2)
+    dq_m, dk_m, dv_m = api.attn_bwd(q, k, v, o, lse, do, causal=True)
     torch.cuda.synchronize()
+    for name, got, want in (("dQ", dq, dq_m), ("dK", dk, dk_m), ("dV", dv, dv_m)):
+        err = float((got - want.float()).abs().max() / want.float().abs().max())
+        assert err <= 3e-2, f"chunked {name} vs monolithic: {err:.3e}"
+    del dq_m, dk_m, dv_m
+    # dQ rows against the oracle
     for b, h in heads[:2]:
         ref = oracle.attention_backward_dq_rows(qf, kf, vf, dof, scale, b, h, rows[:64], oracle.MaskSpec("causal"))
-        assert_grad(f64(dq[b, h, rows[:64]]), ref, f"dQ rows chunked ({b},{h})")
-    # GQA property at full size: dK/dV equal repeated-KV MHA gradients summed per group
+        assert_grad(f64(dq[b, h, rows[:64]]), ref, f"chunked dQ rows ({b},{h})")
+    # dK / dV of the last two key tiles of one kv head: under the causal mask
+    # only the last 256 query rows see them, and those rows' merged LSE and
+    # D come from the oracle's own forward of those rows over all keys
     g = w.Hq // w.Hkv
+    last = np.arange(w.N - 256, w.N)
+    grp = [(0, hk * g + j) for j in range(g)]
+    o_r, l_r = oracle.attention_forward(qf, kf, vf, scale, oracle.MaskSpec("causal"), heads=grp, rows=last)
+    hq = [h for _, h in grp]
+    dsum = (dof[0][hq][:, last] * o_r).sum(-1)
+    _, dk_ref, dv_ref = oracle.partial_backward(qf[:, hq][:, :, last], kf[:, hk:hk + 1, last], vf[:, hk:hk + 1, last],
+                                                dof[:, hq][:, :, last], l_r[None], dsum[None], scale,
+                                                oracle.MaskSpec("causal"), w.N - 256, w.N - 256)
+    assert_grad(f64(dk[0, hk, last]), dk_ref[0, 0], f"chunked dK last key tiles (kv head {hk})")
+    assert_grad(f64(dv[0, hk, last]), dv_ref[0, 0], f"chunked dV last key tiles (kv head {hk})")
+    del dq, dk, dv
+    # GQA property at full size: dK/dV equal repeated-KV MHA gradients summed per group
+    dq, dk, dv = api.attn_bwd(q, k, v, o, lse, do, causal=True)
     kr, vr = k.repeat_interleave(g, dim=1).contiguous(), v.repeat_interleave(g, dim=1).contiguous()
     o_r, l_r = api.attn_fwd(q, kr, vr, causal=True)
     dq_r, dk_r, dv_r = api.attn_bwd(q, kr, vr, o_r, l_r, do, causal=True)

@@ -84,6 +84,28 @@ def test_argument_validation_without_gpu(lib):
     assert need == ((2 * 2 * 4 * 128 * 4 + 255) // 256) * 256
     p = [_ptr(good)] * 10
     assert lib.attn_bwd(*p, need - 256, 2, 4, 2, 100, 64, 0.125, None, None) == -6
+    # chunked backward: workspace, pointer, offset and size checks come before any device call
+    ws = lib.attn_bwd_workspace_bytes(1, 4, 4, 300, 128)
+    assert lib.attn_bwd_preprocess(_ptr(good), _ptr(good), _ptr(good), 1, 4, 300, 128, 0, _ptr(good), ws - 1,
+                                   None) == -6
+    assert lib.attn_bwd_preprocess(_ptr(good), _ptr(good), _ptr(good), 1, 4, 300, 128, 299, _ptr(good), ws,
+                                   None) == -1                                           # head stride < Nq
+    assert lib.attn_bwd_preprocess(_ptr(good), _ptr(good), _ptr(good + 2), 1, 4, 300, 128, 0, _ptr(good), ws,
+                                   None) == -3
+    pb = [_ptr(good)] * 4
+    out = [_ptr(good)] * 3
+    assert lib.attn_partial_bwd(*pb, _ptr(good), ws - 1, *out, 1, 4, 2, 300, 200, 128, 0.088, None, 0, 0, 0, 0, 1,
+                                None) == -6
+    assert lib.attn_partial_bwd(*pb, _ptr(good), ws, _ptr(good), None, _ptr(good), 1, 4, 2, 300, 200, 128, 0.088,
+                                None, 0, 0, 0, 0, 1, None) == -1                         # dk missing
+    assert lib.attn_partial_bwd(*pb, _ptr(good), ws, *out, 1, 4, 2, 300, 200, 128, 0.088, None, 1 << 31, 0, 0, 0,
+                                1, None) == -1                                           # offsets too far apart
+    assert lib.attn_partial_bwd(*pb, _ptr(good), ws, *out, 1, 4, 2, 300, 200, 128, 0.088, None, -1, 0, 0, 0, 1,
+                                None) == -1                                              # negative position
+    assert lib.attn_partial_bwd(*pb, _ptr(good), ws, *out, 1, 4, 2, 300, 200, 128, 0.088, None, 0, 0, 299, 0, 1,
+                                None) == -1                                              # q head stride < Nq
+    assert lib.attn_partial_bwd(*pb, _ptr(good), ws, *out, 1, 4, 3, 300, 200, 128, 0.088, None, 0, 0, 0, 0, 1,
+                                None) == -1                                              # Hq % Hkv
     # sliding window needs a width of at least one
     no_width = _ffi.attn_mask_t(3, 0, None, 0)
     assert lib.attn_fwd(_ptr(good), _ptr(good), _ptr(good), _ptr(good), None, 1, 2, 2, 128, 64, 0.125,

@@ -1,8 +1,11 @@
 """attn_bwd_static_scratch: the backward pass for callers that cannot allocate
 device memory (for example code that runs under an allocator or runtime that
 owns every device allocation, or a process whose memory was reserved up
-front).  It must give the same dQ, dK and dV as attn_bwd, including when it is
-called twice in a row and the second call reuses the one static scratch area.
+front).  It runs the same kernels as attn_bwd on the same inputs, so it must
+give bit-identical dQ, dK and dV, including when it is called twice in a row
+and the second call reuses the one static scratch area; a wait that runs out
+in it would show in attn_get_status, which reads the one status word every
+entry point reports to.
 
 This file is collected last on purpose, so that a run that stops at the first
 failure has already run every other test."""
@@ -41,5 +44,6 @@ def test_static_scratch_backward_matches_attn_bwd(cuda_lib):
         assert rc == 0, lib.attn_last_error_message()
         torch.cuda.synchronize()
         for name, got, want in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+            assert torch.equal(got, want), f"{name} B{B} H{Hq}/{Hkv} N{N} d{d}"
             assert_grad(f64(got), f64(want), f"{name} B{B} H{Hq}/{Hkv} N{N} d{d}")
-    assert api.get_status() == 0
+        assert api.get_status() == 0
