@@ -50,6 +50,7 @@ from .fp8 import (  # noqa: F401
     fp8_row_error_bound,
 )
 from .schedule import (  # noqa: F401
+    chunk_pair_lanes,
     chunk_pair_schedule,
     fwd_work_units,
     kv_tile_range_causal,

@@ -109,20 +109,37 @@ def fwd_work_units(kind: str, B: int, Hq: int, nq: int, nk: int,
     return out
 
 
-def chunk_pair_schedule(n_chunks: int, n_lanes: int = 0):
-    """Load-balanced order of the causal (q-chunk, kv-chunk) pairs."""
+def pair_cost(p) -> int:
+    """Half-tile-squares of work of a causal chunk pair: 2 off the diagonal, 1 on it."""
+    return 1 if p[0] == p[1] else 2
+
+
+def chunk_pair_lanes(n_chunks: int, n_lanes: int = 0):
+    """The causal (q-chunk, kv-chunk) pairs dealt to ``n_lanes`` virtual lanes
+    (``n_chunks`` when ``n_lanes <= 0``): pairs sorted by (cost desc, q-chunk
+    desc, kv-chunk asc), each to the least-loaded lane, lowest lane on ties.
+    Returns one list of pairs per lane, in the order each lane received them."""
     if n_chunks <= 0:
         return []
     lanes = n_lanes if n_lanes > 0 else n_chunks
     pairs = [(qc, kc) for qc in range(n_chunks) for kc in range(qc + 1)]
-    cost = {p: (1 if p[0] == p[1] else 2) for p in pairs}
-    pairs.sort(key=lambda p: (-cost[p], -p[0], p[1]))
+    pairs.sort(key=lambda p: (-pair_cost(p), -p[0], p[1]))
     load = [0] * lanes
     per_lane = [[] for _ in range(lanes)]
     for p in pairs:
         best = min(range(lanes), key=lambda l: (load[l], l))
-        load[best] += cost[p]
+        load[best] += pair_cost(p)
         per_lane[best].append(p)
+    return per_lane
+
+
+def chunk_pair_schedule(n_chunks: int, n_lanes: int = 0):
+    """Load-balanced order of the causal (q-chunk, kv-chunk) pairs: the lanes
+    of ``chunk_pair_lanes`` emitted round-robin by position."""
+    per_lane = chunk_pair_lanes(n_chunks, n_lanes)
+    if not per_lane:
+        return []
+    lanes = len(per_lane)
     out = []
     depth = max(len(x) for x in per_lane)
     for pos in range(depth):

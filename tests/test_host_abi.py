@@ -162,13 +162,19 @@ def test_chunk_schedule_matches_oracle(lib, n, lanes):
 
 
 def test_chunk_schedule_balance():
-    """Costs add up to n^2 half-tiles and each lane's share (positions l, l+L, ...
-    in the interleaved order while lanes stay full) is within one pair of the mean."""
-    for n in (4, 8, 16):
-        pairs = oracle.chunk_pair_schedule(n)
-        total = sum(1 if q == k else 2 for q, k in pairs)
-        assert total == n * n
-        assert len(pairs) == n * (n + 1) // 2
+    """Costs add up to n^2 half-tiles, and each lane's load is within one pair
+    (cost 2) of the mean load."""
+    for n in (3, 4, 8, 16, 32):
+        for lanes in (n, 3, 8):
+            per = oracle.chunk_pair_lanes(n, lanes)
+            pairs = oracle.chunk_pair_schedule(n, lanes)
+            total = sum(1 if q == k else 2 for q, k in pairs)
+            assert total == n * n
+            assert len(pairs) == n * (n + 1) // 2
+            assert sorted(p for lane in per for p in lane) == sorted(pairs)
+            loads = [sum(1 if q == k else 2 for q, k in lane) for lane in per]
+            mean = n * n / lanes
+            assert all(abs(x - mean) <= 2 for x in loads), (n, lanes, loads)
 
 
 CASES = [

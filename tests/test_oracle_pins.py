@@ -136,6 +136,19 @@ def _mask_from(g, n):
 def test_golden(path):
     g = json.load(open(path))
     assert g["source"]
+    if g.get("kind") == "chunk_schedule":
+        for c in g["cases"]:
+            got = oracle.chunk_pair_schedule(c["n_chunks"], c["n_lanes"])
+            assert got == [tuple(p) for p in c["order"]], c
+            loads = [sum(1 if q == k else 2 for q, k in lane)
+                     for lane in oracle.chunk_pair_lanes(c["n_chunks"], c["n_lanes"])]
+            assert loads == c["lane_loads"], c
+        return
+    if g.get("kind") == "fwd_units":
+        for c in g["cases"]:
+            got = oracle.fwd_work_units(c["mask"], c["B"], c["Hq"], c["N"], c["N"], Hkv=c["Hkv"], d=c["d"])
+            assert got == [tuple(u) for u in c["units"]], c
+        return
     if "o_parts" in g:
         o, lse = oracle.merge_partials([np.array(x) for x in g["o_parts"]],
                                        [np.array(x) for x in g["lse_parts"]])
@@ -806,6 +819,53 @@ def test_planted_mistakes(monkeypatch):
     monkeypatch.setattr(oa, "merge_partials", merge_no_weights)
     monkeypatch.setattr(oracle, "merge_partials", merge_no_weights)
     assert _fails(test_chunked_merge_equals_monolithic)
+
+    from oracle import schedule as osch
+    good_lanes = osch.chunk_pair_lanes
+    sched_golden = os.path.join(HERE, "golden", "chunk_schedule_hand_worked.json")
+    units_golden = os.path.join(HERE, "golden", "fwd_units_hand_worked.json")
+
+    def lanes_ties_to_highest(n_chunks, n_lanes=0):        # ties broken toward the highest lane
+        lanes = n_lanes if n_lanes > 0 else n_chunks
+        pairs = sorted(((q, k) for q in range(n_chunks) for k in range(q + 1)),
+                       key=lambda p: (-osch.pair_cost(p), -p[0], p[1]))
+        load, per = [0] * lanes, [[] for _ in range(lanes)]
+        for p in pairs:
+            best = min(range(lanes), key=lambda l: (load[l], -l))
+            load[best] += osch.pair_cost(p)
+            per[best].append(p)
+        return per
+
+    def lanes_qc_ascending(n_chunks, n_lanes=0):           # lighter query chunks first
+        lanes = n_lanes if n_lanes > 0 else n_chunks
+        pairs = sorted(((q, k) for q in range(n_chunks) for k in range(q + 1)),
+                       key=lambda p: (-osch.pair_cost(p), p[0], p[1]))
+        load, per = [0] * lanes, [[] for _ in range(lanes)]
+        for p in pairs:
+            best = min(range(lanes), key=lambda l: (load[l], l))
+            load[best] += osch.pair_cost(p)
+            per[best].append(p)
+        return per
+
+    for bad in (lanes_ties_to_highest, lanes_qc_ascending):
+        monkeypatch.setattr(osch, "chunk_pair_lanes", bad)
+        assert _fails(lambda: test_golden(sched_golden)), bad.__name__
+        monkeypatch.setattr(osch, "chunk_pair_lanes", good_lanes)
+
+    good_units = osch.fwd_work_units
+
+    def units_chunks_ascending(kind, B, Hq, nq, nk, *a, **kw):   # light chunks first
+        u = good_units(kind, B, Hq, nq, nk, *a, **kw)
+        return sorted(u, key=lambda x: (x[1], x[0]))
+
+    def units_heads_outer(kind, B, Hq, nq, nk, *a, **kw):        # head-major, not chunk-major in a group
+        u = good_units(kind, B, Hq, nq, nk, *a, **kw)
+        return sorted(u, key=lambda x: (x[0], -x[1]))
+
+    for bad in (units_chunks_ascending, units_heads_outer):
+        monkeypatch.setattr(oracle, "fwd_work_units", bad)
+        assert _fails(lambda: test_golden(units_golden)), bad.__name__
+        monkeypatch.setattr(oracle, "fwd_work_units", good_units)
 
     good_pb = oa.partial_backward
 
