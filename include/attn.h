@@ -275,9 +275,9 @@ size_t attn_varlen_bwd_workspace_bytes(int B, int64_t total, int Hq);
  *   O = softmax(scale * (q_descale Q8)(k_descale K8)^T) (v_descale V8)
  * with the mask of attn_fwd; O is bf16, LSE natural-log f32 as in attn_fwd.
  * The probabilities enter the second product as e4m3 (relative rounding
- * 2^-4 for weights above 2^-13 of the row max, absolute 2^-17 of it below),
- * so |O - O_exact| <= max|v| (2^-4 + 2^-17 n_small / sum of the relative
- * weights) plus the bf16 rounding of O, max|v| over the row's visible values;
+ * 2^-4 for weights w_j >= 2^-13 of the row max, absolute 2^-17 of it below),
+ * so element by element |O_id - O_exact_id| <= sum_j e_j |v_jd| / sum_j w_j
+ * with e_j = 2^-4 w_j (or 2^-17 below 2^-13), plus the bf16 rounding of O;
  * the row sums and the LSE stay fp32.
  *   q8          device e4m3 [B, Hq,  N, 128]   k8, v8 device e4m3 [B, Hkv, N, 128]
  *   o           device bf16 [B, Hq,  N, 128]   (written)

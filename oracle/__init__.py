@@ -47,7 +47,7 @@ from .fp8 import (  # noqa: F401
     E4M3_MAX,
     e4m3_decode,
     fp8_forward,
-    fp8_row_error_bound,
+    fp8_error_model,
 )
 from .schedule import (  # noqa: F401
     chunk_pair_lanes,

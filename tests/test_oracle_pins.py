@@ -659,8 +659,9 @@ def test_fp8_forward_q_zero_gives_mean_of_visible_values():
 
 
 def _simulated_rounding_error(q8, k8, v8, qd, kd, vd, scale, t):
-    """max_d |O_sim - O_exact| per row, O_sim from weights w * 2^t rounded to
-    E4M3 by torch (round to nearest), normalised by the exact sum."""
+    """O_sim - O_exact per element ([rows, d]) for one head: O_sim from the
+    weights w * 2^t rounded to E4M3 by torch (round to nearest), normalised by
+    the exact sum of the unrounded weights."""
     q = qd * oracle.e4m3_decode(q8)[0, 0]
     k = kd * oracle.e4m3_decode(k8)[0, 0]
     v = vd * oracle.e4m3_decode(v8)[0, 0]
@@ -669,24 +670,65 @@ def _simulated_rounding_error(q8, k8, v8, qd, kd, vd, scale, t):
     p = torch.from_numpy(w * 2.0 ** t).to(torch.float8_e4m3fn).to(torch.float64).numpy()
     o_sim = (p @ v) / (w * 2.0 ** t).sum(axis=1, keepdims=True)
     o_ex = (w @ v) / w.sum(axis=1, keepdims=True)
-    return np.abs(o_sim - o_ex).max(axis=1)
+    return o_sim - o_ex
 
 
-def test_fp8_row_error_bound_holds_for_simulated_rounding():
+def test_fp8_error_bound_holds_for_simulated_rounding():
     rng = np.random.default_rng(13)
     for n, krange in ((40, 60.0), (300, 200.0)):
         q8, k8, v8 = _codes(1, 1, n, 8, rng=rng), _codes(1, 1, n, 8, rng=rng, lo=-krange, hi=krange), \
             _codes(1, 1, n, 8, rng=rng)
-        bound = oracle.fp8_row_error_bound(q8, k8, v8, 0.01, 0.01, 0.02, 0.3)[0, 0]
+        bound, _ = oracle.fp8_error_model(q8, k8, v8, 0.01, 0.01, 0.02, 0.3)
+        for t in (7.0, 7.25, 7.5, 7.75, 8.0):
+            err = np.abs(_simulated_rounding_error(q8, k8, v8, 0.01, 0.01, 0.02, 0.3, t))
+            assert np.all(err <= bound[0, 0]), (n, t)
+
+
+def test_fp8_error_bound_is_nearly_reached():
+    """Two keys: one at the row max with v = 0, one whose weight 2^7 w lands
+    just above the midpoint 1 + 2^-4 of two E4M3 neighbours, so it rounds down
+    by almost 2^-4 of itself (1 - 2^-8 from 17 - 2^-8 to 16): the error is
+    16 (1 - 2^-8) / (17 - 2^-8) = 0.938 of the bound."""
+    q8 = np.full((1, 1, 1, 1), 0x38, np.uint8)              # q = 1
+    k8 = np.array([0x00, 0xB8], np.uint8).reshape(1, 1, 2, 1)   # scores 0 and -scale
+    v8 = np.array([0x00, 0x38], np.uint8).reshape(1, 1, 2, 1)   # v = 0 and 1
+    w2 = (1.0 + 2.0 ** -4 - 2.0 ** -12) * 2.0 ** -3          # P = 2^7 w2 = 16 (1 + 2^-4 - 2^-12)
+    scale = -np.log(w2)
+    err = abs(_simulated_rounding_error(q8, k8, v8, 1.0, 1.0, 1.0, scale, 7.0)[0, 0])
+    bound, _ = oracle.fp8_error_model(q8, k8, v8, 1.0, 1.0, 1.0, scale)
+    assert err <= bound[0, 0, 0, 0] and err >= 0.93 * bound[0, 0, 0, 0], (err, bound[0, 0, 0, 0])
+
+
+def test_fp8_expected_squared_error_brackets_simulated_rounding():
+    """Over many elements the mean squared rounding error lies between a
+    quarter of the model's upper estimate (grid steps half as large) and the
+    estimate itself, for every offset t in [7, 8]."""
+    rng = np.random.default_rng(17)
+    n = 400
+    q8, k8, v8 = _codes(1, 1, n, 16, rng=rng), _codes(1, 1, n, 16, rng=rng, lo=-100.0, hi=100.0), \
+        _codes(1, 1, n, 16, rng=rng)
+    for mask in (MaskSpec("none"), MaskSpec("causal")):
+        _, msq = oracle.fp8_error_model(q8, k8, v8, 0.01, 0.01, 0.02, 0.3, mask)
         for t in (7.0, 7.5, 8.0):
-            err = _simulated_rounding_error(q8, k8, v8, 0.01, 0.01, 0.02, 0.3, t)
-            assert np.all(err <= bound), (n, t)
+            if mask.kind == "causal":
+                q = 0.01 * oracle.e4m3_decode(q8)[0, 0]
+                k = 0.01 * oracle.e4m3_decode(k8)[0, 0]
+                v = 0.02 * oracle.e4m3_decode(v8)[0, 0]
+                s = np.where(np.tril(np.ones((n, n), bool)), 0.3 * q @ k.T, -np.inf)
+                w = np.exp(s - s.max(axis=1, keepdims=True))
+                p = torch.from_numpy(w * 2.0 ** t).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+                err = (p @ v) / (w * 2.0 ** t).sum(1, keepdims=True) - (w @ v) / w.sum(1, keepdims=True)
+            else:
+                err = _simulated_rounding_error(q8, k8, v8, 0.01, 0.01, 0.02, 0.3, t)
+            m_sim, m_mod = float((err ** 2).mean()), float(msq.mean())
+            assert m_mod / 8 <= m_sim <= 1.25 * m_mod, (mask.kind, t, m_sim, m_mod)
 
 
-def test_fp8_row_error_bound_subnormal_term():
+def test_fp8_error_bound_subnormal_term():
     """One key at the row max and 16384 keys whose weights (2.45 * 2^-16 of it)
     land on the subnormal grid at t = 7, all rounded the same way: the error
-    exceeds 2^-4 max|v| and the bound still covers it."""
+    exceeds the 2^-4 relative term (0 here: the only normal weight meets
+    v = 0) and the bound still covers it."""
     n = 16384
     q8 = np.full((1, 1, 1, 1), 0x38, np.uint8)               # q = 1
     k8 = np.full((1, 1, n + 1, 1), 0xB8, np.uint8)           # k = -1 ...
@@ -694,10 +736,10 @@ def test_fp8_row_error_bound_subnormal_term():
     v8 = np.full((1, 1, n + 1, 1), 0x38, np.uint8)           # v = 1 ...
     v8[0, 0, 0, 0] = 0x00                                    # ... but 0 for the max key
     scale = -np.log(2.45 * 2.0 ** -16)
-    err = _simulated_rounding_error(q8, k8, v8, 1.0, 1.0, 1.0, scale, 7.0)[0]
-    bound = oracle.fp8_row_error_bound(q8, k8, v8, 1.0, 1.0, 1.0, scale)[0, 0, 0]
+    err = abs(_simulated_rounding_error(q8, k8, v8, 1.0, 1.0, 1.0, scale, 7.0)[0, 0])
+    bound, _ = oracle.fp8_error_model(q8, k8, v8, 1.0, 1.0, 1.0, scale)
     assert err > 2.0 ** -4
-    assert err <= bound
+    assert err <= bound[0, 0, 0, 0]
 
 
 # ---------------------------------------------------------------- planted mistakes
@@ -800,21 +842,35 @@ def test_planted_mistakes(monkeypatch):
     assert _fails(test_fp8_forward_descale_invariances)
     monkeypatch.setattr(oracle, "fp8_forward", good_fp8)
 
-    def bound_normal_only(q8, k8, v8, qd, kd, vd, scale, mask=MaskSpec(), heads=None, rows=None):
-        q = qd * of.e4m3_decode(q8)
-        k = kd * of.e4m3_decode(k8)
-        v = vd * of.e4m3_decode(v8)
-        out = np.zeros(q.shape[:3])
-        for b in range(q.shape[0]):
-            for h in range(q.shape[1]):
-                vis = oracle.visible(np.arange(q.shape[2]), k.shape[2], mask)
-                vmax = np.where(vis, np.abs(v[b, h // (q.shape[1] // k.shape[1])]).max(axis=1)[None, :], 0).max(1)
-                out[b, h] = vmax * 2.0 ** -4
-        return out
+    good_model = of.fp8_error_model
 
-    monkeypatch.setattr(oracle, "fp8_row_error_bound", bound_normal_only)
-    assert _fails(test_fp8_row_error_bound_subnormal_term)
-    monkeypatch.setattr(oracle, "fp8_row_error_bound", of.fp8_row_error_bound)
+    def model_normal_only(*a, **kw):                     # subnormal term dropped
+        q8, k8, v8, qd, kd, vd, scale = a[:7]
+        mask = a[7] if len(a) > 7 else kw.get("mask", MaskSpec())
+        q = qd * of.e4m3_decode(q8)[0, 0]
+        k = kd * of.e4m3_decode(k8)[0, 0]
+        v = vd * of.e4m3_decode(v8)[0, 0]
+        vis = oracle.visible(np.arange(q.shape[0]), k.shape[0], mask)
+        s = np.where(vis, scale * q @ k.T, -np.inf)
+        w = np.exp(s - s.max(axis=1, keepdims=True))
+        b = (2.0 ** -4 * w) @ np.abs(v) / w.sum(1, keepdims=True)
+        return b[None, None], good_model(*a, **kw)[1]
+
+    def model_half_relative(*a, **kw):                   # 2^-5 instead of 2^-4
+        b, m = good_model(*a, **kw)
+        return 0.5 * b, m
+
+    def model_step_too_small(*a, **kw):                  # expected error from half the grid step
+        b, m = good_model(*a, **kw)
+        return b, m / 4
+
+    monkeypatch.setattr(oracle, "fp8_error_model", model_normal_only)
+    assert _fails(test_fp8_error_bound_subnormal_term)
+    monkeypatch.setattr(oracle, "fp8_error_model", model_half_relative)
+    assert _fails(test_fp8_error_bound_is_nearly_reached)
+    monkeypatch.setattr(oracle, "fp8_error_model", model_step_too_small)
+    assert _fails(test_fp8_expected_squared_error_brackets_simulated_rounding)
+    monkeypatch.setattr(oracle, "fp8_error_model", good_model)
 
     monkeypatch.setattr(oa, "merge_partials", merge_no_weights)
     monkeypatch.setattr(oracle, "merge_partials", merge_no_weights)
