@@ -28,8 +28,10 @@
  *     capture).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
  *     launches are asynchronous on it.  The return value reports host-side
- *     validation and launch errors only; errors seen by a kernel (a bounded
- *     wait that ran out) are read back with attn_get_status().
+ *     validation and launch errors only; errors seen by a kernel are read back
+ *     with attn_get_status(): a bounded wait that ran out, or a device-side
+ *     index array the host cannot check (cu_seqlens, seq_lens) holding an
+ *     entry out of range.
  *   - A query row that sees no key gets O = 0 and LSE = -inf.
  *   - Return codes are attn_status_t values; on error a message is available
  *     from attn_last_error_message() (thread-local) and nothing was launched.
@@ -52,7 +54,8 @@ typedef enum {
   ATTN_ERR_CUDA = -4,           /* a CUDA runtime/driver call failed */
   ATTN_ERR_DEVICE_TIMEOUT = -5, /* a kernel's bounded wait ran out (device-side) */
   ATTN_ERR_WORKSPACE = -6,      /* workspace too small */
-  ATTN_ERR_NO_DEVICE = -7       /* no usable sm_103 device */
+  ATTN_ERR_NO_DEVICE = -7,      /* no usable sm_103 device */
+  ATTN_ERR_DEVICE_BOUNDS = -8   /* a device-side index array was out of range (device-side) */
 } attn_status_t;
 
 typedef enum {
@@ -398,9 +401,13 @@ int attn_build_chunk_schedule(int n_chunks, int n_lanes, int32_t* pairs_out,
 
 /*
  * attn_get_status -- synchronises `stream`, then reads and clears the current
- * device's status word.  Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT if a
- * kernel's bounded wait ran out since the last call, or ATTN_ERR_CUDA if the
- * synchronisation itself failed.
+ * device's status word.  Returns ATTN_OK; ATTN_ERR_DEVICE_BOUNDS if, since the
+ * last call, a kernel met a malformed device-side index array (a sequence of
+ * cu_seqlens with cu[b] < 0, cu[b+1] < cu[b], cu[b+1] > total or more than
+ * max_len tokens: that sequence was skipped, its outputs left unwritten; a
+ * seq_lens entry outside [0, Nk]: clamped into the cache); otherwise
+ * ATTN_ERR_DEVICE_TIMEOUT if a kernel's bounded wait ran out; ATTN_ERR_CUDA if
+ * the synchronisation itself failed.
  */
 int attn_get_status(void* stream);
 

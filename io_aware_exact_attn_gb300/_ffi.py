@@ -32,7 +32,7 @@ MASK_NONE, MASK_CAUSAL, MASK_BLOCK_SPARSE, MASK_SLIDING_WINDOW = 0, 1, 2, 3
 DTYPE_BF16, DTYPE_F32 = 0, 1
 STATUS = {0: "ATTN_OK", -1: "ATTN_ERR_INVALID_ARG", -2: "ATTN_ERR_UNSUPPORTED", -3: "ATTN_ERR_MISALIGNED",
           -4: "ATTN_ERR_CUDA", -5: "ATTN_ERR_DEVICE_TIMEOUT", -6: "ATTN_ERR_WORKSPACE",
-          -7: "ATTN_ERR_NO_DEVICE"}
+          -7: "ATTN_ERR_NO_DEVICE", -8: "ATTN_ERR_DEVICE_BOUNDS"}
 
 # name -> (restype, argtypes); the full exported surface of attn.h
 SIGNATURES = {

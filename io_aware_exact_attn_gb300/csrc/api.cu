@@ -237,6 +237,7 @@ const char* attn_status_string(int s) {
     case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait ran out";
     case ATTN_ERR_WORKSPACE: return "workspace too small";
     case ATTN_ERR_NO_DEVICE: return "no usable sm_103 device";
+    case ATTN_ERR_DEVICE_BOUNDS: return "a device-side index array was out of range";
     default: return "unknown status";
   }
 }
@@ -373,6 +374,7 @@ int attn_varlen_fwd(const void* q, const void* k, const void* v, void* o, float*
   p.dec_nq = 1;
   p.cu_seqlens = cu_seqlens;
   p.varlen_nqc = p.nqc;
+  p.total = total;
   p.status = status;
   p.wait_limit_ns = wait_limit();
   if ((rc = debug_records(0, fwd_grid(p), &p.tile_counts))) return rc;
@@ -797,9 +799,9 @@ int attn_varlen_bwd(const void* q, const void* k, const void* v, const void* o, 
   cudaError_t e;
   {
     TraceScope ts(ATTN_KERNEL_BWD_PREPROCESS, s);
-    e = launch_varlen_pad(cu_seqlens, B, pcu, s);
+    e = launch_varlen_pad(cu_seqlens, B, total, max_len, pcu, status, s);
     if (e == cudaSuccess)
-      e = launch_bwd_preprocess_varlen(o, dout, lse, dsum, lse2, Hq, total, cu_seqlens, pcu, B, bound, d, s);
+      e = launch_bwd_preprocess_varlen(o, dout, lse, dsum, lse2, Hq, total, cu_seqlens, pcu, B, max_len, bound, d, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "ragged backward preprocess launch");
   BwdParams p{};
@@ -814,6 +816,7 @@ int attn_varlen_bwd(const void* q, const void* k, const void* v, const void* o, 
   p.nkb = (int)cdiv(max_len, TILE);
   p.cu_seqlens = cu_seqlens;
   p.pcu = pcu;
+  p.total = total;
   p.kv_group = 1;
   p.q_group = 1;
   p.status = status;
@@ -917,6 +920,9 @@ int attn_get_status(void* stream) {
     if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    if (h & ATTN_DEV_BOUNDS)
+      return fail(ATTN_ERR_DEVICE_BOUNDS, "a device-side index array was out of range; the affected sequences were "
+                                          "skipped (status 0x%x)", h);
     return fail(ATTN_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out (status 0x%x)", h);
   }
   return ATTN_OK;

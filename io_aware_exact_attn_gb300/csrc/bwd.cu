@@ -144,6 +144,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
   // the unit's sequence: its first token's row in the maps, its keys and
   // query rows, and where its rows start in lse2 / dsum (head 0) and between
   // query heads
+  if (ragged && !seq_range_ok(p.cu_seqlens, b, p.total, p.Nq)) {   // malformed: skipped and reported
+    if (threadIdx.x == 0) atomicOr(p.status, ATTN_DEV_BOUNDS);
+    return;
+  }
   const int tok0 = ragged ? p.cu_seqlens[b] : 0;    // packed tensors hold fewer than 2^31 tokens
   const int n_seq = ragged ? p.cu_seqlens[b + 1] - tok0 : p.Nk;
   const int nq_seq = ragged ? n_seq : p.Nq;
@@ -567,6 +571,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
   const int qt = nqt_all - 1 - qpos;  // latest query tile first: heaviest under a causal mask
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int bkv = b * p.Hkv + h / (p.Hq / p.Hkv);
+  if (ragged && !seq_range_ok(p.cu_seqlens, b, p.total, p.Nq)) {   // malformed: skipped and reported
+    if (threadIdx.x == 0) atomicOr(p.status, ATTN_DEV_BOUNDS);
+    return;
+  }
   const int tok0 = ragged ? p.cu_seqlens[b] : 0;    // packed tensors hold fewer than 2^31 tokens
   const int n_seq = ragged ? p.cu_seqlens[b + 1] - tok0 : p.Nq;   // query rows of the unit's sequence
   const int nk_seq = ragged ? n_seq : p.Nk;                       // and its keys

@@ -9,6 +9,10 @@
 namespace attn {
 
 constexpr int TILE = 128;       // query-tile rows, key-tile rows, block-mask granularity
+
+// Bits of the device status word (attn_get_status maps them to error codes).
+constexpr unsigned int ATTN_DEV_TIMEOUT = 1u;   // a bounded wait ran out
+constexpr unsigned int ATTN_DEV_BOUNDS = 2u;    // a device-side index array (cu_seqlens, seq_lens) was out of range
 constexpr int UNIT_ROWS = 256;  // query rows per forward work unit (two query tiles)
 
 enum MaskKind : int { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_BLOCK_SPARSE = 2, MASK_SLIDING_WINDOW = 3 };
@@ -39,6 +43,7 @@ struct FwdParams {
   // [total, heads, d]; sequence b holds tokens [cu_seqlens[b], cu_seqlens[b+1])
   const int* cu_seqlens;      // device [B + 1]
   int varlen_nqc;             // 256-row chunks of the longest sequence
+  int64_t total;              // tokens in the packed tensors
   // output element strides: O[head h, row r] at h * o_hs + r * o_rs (plus the
   // split offset when decoding), LSE at h * l_hs + r * l_rs
   int64_t o_hs, o_rs, l_hs, l_rs;
@@ -75,6 +80,7 @@ struct BwdParams {
   // sequence b start at h * pcu[B] + pcu[b] (sequences padded to whole tiles)
   const int* cu_seqlens;
   const int* pcu;
+  int64_t total;            // tokens in the packed tensors
   int kv_group;             // kv heads per L2 group of the dK/dV kernel
   int q_group;              // query heads per L2 group of the dQ kernel
   unsigned int* status;
@@ -123,10 +129,13 @@ cudaError_t launch_merge(const float* const* o_parts, const float* const* lse_pa
 // Rows of head h of o / dout start at h * in_hs (in rows of d), of lse at h * in_hs.
 cudaError_t launch_bwd_preprocess(const void* o, const void* dout, const float* lse, float* dsum, float* lse2,
                                   int64_t heads, int N, int Np, int64_t in_hs, int d, cudaStream_t s);
-cudaError_t launch_varlen_pad(const int* cu_seqlens, int B, int* pcu, cudaStream_t s);
+// Malformed sequences (seq_range_ok in schedule.h) count as empty and set
+// the bounds bit of *status.
+cudaError_t launch_varlen_pad(const int* cu_seqlens, int B, int64_t total, int max_len, int* pcu,
+                              unsigned int* status, cudaStream_t s);
 cudaError_t launch_bwd_preprocess_varlen(const void* o, const void* dout, const float* lse, float* dsum, float* lse2,
                                          int heads, int64_t total, const int* cu_seqlens, const int* pcu, int B,
-                                         int64_t padded_rows_bound, int d, cudaStream_t s);
+                                         int max_len, int64_t padded_rows_bound, int d, cudaStream_t s);
 
 // out_f32: dq / dk / dv are float32 (stored, or added with p.accumulate).
 cudaError_t launch_bwd_dkdv(int d, bool out_f32, const CUtensorMap& tq, const CUtensorMap& tk,

@@ -11,6 +11,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "schedule.h"
 
 namespace attn {
 
@@ -90,16 +91,24 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
 
 // Ragged backward passes pad every sequence to whole 128-row tiles in the
 // D / lse2 arrays: pcu[b] = sum over b' < b of len(b') rounded up to a tile,
-// pcu[B] their total.  One warp, 32 sequences per step.
-__global__ void __launch_bounds__(32) varlen_pad_kernel(const int* __restrict__ cu, int B, int* __restrict__ pcu) {
+// pcu[B] their total.  A malformed sequence (seq_range_ok) counts as empty, so
+// pcu[B] never exceeds total + 127 B (the workspace's size), and is reported.
+// One warp, 32 sequences per step.
+__global__ void __launch_bounds__(32) varlen_pad_kernel(const int* __restrict__ cu, int B, int64_t total,
+                                                        int max_len, int* __restrict__ pcu,
+                                                        unsigned int* __restrict__ status) {
   const int lane = threadIdx.x;
   int carry = 0;
   for (int base = 0; base <= B; base += 32) {
     const int b = base + lane;
     int v = 0;
     if (b < B) {
-      const int len = cu[b + 1] - cu[b];
-      v = len > 0 ? (len + TILE - 1) / TILE * TILE : 0;
+      if (seq_range_ok(cu, b, total, max_len)) {
+        const int len = cu[b + 1] - cu[b];
+        v = len > 0 ? (len + TILE - 1) / TILE * TILE : 0;
+      } else {
+        atomicOr(status, ATTN_DEV_BOUNDS);
+      }
     }
     int x = v;   // inclusive scan over the warp
 #pragma unroll
@@ -128,7 +137,8 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
                                                          float* __restrict__ dsum, float* __restrict__ lse2,
                                                          int64_t heads, int N, int Np, int64_t in_hs,
                                                          const int* __restrict__ cu,
-                                                         const int* __restrict__ pcu, int B, int64_t total) {
+                                                         const int* __restrict__ pcu, int B, int64_t total,
+                                                         int max_len) {
   constexpr int LPR = D / 8;
   constexpr int RPW = 32 / LPR;
   const int lane = threadIdx.x & 31;
@@ -151,7 +161,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
         else hi = mid;
       }
       const int64_t i = pr - pcu[lo];
-      valid = prow < rows && i < (int64_t)(cu[lo + 1] - cu[lo]);
+      valid = prow < rows && seq_range_ok(cu, lo, total, max_len) && i < (int64_t)(cu[lo + 1] - cu[lo]);
       const int64_t t = cu[lo] + i;               // token
       row = t * heads + head;
       lrow = head * total + t;
@@ -244,31 +254,32 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dout, const float* 
   const auto* pd = static_cast<const __nv_bfloat16*>(dout);
   if (d == 128)
     preprocess_kernel<128, false><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, N, Np, in_hs, nullptr, nullptr,
-                                                       0, 0);
+                                                       0, 0, 0);
   else
     preprocess_kernel<64, false><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, N, Np, in_hs, nullptr, nullptr,
-                                                      0, 0);
+                                                      0, 0, 0);
   return cudaGetLastError();
 }
 
-cudaError_t launch_varlen_pad(const int* cu_seqlens, int B, int* pcu, cudaStream_t s) {
-  varlen_pad_kernel<<<1, 32, 0, s>>>(cu_seqlens, B, pcu);
+cudaError_t launch_varlen_pad(const int* cu_seqlens, int B, int64_t total, int max_len, int* pcu,
+                              unsigned int* status, cudaStream_t s) {
+  varlen_pad_kernel<<<1, 32, 0, s>>>(cu_seqlens, B, total, max_len, pcu, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_preprocess_varlen(const void* o, const void* dout, const float* lse, float* dsum, float* lse2,
                                          int heads, int64_t total, const int* cu_seqlens, const int* pcu, int B,
-                                         int64_t padded_rows_bound, int d, cudaStream_t s) {
+                                         int max_len, int64_t padded_rows_bound, int d, cudaStream_t s) {
   const int rpw = 32 / (d / 8);
   const int grid = grid_for((heads * padded_rows_bound + rpw - 1) / rpw);
   const auto* po = static_cast<const __nv_bfloat16*>(o);
   const auto* pd = static_cast<const __nv_bfloat16*>(dout);
   if (d == 128)
     preprocess_kernel<128, true><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, 0, 0, 0, cu_seqlens, pcu, B,
-                                                      total);
+                                                      total, max_len);
   else
     preprocess_kernel<64, true><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, 0, 0, 0, cu_seqlens, pcu, B,
-                                                     total);
+                                                     total, max_len);
   return cudaGetLastError();
 }
 

@@ -22,9 +22,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "internal.h"
+
 namespace attn {
 
-constexpr unsigned int ATTN_DEV_TIMEOUT = 1u;
 
 // ------------------------------------------------------------------ basics
 

@@ -35,10 +35,19 @@ struct Unit {
   int nq;           // query rows of the unit's sequence (rows at or past it are not written)
   int64_t seq0;     // variable-length batches: first token of the sequence (0 otherwise)
   bool empty;       // variable-length batches: no rows of this sequence in the unit
+  bool bad;         // a device-side index (cu_seqlens, seq_lens) was out of range
   int lo[2], lim[2];  // per query tile t: key tiles [lo[t], lim[t]) may be visible
   int kt_begin, kt_end;  // min(lo), max(lim) over the unit's tiles
   const uint8_t* mrow[2];  // block-sparse mask row per tile, or null
 };
+
+// Sequence b of a packed batch is usable iff 0 <= cu[b] <= cu[b+1] <= total and
+// it holds at most max_len tokens.  The kernels treat any other sequence as
+// empty (so no index derived from it is ever used) and report a bounds error.
+ATTN_HD bool seq_range_ok(const int* cu, int b, int64_t total, int max_len) {
+  const int a = cu[b], e = cu[b + 1];
+  return a >= 0 && e >= a && (int64_t)e <= total && e - a <= max_len;
+}
 
 // Key tiles [0, n) hold a key visible to local query row `last_row` under the
 // causal rule kv_offset + j <= q_offset + i.
@@ -125,6 +134,7 @@ ATTN_HD Unit fwd_unit(int64_t i, int B, int Hq, int Hkv, int Nq, int Nk, int nqc
   u.nq = Nq;
   u.seq0 = 0;
   u.empty = false;
+  u.bad = false;
   const bool causal = mask_is_causal(mask_kind, causal_in_blocks);
   u.kt_begin = u.nkt;
   u.kt_end = 0;
@@ -164,6 +174,7 @@ ATTN_HD Unit decode_unit(int64_t i, int B, int Hq, int Hkv, int nq, int Nk, cons
   u.kvh = bkv;
   u.row0 = 0;
   int len = seq_lens != nullptr ? seq_lens[b] : Nk;
+  u.bad = len < 0 || len > Nk;   // reported, and clamped into the cache
   len = len < 0 ? 0 : (len > Nk ? Nk : len);
   u.nk = len;
   u.nkt = (len + TILE - 1) / TILE;
@@ -190,19 +201,24 @@ ATTN_HD Unit decode_unit(int64_t i, int B, int Hq, int Hkv, int nq, int Nk, cons
 // (batch, head) pairs inner, so every sequence's latest (heaviest) chunk comes
 // first; chunks past a sequence's end are empty.  Inside its sequence a unit
 // is an ordinary forward unit (local positions, the same masks).
-ATTN_HD Unit varlen_unit(int64_t i, int B, int Hq, int Hkv, int nqc_max, const int* cu_seqlens, int mask_kind,
-                         int window) {
+ATTN_HD Unit varlen_unit(int64_t i, int B, int Hq, int Hkv, int nqc_max, const int* cu_seqlens, int64_t total,
+                         int max_len, int mask_kind, int window) {
   const int64_t bh = i % ((int64_t)B * Hq);
   const int pos = (int)(i / ((int64_t)B * Hq));
   const int b = (int)(bh / Hq), h = (int)(bh % Hq);
+  Unit u;
+  if (!seq_range_ok(cu_seqlens, b, total, max_len)) {
+    u.empty = true;
+    u.bad = true;
+    return u;
+  }
   const int64_t seq0 = cu_seqlens[b];
-  int len = (int)(cu_seqlens[b + 1] - seq0);
-  len = len < 0 ? 0 : len;
+  const int len = (int)(cu_seqlens[b + 1] - seq0);
   const int qc = nqc_max - 1 - pos;
   const int nqc = (len + UNIT_ROWS - 1) / UNIT_ROWS;
-  Unit u;
   if (qc >= nqc) {
     u.empty = true;
+    u.bad = false;
     return u;
   }
   u = fwd_unit(nqc - 1 - qc, 1, 1, 1, len, len, nqc, 1, mask_kind, 0, nullptr, 0, window, 0, 0);

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from io_aware_exact_attn_gb300 import api, inputs
-from _gpu_helpers import assert_o_lse, f64
+from _gpu_helpers import assert_o_lse, f64, make
 
 pytestmark = pytest.mark.gpu
 
@@ -81,3 +81,16 @@ def test_decode_equals_last_rows_of_forward():
     torch.cuda.synchronize()
     assert float((o_d.float() - o_f[:, :, N - Nq:].float()).abs().max()) <= 1e-2
     assert float((l_d - l_f[:, :, N - Nq:]).abs().max()) <= 2e-3
+
+
+def test_out_of_range_seq_lens_are_clamped_and_reported():
+    """Device-side bounds check: a cached length outside [0, Nk] is clamped into
+    the cache and reported by attn_get_status as ATTN_ERR_DEVICE_BOUNDS."""
+    B, Hq, Hkv, Nq, Nk, d = 3, 8, 2, 1, 640, 128
+    q, k, v, _ = make(B, Hq, Hkv, Nq, d, Nk=Nk)
+    bad = torch.tensor([700, 640, -5], dtype=torch.int32).cuda()
+    o_bad, l_bad = api.attn_decode(q, k, v, bad)
+    assert api.get_status() == -8
+    o_ok, l_ok = api.attn_decode(q, k, v, torch.tensor([640, 640, 0], dtype=torch.int32).cuda())
+    assert api.get_status() == 0
+    assert torch.equal(o_bad, o_ok) and torch.equal(l_bad, l_ok)

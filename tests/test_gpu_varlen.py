@@ -113,3 +113,43 @@ def test_varlen_backward_equal_lengths_match_batched_backward():
     torch.cuda.synchronize()
     for a, b in zip(grads, gb):
         assert max_err(f64(a), f64(b.transpose(1, 2).reshape(B * n, b.shape[1], d))) == 0.0
+
+
+def test_malformed_cu_seqlens_are_skipped_and_reported():
+    """Device-side bounds check: a sequence whose cu_seqlens range runs past
+    the packed tensors (or holds more than max_len tokens) is skipped by every
+    kernel and reported by attn_get_status as ATTN_ERR_DEVICE_BOUNDS; the
+    well-formed sequences of the same call are still exact."""
+    from io_aware_exact_attn_gb300 import _ffi
+    Hq, Hkv, d = 4, 2, 128
+    total = 700
+    q, k, v, _ = packed([total], Hq, Hkv, d)
+    do = torch.randn(total, Hq, d, generator=torch.Generator().manual_seed(9)).to(torch.bfloat16).cuda()
+    cu = torch.tensor([0, 300, 600, 900], dtype=torch.int32).cuda()   # sequence 2 ends past total
+    sentinel = 5.0
+    o = torch.full_like(q, sentinel)
+    lse = torch.full((Hq, total), sentinel, device="cuda")
+    api.attn_varlen_fwd(q, k, v, cu, max_len=300, causal=True, out=o, lse=lse)
+    dq = torch.full_like(q, sentinel)
+    dk = torch.full_like(k, sentinel)
+    dv = torch.full_like(v, sentinel)
+    api.attn_varlen_bwd(q, k, v, o, lse, do, cu, max_len=300, causal=True, dq=dq, dk=dk, dv=dv)
+    assert api.get_status() == -8 and _ffi.STATUS[-8] == "ATTN_ERR_DEVICE_BOUNDS"
+    assert api.get_status() == 0              # read and cleared
+    # the skipped sequence's rows are untouched, the others are exact
+    assert bool((o[600:] == sentinel).all()) and bool((dq[600:] == sentinel).all())
+    good = cu[:3].cpu().numpy()
+    qf, kf, vf, dof = (f64(t[:600]) for t in (q, k, v, do))
+    mask = oracle.MaskSpec("causal")
+    o_ref, l_ref = oracle.varlen_forward(qf, kf, vf, good, 1 / math.sqrt(d), mask)
+    assert_o_lse(f64(o[:600]), f64(lse[:, :600]), o_ref, l_ref, "well-formed sequences")
+    gq, gk, gv = oracle.varlen_backward(qf, kf, vf, dof, good, 1 / math.sqrt(d), mask)
+    for name, got, want in (("dQ", dq[:600], gq), ("dK", dk[:600], gk), ("dV", dv[:600], gv)):
+        e = max_err(f64(got), want) / np.abs(want).max()
+        assert e <= 3e-2, f"{name} of well-formed sequences: {e:.3e}"
+    # a sequence longer than the max_len the caller promised is skipped too,
+    # and so is one whose end precedes its start
+    for bad in ([0, 300, 600], [0, 300, 200, 700]):
+        api.attn_varlen_fwd(q[:bad[-1]], k[:bad[-1]], v[:bad[-1]], torch.tensor(bad, dtype=torch.int32).cuda(),
+                            max_len=256 if len(bad) == 3 else 500, causal=True)
+        assert api.get_status() == -8
