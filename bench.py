@@ -266,6 +266,10 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the e2e, chunked and CPU legs")
     ap.add_argument("--profile-pass", action="store_true",
                     help="one untimed step and one E4M3 forward only (for profiler captures); prints nothing")
+    ap.add_argument("--profile-workload", default=None,
+                    choices=["gpt", "gpt_noncausal", "block_sparse", "bert_large", "decode", "varlen", "chunked_bwd"],
+                    help="one untimed forward + backward of the named workload only (for profiler captures; the "
+                         "ragged batch is cut to 8 sequences); prints nothing")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -292,6 +296,12 @@ def main():
     def barrier():
         if dist is not None:
             dist.barrier()
+
+    if args.profile_workload:
+        profile_workload(args.profile_workload, api, inputs, torch)
+        torch.cuda.synchronize()
+        assert api.get_status() == 0
+        return 0
 
     w = WORKLOAD
     causal = w["mask"] == "causal"
@@ -433,6 +443,44 @@ def main():
     if rank == 0:
         print(json.dumps(out), flush=True)
     return 0
+
+
+def profile_workload(name, api, inputs, torch):
+    """One untimed pass of a workload, for a profiler to capture: launches in
+    the order forward, then backward (preprocess, dK/dV, dQ)."""
+    if name in ("gpt", "gpt_noncausal", "block_sparse", "bert_large"):
+        w = inputs.WORKLOADS["gpt_causal" if name == "gpt" else name]
+        q, k, v, do = (t.cuda() for t in w.tensors())
+        bm_np = w.block_mask()
+        bm = None if bm_np is None else torch.as_tensor(bm_np, dtype=torch.uint8).cuda()
+        causal = w.mask == "causal"
+        o, lse = api.attn_fwd(q, k, v, causal=causal, block_mask=bm)
+        api.attn_bwd(q, k, v, o, lse, do, causal=causal, block_mask=bm)
+    elif name == "decode":
+        c = DECODE
+        g = torch.Generator().manual_seed(inputs.SEED + 9)
+        q = torch.randn(c["B"], c["Hq"], c["Nq"], c["d"], generator=g).to(torch.bfloat16).cuda()
+        k = torch.randn(c["B"], c["Hkv"], c["Nk"], c["d"], generator=g).to(torch.bfloat16).cuda()
+        v = torch.randn(c["B"], c["Hkv"], c["Nk"], c["d"], generator=g).to(torch.bfloat16).cuda()
+        api.attn_decode(q, k, v)
+    elif name == "varlen":
+        import numpy as np
+        c = VARLEN
+        lens = varlen_lengths(inputs.SEED + 11)[:8]
+        total = sum(lens)
+        g = torch.Generator().manual_seed(inputs.SEED + 12)
+        q, k, v, do = (torch.randn(total, h, c["d"], generator=g).to(torch.bfloat16).cuda()
+                       for h in (c["Hq"], c["Hkv"], c["Hkv"], c["Hq"]))
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32).cuda()
+        o, lse = api.attn_varlen_fwd(q, k, v, cu, max(lens), causal=True)
+        api.attn_varlen_bwd(q, k, v, o, lse, do, cu, max(lens), causal=True)
+    elif name == "chunked_bwd":
+        c = CHUNKED
+        q, k, v, o, lse, run = chunked_setup(api, inputs, torch, 0)
+        run()
+        g = torch.Generator().manual_seed(inputs.SEED + 4)
+        do = torch.randn(c["B"], c["Hq"], c["N"], c["d"], generator=g).to(torch.bfloat16).cuda()
+        api.chunked_bwd(q, k, v, o, lse, do, c["chunks"])
 
 
 def e2e_leg(api, inputs, torch, w, causal, rank, steps=30, chunks_per_batch=2):

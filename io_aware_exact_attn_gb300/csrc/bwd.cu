@@ -74,6 +74,25 @@ __device__ __forceinline__ bool tile_pair_visible(const BwdParams& p, int qt, in
   return true;
 }
 
+// Ragged batches: the sequence b owning backward unit `cta` when every
+// sequence owns heads * (its 128-row tiles) consecutive units, in index order
+// (pcu: the tile-padded row offsets of the preprocess pass, so a malformed
+// sequence owns none), and the unit's index j inside it.  False past the last.
+__device__ __forceinline__ bool ragged_tile_unit(const int* pcu, int B, int heads, int64_t cta, int* b, int* nt,
+                                                 int64_t* j) {
+  if (cta >= (int64_t)heads * (pcu[B] / TILE)) return false;
+  int lo = 0, hi = B;   // the largest b with heads * pcu[b] / 128 <= cta
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((int64_t)heads * (pcu[mid] / TILE) <= cta) lo = mid;
+    else hi = mid;
+  }
+  *b = lo;
+  *nt = (pcu[lo + 1] - pcu[lo]) / TILE;
+  *j = cta - (int64_t)heads * (pcu[lo] / TILE);
+  return true;
+}
+
 // Causal masks: the first query tile with a query at or after the first key
 // of key tile kt (base + 127 >= 0).
 __device__ __forceinline__ int first_query_tile(const BwdParams& p, int kt) {
@@ -133,9 +152,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
   const int nkt_all = (p.Nk + TILE - 1) / TILE;
   const bool ragged = p.cu_seqlens != nullptr;
   int kt = 0, bkv = 0;
-  if (ragged) {   // key tiles ascending (heaviest first), every sequence and kv head inner
-    kt = (int)(blockIdx.x / ((unsigned)p.B * p.Hkv));
-    bkv = (int)(blockIdx.x % ((unsigned)p.B * p.Hkv));
+  if (ragged) {   // sequence by sequence; inside one, kv-head groups sized for L2, key tiles ascending
+    int sb = 0, nt = 0;
+    int64_t j = 0;
+    if (!ragged_tile_unit(p.pcu, p.B, p.Hkv, blockIdx.x, &sb, &nt, &j)) return;
+    const int len = p.cu_seqlens[sb + 1] - p.cu_seqlens[sb];
+    int hk = 0;
+    grouped_unit(j, p.Hkv, nt, q_stream_group(1, p.Hq, p.Hkv, len, D), &hk, &kt);
+    bkv = sb * p.Hkv + hk;
   } else {
     grouped_unit(blockIdx.x, p.B * p.Hkv, nkt_all, p.kv_group, &bkv, &kt);  // key tiles ascending: heaviest first
   }
@@ -559,16 +583,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
   auto bar_ds = [&](int j) { return smem_u32(&bars[1 + 2 * KS + 2 * VS + 5 + (j & 1)]); };
   auto bar_dq = [&](int j) { return smem_u32(&bars[1 + 2 * KS + 2 * VS + 7 + (j & 1)]); };
 
-  const int nqt_all = (p.Nq + TILE - 1) / TILE;
   const bool ragged = p.cu_seqlens != nullptr;
-  int bh = 0, qpos = 0;
-  if (ragged) {   // latest query tiles first, every sequence and head inner
-    qpos = (int)(blockIdx.x / ((unsigned)p.B * p.Hq));
-    bh = (int)(blockIdx.x % ((unsigned)p.B * p.Hq));
+  int bh = 0, qt = 0;
+  if (ragged) {   // sequence by sequence; inside one, head groups sized for L2, latest query tiles first
+    int sb = 0, nt = 0;
+    int64_t j = 0;
+    if (!ragged_tile_unit(p.pcu, p.B, p.Hq, blockIdx.x, &sb, &nt, &j)) return;
+    const int len = p.cu_seqlens[sb + 1] - p.cu_seqlens[sb];
+    int h = 0, qpos = 0;
+    grouped_unit(j, p.Hq, nt, kv_stream_group(1, p.Hq, p.Hkv, len, D), &h, &qpos);
+    bh = sb * p.Hq + h;
+    qt = nt - 1 - qpos;
   } else {
+    const int nqt_all = (p.Nq + TILE - 1) / TILE;
+    int qpos = 0;
     grouped_unit(blockIdx.x, p.B * p.Hq, nqt_all, p.q_group, &bh, &qpos);
+    qt = nqt_all - 1 - qpos;  // latest query tile first: heaviest under a causal mask
   }
-  const int qt = nqt_all - 1 - qpos;  // latest query tile first: heaviest under a causal mask
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int bkv = b * p.Hkv + h / (p.Hq / p.Hkv);
   if (ragged && !seq_range_ok(p.cu_seqlens, b, p.total, p.Nq)) {   // malformed: skipped and reported

@@ -97,12 +97,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   auto bar_o = [&](int t) { return smem_u32(&bars[1 + 4 * NS + 4 + t]); };
   const uint32_t bar_done = smem_u32(&bars[1 + 4 * NS + 6]);
 
-  const Unit u =
-      p.n_splits > 0 ? decode_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.dec_nq, p.Nk, p.seq_lens, p.n_splits, p.split_tiles)
-      : p.cu_seqlens != nullptr
-          ? varlen_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.varlen_nqc, p.cu_seqlens, p.total, p.Nq, p.mask_kind, p.window)
-          : fwd_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.Nq, p.Nk, p.nqc, p.head_group, p.mask_kind, p.causal_in_blocks,
-                     p.block_mask, p.nkb, p.window, p.q_offset, p.kv_offset);
+  Unit u;   // warp-uniform: every warp works it out for itself
+  if (p.n_splits > 0)
+    u = decode_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.dec_nq, p.Nk, p.seq_lens, p.n_splits, p.split_tiles);
+  else if (p.cu_seqlens != nullptr)
+    u = varlen_unit(blockIdx.x, p.B, p.Hq, p.Hkv, D, p.cu_seqlens, p.total, p.Nq, p.mask_kind, p.window);
+  else
+    u = fwd_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.Nq, p.Nk, p.nqc, p.head_group, p.mask_kind, p.causal_in_blocks,
+                 p.block_mask, p.nkb, p.window, p.q_offset, p.kv_offset);
   if (u.bad && threadIdx.x == 0) atomicOr(p.status, ATTN_DEV_BOUNDS);
   if (u.empty) return;   // a chunk past the end of its sequence (or of a malformed one): nothing set up yet
   WaitCtx wc{p.wait_limit_ns, p.status, &abort_flag};

@@ -96,13 +96,26 @@ constexpr int DEBUG_FIELDS = 8;
 
 // Grid sizes (one CTA per work unit), shared by the launchers and by the
 // front end's check of the debug record's capacity.
+// Ragged batches launch at most heads * (ceil(total / rows) + B) units
+// (ragged_units_bound in schedule.h, repeated here for the host).
+inline unsigned ragged_grid(int B, int heads, int64_t total, int max_len, int rows) {
+  const int64_t padded = (int64_t)B * ((max_len + rows - 1) / rows);
+  const int64_t tight = (total + rows - 1) / rows + B;
+  return (unsigned)((int64_t)heads * (padded < tight ? padded : tight));
+}
 inline unsigned fwd_grid(const FwdParams& p) {
   return p.n_splits > 0           ? (unsigned)(p.B * p.Hkv) * (unsigned)p.n_splits
-         : p.cu_seqlens != nullptr ? (unsigned)(p.B * p.Hq) * (unsigned)p.varlen_nqc
+         : p.cu_seqlens != nullptr ? ragged_grid(p.B, p.Hq, p.total, p.Nq, UNIT_ROWS)
                                    : (unsigned)(p.B * p.Hq) * (unsigned)p.nqc;
 }
-inline unsigned dkdv_grid(const BwdParams& p) { return (unsigned)(p.B * p.Hkv) * (unsigned)((p.Nk + TILE - 1) / TILE); }
-inline unsigned dq_grid(const BwdParams& p) { return (unsigned)(p.B * p.Hq) * (unsigned)((p.Nq + TILE - 1) / TILE); }
+inline unsigned dkdv_grid(const BwdParams& p) {
+  return p.cu_seqlens != nullptr ? ragged_grid(p.B, p.Hkv, p.total, p.Nk, TILE)
+                                 : (unsigned)(p.B * p.Hkv) * (unsigned)((p.Nk + TILE - 1) / TILE);
+}
+inline unsigned dq_grid(const BwdParams& p) {
+  return p.cu_seqlens != nullptr ? ragged_grid(p.B, p.Hq, p.total, p.Nq, TILE)
+                                 : (unsigned)(p.B * p.Hq) * (unsigned)((p.Nq + TILE - 1) / TILE);
+}
 
 struct TensorMaps {
   CUtensorMap a, b, c, d;

@@ -197,36 +197,88 @@ ATTN_HD Unit decode_unit(int64_t i, int B, int Hq, int Hkv, int nq, int Nk, cons
   return u;
 }
 
-// Variable-length unit i of B * Hq * nqc_max: position-major with the
-// (batch, head) pairs inner, so every sequence's latest (heaviest) chunk comes
-// first; chunks past a sequence's end are empty.  Inside its sequence a unit
-// is an ordinary forward unit (local positions, the same masks).
-ATTN_HD Unit varlen_unit(int64_t i, int B, int Hq, int Hkv, int nqc_max, const int* cu_seqlens, int64_t total,
-                         int max_len, int mask_kind, int window) {
-  const int64_t bh = i % ((int64_t)B * Hq);
-  const int pos = (int)(i / ((int64_t)B * Hq));
-  const int b = (int)(bh / Hq), h = (int)(bh % Hq);
+// Work units of a ragged batch, in the launch order of every ragged kernel:
+// sequence by sequence (index order; a malformed sequence has none), and
+// inside a sequence grouped by heads like the dense kernels (grouped_unit,
+// groups sized for L2 from the sequence's own length, heaviest tiles first,
+// heads inner), so concurrent CTAs share one group's streamed operand in L2.
+// Launches cover at most heads * (ceil(total / rows) + B) units (each
+// sequence wastes less than one unit per head), capped by the padded count.
+ATTN_HD int64_t ragged_units_bound(int B, int heads, int64_t total, int max_len, int rows) {
+  const int64_t padded = (int64_t)B * ((max_len + rows - 1) / rows);
+  const int64_t tight = (total + rows - 1) / rows + B;
+  return (int64_t)heads * (padded < tight ? padded : tight);
+}
+
+#if defined(__CUDACC__)
+// The sequence that owns ragged unit `cta` when sequence b owns
+// heads * ceil(len_b / rows) consecutive units: one warp (all 32 lanes, same
+// arguments) scans cu_seqlens.  Returns false past the last unit; *any_bad
+// tells whether some sequence was malformed (every call scans them all).
+__device__ __forceinline__ bool ragged_locate(const int* cu, int B, int64_t total, int max_len, int heads, int rows,
+                                              int64_t cta, int* seq, int64_t* first, bool* any_bad) {
+  const int lane = threadIdx.x & 31;
+  int64_t carry = 0, f = 0;
+  int found = -1;
+  bool bad = false;
+  for (int base = 0; base < B; base += 32) {
+    const int b = base + lane;
+    int64_t n = 0;
+    if (b < B) {
+      if (seq_range_ok(cu, b, total, max_len)) n = (int64_t)heads * ((cu[b + 1] - cu[b] + rows - 1) / rows);
+      else bad = true;
+    }
+    int64_t x = n;   // inclusive scan over the warp
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    const int64_t excl = carry + x - n;
+    const unsigned hit = __ballot_sync(0xffffffffu, n > 0 && cta >= excl && cta < excl + n);
+    if (hit != 0u && found < 0) {
+      const int src = __ffs(hit) - 1;
+      found = __shfl_sync(0xffffffffu, b, src);
+      f = __shfl_sync(0xffffffffu, excl, src);
+    }
+    carry += __shfl_sync(0xffffffffu, x, 31);
+  }
+  *any_bad = __any_sync(0xffffffffu, bad) != 0;
+  *seq = found;
+  *first = f;
+  return found >= 0;
+}
+
+// Forward unit `cta` of a ragged batch (256-row chunks; see ragged_locate).
+// Called by whole warps.  Inside its sequence a unit is an ordinary forward
+// unit (local positions, the same masks); bad reports a malformed sequence
+// seen by CTA 0's scan.
+__device__ __forceinline__ Unit varlen_unit(int64_t cta, int B, int Hq, int Hkv, int d, const int* cu_seqlens,
+                                            int64_t total, int max_len, int mask_kind, int window) {
+  int b = 0;
+  int64_t first = 0;
+  bool any_bad = false;
+  const bool ok = ragged_locate(cu_seqlens, B, total, max_len, Hq, UNIT_ROWS, cta, &b, &first, &any_bad);
   Unit u;
-  if (!seq_range_ok(cu_seqlens, b, total, max_len)) {
+  u.bad = any_bad && cta == 0;
+  if (!ok) {
     u.empty = true;
-    u.bad = true;
     return u;
   }
   const int64_t seq0 = cu_seqlens[b];
   const int len = (int)(cu_seqlens[b + 1] - seq0);
-  const int qc = nqc_max - 1 - pos;
   const int nqc = (len + UNIT_ROWS - 1) / UNIT_ROWS;
-  if (qc >= nqc) {
-    u.empty = true;
-    u.bad = false;
-    return u;
-  }
-  u = fwd_unit(nqc - 1 - qc, 1, 1, 1, len, len, nqc, 1, mask_kind, 0, nullptr, 0, window, 0, 0);
+  int h = 0, pos = 0;
+  grouped_unit(cta - first, Hq, nqc, kv_stream_group(1, Hq, Hkv, len, d), &h, &pos);
+  const bool bad = u.bad;
+  u = fwd_unit(pos, 1, 1, 1, len, len, nqc, 1, mask_kind, 0, nullptr, 0, window, 0, 0);
   u.bh = h;
   u.kvh = h / (Hq / Hkv);
   u.seq0 = seq0;
+  u.bad = bad;
   return u;
 }
+#endif
 
 // Bit t set: query tile t of the unit sees key tile kt.
 ATTN_HD uint32_t unit_uses(const Unit& u, int kt) {

@@ -83,6 +83,13 @@ def check_records(recs, expected, allow_empty=0):
     assert not bad, f"{len(bad)} units differ, e.g. {list(bad.items())[:3]}"
 
 
+def ragged_grid(B, heads, total, max_len, rows):
+    """CTAs a ragged launch has: one unit per head and tile of every sequence,
+    bounded by heads * (ceil(total / rows) + B) (the unit order is sequence
+    by sequence, so the CTAs past the last unit do nothing)."""
+    return heads * min(B * cdiv(max_len, rows), cdiv(total, rows) + B)
+
+
 def fwd_expected(B, Hq, Nq, Nk, spec, q_off=0, kv_off=0):
     exp = {}
     for qc in range(cdiv(Nq, 256)):
@@ -157,8 +164,9 @@ def test_varlen_forward_records():
     v = inputs.randn_bf16((total, Hkv, d), seed=33).cuda()
     cu_h = np.concatenate([[0], np.cumsum(lens)])
     cu = torch.tensor(cu_h, dtype=torch.int32).cuda()
-    B, nqc_max = len(lens), cdiv(max(lens), 256)
-    rec = Recorder(B * Hq * nqc_max)
+    B = len(lens)
+    grid = ragged_grid(B, Hq, total, max(lens), 256)
+    rec = Recorder(grid)
     api.attn_varlen_fwd(q, k, v, cu, causal=True)
     exp = {}
     spec = oracle.MaskSpec("causal")
@@ -167,8 +175,7 @@ def test_varlen_forward_records():
             per_t = [tiles_seen(range(qc * 256 + t * T, min(n, qc * 256 + t * T + T)), n, spec) for t in range(2)]
             for h in range(Hq):
                 exp[(h, qc * 256, 0, int(cu_h[b]))] = (len(per_t[0] | per_t[1]), 0, len(per_t[0]), len(per_t[1]))
-    empty = B * Hq * nqc_max - len(exp)
-    check_records(rec.records(), exp, allow_empty=empty)
+    check_records(rec.records(), exp, allow_empty=grid - len(exp))
 
 
 def test_decode_records():
@@ -269,8 +276,8 @@ def test_varlen_backward_records():
     cu_h = np.concatenate([[0], np.cumsum(lens)])
     cu = torch.tensor(cu_h, dtype=torch.int32).cuda()
     o, lse = api.attn_varlen_fwd(q, k, v, cu, causal=True)
-    B, nt = len(lens), cdiv(max(lens), T)
-    n_dkdv, n_dq = B * Hkv * nt, B * Hq * nt
+    B = len(lens)
+    n_dkdv, n_dq = ragged_grid(B, Hkv, total, max(lens), T), ragged_grid(B, Hq, total, max(lens), T)
     rec = Recorder(n_dkdv + n_dq)
     api.attn_varlen_bwd(q, k, v, o, lse, do, cu, causal=True)
     exp_dkdv, exp_dq = {}, {}
