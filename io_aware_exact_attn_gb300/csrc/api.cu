@@ -261,6 +261,43 @@ int attn_debug_set_tile_counts(int32_t* counts, int64_t capacity) {
   return ATTN_OK;
 }
 
+// Work units of the dK/dV kernel and how many consecutive ones each CTA takes
+// (at most 8): the per-CTA setup and epilogue are paid once per run and
+// overlap the neighbouring units' work, while the hardware still balances the
+// CTAs.  Runs grow (up to 4) while they leave twelve waves of CTAs (one CTA
+// per SM), and
+// light units (few query tiles each: a unit costs about the fixed part of
+// 16 tiles' work) get runs of about 16 tiles even with fewer waves.  Long
+// runs of equal-cost units fill the last wave badly, so nothing else lengthens
+// them.  (Measured on GB300: a causal 2x32x8192 head set and the BERT-shaped
+// shape gain from runs; a random 1/8 block mask, whose units all cost the
+// same, does best with single units.)
+static void set_kv_run(BwdParams* p) {
+  static int sms[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && sms[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    sms[dev] = n > 0 ? n : 148;
+  }
+  const int64_t n_sm = (dev >= 0 && dev < 64) ? sms[dev] : 148;
+  p->kv_units = dkdv_units(*p);
+  // query tiles a unit visits, expected: the query heads of its group times
+  // the query tiles its key tile sees (half of them under a causal mask, the
+  // window's share under a sliding window; all of them otherwise, a block
+  // mask's density being unknown on the host)
+  const int64_t nqt = (p->Nq + TILE - 1) / TILE;
+  int64_t seen = nqt;
+  if (p->mask_kind == MASK_CAUSAL || (p->mask_kind == MASK_BLOCK_SPARSE && p->causal_in_blocks)) seen = (nqt + 1) / 2;
+  if (p->mask_kind == MASK_SLIDING_WINDOW) seen = std::min<int64_t>(nqt, p->window / TILE + 1);
+  const int64_t tiles = std::max<int64_t>(1, seen * (p->Hq / p->Hkv));
+  const int64_t by_waves = std::min<int64_t>(4, p->kv_units / (12 * n_sm));
+  const int64_t by_weight = 16 / tiles;
+  const int64_t run = std::max(by_waves, by_weight);
+  p->kv_run = (int)(run < 1 ? 1 : (run > 8 ? 8 : run));   // at most the kernel's table of 8 units
+}
+
 // The debug record array for a launch of `ctas` CTAs (after `skip` records
 // of an earlier kernel of the same call), or null when recording is off.
 static int debug_records(int64_t skip, int64_t ctas, int32_t** out) {
@@ -642,8 +679,9 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   p.q_group = kv_stream_group(B, Hq, Hkv, N, d);
   p.status = status;
   p.wait_limit_ns = wait_limit();
-  if ((rc = debug_records(0, dkdv_grid(p), &p.dkdv_counts)) ||
-      (rc = debug_records(dkdv_grid(p), dq_grid(p), &p.dq_counts)))
+  set_kv_run(&p);
+  if ((rc = debug_records(0, p.kv_units, &p.dkdv_counts)) ||
+      (rc = debug_records(p.kv_units, dq_grid(p), &p.dq_counts)))
     return rc;
   {
     TraceScope ts(ATTN_KERNEL_BWD_DKDV, s);
@@ -737,8 +775,9 @@ int attn_partial_bwd(const void* q, const void* k, const void* v, const void* do
   p.q_group = kv_stream_group(B, Hq, Hkv, Nk, d);
   p.status = status;
   p.wait_limit_ns = wait_limit();
-  if ((rc = debug_records(0, dkdv_grid(p), &p.dkdv_counts)) ||
-      (rc = debug_records(dkdv_grid(p), dq_grid(p), &p.dq_counts)))
+  set_kv_run(&p);
+  if ((rc = debug_records(0, p.kv_units, &p.dkdv_counts)) ||
+      (rc = debug_records(p.kv_units, dq_grid(p), &p.dq_counts)))
     return rc;
   cudaError_t e;
   {
@@ -821,8 +860,9 @@ int attn_varlen_bwd(const void* q, const void* k, const void* v, const void* o, 
   p.q_group = 1;
   p.status = status;
   p.wait_limit_ns = wait_limit();
-  if ((rc = debug_records(0, dkdv_grid(p), &p.dkdv_counts)) ||
-      (rc = debug_records(dkdv_grid(p), dq_grid(p), &p.dq_counts)))
+  set_kv_run(&p);
+  if ((rc = debug_records(0, p.kv_units, &p.dkdv_counts)) ||
+      (rc = debug_records(p.kv_units, dq_grid(p), &p.dq_counts)))
     return rc;
   {
     TraceScope ts(ATTN_KERNEL_BWD_DKDV, s);
@@ -1074,8 +1114,9 @@ extern "C" int attn_bwd_static_scratch(const void* q, const void* k, const void*
   p.q_group = kv_stream_group(B, Hq, Hkv, N, d);
   p.status = status;
   p.wait_limit_ns = wait_limit();
-  if ((rc = debug_records(0, dkdv_grid(p), &p.dkdv_counts)) ||
-      (rc = debug_records(dkdv_grid(p), dq_grid(p), &p.dq_counts)))
+  set_kv_run(&p);
+  if ((rc = debug_records(0, p.kv_units, &p.dkdv_counts)) ||
+      (rc = debug_records(p.kv_units, dq_grid(p), &p.dq_counts)))
     return rc;
   {
     TraceScope ts(ATTN_KERNEL_BWD_DKDV, s);

@@ -41,10 +41,12 @@ struct BwdCfg {
   static constexpr uint32_t TILE_BYTES = NBOX * BOX_BYTES;
   static constexpr int NS = (D == 128) ? 2 : 4;  // ring depth
   // both kernels: 12 warps; the control warpgroup gives registers back to the
-  // two elementwise warpgroups: 128*64 + 256*216 = 63488 <= 384*168 (launch
-  // allotment); at this split neither role spills
+  // two elementwise warpgroups: 128*80 + 256*208 = 63488 <= 384*168 (launch
+  // allotment).  The dK/dV control warps walk a run of units and need 80
+  // (ptxas reports their spills at 64); the elementwise warps do not spill
+  // more at 208 than at 216
   static constexpr int SPLIT_THREADS = 384;
-  static constexpr uint32_t REGS_CTRL = 64, REGS_ELEM = 216;
+  static constexpr uint32_t REGS_CTRL = 80, REGS_ELEM = 208;
 };
 
 // The sliding window includes the causal rule.
@@ -116,10 +118,70 @@ __host__ __device__ constexpr uint32_t half_col(int kk) { return kk < 4 ? kk * 8
 // dK / dV
 // Tensor memory: S^T [0,128) (P^T bf16 overwrites [0,64)), dP^T [128,256)
 // (dS^T bf16 overwrites [128,192)), dV [256,256+d), dK [256+d,256+2d).
-// Shared memory: K, V (resident), NS-deep ring of {Q_i, dO_i, lse2_i, D_i}.
+// Shared memory: K, V (resident per unit), NS-deep ring of {Q_i, dO_i,
+// lse2_i, D_i}, and 1 KB per elementwise warp to stage the epilogue's rows.
 // Order on the tensor core: S^T_0, dP^T_0, then dV_i, S^T_{i+1}, dK_i,
 // dP^T_{i+1} per query tile i (see the MMA issuer).
+//
+// A CTA takes a run of kv_run consecutive units of the launch order (similar
+// costs; the hardware still balances the CTAs).  The ring, the barriers and
+// tensor memory carry on from one unit to the next, so the next unit's K/V
+// load (as soon as its predecessor's last S^T and dP^T products are done) and
+// first two products overlap the current unit's last tile and epilogue; the
+// next unit's first dV product waits until the epilogue has read the
+// accumulators.
 // =========================================================================
+
+// One work unit of the dK/dV kernel: a 128-key tile of one (batch, kv head).
+struct KvUnit {
+  int kt, bkv, b, hkv, tok0, n_seq, nqt, qt_first, kv_head;
+  int ntile;                 // (query head, query tile) pairs it visits
+  int64_t lrow_b, lrow_hs;   // rows of its lse2 / D entries: sequence start, distance between query heads
+};
+constexpr int MAX_KV_RUN = 8;   // units per CTA at most
+
+// Unit u of the launch order (heaviest first inside each head group); false
+// when it does nothing (past the last unit, or past the end of a shorter
+// ragged sequence).  Every role of a CTA walks the same units.  Called by a
+// whole warp (the visible query tiles are counted 32 at a time).
+template <int D>
+__device__ __forceinline__ bool kv_unit(const BwdParams& p, int64_t u, KvUnit& x) {
+  const bool ragged = p.cu_seqlens != nullptr;
+  if (ragged) {   // sequence by sequence; inside one, kv-head groups sized for L2, key tiles ascending
+    int sb = 0, nt = 0;
+    int64_t j = 0;
+    if (!ragged_tile_unit(p.pcu, p.B, p.Hkv, u, &sb, &nt, &j)) return false;
+    if (!seq_range_ok(p.cu_seqlens, sb, p.total, p.Nq)) return false;   // never: such a sequence owns no tile
+    const int len = p.cu_seqlens[sb + 1] - p.cu_seqlens[sb];
+    int hk = 0;
+    grouped_unit(j, p.Hkv, nt, q_stream_group(1, p.Hq, p.Hkv, len, D), &hk, &x.kt);
+    x.bkv = sb * p.Hkv + hk;
+  } else {
+    const int nkt_all = (p.Nk + TILE - 1) / TILE;
+    if (u >= (int64_t)p.B * p.Hkv * nkt_all) return false;
+    grouped_unit(u, p.B * p.Hkv, nkt_all, p.kv_group, &x.bkv, &x.kt);  // key tiles ascending: heaviest first
+  }
+  x.b = x.bkv / p.Hkv;
+  x.hkv = x.bkv % p.Hkv;
+  x.tok0 = ragged ? p.cu_seqlens[x.b] : 0;    // packed tensors hold fewer than 2^31 tokens
+  x.n_seq = ragged ? p.cu_seqlens[x.b + 1] - x.tok0 : p.Nk;
+  if (x.kt * TILE >= x.n_seq) return false;
+  const int nq_seq = ragged ? x.n_seq : p.Nq;
+  x.lrow_hs = ragged ? (int64_t)p.pcu[p.B] : (int64_t)p.Np;
+  x.lrow_b = ragged ? (int64_t)p.pcu[x.b] : (int64_t)x.b * p.Hq * p.Np;
+  x.kv_head = ragged ? x.hkv : x.bkv;   // head coordinate in the K / V maps
+  x.nqt = (nq_seq + TILE - 1) / TILE;
+  x.qt_first = causal_of(p) ? first_query_tile(p, x.kt) : 0;
+  const int lane = threadIdx.x & 31;
+  int nvis = 0;
+  for (int q0 = x.qt_first; q0 < x.nqt; q0 += 32) {
+    const int qt = q0 + lane;
+    nvis += __popc(__ballot_sync(0xffffffffu, qt < x.nqt && tile_pair_visible(p, qt, x.kt)));
+  }
+  x.ntile = nvis * (p.Hq / p.Hkv);
+  return true;
+}
+
 template <int D, bool F32>
 __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -130,11 +192,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
   constexpr uint32_t OFF_V = C::TILE_BYTES;
   constexpr uint32_t OFF_RING = 2 * C::TILE_BYTES;
   constexpr uint32_t STAGE = 2 * C::TILE_BYTES + 1024;  // Q, dO, lse2[128], D[128]
+  constexpr uint32_t OFF_EPI = OFF_RING + NS * STAGE;   // 8 x 1 KB epilogue staging
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bars[1 + 2 * NS + 7];
+  __shared__ __align__(8) uint64_t bars[1 + 2 * NS + 9];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ KvUnit units[MAX_KV_RUN];   // this CTA's units, decoded once
+  __shared__ int unit_ok[MAX_KV_RUN];    // 0: the unit does nothing
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t s_base = smem_u32(smem);
@@ -148,41 +213,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
   const uint32_t bar_dv = smem_u32(&bars[1 + 2 * NS + 4]);
   const uint32_t bar_dk = smem_u32(&bars[1 + 2 * NS + 5]);
   const uint32_t bar_done = smem_u32(&bars[1 + 2 * NS + 6]);
+  const uint32_t bar_kvfree = smem_u32(&bars[1 + 2 * NS + 7]);   // a unit's K and V are read by no further MMA
+  const uint32_t bar_accfree = smem_u32(&bars[1 + 2 * NS + 8]);  // a unit's dV, dK have been read out
 
-  const int nkt_all = (p.Nk + TILE - 1) / TILE;
-  const bool ragged = p.cu_seqlens != nullptr;
-  int kt = 0, bkv = 0;
-  if (ragged) {   // sequence by sequence; inside one, kv-head groups sized for L2, key tiles ascending
-    int sb = 0, nt = 0;
-    int64_t j = 0;
-    if (!ragged_tile_unit(p.pcu, p.B, p.Hkv, blockIdx.x, &sb, &nt, &j)) return;
-    const int len = p.cu_seqlens[sb + 1] - p.cu_seqlens[sb];
-    int hk = 0;
-    grouped_unit(j, p.Hkv, nt, q_stream_group(1, p.Hq, p.Hkv, len, D), &hk, &kt);
-    bkv = sb * p.Hkv + hk;
-  } else {
-    grouped_unit(blockIdx.x, p.B * p.Hkv, nkt_all, p.kv_group, &bkv, &kt);  // key tiles ascending: heaviest first
-  }
-  const int b = bkv / p.Hkv, hkv = bkv % p.Hkv;
+  const int64_t u_begin = (int64_t)blockIdx.x * p.kv_run;
+  const int run = (int)min((int64_t)p.kv_run, p.kv_units - u_begin);   // units of this CTA: u_begin + j
   const int g = p.Hq / p.Hkv;
-  // the unit's sequence: its first token's row in the maps, its keys and
-  // query rows, and where its rows start in lse2 / dsum (head 0) and between
-  // query heads
-  if (ragged && !seq_range_ok(p.cu_seqlens, b, p.total, p.Nq)) {   // malformed: skipped and reported
-    if (threadIdx.x == 0) atomicOr(p.status, ATTN_DEV_BOUNDS);
-    return;
-  }
-  const int tok0 = ragged ? p.cu_seqlens[b] : 0;    // packed tensors hold fewer than 2^31 tokens
-  const int n_seq = ragged ? p.cu_seqlens[b + 1] - tok0 : p.Nk;
-  const int nq_seq = ragged ? n_seq : p.Nq;
-  if (kt * TILE >= n_seq) return;   // past the end of a shorter sequence; nothing is set up yet
-  const int64_t lrow_hs = ragged ? (int64_t)p.pcu[p.B] : (int64_t)p.Np;
-  const int64_t lrow_b = ragged ? (int64_t)p.pcu[b] : (int64_t)b * p.Hq * p.Np;
-  const int kv_head = ragged ? hkv : bkv;   // head coordinate in the K / V maps
-  const int nqt = (nq_seq + TILE - 1) / TILE;
-  const int qt_first = causal_of(p) ? first_query_tile(p, kt) : 0;
   WaitCtx wc{p.wait_limit_ns, p.status, &abort_flag};
 
+  if (warp >= 1 && warp < 4) {   // warps 1-3 decode the run's units, one warp per unit
+    for (int j = warp - 1; j < run; j += 3) {
+      KvUnit x;
+      const bool ok = kv_unit<D>(p, u_begin + j, x);
+      if (lane == 0) {
+        unit_ok[j] = ok ? 1 : 0;
+        if (ok) units[j] = x;
+      }
+    }
+  }
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(bar_kv, 1);
@@ -197,6 +245,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
     mbar_init(bar_dv, 1);
     mbar_init(bar_dk, 1);
     mbar_init(bar_done, 1);
+    mbar_init(bar_kvfree, 1);
+    mbar_init(bar_accfree, 256);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -219,49 +269,63 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
    if (warp == 0) {
     // ---------------------------------------------------------- producer
     // one lane per TMA copy (copies issued by one thread are serialised)
-    if (lane == 0) mbar_arrive_expect_tx(bar_kv, 2 * C::TILE_BYTES);
-    __syncwarp();
-    const int krow = tok0 + kt * TILE;
-    if (lane < C::NBOX) tma_load_3d(s_base + lane * C::BOX_BYTES, &tk, lane * 64, krow, kv_head, bar_kv);
-    else if (lane < 2 * C::NBOX)
-      tma_load_3d(s_base + OFF_V + (lane - C::NBOX) * C::BOX_BYTES, &tv, (lane - C::NBOX) * 64, krow, kv_head, bar_kv);
-    if (p.dkdv_counts != nullptr && lane == 0) {   // the unit's identity in the debug record
-      int32_t* rec = p.dkdv_counts + (size_t)DEBUG_FIELDS * blockIdx.x;
-      rec[0] = bkv;
-      rec[1] = kt;
-      rec[2] = 0;
-      rec[3] = tok0;
-    }
-    int n = 0;
+    int n = 0;    // stages loaded, over all units
+    int uc = 0;   // units whose K and V were loaded
     bool ok = true;
-    for (int h = 0; h < g && ok; ++h) {
-      const int hq = hkv * g + h;                 // query head within the batch
-      const int q_head = ragged ? hq : b * p.Hq + hq;
-      for (int qt = qt_first; qt < nqt && ok; ++qt) {
-        if (!tile_pair_visible(p, qt, kt)) continue;
-        const int s = n % NS;
-        if (n >= NS) ok = wait_bar(bar_qfree(s), ((n / NS) - 1) & 1, wc);
-        if (!(ok = __all_sync(0xffffffffu, ok))) break;
-        const uint32_t st = s_base + OFF_RING + s * STAGE;
-        if (lane == 0) mbar_arrive_expect_tx(bar_q(s), 2 * C::TILE_BYTES + 1024);
-        __syncwarp();
-        const size_t roff = (size_t)(lrow_b + hq * lrow_hs) + (size_t)qt * TILE;
-        const int qrow0 = tok0 + qt * TILE;
-        if (lane < C::NBOX)
-          tma_load_3d(st + lane * C::BOX_BYTES, &tq, lane * 64, qrow0, q_head, bar_q(s));
-        else if (lane < 2 * C::NBOX)
-          tma_load_3d(st + C::TILE_BYTES + (lane - C::NBOX) * C::BOX_BYTES, &tdo, (lane - C::NBOX) * 64, qrow0, q_head,
-                      bar_q(s));
-        else if (lane == 2 * C::NBOX)
-          bulk_load(st + 2 * C::TILE_BYTES, p.lse2 + roff, 512, bar_q(s));
-        else if (lane == 2 * C::NBOX + 1)
-          bulk_load(st + 2 * C::TILE_BYTES + 512, p.dsum + roff, 512, bar_q(s));
-        ++n;
+    for (int ju = 0; ju < run && ok; ++ju) {
+      if (!unit_ok[ju]) continue;
+      const KvUnit x = units[ju];   // in registers: asm with memory clobbers would force reloads
+      const int64_t u = u_begin + ju;
+      // K, V go into the same slots as the previous unit's: wait until its
+      // last S^T and dP^T products have read them
+      if (uc > 0) ok = wait_bar(bar_kvfree, (uint32_t)(uc - 1) & 1u, wc);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      if (lane == 0) mbar_arrive_expect_tx(bar_kv, 2 * C::TILE_BYTES);
+      __syncwarp();
+      const int krow = x.tok0 + x.kt * TILE;
+      if (lane < C::NBOX) tma_load_3d(s_base + lane * C::BOX_BYTES, &tk, lane * 64, krow, x.kv_head, bar_kv);
+      else if (lane < 2 * C::NBOX)
+        tma_load_3d(s_base + OFF_V + (lane - C::NBOX) * C::BOX_BYTES, &tv, (lane - C::NBOX) * 64, krow, x.kv_head,
+                    bar_kv);
+      ++uc;
+      int nu = 0;   // stages of this unit
+      for (int h = 0; h < g && ok; ++h) {
+        const int hq = x.hkv * g + h;                 // query head within the batch
+        const int q_head = p.cu_seqlens != nullptr ? hq : x.b * p.Hq + hq;
+        for (int qt = x.qt_first; qt < x.nqt && ok; ++qt) {
+          if (!tile_pair_visible(p, qt, x.kt)) continue;
+          const int s = n % NS;
+          if (n >= NS) ok = wait_bar(bar_qfree(s), ((n / NS) - 1) & 1, wc);
+          if (!(ok = __all_sync(0xffffffffu, ok))) break;
+          const uint32_t st = s_base + OFF_RING + s * STAGE;
+          if (lane == 0) mbar_arrive_expect_tx(bar_q(s), 2 * C::TILE_BYTES + 1024);
+          __syncwarp();
+          const size_t roff = (size_t)(x.lrow_b + hq * x.lrow_hs) + (size_t)qt * TILE;
+          const int qrow0 = x.tok0 + qt * TILE;
+          if (lane < C::NBOX)
+            tma_load_3d(st + lane * C::BOX_BYTES, &tq, lane * 64, qrow0, q_head, bar_q(s));
+          else if (lane < 2 * C::NBOX)
+            tma_load_3d(st + C::TILE_BYTES + (lane - C::NBOX) * C::BOX_BYTES, &tdo, (lane - C::NBOX) * 64, qrow0,
+                        q_head, bar_q(s));
+          else if (lane == 2 * C::NBOX)
+            bulk_load(st + 2 * C::TILE_BYTES, p.lse2 + roff, 512, bar_q(s));
+          else if (lane == 2 * C::NBOX + 1)
+            bulk_load(st + 2 * C::TILE_BYTES + 512, p.dsum + roff, 512, bar_q(s));
+          ++n;
+          ++nu;
+        }
+      }
+      if (p.dkdv_counts != nullptr && lane == 0) {   // the unit's identity and stages in its debug record
+        int32_t* rec = p.dkdv_counts + (size_t)DEBUG_FIELDS * u;
+        rec[0] = x.bkv;
+        rec[1] = x.kt;
+        rec[2] = 0;
+        rec[3] = x.tok0;
+        rec[4] = nu;
       }
     }
-    if (p.dkdv_counts != nullptr && lane == 0) p.dkdv_counts[(size_t)DEBUG_FIELDS * blockIdx.x + 4] = n;   // stages loaded
-    if ((!ok || abort_flag) && lane == 0) {
-      wait_bar(bar_kv, 0, wc, false);
+    if ((!ok || abort_flag) && lane == 0) {   // drain the copies still in flight
+      if (uc > 0) wait_bar(bar_kv, (uint32_t)(uc - 1) & 1u, wc, false);
       for (int j = n - NS < 0 ? 0 : n - NS; j < n; ++j) wait_bar(bar_q(j % NS), (j / NS) & 1, wc, false);
     }
    } else if (warp == 1) {
@@ -273,7 +337,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       // dP^T_{i+1}.  S^T_{i+1} overwrites the P^T_i columns dV_i reads and
       // dP^T_{i+1} the dS^T_i columns dK_i reads; each is issued right after
       // that reader (tcgen05.mma from one thread execute in issue order).
-      // Each elementwise phase has two MMAs of cover.
+      // Each elementwise phase has two MMAs of cover.  The next unit's S^T_0
+      // and dP^T_0 follow the last dK the same way.
       // tcgen05.mma issue stalls once a few MMAs are queued, so the issuer
       // is held for most of each group and anything it does between groups
       // idles the tensor pipe: it keeps ring counters only, and descriptors
@@ -305,54 +370,65 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
           mma_ss_e(tmem + 128, desc(d_v + kstep(kk)), desc(dd + kstep(kk)), id_s, kk > 0);
         mma_commit_e(bar_dp);
       };
-      int nvis = 0;
-      for (int qt = qt_first; qt < nqt; ++qt) nvis += tile_pair_visible(p, qt, kt) ? 1 : 0;
-      const int ntile = nvis * g;   // (query head, query tile) pairs, in the producer's order
-      bool ok = wt(bar_kv, 0);
-      if (ok && ntile > 0) {
-        ok = wt(bar_q(0), 0);
-        if (ok) {
-          tc_fence_after();
-          issue_st(0);
-          issue_dpt(0);
-        }
-      }
       int s = 0;
-      uint32_t spar = 0;   // ring slot of tile i and the parity of its fill
-      int i = 0;           // after the loop: query tiles whose dV and dK products were issued
-      for (; ok && i < ntile; ++i) {
-        const bool more = i + 1 < ntile;
-        const int sn = (s + 1 == NS) ? 0 : s + 1;
-        const uint32_t snpar = (s + 1 == NS) ? spar ^ 1u : spar;
-        const uint32_t par = (uint32_t)i & 1u;
-        const uint32_t md = d_ring_mn + (uint32_t)s * STAGE16;
-        // dV += P^T dO   (dO as an MN-major operand: N = d, K = query rows)
-        if (!(ok = wt(bar_p, par))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < TILE / 16; ++kk)
-          mma_ts_e(tmem + 256, tmem + half_col(kk), desc(md + TILE16 + (uint32_t)kk * (2048 >> 4)), id_acc,
-                 (i > 0 || kk > 0));
-        mma_commit_e(bar_dv);
-        if (more) {
-          if (!(ok = wt(bar_q(sn), snpar))) break;
+      uint32_t spar = 0;   // ring slot of the next query tile and the parity of its fill
+      int itot = 0;        // query tiles whose dV and dK products were issued, over all units
+      int uc = 0;          // units started
+      bool ok = true;
+      for (int ju = 0; ju < run && ok; ++ju) {
+        if (!unit_ok[ju]) continue;
+        const int ntile = units[ju].ntile;   // (query head, query tile) pairs, in the producer's order
+        if (!(ok = wt(bar_kv, (uint32_t)uc & 1u))) break;
+        if (ntile > 0) {
+          if (!(ok = wt(bar_q(s), spar))) break;
           tc_fence_after();
-          issue_st(sn);
+          issue_st(s);
+          issue_dpt(s);
         }
-        // dK += dS^T Q
-        if (!(ok = wt(bar_ds, par))) break;
-        tc_fence_after();
+        if (ntile <= 1) mma_commit_e(bar_kvfree);   // no later S^T or dP^T reads this unit's K and V
+        int i = 0;   // after the loop: query tiles of this unit whose dV and dK products were issued
+        for (; i < ntile; ++i) {
+          const bool more = i + 1 < ntile;
+          const int sn = (s + 1 == NS) ? 0 : s + 1;
+          const uint32_t snpar = (s + 1 == NS) ? spar ^ 1u : spar;
+          const uint32_t par = (uint32_t)itot & 1u;
+          const uint32_t md = d_ring_mn + (uint32_t)s * STAGE16;
+          // dV += P^T dO   (dO as an MN-major operand: N = d, K = query rows);
+          // the first dV of a unit overwrites the accumulator the previous
+          // unit's epilogue reads
+          if (!(ok = wt(bar_p, par))) break;
+          if (i == 0 && uc > 0 && !(ok = wt(bar_accfree, (uint32_t)(uc - 1) & 1u))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < TILE / 16; ++kk)
-          mma_ts_e(tmem + 256 + D, tmem + 128 + half_col(kk), desc(md + (uint32_t)kk * (2048 >> 4)), id_acc,
-                 (i > 0 || kk > 0));
-        mma_commit_e(bar_dk);
-        mma_commit_e(bar_qfree(s));
-        if (more) issue_dpt(sn);
-        s = sn;
-        spar = snpar;
+          for (int kk = 0; kk < TILE / 16; ++kk)
+            mma_ts_e(tmem + 256, tmem + half_col(kk), desc(md + TILE16 + (uint32_t)kk * (2048 >> 4)), id_acc,
+                     (i > 0 || kk > 0));
+          mma_commit_e(bar_dv);
+          if (more) {
+            if (!(ok = wt(bar_q(sn), snpar))) break;
+            tc_fence_after();
+            issue_st(sn);
+          }
+          // dK += dS^T Q
+          if (!(ok = wt(bar_ds, par))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < TILE / 16; ++kk)
+            mma_ts_e(tmem + 256 + D, tmem + 128 + half_col(kk), desc(md + (uint32_t)kk * (2048 >> 4)), id_acc,
+                     (i > 0 || kk > 0));
+          mma_commit_e(bar_dk);
+          mma_commit_e(bar_qfree(s));
+          if (more) {
+            issue_dpt(sn);
+            if (i + 2 == ntile) mma_commit_e(bar_kvfree);   // the unit's last S^T and dP^T are issued
+          }
+          s = sn;
+          spar = snpar;
+          ++itot;
+        }
+        if (p.dkdv_counts != nullptr && lane == 0) p.dkdv_counts[(size_t)DEBUG_FIELDS * (u_begin + ju) + 5] = i;
+        ++uc;
       }
-      if (p.dkdv_counts != nullptr && lane == 0) p.dkdv_counts[(size_t)DEBUG_FIELDS * blockIdx.x + 5] = i;
       mma_commit_e(bar_done);
       wait_bar(bar_done, 0, wc, false);
     }
@@ -368,138 +444,156 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
     const int wq = warp & 3;
     const int r = wq * 32 + lane;                   // key row inside the tile
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t stage = s_base + OFF_EPI + (uint32_t)(warp - 4) * 1024u;
     const float c = p.scale_log2;
     const bool causal = causal_of(p);
-    int i = 0;
+    const bool ragged = p.cu_seqlens != nullptr;
+    int i = 0;   // query tiles processed, over all units
     bool ok = true;
-    for (int h = 0; h < g && ok; ++h) {
-      for (int qt = qt_first; qt < nqt; ++qt) {
-        if (!tile_pair_visible(p, qt, kt)) continue;
-        const int s = i % NS;
-        const float* lse2 = reinterpret_cast<const float*>(smem + OFF_RING + s * STAGE + 2 * C::TILE_BYTES);
-        const float* dsum = lse2 + 128;
-        ok = wait_bar(bar_q(s), (i / NS) & 1, wc) && wait_bar(bar_s, i & 1, wc);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-        // key r sees query column j iff 0 <= base + j - r < window: j >= lo
-        // where the causal edge crosses the tile, j < hi where the window's
-        // edge does
-        const int base = tile_base(p, qt, kt);
-        const bool cedge = causal && base < TILE - 1;
-        const bool wedge = base + (TILE - 1) >= window_of(p);
-        const int hi = wedge ? window_of(p) + r - base : TILE;
-        const float4* l4 = reinterpret_cast<const float4*>(lse2) + 16 * hf;
-        const float4* d4 = reinterpret_cast<const float4*>(dsum) + 16 * hf;
-        // phase A: P^T = 2^(S^T c - lse2) for this warpgroup's 64 query columns,
-        // kept in fp32 for phase B and rounded to bf16 pairs for dV = P^T dO.
-        // Masked tiles (the diagonal, a window's edge) take their own copy of
-        // the loop so that the others carry no mask arithmetic at all.
-        float pf[64];
-        auto phase_a = [&](auto masked) {
-          uint32_t sr[64];
-          tmem_ld64(tmem + lane_off + cb, sr);
-          const int lo = cedge ? r - base : 0;        // visible query columns: lo <= j < hi
+    for (int ju = 0; ju < run && ok; ++ju) {
+      if (!unit_ok[ju]) continue;
+      const KvUnit x = units[ju];   // in registers: asm with memory clobbers would force reloads
+      const int64_t u = u_begin + ju;
+      const int kt = x.kt;
+      const int i0 = i;
+      for (int h = 0; h < g && ok; ++h) {
+        for (int qt = x.qt_first; qt < x.nqt; ++qt) {
+          if (!tile_pair_visible(p, qt, kt)) continue;
+          const int s = i % NS;
+          const float* lse2 = reinterpret_cast<const float*>(smem + OFF_RING + s * STAGE + 2 * C::TILE_BYTES);
+          const float* dsum = lse2 + 128;
+          ok = wait_bar(bar_q(s), (i / NS) & 1, wc) && wait_bar(bar_s, i & 1, wc);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+          // key r sees query column j iff 0 <= base + j - r < window: j >= lo
+          // where the causal edge crosses the tile, j < hi where the window's
+          // edge does
+          const int base = tile_base(p, qt, kt);
+          const bool cedge = causal && base < TILE - 1;
+          const bool wedge = base + (TILE - 1) >= window_of(p);
+          const int hi = wedge ? window_of(p) + r - base : TILE;
+          const float4* l4 = reinterpret_cast<const float4*>(lse2) + 16 * hf;
+          const float4* d4 = reinterpret_cast<const float4*>(dsum) + 16 * hf;
+          // phase A: P^T = 2^(S^T c - lse2) for this warpgroup's 64 query columns,
+          // kept in fp32 for phase B and rounded to bf16 pairs for dV = P^T dO.
+          // Masked tiles (the diagonal, a window's edge) take their own copy of
+          // the loop so that the others carry no mask arithmetic at all.
+          float pf[64];
+          auto phase_a = [&](auto masked) {
+            uint32_t sr[64];
+            tmem_ld64(tmem + lane_off + cb, sr);
+            const int lo = cedge ? r - base : 0;        // visible query columns: lo <= j < hi
 #pragma unroll
-          for (int j4 = 0; j4 < 16; ++j4) {
-            const float4 L = l4[j4];
-            const int col = cb + 4 * j4;
-            float x0, x1, x2, x3;
-            fma2(x0, x1, __uint_as_float(sr[4 * j4 + 0]), __uint_as_float(sr[4 * j4 + 1]), c, c, -L.x, -L.y);
-            fma2(x2, x3, __uint_as_float(sr[4 * j4 + 2]), __uint_as_float(sr[4 * j4 + 3]), c, c, -L.z, -L.w);
-            float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-            if constexpr (decltype(masked)::value) {
-              p0 = (col + 0 >= lo && col + 0 < hi) ? p0 : 0.f;
-              p1 = (col + 1 >= lo && col + 1 < hi) ? p1 : 0.f;
-              p2 = (col + 2 >= lo && col + 2 < hi) ? p2 : 0.f;
-              p3 = (col + 3 >= lo && col + 3 < hi) ? p3 : 0.f;
-            }
-            pf[4 * j4 + 0] = p0;
-            pf[4 * j4 + 1] = p1;
-            pf[4 * j4 + 2] = p2;
-            pf[4 * j4 + 3] = p3;
-          }
-        };
-        if (cedge || wedge) phase_a(std::true_type{});
-        else phase_a(std::false_type{});
-        {
-          uint32_t pk[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) pk[j] = pack_bf16(pf[2 * j], pf[2 * j + 1]);
-          tmem_st32(tmem + lane_off + cb, pk);
-        }
-        tc_fence_before();
-        mbar_arrive(bar_p);
-        ok = wait_bar(bar_dp, i & 1, wc);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-        // phase B: dS^T = P^T * (dP^T - D) for the same 64 columns; the bf16
-        // pairs go over the first 32 dP^T columns of the half
-        {
-          uint32_t dr[64];
-          tmem_ld64(tmem + lane_off + 128 + cb, dr);
-          uint32_t ds[32];
-#pragma unroll
-          for (int j4 = 0; j4 < 16; ++j4) {
-            const float4 Dv = d4[j4];
-            float t0, t1, t2, t3, d0, d1, d2, d3;
-            add2(t0, t1, __uint_as_float(dr[4 * j4 + 0]), __uint_as_float(dr[4 * j4 + 1]), -Dv.x, -Dv.y);
-            add2(t2, t3, __uint_as_float(dr[4 * j4 + 2]), __uint_as_float(dr[4 * j4 + 3]), -Dv.z, -Dv.w);
-            mul2(d0, d1, pf[4 * j4 + 0], pf[4 * j4 + 1], t0, t1);
-            mul2(d2, d3, pf[4 * j4 + 2], pf[4 * j4 + 3], t2, t3);
-            ds[2 * j4] = pack_bf16(d0, d1);
-            ds[2 * j4 + 1] = pack_bf16(d2, d3);
-          }
-          tmem_st32(tmem + lane_off + 128 + cb, ds);
-        }
-        tc_fence_before();
-        mbar_arrive(bar_ds);
-        ++i;
-      }
-    }
-    if (p.dkdv_counts != nullptr && r == 0) p.dkdv_counts[(size_t)DEBUG_FIELDS * blockIdx.x + 6 + hf] = i;
-    // ---------------------------------------------------------- epilogue
-    if (ok && !abort_flag) {
-      if (i > 0) {
-        ok = wait_bar(bar_dv, (i - 1) & 1, wc) && wait_bar(bar_dk, (i - 1) & 1, wc);
-        ok = __all_sync(0xffffffffu, ok);
-      }
-      if (ok) {
-        tc_fence_after();
-        // warpgroup 0 writes dV, warpgroup 1 writes scale * dK; the rows are
-        // staged through shared memory no MMA or copy uses any more (the K and
-        // V tiles') so that each store instruction covers whole rows
-        const float mul = hf == 0 ? 1.f : p.scale;
-        const int wkey0 = kt * TILE + wq * 32;   // this warp's first key
-        if constexpr (F32) {
-          // float32 rows, 32 columns at a time through this warp's 4 KB of
-          // staging; added (p.accumulate) or stored.  With no visible query
-          // tile an add has nothing to contribute and a store writes zeros.
-          float* base = static_cast<float*>(hf == 0 ? p.dv : p.dk) + ((size_t)bkv * p.dkv_hs + wkey0) * D;
-          const uint32_t stage = s_base + (uint32_t)(warp - 4) * (32u * 32u * 4u);
-          if (i > 0 || !p.accumulate) {
-#pragma unroll
-            for (int q4 = 0; q4 < D / 32; ++q4) {
-              uint32_t rv[32];
-              if (i > 0) {
-                tmem_ld32(tmem + lane_off + 256 + hf * D + q4 * 32, rv);
-              } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) rv[j] = 0u;
+            for (int j4 = 0; j4 < 16; ++j4) {
+              const float4 L = l4[j4];
+              const int col = cb + 4 * j4;
+              float x0, x1, x2, x3;
+              fma2(x0, x1, __uint_as_float(sr[4 * j4 + 0]), __uint_as_float(sr[4 * j4 + 1]), c, c, -L.x, -L.y);
+              fma2(x2, x3, __uint_as_float(sr[4 * j4 + 2]), __uint_as_float(sr[4 * j4 + 3]), c, c, -L.z, -L.w);
+              float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+              if constexpr (decltype(masked)::value) {
+                p0 = (col + 0 >= lo && col + 0 < hi) ? p0 : 0.f;
+                p1 = (col + 1 >= lo && col + 1 < hi) ? p1 : 0.f;
+                p2 = (col + 2 >= lo && col + 2 < hi) ? p2 : 0.f;
+                p3 = (col + 3 >= lo && col + 3 < hi) ? p3 : 0.f;
               }
+              pf[4 * j4 + 0] = p0;
+              pf[4 * j4 + 1] = p1;
+              pf[4 * j4 + 2] = p2;
+              pf[4 * j4 + 3] = p3;
+            }
+          };
+          if (cedge || wedge) phase_a(std::true_type{});
+          else phase_a(std::false_type{});
+          {
+            uint32_t pk[32];
 #pragma unroll
-              for (int j = 0; j < 32; ++j) rv[j] = __float_as_uint(__uint_as_float(rv[j]) * mul);
-              char* dst = reinterpret_cast<char*>(base + q4 * 32);
-              if (p.accumulate) warp_store_rows<8, true>(stage, rv, dst, (size_t)D * 4, n_seq - wkey0);
-              else warp_store_rows<8>(stage, rv, dst, (size_t)D * 4, n_seq - wkey0);
+            for (int j = 0; j < 32; ++j) pk[j] = pack_bf16(pf[2 * j], pf[2 * j + 1]);
+            tmem_st32(tmem + lane_off + cb, pk);
+          }
+          tc_fence_before();
+          mbar_arrive(bar_p);
+          ok = wait_bar(bar_dp, i & 1, wc);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+          // phase B: dS^T = P^T * (dP^T - D) for the same 64 columns; the bf16
+          // pairs go over the first 32 dP^T columns of the half
+          {
+            uint32_t dr[64];
+            tmem_ld64(tmem + lane_off + 128 + cb, dr);
+            uint32_t ds[32];
+#pragma unroll
+            for (int j4 = 0; j4 < 16; ++j4) {
+              const float4 Dv = d4[j4];
+              float t0, t1, t2, t3, d0, d1, d2, d3;
+              add2(t0, t1, __uint_as_float(dr[4 * j4 + 0]), __uint_as_float(dr[4 * j4 + 1]), -Dv.x, -Dv.y);
+              add2(t2, t3, __uint_as_float(dr[4 * j4 + 2]), __uint_as_float(dr[4 * j4 + 3]), -Dv.z, -Dv.w);
+              mul2(d0, d1, pf[4 * j4 + 0], pf[4 * j4 + 1], t0, t1);
+              mul2(d2, d3, pf[4 * j4 + 2], pf[4 * j4 + 3], t2, t3);
+              ds[2 * j4] = pack_bf16(d0, d1);
+              ds[2 * j4 + 1] = pack_bf16(d2, d3);
+            }
+            tmem_st32(tmem + lane_off + 128 + cb, ds);
+          }
+          tc_fence_before();
+          mbar_arrive(bar_ds);
+          ++i;
+        }
+      }
+      const int nt = i - i0;   // query tiles of this unit
+      if (p.dkdv_counts != nullptr && r == 0) p.dkdv_counts[(size_t)DEBUG_FIELDS * u + 6 + hf] = nt;
+      if (!ok || abort_flag) break;
+      // ---------------------------------------------------------- epilogue
+      // warpgroup 0 writes dV, warpgroup 1 writes scale * dK, each row
+      // through this warp's 1 KB of staging so that every store instruction
+      // covers 32-byte pieces of 16 rows
+      if (nt > 0) {
+        ok = wait_bar(bar_dv, (uint32_t)(i - 1) & 1u, wc) && wait_bar(bar_dk, (uint32_t)(i - 1) & 1u, wc);
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
+        tc_fence_after();
+      }
+      const float mul = hf == 0 ? 1.f : p.scale;
+      const int wkey0 = kt * TILE + wq * 32;   // this warp's first key
+      const uint32_t acc = tmem + lane_off + 256 + hf * D;
+      if constexpr (F32) {
+        // float32 rows, 16 columns at a time (two 32-byte pieces); added
+        // (p.accumulate) or stored.  With no visible query tile an add has
+        // nothing to contribute and a store writes zeros.
+        char* base = reinterpret_cast<char*>(static_cast<float*>(hf == 0 ? p.dv : p.dk) +
+                                             ((size_t)x.bkv * p.dkv_hs + wkey0) * D);
+        if (nt > 0 || !p.accumulate) {
+#pragma unroll 1
+          for (int q = 0; q < D / 16; ++q) {
+            uint32_t rv[16];
+            if (nt > 0) {
+              tmem_ld16(acc + q * 16, rv);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) rv[j] = 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) rv[j] = __float_as_uint(__uint_as_float(rv[j]) * mul);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              if (p.accumulate)
+                warp_store_rows<2, true>(stage, rv + 8 * hh, base + q * 64 + hh * 32, (size_t)D * 4, x.n_seq - wkey0);
+              else
+                warp_store_rows<2>(stage, rv + 8 * hh, base + q * 64 + hh * 32, (size_t)D * 4, x.n_seq - wkey0);
             }
           }
-        } else {
+        }
+        tc_fence_before();
+        mbar_arrive(bar_accfree);   // the accumulators have been read
+      } else {
+        // read all of the row's accumulator columns first (the next unit's
+        // first dV product waits for them), then store 32 bytes of each row
+        // per round from registers
         uint32_t w[D / 2];
 #pragma unroll
         for (int q4 = 0; q4 < D / 32; ++q4) {
           uint32_t rv[32];
-          if (i > 0) {
-            tmem_ld32(tmem + lane_off + 256 + hf * D + q4 * 32, rv);
+          if (nt > 0) {
+            tmem_ld32(acc + q4 * 32, rv);
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) rv[j] = 0u;
@@ -508,11 +602,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
           for (int j = 0; j < 16; ++j)
             w[q4 * 16 + j] = pack_bf16(__uint_as_float(rv[2 * j]) * mul, __uint_as_float(rv[2 * j + 1]) * mul);
         }
-        const size_t orow0 = ragged ? (size_t)(tok0 + wkey0) * p.Hkv + hkv : (size_t)bkv * p.dkv_hs + wkey0;
+        tc_fence_before();
+        mbar_arrive(bar_accfree);   // the accumulators have been read
+        const size_t orow0 = ragged ? (size_t)(x.tok0 + wkey0) * p.Hkv + x.hkv : (size_t)x.bkv * p.dkv_hs + wkey0;
         char* base = reinterpret_cast<char*>(static_cast<__nv_bfloat16*>(hf == 0 ? p.dv : p.dk) + orow0 * D);
         const size_t stride = (ragged ? (size_t)p.Hkv : (size_t)1) * D * sizeof(__nv_bfloat16);
-        warp_store_rows<D / 8>(s_base + (uint32_t)(warp - 4) * (32u * D * 2), w, base, stride, n_seq - wkey0);
-        }
+#pragma unroll
+        for (int q = 0; q < D / 16; ++q) warp_store_rows<2>(stage, w + 8 * q, base + q * 32, stride, x.n_seq - wkey0);
       }
     }
   }
@@ -947,15 +1043,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
 }
 
 template <int D>
-constexpr uint32_t dkdv_smem() {
-  return 2 * BwdCfg<D>::TILE_BYTES + BwdCfg<D>::NS * (2 * BwdCfg<D>::TILE_BYTES + 1024) + 1024;
+constexpr uint32_t dkdv_smem() {   // K, V, the ring, 8 x 1 KB of epilogue staging, alignment slack
+  return 2 * BwdCfg<D>::TILE_BYTES + BwdCfg<D>::NS * (2 * BwdCfg<D>::TILE_BYTES + 1024) + 8 * 1024 + 1024;
 }
 template <int D, bool F32>
 cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const BwdParams& p, cudaStream_t s) {
   constexpr uint32_t smem = dkdv_smem<D>();
   static_assert(smem <= 232448 - 256, "dK/dV shared memory");
-  static_assert(8 * 32 * 32 * 4 <= 2 * BwdCfg<D>::TILE_BYTES, "f32 epilogue staging fits in the K and V tiles");
   cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = dkdv_grid(p);

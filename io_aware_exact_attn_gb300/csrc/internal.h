@@ -83,15 +83,18 @@ struct BwdParams {
   int64_t total;            // tokens in the packed tensors
   int kv_group;             // kv heads per L2 group of the dK/dV kernel
   int q_group;              // query heads per L2 group of the dQ kernel
+  int64_t kv_units;         // dK/dV work units in launch order (dkdv_units)
+  int kv_run;               // consecutive dK/dV units per CTA
   unsigned int* status;
   int64_t wait_limit_ns;
   int32_t* dkdv_counts;     // per-CTA debug records of the two kernels, or null
   int32_t* dq_counts;
 };
 
-// Per-CTA debug record: DEBUG_FIELDS int32 at [DEBUG_FIELDS * blockIdx.x] of
-// the launch's record array; the fields of each kernel are listed with
-// attn_debug_set_tile_counts in attn.h.
+// Debug record: DEBUG_FIELDS int32 per work unit (the forward and dQ kernels:
+// per CTA, [DEBUG_FIELDS * blockIdx.x]; the dK/dV kernel: per unit of its
+// launch order) of the launch's record array; the fields of each kernel are
+// listed with attn_debug_set_tile_counts in attn.h.
 constexpr int DEBUG_FIELDS = 8;
 
 // Grid sizes (one CTA per work unit), shared by the launchers and by the
@@ -108,9 +111,13 @@ inline unsigned fwd_grid(const FwdParams& p) {
          : p.cu_seqlens != nullptr ? ragged_grid(p.B, p.Hq, p.total, p.Nq, UNIT_ROWS)
                                    : (unsigned)(p.B * p.Hq) * (unsigned)p.nqc;
 }
-inline unsigned dkdv_grid(const BwdParams& p) {
+inline unsigned dkdv_units(const BwdParams& p) {
   return p.cu_seqlens != nullptr ? ragged_grid(p.B, p.Hkv, p.total, p.Nk, TILE)
                                  : (unsigned)(p.B * p.Hkv) * (unsigned)((p.Nk + TILE - 1) / TILE);
+}
+// The dK/dV kernel gives each CTA a run of kv_run consecutive units.
+inline unsigned dkdv_grid(const BwdParams& p) {
+  return (unsigned)((p.kv_units + p.kv_run - 1) / p.kv_run);
 }
 inline unsigned dq_grid(const BwdParams& p) {
   return p.cu_seqlens != nullptr ? ragged_grid(p.B, p.Hq, p.total, p.Nq, TILE)
