@@ -13,10 +13,11 @@
 //   - every operand is K-major (128-byte rows = 128 e4m3 values): Q and K as
 //     stored, V as V^T (head-dim rows, keys contiguous), written to a
 //     workspace by a transpose kernel first;
-//   - P goes to shared memory as e4m3, and PV is a shared x shared product;
-//     with P out of tensor memory, S_t of the next key tile no longer waits
-//     for PV_t: it is issued as soon as the softmax has read S_t, so the next
-//     scores are ready when the softmax finishes;
+//   - P goes back to tensor memory as e4m3 (four per 32-bit column) over the
+//     first 32 columns of S_t, and PV takes it from there (the TS form): of
+//     the two products only S reads both operands from shared memory, and
+//     nothing writes P to shared memory.  As in fwd.cu, S_t of the next key
+//     tile is issued right behind the PV_t that reads those columns;
 //   - P is taken against the running max minus 7 and the max moves as soon as
 //     it grows by more than 1 (log2 units), so P <= 2^8 fits e4m3 (largest
 //     finite 448) and weights down to 2^-16 of the row max stay representable;
@@ -43,12 +44,11 @@ constexpr float FP8_P_OFFSET = 7.0f;   // P = 2^(x - m + 7) <= 2^(1 + 7)
 
 struct Fp8Cfg {
   static constexpr int D = 128;
-  static constexpr int NS = 4;                                // K / V^T ring depth
+  static constexpr int NS = 6;                                // K / V^T ring depth
   static constexpr uint32_t TILE_BYTES = 128 * 128;           // 128 rows x 128 bytes
   static constexpr uint32_t OFF_K = 2 * TILE_BYTES;           // after Q_0, Q_1
   static constexpr uint32_t OFF_V = OFF_K + NS * TILE_BYTES;  // V^T tiles: 128 head-dim rows x 128 keys
-  static constexpr uint32_t OFF_P = OFF_V + NS * TILE_BYTES;  // P_0, P_1: 128 query rows x 128 keys
-  static constexpr uint32_t SMEM_BYTES = OFF_P + 2 * TILE_BYTES + 1024;
+  static constexpr uint32_t SMEM_BYTES = OFF_V + NS * TILE_BYTES + 1024;
   static constexpr uint32_t TMEM_O = 256;
   static constexpr int THREADS = 384;
   static constexpr uint32_t REGS_CTRL = 56, REGS_SOFTMAX = 224;
@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
   constexpr int D = C::D;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bars[1 + 4 * NS + 9];
+  __shared__ __align__(8) uint64_t bars[1 + 4 * NS + 7];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -74,10 +74,9 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
   auto bar_kfree = [&](int s) { return smem_u32(&bars[1 + 2 * NS + s]); };  // K slot read by both S MMAs
   auto bar_vfree = [&](int s) { return smem_u32(&bars[1 + 3 * NS + s]); };  // V^T slot read by both PV MMAs
   auto bar_s = [&](int t) { return smem_u32(&bars[1 + 4 * NS + t]); };       // S_t in TMEM
-  auto bar_sread = [&](int t) { return smem_u32(&bars[1 + 4 * NS + 2 + t]); };  // softmax t has read S_t
-  auto bar_p = [&](int t) { return smem_u32(&bars[1 + 4 * NS + 4 + t]); };   // P_t in shared memory
-  auto bar_o = [&](int t) { return smem_u32(&bars[1 + 4 * NS + 6 + t]); };   // PV_t done
-  const uint32_t bar_done = smem_u32(&bars[1 + 4 * NS + 8]);
+  auto bar_p = [&](int t) { return smem_u32(&bars[1 + 4 * NS + 2 + t]); };   // P_t in TMEM
+  auto bar_o = [&](int t) { return smem_u32(&bars[1 + 4 * NS + 4 + t]); };   // PV_t done
+  const uint32_t bar_done = smem_u32(&bars[1 + 4 * NS + 6]);
 
   const Unit u = fwd_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.Nq, p.Nk, p.nqc, p.head_group, p.mask_kind,
                           p.causal_in_blocks, p.block_mask, p.nkb, p.window, p.q_offset, p.kv_offset);
@@ -94,7 +93,6 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_s(t), 1);
-      mbar_init(bar_sread(t), 128);
       mbar_init(bar_p(t), 128);
       mbar_init(bar_o(t), 1);
     }
@@ -151,10 +149,13 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
     }
    } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // S_0(0), S_1(0); then per key tile n: S_t(n+1) as soon as softmax t has
-    // read S_t(n) out of tensor memory, and PV_t(n) once P_t(n) is in shared
-    // memory.  Each product is four MMAs of K = 32; a k-step adds 32 bytes (2
-    // in the descriptor's 16-byte units) inside the 128-byte swizzled rows.
+    // Order per key tile n: PV_0(n), S_0(n+1), PV_1(n), S_1(n+1).  S_t(n+1)
+    // overwrites the columns P_t(n) occupies; it is issued right after the
+    // PV_t(n) that reads them (tcgen05.mma from one thread execute in issue
+    // order), so each softmax has the other tile's PV and S of cover.  Each
+    // product is four MMAs of K = 32; a k-step adds 32 bytes (2 in the
+    // descriptor's 16-byte units) inside the 128-byte swizzled rows, or 8
+    // tensor-memory columns of P.
     // The loop keeps ring counters only, with the descriptors' upper words
     // fixed and the lower words built once; the whole warp runs it and
     // elect.sync picks the issuing lane (always the same one while the warp
@@ -168,7 +169,6 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
       const uint32_t d_q = (uint32_t)sdesc_sw128(s_base, 16, 1024);
       const uint32_t d_k = (uint32_t)sdesc_sw128(s_base + C::OFF_K, 16, 1024);
       const uint32_t d_v = (uint32_t)sdesc_sw128(s_base + C::OFF_V, 16, 1024);
-      const uint32_t d_p = (uint32_t)sdesc_sw128(s_base + C::OFF_P, 16, 1024);
       auto desc = [&](uint32_t lo) { return ((uint64_t)HI << 32) | lo; };
       auto next_kt = [&](int from) {
         int k = from;
@@ -182,14 +182,13 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
           mma_ss_f8_e(tmem + t * 128, desc(qd + kk * 2), desc(kd + kk * 2), ID, kk > 0);
         mma_commit_e(bar_s(t));
       };
-      auto issue_pv = [&](int t, int slot, bool acc) {   // O_t += P_t (V^T)^T
-        const uint32_t vd = d_v + (uint32_t)slot * TILE16, pd = d_p + (uint32_t)t * TILE16;
+      auto issue_pv = [&](int t, int slot, bool acc) {   // O_t += P_t (V^T)^T, P_t from tensor memory
+        const uint32_t vd = d_v + (uint32_t)slot * TILE16;
 #pragma unroll
         for (int kk = 0; kk < TILE / 32; ++kk)
-          mma_ss_f8_e(tmem + C::TMEM_O + t * D, desc(pd + kk * 2), desc(vd + kk * 2), ID, acc || kk > 0);
+          mma_ts_f8_e(tmem + C::TMEM_O + t * D, tmem + t * 128 + kk * 8, desc(vd + kk * 2), ID, acc || kk > 0);
         mma_commit_e(bar_o(t));
       };
-      int cs0 = 0, cs1 = 0;   // S MMAs issued per query tile
       int cp0 = 0, cp1 = 0;   // PV MMAs issued per query tile
       bool ok = wt(bar_q, 0);
       int kt = next_kt(u.kt_begin);
@@ -198,8 +197,8 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
         ok = wt(bar_k(0), 0);
         if (ok) {
           tc_fence_after();
-          if (use & 1u) { issue_s(0, 0); ++cs0; }
-          if (use & 2u) { issue_s(1, 0); ++cs1; }
+          if (use & 1u) issue_s(0, 0);
+          if (use & 2u) issue_s(1, 0);
           mma_commit_e(bar_kfree(0));
         }
       }
@@ -210,24 +209,7 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
         const uint32_t phn = (s + 1 == NS) ? ph ^ 1u : ph;
         const int ktn = next_kt(kt + 1);
         const uint32_t usen = ktn < u.kt_end ? unit_uses(u, ktn) : 0u;
-        if (usen) {
-          // the next scores, each as soon as its softmax has read the current ones
-          if (!(ok = wt(bar_k(sn), phn))) break;
-          if (usen & 1u) {
-            if (cs0 > 0 && !(ok = wt(bar_sread(0), (uint32_t)(cs0 - 1) & 1u))) break;
-            tc_fence_after();
-            issue_s(0, sn);
-            ++cs0;
-          }
-          if (usen & 2u) {
-            if (cs1 > 0 && !(ok = wt(bar_sread(1), (uint32_t)(cs1 - 1) & 1u))) break;
-            tc_fence_after();
-            issue_s(1, sn);
-            ++cs1;
-          }
-          mma_commit_e(bar_kfree(sn));
-        }
-        // this key tile's P.V products
+        bool kwaited = false;
         if (!(ok = wt(bar_v(s), ph))) break;
         if (use & 1u) {
           if (!(ok = wt(bar_p(0), (uint32_t)cp0 & 1u))) break;
@@ -235,13 +217,25 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
           issue_pv(0, s, cp0 > 0);
           ++cp0;
         }
+        if (usen & 1u) {
+          if (!(ok = wt(bar_k(sn), phn))) break;
+          tc_fence_after();
+          kwaited = true;
+          issue_s(0, sn);
+        }
         if (use & 2u) {
           if (!(ok = wt(bar_p(1), (uint32_t)cp1 & 1u))) break;
           tc_fence_after();
           issue_pv(1, s, cp1 > 0);
           ++cp1;
         }
-        mma_commit_e(bar_vfree(s));
+        mma_commit_e(bar_vfree(s));   // both P.V products of this key tile issued
+        if (usen & 2u) {
+          if (!kwaited && !(ok = wt(bar_k(sn), phn))) break;
+          tc_fence_after();
+          issue_s(1, sn);
+        }
+        if (usen) mma_commit_e(bar_kfree(sn));
         kt = ktn;
         use = usen;
         s = sn;
@@ -262,7 +256,6 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + t * 128;
     const uint32_t tO = tmem + lane_off + C::TMEM_O + t * D;
-    const uint32_t p_row = s_base + C::OFF_P + t * C::TILE_BYTES + r * 128;   // this row of P_t
     const float c = p.scale_log2;                  // scale * log2(e) * dequantisation of Q and K
     const bool causal = mask_is_causal(p.mask_kind, p.causal_in_blocks);
     const int64_t row_first_pos = p.q_offset + u.row0 + t * TILE;
@@ -294,8 +287,8 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
           lo = (int)(f64 < 0 ? 0 : (f64 > 128 ? 128 : f64));
         }
       }
-      // the whole score row into registers; S_t may then be overwritten by the
-      // next key tile's scores, so everything below works from registers
+      // the whole score row into registers (P_t then goes over its first 32
+      // columns)
       float s[128];
       {
         uint32_t rr[128];
@@ -303,8 +296,6 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 128; ++j) s[j] = __uint_as_float(rr[j]);
       }
-      tc_fence_before();
-      mbar_arrive(bar_sread(t));
       if (edge) {
 #pragma unroll
         for (int j = 0; j < 128; ++j) s[j] = (j >= lo && j < lim) ? s[j] : -INFINITY;
@@ -341,25 +332,21 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
         const int a = (j >> 1) & 3;
         add2(la[2 * a], la[2 * a + 1], la[2 * a], la[2 * a + 1], s[j], s[j + 1]);
       }
-      // P_t of the previous key tile must have been read by its PV (and O_t
-      // must hold it before a rescale)
-      if (it > 0) {
+      // P as e4m3 into the first 32 columns of S_t: column j holds keys
+      // 4j..4j+3, the first in the lowest byte
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pk[j] = pack_e4m3x4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]);
+        tmem_st32(tS, pk);
+      }
+      // O_t must hold the previous PV before a rescale (PV_t of this key tile
+      // follows it on the tensor core, so nothing else has to wait)
+      if (rescale) {
         ok = wait_bar(bar_o(t), (it - 1) & 1, wc);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
       }
-      // P as e4m3 into this row of P_t: 16-byte chunk k (keys 16k..16k+15) at
-      // chunk k ^ (row & 7) of the 128-byte row (the 128-byte swizzle)
-#pragma unroll
-      for (int k16 = 0; k16 < 8; ++k16) {
-        const int j = 16 * k16;
-        const uint32_t w0 = pack_e4m3x4(s[j + 0], s[j + 1], s[j + 2], s[j + 3]);
-        const uint32_t w1 = pack_e4m3x4(s[j + 4], s[j + 5], s[j + 6], s[j + 7]);
-        const uint32_t w2 = pack_e4m3x4(s[j + 8], s[j + 9], s[j + 10], s[j + 11]);
-        const uint32_t w3 = pack_e4m3x4(s[j + 12], s[j + 13], s[j + 14], s[j + 15]);
-        st_shared_v4(p_row + (uint32_t)((k16 ^ (r & 7)) << 4), w0, w1, w2, w3);
-      }
-      fence_proxy_async_smem();   // the tensor core reads P through the async proxy
       if (rescale) {
 #pragma unroll
         for (int h64 = 0; h64 < D / 64; ++h64) {

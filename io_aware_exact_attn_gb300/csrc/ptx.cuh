@@ -201,6 +201,20 @@ __device__ __forceinline__ void mma_ss_f8_e(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// e4m3 x e4m3 with A from tensor memory: 4 values of a row per 32-bit
+// column, consecutive along K (the first in the lowest byte), so a K = 32
+// step reads 8 columns.
+__device__ __forceinline__ void mma_ts_f8_e(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 op issued so far by the elected
 // thread completes.
 __device__ __forceinline__ void mma_commit_e(uint32_t bar) {
