@@ -267,7 +267,8 @@ def main():
     ap.add_argument("--profile-pass", action="store_true",
                     help="one untimed step and one E4M3 forward only (for profiler captures); prints nothing")
     ap.add_argument("--profile-workload", default=None,
-                    choices=["gpt", "gpt_noncausal", "block_sparse", "bert_large", "decode", "varlen", "chunked_bwd"],
+                    choices=["gpt", "gpt_noncausal", "block_sparse", "bert_large", "decode", "varlen", "chunked_bwd",
+                             "fp8"],
                     help="one untimed forward + backward of the named workload only (for profiler captures; the "
                          "ragged batch is cut to 8 sequences); prints nothing")
     args = ap.parse_args()
@@ -474,6 +475,10 @@ def profile_workload(name, api, inputs, torch):
         cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32).cuda()
         o, lse = api.attn_varlen_fwd(q, k, v, cu, max(lens), causal=True)
         api.attn_varlen_bwd(q, k, v, o, lse, do, cu, max(lens), causal=True)
+    elif name == "fp8":
+        f = FP8
+        q8, k8, v8, (qd, kd, vd) = inputs.make_qkv_e4m3(f["B"], f["Hq"], f["Hkv"], f["N"], f["d"])
+        api.attn_fwd_fp8(q8.cuda(), k8.cuda(), v8.cuda(), qd, kd, vd, causal=True)
     elif name == "chunked_bwd":
         c = CHUNKED
         q, k, v, o, lse, run = chunked_setup(api, inputs, torch, 0)
