@@ -329,8 +329,11 @@ int attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
 /* Splits attn_decode_fwd uses for n_splits = 0 (at least one key tile each). */
 int attn_decode_splits(int B, int Hkv, int Nk);
 
-/* Workspace for attn_decode_fwd: per split, fp32 O and LSE of every query row,
- * rounded up to 256 bytes per split.  n_splits = 0 means attn_decode_splits. */
+/* Workspace for attn_decode_fwd: per partial result, fp32 O and LSE of every
+ * query row, each rounded up to 256 bytes.  A split leaves two partials when
+ * a kv head's (Hq/Hkv)*Nq rows fit one 128-row tile and 2*n_splits <= 64
+ * (the kernel's two query tiles then take alternate key tiles of the split),
+ * one otherwise.  n_splits = 0 means attn_decode_splits. */
 size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d,
                                    int n_splits);
 

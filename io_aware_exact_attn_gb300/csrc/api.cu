@@ -512,12 +512,21 @@ int attn_decode_splits(int B, int Hkv, int Nk) {
   return n < 1 ? 1 : (int)n;
 }
 
+// Decoding units whose g * Nq rows fit one 128-row tile give the second query
+// tile (otherwise idle) the same rows and every other key tile of the split;
+// each tile writes its own partial, so a split leaves two (within the
+// merge's 64 parts).
+static int decode_parts(int Hq, int Hkv, int Nq, int n_splits) {
+  const bool alternate = Hkv > 0 && (Hq / Hkv) * Nq <= TILE && 2 * n_splits <= 64;
+  return alternate ? 2 * n_splits : n_splits;
+}
+
 size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d, int n_splits) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || d < 1) return 0;
   const int ns = n_splits > 0 ? n_splits : attn_decode_splits(B, Hkv, Nk);
   const size_t rows = (size_t)B * Hq * Nq;
   const size_t per = ((rows * (size_t)d * 4 + 255) & ~(size_t)255) + ((rows * 4 + 255) & ~(size_t)255);
-  return per * (size_t)ns;
+  return per * (size_t)decode_parts(Hq, Hkv, Nq, ns);
 }
 
 int attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens, void* o,
@@ -536,6 +545,7 @@ int attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, con
   if (Nq > Nk) return fail(ATTN_ERR_INVALID_ARG, "Nq=%d exceeds the cache length Nk=%d", Nq, Nk);
   if (n_splits < 0 || n_splits > 64) return fail(ATTN_ERR_INVALID_ARG, "n_splits=%d outside [0, 64]", n_splits);
   const int ns = n_splits > 0 ? n_splits : attn_decode_splits(B, Hkv, Nk);
+  const int parts = decode_parts(Hq, Hkv, Nq, ns);
   if (workspace_bytes < attn_decode_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, ns))
     return fail(ATTN_ERR_WORKSPACE, "decode workspace of %zu bytes is too small", workspace_bytes);
   unsigned int* status = nullptr;
@@ -550,7 +560,7 @@ int attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, con
   const int64_t total_rows = (int64_t)B * Hq * Nq;
   const size_t o_bytes = ((size_t)total_rows * d * 4 + 255) & ~(size_t)255;
   float* ws_o = static_cast<float*>(workspace);
-  float* ws_l = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes * ns);
+  float* ws_l = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes * parts);
   FwdParams p{};
   p.o = ws_o;
   p.lse = ws_l;
@@ -569,6 +579,7 @@ int attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, con
   p.split_tiles = (int)cdiv(cdiv(Nk, TILE), ns);
   p.dec_nq = Nq;
   p.split_rows = total_rows;
+  p.dec_interleave = parts > ns ? 1 : 0;
   p.status = status;
   p.wait_limit_ns = wait_limit();
   if ((rc = debug_records(0, fwd_grid(p), &p.tile_counts))) return rc;
@@ -581,13 +592,13 @@ int attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, con
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   const float* op[64];
   const float* lp[64];
-  for (int c = 0; c < ns; ++c) {
+  for (int c = 0; c < parts; ++c) {
     op[c] = ws_o + (size_t)c * total_rows * d;
     lp[c] = ws_l + (size_t)c * total_rows;
   }
   {
     TraceScope ts(ATTN_KERNEL_MERGE, s);
-    e = launch_merge(op, lp, ns, o, false, lse, Nq, B * Hq, d, Nq, s);
+    e = launch_merge(op, lp, parts, o, false, lse, Nq, B * Hq, d, Nq, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "decode merge launch");
   return ATTN_OK;

@@ -99,7 +99,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 
   Unit u;   // warp-uniform: every warp works it out for itself
   if (p.n_splits > 0)
-    u = decode_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.dec_nq, p.Nk, p.seq_lens, p.n_splits, p.split_tiles);
+    u = decode_unit(blockIdx.x, p.B, p.Hq, p.Hkv, p.dec_nq, p.Nk, p.seq_lens, p.n_splits, p.split_tiles,
+                    p.dec_interleave != 0);
   else if (p.cu_seqlens != nullptr)
     u = varlen_unit(blockIdx.x, p.B, p.Hq, p.Hkv, D, p.cu_seqlens, p.total, p.Nq, p.mask_kind, p.window);
   else
@@ -154,9 +155,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     // Each box of a tile is issued by its own lane: TMA copies issued by one
     // thread are processed one after another, so spreading them over lanes is
     // what lets several 16 KB boxes stream into the SM at the same time.
-    if (lane == 0) mbar_arrive_expect_tx(bar_q, 2 * C::TILE_BYTES);
+    // decoding with alternating tiles: both query tiles read the rows of tile 0
+    const int q_tiles = u.alternate ? 1 : 2;
+    if (lane == 0) mbar_arrive_expect_tx(bar_q, q_tiles * C::TILE_BYTES);
     __syncwarp();
-    if (lane < 2 * C::NBOX) {
+    if (lane < q_tiles * C::NBOX) {
       const int t = lane / C::NBOX, bx = lane % C::NBOX;
       tma_load_3d(s_base + t * C::TILE_BYTES + bx * C::BOX_BYTES, &tq, bx * 64, (int)(u.seq0 + u.row0 + t * TILE), u.bh,
                   bar_q);
@@ -239,9 +242,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         while (k < u.kt_end && !unit_uses(u, k)) ++k;
         return k;
       };
+      const uint32_t q_step = u.alternate ? 0u : TILE16;   // alternating decode: one Q tile for both
       auto issue_s = [&](int t, int slot) {
         const uint32_t kd = d_k + (uint32_t)slot * TILE16;
-        const uint32_t qd = d_q + (uint32_t)t * TILE16;
+        const uint32_t qd = d_q + (uint32_t)t * q_step;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss_e(tmem + t * 128, desc(qd + kstep(kk)), desc(kd + kstep(kk)), id_s, kk > 0);
@@ -318,7 +322,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const int t = (warp - 4) >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;                  // row inside the tile == TMEM lane
-    const int qrow = u.row0 + t * TILE + r;        // local query row
+    const int trow0 = u.row0 + (u.alternate ? 0 : t * TILE);   // first local row of the tile
+    const int qrow = trow0 + r;                    // local query row
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + t * 128;
     const uint32_t tO = tmem + lane_off + C::TMEM_O + t * C::O_STRIDE;
@@ -327,7 +332,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     // positions: row i of the call sits at q_offset + i; when decoding, row r
     // is query r % dec_nq of its head, at u.pos0 + r % dec_nq
     const bool decoding = p.n_splits > 0;
-    const int64_t row_first_pos = decoding ? u.pos0 : p.q_offset + u.row0 + t * TILE;  // earliest row of the tile
+    const int64_t row_first_pos = decoding ? u.pos0 : p.q_offset + trow0;  // earliest row of the tile
     const int64_t qpos = decoding ? u.pos0 + qrow % p.dec_nq : p.q_offset + qrow;
     float m = -INFINITY, l = 0.f, lr = 0.f;
     int it = 0;
@@ -486,7 +491,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         }
         const float inv_l = (lr > 0.f) ? 1.f / lr : 0.f;
         const int64_t grow = u.seq0 + qrow;   // row within the head (token index when batches are ragged)
-        const int64_t split_off = (int64_t)u.split * p.split_rows;
+        // alternating decode: tile t's partial is split 2 * split + t
+        const int64_t split_off = (int64_t)(u.alternate ? 2 * u.split + t : u.split) * p.split_rows;
         const size_t o_off = (size_t)(split_off * D + (int64_t)u.bh * p.o_hs + grow * p.o_rs);
         const size_t l_off = (size_t)(split_off + (int64_t)u.bh * p.l_hs + grow * p.l_rs);
         uint32_t ob[OUT_F32 ? 1 : D / 2];   // the bf16 row (OUT_F32 writes fp32 rows directly)
@@ -518,7 +524,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         if constexpr (!OUT_F32) {
           // bf16 rows staged through the Q tiles (no MMA reads them once this
           // tile's last P.V has completed), so each store covers whole rows
-          const int wrow = u.row0 + t * TILE + wq * 32;   // this warp's first local row
+          const int wrow = trow0 + wq * 32;   // this warp's first local row
           char* base = reinterpret_cast<char*>(static_cast<__nv_bfloat16*>(p.o) +
                                                (size_t)(split_off * D + (int64_t)u.bh * p.o_hs +
                                                         (u.seq0 + wrow) * p.o_rs));

@@ -39,6 +39,9 @@ struct FwdParams {
   int split_tiles;
   int dec_nq;                 // query positions per head
   int64_t split_rows;         // output rows between consecutive splits' partials
+  int dec_interleave;         // the unit's rows fit one tile: both query tiles take
+                              // them, tile t the key tiles kt with kt % 2 == t, and
+                              // writes partial 2 * split + t
   // variable-length batches (cu_seqlens != null): q, k, v, o are token-major
   // [total, heads, d]; sequence b holds tokens [cu_seqlens[b], cu_seqlens[b+1])
   const int* cu_seqlens;      // device [B + 1]

@@ -36,6 +36,8 @@ struct Unit {
   int64_t seq0;     // variable-length batches: first token of the sequence (0 otherwise)
   bool empty;       // variable-length batches: no rows of this sequence in the unit
   bool bad;         // a device-side index (cu_seqlens, seq_lens) was out of range
+  bool alternate;   // decoding: both query tiles hold the same rows, tile t takes
+                    // the key tiles kt of its range with kt % 2 == t
   int lo[2], lim[2];  // per query tile t: key tiles [lo[t], lim[t]) may be visible
   int kt_begin, kt_end;  // min(lo), max(lim) over the unit's tiles
   const uint8_t* mrow[2];  // block-sparse mask row per tile, or null
@@ -135,6 +137,7 @@ ATTN_HD Unit fwd_unit(int64_t i, int B, int Hq, int Hkv, int Nq, int Nk, int nqc
   u.seq0 = 0;
   u.empty = false;
   u.bad = false;
+  u.alternate = false;
   const bool causal = mask_is_causal(mask_kind, causal_in_blocks);
   u.kt_begin = u.nkt;
   u.kt_end = 0;
@@ -165,7 +168,7 @@ ATTN_HD Unit fwd_unit(int64_t i, int B, int Hq, int Hkv, int Nq, int Nk, int nqc
 // r % nq of head hk * g + r / nq.  Key tiles [split * split_tiles, ...) of the
 // sequence's len = seq_lens[b] cached keys; a split past the end is empty.
 ATTN_HD Unit decode_unit(int64_t i, int B, int Hq, int Hkv, int nq, int Nk, const int* seq_lens, int n_splits,
-                         int split_tiles) {
+                         int split_tiles, bool alternate) {
   Unit u;
   u.split = (int)(i % n_splits);
   const int bkv = (int)(i / n_splits);
@@ -183,13 +186,14 @@ ATTN_HD Unit decode_unit(int64_t i, int B, int Hq, int Hkv, int nq, int Nk, cons
   u.nq = rows;
   u.seq0 = 0;
   u.empty = false;
+  u.alternate = alternate;
   int lo = u.split * split_tiles, lim = lo + split_tiles;
   if (lim > u.nkt) lim = u.nkt;
   if (lo > lim) lo = lim;
   u.kt_begin = lo;
   u.kt_end = lim;
   for (int t = 0; t < 2; ++t) {
-    const bool has_rows = t * TILE < rows;
+    const bool has_rows = alternate || t * TILE < rows;
     u.lo[t] = has_rows ? lo : 0;
     u.lim[t] = has_rows ? lim : 0;
     u.mrow[t] = nullptr;
@@ -282,6 +286,7 @@ __device__ __forceinline__ Unit varlen_unit(int64_t cta, int B, int Hq, int Hkv,
 
 // Bit t set: query tile t of the unit sees key tile kt.
 ATTN_HD uint32_t unit_uses(const Unit& u, int kt) {
+  if (u.alternate) return (kt >= u.lo[0] && kt < u.lim[0]) ? (1u << (kt & 1)) : 0u;
   uint32_t m = 0;
   if (kt >= u.lo[0] && kt < u.lim[0] && (u.mrow[0] == nullptr || u.mrow[0][kt] != 0)) m |= 1u;
   if (kt >= u.lo[1] && kt < u.lim[1] && (u.mrow[1] == nullptr || u.mrow[1][kt] != 0)) m |= 2u;

@@ -192,6 +192,9 @@ def test_decode_records():
     st = cdiv(cdiv(Nk, T), ns)   # key tiles per split
     g = Hq // Hkv
     rows = g * Nq
+    # the g * Nq rows fit one tile: both query tiles take them, tile t the
+    # split's key tiles kt with kt % 2 == t
+    assert rows <= T and 2 * ns <= 64
     exp = {}
     for b in range(B):
         n = lens[b]
@@ -199,10 +202,8 @@ def test_decode_records():
         for hk in range(Hkv):
             for s in range(ns):
                 kr = range(min(s * st, nkt), min((s + 1) * st, nkt))
-                per_t = []
-                for t in range(2):
-                    rs = np.arange(t * T, min(rows, t * T + T))
-                    per_t.append(tiles_seen(rs % Nq, n, oracle.MaskSpec("causal"), q_off=n - Nq, kt_range=kr))
+                seen = tiles_seen(np.arange(rows) % Nq, n, oracle.MaskSpec("causal"), q_off=n - Nq, kt_range=kr)
+                per_t = [{kt for kt in seen if kt % 2 == t} for t in range(2)]
                 exp[(b * Hkv + hk, 0, s, 0)] = (len(per_t[0] | per_t[1]), 0, len(per_t[0]), len(per_t[1]))
     check_records(rec.records(), exp)
 

@@ -116,7 +116,10 @@ def test_argument_validation_without_gpu(lib):
     assert lib.attn_decode_splits(1, 1, 1 << 20) == 64
     wsb = lib.attn_decode_workspace_bytes(2, 8, 2, 3, 1000, 64, 4)
     rows = 2 * 8 * 3
-    assert wsb == 4 * (((rows * 64 * 4 + 255) // 256) * 256 + ((rows * 4 + 255) // 256) * 256)
+    per = ((rows * 64 * 4 + 255) // 256) * 256 + ((rows * 4 + 255) // 256) * 256
+    assert wsb == 2 * 4 * per          # 4 * 3 rows per kv head fit one tile: two partials per split
+    assert lib.attn_decode_workspace_bytes(2, 8, 2, 3, 1000, 64, 40) == 40 * per    # 80 partials would not merge
+    assert lib.attn_decode_workspace_bytes(2, 64, 1, 3, 1000, 64, 4) == 4 * 2 * 64 * 3 * (64 * 4 + 4)  # 192 rows
     q = [_ptr(good)] * 3
     assert lib.attn_decode_fwd(*q, None, _ptr(good), None, 2, 8, 2, 3, 1000, 64, 0.125, 1, 4, _ptr(good),
                                wsb - 1, None) == -6
