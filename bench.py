@@ -82,6 +82,13 @@ def kernel_work(w):
     }
 
 
+def executed_gemms(kernel):
+    """N x N x d products each kernel runs per step, counted or not: the dQ
+    kernel recomputes S and dP next to its dQ product, so the backward runs
+    seven products for the five the metric's 2.5x convention credits."""
+    return {"fwd": 2, "bwd_dkdv": 4, "bwd_dq": 3}.get(kernel)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -379,6 +386,8 @@ def main():
         entry = dict(launches=len(lst), avg_ms=avg, share=sum(lst) / sum(sum(x) for x in per.values()))
         if kind == "tensor":
             entry["tflops"] = amount / (avg * 1e-3) / 1e12
+            gem = 2.0 * w["B"] * w["Hq"] * w["N"] * w["N"] * w["d"] * (0.5 if w["mask"] == "causal" else 1.0)
+            entry["tflops_executed"] = executed_gemms(name) * gem / (avg * 1e-3) / 1e12
         elif kind == "hbm":
             entry["gbs"] = amount / (avg * 1e-3) / 1e9
         kernels[name] = entry
