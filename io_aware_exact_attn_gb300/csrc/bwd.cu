@@ -462,7 +462,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
           const int s = i % NS;
           const float* lse2 = reinterpret_cast<const float*>(smem + OFF_RING + s * STAGE + 2 * C::TILE_BYTES);
           const float* dsum = lse2 + 128;
-          ok = wait_bar(bar_q(s), (i / NS) & 1, wc) && wait_bar(bar_s, i & 1, wc);
+          const float4* l4 = reinterpret_cast<const float4*>(lse2) + 16 * hf;
+          const float4* d4 = reinterpret_cast<const float4*>(dsum) + 16 * hf;
+          // this warpgroup's 64 lse2 values go to registers while S^T is
+          // still being computed (the same for every lane: broadcast loads),
+          // so that phase A does not wait on shared-memory loads
+          ok = wait_bar(bar_q(s), (i / NS) & 1, wc);
+          float4 Lr[16];
+#pragma unroll
+          for (int j4 = 0; j4 < 16; ++j4) Lr[j4] = l4[j4];
+          ok = ok && wait_bar(bar_s, i & 1, wc);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
           // key r sees query column j iff 0 <= base + j - r < window: j >= lo
@@ -472,8 +481,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
           const bool cedge = causal && base < TILE - 1;
           const bool wedge = base + (TILE - 1) >= window_of(p);
           const int hi = wedge ? window_of(p) + r - base : TILE;
-          const float4* l4 = reinterpret_cast<const float4*>(lse2) + 16 * hf;
-          const float4* d4 = reinterpret_cast<const float4*>(dsum) + 16 * hf;
           // phase A: P^T = 2^(S^T c - lse2) for this warpgroup's 64 query columns,
           // kept in fp32 for phase B and rounded to bf16 pairs for dV = P^T dO.
           // Masked tiles (the diagonal, a window's edge) take their own copy of
@@ -485,7 +492,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
             const int lo = cedge ? r - base : 0;        // visible query columns: lo <= j < hi
 #pragma unroll
             for (int j4 = 0; j4 < 16; ++j4) {
-              const float4 L = l4[j4];
+              const float4 L = Lr[j4];
               const int col = cb + 4 * j4;
               float x0, x1, x2, x3;
               fma2(x0, x1, __uint_as_float(sr[4 * j4 + 0]), __uint_as_float(sr[4 * j4 + 1]), c, c, -L.x, -L.y);
@@ -513,6 +520,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
           }
           tc_fence_before();
           mbar_arrive(bar_p);
+          float4 Dr[16];   // D likewise, before the wait for dP^T
+#pragma unroll
+          for (int j4 = 0; j4 < 16; ++j4) Dr[j4] = d4[j4];
           ok = wait_bar(bar_dp, i & 1, wc);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
@@ -524,7 +534,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
             uint32_t ds[32];
 #pragma unroll
             for (int j4 = 0; j4 < 16; ++j4) {
-              const float4 Dv = d4[j4];
+              const float4 Dv = Dr[j4];
               float t0, t1, t2, t3, d0, d1, d2, d3;
               add2(t0, t1, __uint_as_float(dr[4 * j4 + 0]), __uint_as_float(dr[4 * j4 + 1]), -Dv.x, -Dv.y);
               add2(t2, t3, __uint_as_float(dr[4 * j4 + 2]), __uint_as_float(dr[4 * j4 + 3]), -Dv.z, -Dv.w);
