@@ -191,8 +191,13 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o,
  *              (0 means Nq): [B, Hq, *, d] row slices of longer tensors work.
  *   lse        device f32, Nq entries per head, heads head_stride apart.
  *   workspace  device, >= attn_bwd_workspace_bytes(B, Hq, Hq, Nq, d) bytes,
- *              16-byte aligned, caller-owned: D then LSE*log2 e, each
- *              [B*Hq][ceil(Nq/128)*128] (rows past Nq hold 0 and +inf).
+ *              16-byte aligned, caller-owned: D then LSE*log2 e, each a
+ *              float array [B*Hq][ceil(Nq/128)*128] (rows past Nq hold 0 and
+ *              +inf) rounded up to 256 bytes, then 32 bytes per row: -LSE*log2 e
+ *              (-2^100 for +inf) and -D, each as three bf16 terms summing to
+ *              the float32 value, laid out as the K = 16 operand the dK/dV
+ *              kernel adds to its S^T and dP^T products (blocks of 128 rows,
+ *              4 KB each, two 16-byte-per-row planes).
  */
 int attn_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, int Hq, int Nq, int d,
                         int64_t head_stride, void* workspace, size_t workspace_bytes, void* stream);
@@ -266,8 +271,9 @@ int attn_varlen_bwd(const void* q, const void* k, const void* v, const void* o,
                     int Hq, int Hkv, int d, float scale, const attn_mask_t* mask,
                     void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace bytes for attn_varlen_bwd: (B+1) ints, then two float arrays of
- * Hq * (total + 127*B) rows, each rounded up to 256 bytes. */
+/* Workspace bytes for attn_varlen_bwd: (B+1) ints rounded up to 256 bytes,
+ * then the statistics of attn_bwd_workspace_bytes for Hq * (total + 127*B)
+ * rows (two float arrays, then 32 bytes per row in whole 128-row blocks). */
 size_t attn_varlen_bwd_workspace_bytes(int B, int64_t total, int Hq);
 
 /*
@@ -343,14 +349,14 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d
  * allowed or would break a memory budget fixed up front (an allocator or
  * runtime that owns every device allocation, a pre-reserved serving process,
  * a host that has set up its memory pools before the hot loop).  It takes no
- * workspace and allocates nothing: its scratch (D and LSE*log2 e) lives in a
- * static device array of ATTN_STATIC_SCRATCH_BYTES inside the library, which
- * every GPU that loads the library holds until the process exits.  The pages
- * describe no such variant; it is an integration aid only.
+ * workspace and allocates nothing: its scratch (the per-row statistics that
+ * attn_bwd keeps in its workspace) lives in a static device array of
+ * ATTN_STATIC_SCRATCH_BYTES inside the library, which every GPU that loads
+ * the library holds until the process exits.  The pages describe no such
+ * variant; it is an integration aid only.
  *   Arguments, layouts and results are those of attn_bwd.
- *   Limit: 2 * B*Hq*ceil(N/128)*128 floats must fit in the array, i.e.
- *   B*Hq*ceil(N/128)*128 <= 2^21 query rows; larger calls return
- *   ATTN_ERR_WORKSPACE and launch nothing.
+ *   Limit: B*Hq*ceil(N/128)*128 <= ATTN_STATIC_SCRATCH_ROWS (2^20) query
+ *   rows; larger calls return ATTN_ERR_WORKSPACE and launch nothing.
  *   The first call on each device looks up the array's device address (and
  *   the status word's) with cudaGetSymbolAddress while that device is
  *   current; make that first call before any stream capture.
@@ -361,14 +367,17 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d
  *   A kernel wait that runs out is reported by attn_get_status(), as for
  *   every other entry point (one status word per device serves them all).
  */
-#define ATTN_STATIC_SCRATCH_BYTES (16u << 20)
+#define ATTN_STATIC_SCRATCH_ROWS (1 << 20)
+#define ATTN_STATIC_SCRATCH_BYTES (40u << 20)
 int attn_bwd_static_scratch(const void* q, const void* k, const void* v, const void* o,
                             const float* lse, const void* dout, void* dq, void* dk,
                             void* dv, int B, int Hq, int Hkv, int N, int d, float scale,
                             const attn_mask_t* mask, void* stream);
 
-/* Bytes of workspace attn_bwd needs: two float arrays (D and LSE*log2 e) of
- * B*Hq*ceil(N/128)*128 entries, rounded up to 256 bytes. */
+/* Bytes of workspace attn_bwd needs: 40 per query row, rows padded to whole
+ * tiles (B*Hq*ceil(N/128)*128 rows): D and LSE*log2 e (two float arrays, each
+ * rounded up to 256 bytes), then the same statistics as the dK/dV kernel's
+ * 32-byte-per-row bf16 operand (see attn_bwd_preprocess). */
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
 
 /*

@@ -636,9 +636,9 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
   (void)Hkv;
   (void)d;
   if (B < 1 || Hq < 1 || N < 1) return 0;
-  // D and LSE*log2(e), one float per query row each, rows padded to whole tiles
-  const size_t bytes = 2 * (size_t)B * Hq * (size_t)cdiv(N, TILE) * TILE * sizeof(float);
-  return (bytes + 255) & ~(size_t)255;
+  // D, LSE*log2(e) and the dK/dV statistics operand per query row, rows
+  // padded to whole tiles
+  return stats_layout((int64_t)B * Hq * cdiv(N, TILE) * TILE).bytes;
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
@@ -664,17 +664,20 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
     return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int Np = (int)(cdiv(N, TILE) * TILE);
+  const StatsLayout sl = stats_layout((int64_t)B * Hq * Np);
   float* dsum = static_cast<float*>(workspace);
-  float* lse2 = dsum + (size_t)B * Hq * Np;
+  float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + sl.lse2_off);
+  uint8_t* qx = static_cast<uint8_t*>(workspace) + sl.qx_off;
   cudaError_t e;
   {
     TraceScope ts(ATTN_KERNEL_BWD_PREPROCESS, s);
-    e = launch_bwd_preprocess(o, dout, lse, dsum, lse2, (int64_t)B * Hq, N, Np, N, d, s);
+    e = launch_bwd_preprocess(o, dout, lse, dsum, lse2, qx, (int64_t)B * Hq, N, Np, N, d, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
   BwdParams p{};
   p.lse2 = lse2;
   p.dsum = dsum;
+  p.qx = qx;
   p.Np = Np;
   p.dq = dq; p.dk = dk; p.dv = dv;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = N; p.Nk = N;
@@ -724,12 +727,14 @@ int attn_bwd_preprocess(const void* o, const void* dout, const float* lse, int B
   if ((rc = device_ready(&status))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int Np = (int)(cdiv(Nq, TILE) * TILE);
+  const StatsLayout sl = stats_layout((int64_t)B * Hq * Np);
   float* dsum = static_cast<float*>(workspace);
-  float* lse2 = dsum + (size_t)B * Hq * Np;
+  float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + sl.lse2_off);
+  uint8_t* qx = static_cast<uint8_t*>(workspace) + sl.qx_off;
   cudaError_t e;
   {
     TraceScope ts(ATTN_KERNEL_BWD_PREPROCESS, s);
-    e = launch_bwd_preprocess(o, dout, lse, dsum, lse2, (int64_t)B * Hq, Nq, Np, hs, d, s);
+    e = launch_bwd_preprocess(o, dout, lse, dsum, lse2, qx, (int64_t)B * Hq, Nq, Np, hs, d, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
   return ATTN_OK;
@@ -766,9 +771,11 @@ int attn_partial_bwd(const void* q, const void* k, const void* v, const void* do
     return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int Np = (int)(cdiv(Nq, TILE) * TILE);
+  const StatsLayout sl = stats_layout((int64_t)B * Hq * Np);
   BwdParams p{};
   p.dsum = static_cast<const float*>(workspace);
-  p.lse2 = p.dsum + (size_t)B * Hq * Np;
+  p.lse2 = reinterpret_cast<const float*>(static_cast<const char*>(workspace) + sl.lse2_off);
+  p.qx = static_cast<const uint8_t*>(workspace) + sl.qx_off;
   p.Np = Np;
   p.dq = dq; p.dk = dk; p.dv = dv;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = Nq; p.Nk = Nk;
@@ -808,9 +815,7 @@ size_t attn_varlen_bwd_workspace_bytes(int B, int64_t total, int Hq) {
   if (B < 1 || total < 1 || Hq < 1) return 0;
   const size_t pcu = ((size_t)(B + 1) * sizeof(int) + 255) & ~(size_t)255;
   // each sequence padded to whole tiles: at most total + 127 B rows per head
-  const size_t rows = (size_t)Hq * (size_t)(total + (int64_t)(TILE - 1) * B);
-  const size_t arr = (rows * sizeof(float) + 255) & ~(size_t)255;
-  return pcu + 2 * arr;
+  return pcu + stats_layout((int64_t)Hq * (total + (int64_t)(TILE - 1) * B)).bytes;
 }
 
 int attn_varlen_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
@@ -844,19 +849,24 @@ int attn_varlen_bwd(const void* q, const void* k, const void* v, const void* o, 
   int* pcu = static_cast<int*>(workspace);
   const size_t pcu_bytes = ((size_t)(B + 1) * sizeof(int) + 255) & ~(size_t)255;
   const int64_t bound = total + (int64_t)(TILE - 1) * B;   // padded rows per head, at most
-  float* dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) + pcu_bytes);
-  float* lse2 = dsum + (((size_t)Hq * bound * sizeof(float) + 255) & ~(size_t)255) / sizeof(float);
+  char* stats = static_cast<char*>(workspace) + pcu_bytes;
+  const StatsLayout sl = stats_layout((int64_t)Hq * bound);
+  float* dsum = reinterpret_cast<float*>(stats);
+  float* lse2 = reinterpret_cast<float*>(stats + sl.lse2_off);
+  uint8_t* qx = reinterpret_cast<uint8_t*>(stats + sl.qx_off);
   cudaError_t e;
   {
     TraceScope ts(ATTN_KERNEL_BWD_PREPROCESS, s);
     e = launch_varlen_pad(cu_seqlens, B, total, max_len, pcu, status, s);
     if (e == cudaSuccess)
-      e = launch_bwd_preprocess_varlen(o, dout, lse, dsum, lse2, Hq, total, cu_seqlens, pcu, B, max_len, bound, d, s);
+      e = launch_bwd_preprocess_varlen(o, dout, lse, dsum, lse2, qx, Hq, total, cu_seqlens, pcu, B, max_len, bound, d,
+                                       s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "ragged backward preprocess launch");
   BwdParams p{};
   p.lse2 = lse2;
   p.dsum = dsum;
+  p.qx = qx;
   p.dq = dq; p.dk = dk; p.dv = dv;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = max_len; p.Nk = max_len;
   p.scale = scale;
@@ -1047,6 +1057,8 @@ int attn_trace_read(attn_trace_record_t* out, int cap, int* n_out) {
 // address, looked up once per device with cudaGetSymbolAddress.
 namespace {
 
+static_assert(stats_layout(ATTN_STATIC_SCRATCH_ROWS).bytes <= ATTN_STATIC_SCRATCH_BYTES,
+              "the static scratch holds the statistics of ATTN_STATIC_SCRATCH_ROWS query rows");
 static __device__ __align__(256) float g_static_scratch[ATTN_STATIC_SCRATCH_BYTES / sizeof(float)];
 
 float* g_static_dev[MAX_DEVICES] = {};
@@ -1084,10 +1096,11 @@ extern "C" int attn_bwd_static_scratch(const void* q, const void* k, const void*
   if ((rc = check_dims(B, Hq, Hkv, N, N, d, scale))) return rc;
   const int64_t Np = cdiv(N, TILE) * TILE;
   const int64_t rows = (int64_t)B * Hq * Np;
-  if (2 * rows * (int64_t)sizeof(float) > (int64_t)ATTN_STATIC_SCRATCH_BYTES)
+  if (rows > ATTN_STATIC_SCRATCH_ROWS)
     return fail(ATTN_ERR_WORKSPACE,
                 "B*Hq*ceil(N/128)*128 = %lld query rows exceed the static scratch limit of %lld rows",
-                (long long)rows, (long long)(ATTN_STATIC_SCRATCH_BYTES / (2 * sizeof(float))));
+                (long long)rows, (long long)ATTN_STATIC_SCRATCH_ROWS);
+  static_assert(ATTN_STATIC_SCRATCH_ROWS % TILE == 0, "whole tiles");
   MaskArgs m;
   if ((rc = read_mask(mask, &m))) return rc;
   unsigned int* status = nullptr;
@@ -1099,17 +1112,20 @@ extern "C" int attn_bwd_static_scratch(const void* q, const void* k, const void*
       (rc = encode_rows_map(&tv, v, d, N, B * Hkv, N)) || (rc = encode_rows_map(&tdo, dout, d, N, B * Hq, N)))
     return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const StatsLayout sl = stats_layout(rows);
   float* dsum = scratch;
-  float* lse2 = scratch + rows;
+  float* lse2 = reinterpret_cast<float*>(reinterpret_cast<char*>(scratch) + sl.lse2_off);
+  uint8_t* qx = reinterpret_cast<uint8_t*>(scratch) + sl.qx_off;
   cudaError_t e;
   {
     TraceScope ts(ATTN_KERNEL_BWD_PREPROCESS, s);
-    e = launch_bwd_preprocess(o, dout, lse, dsum, lse2, (int64_t)B * Hq, N, (int)Np, N, d, s);
+    e = launch_bwd_preprocess(o, dout, lse, dsum, lse2, qx, (int64_t)B * Hq, N, (int)Np, N, d, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
   BwdParams p{};
   p.lse2 = lse2;
   p.dsum = dsum;
+  p.qx = qx;
   p.Np = (int)Np;
   p.dq = dq; p.dk = dk; p.dv = dv;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = N; p.Nk = N;

@@ -41,12 +41,12 @@ struct BwdCfg {
   static constexpr uint32_t TILE_BYTES = NBOX * BOX_BYTES;
   static constexpr int NS = (D == 128) ? 2 : 4;  // ring depth
   // both kernels: 12 warps; the control warpgroup gives registers back to the
-  // two elementwise warpgroups: 128*80 + 256*208 = 63488 <= 384*168 (launch
-  // allotment).  The dK/dV control warps walk a run of units and need 80
-  // (ptxas reports their spills at 64); the elementwise warps do not spill
-  // more at 208 than at 216
+  // two elementwise warpgroups: 128*88 + 256*200 = 62464 <= 384*168 (launch
+  // allotment).  The dK/dV control warps walk a run of units and keep two
+  // kinds of operand descriptors: ptxas reports spills for them at 80, none at
+  // 88; the elementwise warps need no more than 200
   static constexpr int SPLIT_THREADS = 384;
-  static constexpr uint32_t REGS_CTRL = 80, REGS_ELEM = 208;
+  static constexpr uint32_t REGS_CTRL = 88, REGS_ELEM = 200;
 };
 
 // The sliding window includes the causal rule.
@@ -118,8 +118,20 @@ __host__ __device__ constexpr uint32_t half_col(int kk) { return kk < 4 ? kk * 8
 // dK / dV
 // Tensor memory: S^T [0,128) (P^T bf16 overwrites [0,64)), dP^T [128,256)
 // (dS^T bf16 overwrites [128,192)), dV [256,256+d), dK [256+d,256+2d).
-// Shared memory: K, V (resident per unit), NS-deep ring of {Q_i, dO_i,
-// lse2_i, D_i}, and 1 KB per elementwise warp to stage the epilogue's rows.
+// Shared memory: K, V (resident per unit), NS-deep ring of {Q_i, dO_i, the
+// statistics operand of query tile i}, the two constant A operands of the
+// statistics steps, and 1 KB per elementwise warp to stage the epilogue's
+// rows.
+// Each S^T and dP^T product has one more K = 16 step whose B operand is the
+// query tile's block of the statistics operand (the preprocessing kernel
+// writes it: -lse2 and -D as bf16 triples) and whose A operand is constant:
+// the bf16 split of 1/c (c = scale * log2 e) under the lse2 columns for S^T,
+// ones under the D columns for dP^T.  So the accumulators already hold
+// S^T - lse2/c and dP^T - D, and the elementwise phases read no per-column
+// values from shared memory: such loads wait behind the tensor core's operand
+// reads while a product with both operands in shared memory runs (measured on
+// GB300: the two phases took 2.2 times as long under such products when each
+// lane loaded its columns' lse2 and D, and no longer without those loads).
 // Order on the tensor core: S^T_0, dP^T_0, then dV_i, S^T_{i+1}, dK_i,
 // dP^T_{i+1} per query tile i (see the MMA issuer).
 //
@@ -191,8 +203,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
   constexpr int NS = C::NS;
   constexpr uint32_t OFF_V = C::TILE_BYTES;
   constexpr uint32_t OFF_RING = 2 * C::TILE_BYTES;
-  constexpr uint32_t STAGE = 2 * C::TILE_BYTES + 1024;  // Q, dO, lse2[128], D[128]
-  constexpr uint32_t OFF_EPI = OFF_RING + NS * STAGE;   // 8 x 1 KB epilogue staging
+  constexpr uint32_t STAGE = 2 * C::TILE_BYTES + (uint32_t)QX_TILE_BYTES;   // Q, dO, statistics block
+  constexpr uint32_t OFF_CONST = OFF_RING + NS * STAGE;   // constant A operands: K side, V side
+  constexpr uint32_t OFF_EPI = OFF_CONST + 2 * (uint32_t)QX_TILE_BYTES;   // 8 x 1 KB epilogue staging
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t bars[1 + 2 * NS + 9];
@@ -259,6 +272,25 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
     tmem_alloc(smem_u32(&tmem_slot), 512);
     tmem_relinquish();
   }
+  if (warp >= 4) {   // the constant A operands of the statistics steps, one row per thread
+    const int t = threadIdx.x - 128, row = t & (TILE - 1);
+    float ah = 0.f, am = 0.f, al = 0.f;
+    const float a = 1.f / p.scale_log2;
+    ah = __bfloat162float(__float2bfloat16_rn(a));
+    am = __bfloat162float(__float2bfloat16_rn(a - ah));
+    al = __bfloat162float(__float2bfloat16_rn(a - ah - am));
+    uint8_t* dst = smem + OFF_CONST + (t >= TILE ? QX_TILE_BYTES : 0) + row * 16;
+    const uint32_t one2 = pack_bf16(1.f, 1.f);
+    if (t < TILE) {   // S^T: (ah + am + al) times each of the three lse2 terms
+      *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16(ah, ah), pack_bf16(ah, am), pack_bf16(am, am),
+                                                  pack_bf16(al, al));
+      *reinterpret_cast<uint4*>(dst + QX_TILE_BYTES / 2) = make_uint4(pack_bf16(al, 0.f), 0u, 0u, 0u);
+    } else {          // dP^T: ones under the three D terms
+      *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(dst + QX_TILE_BYTES / 2) = make_uint4(pack_bf16(0.f, 1.f), one2, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -298,7 +330,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
           if (n >= NS) ok = wait_bar(bar_qfree(s), ((n / NS) - 1) & 1, wc);
           if (!(ok = __all_sync(0xffffffffu, ok))) break;
           const uint32_t st = s_base + OFF_RING + s * STAGE;
-          if (lane == 0) mbar_arrive_expect_tx(bar_q(s), 2 * C::TILE_BYTES + 1024);
+          if (lane == 0) mbar_arrive_expect_tx(bar_q(s), 2 * C::TILE_BYTES + (uint32_t)QX_TILE_BYTES);
           __syncwarp();
           const size_t roff = (size_t)(x.lrow_b + hq * x.lrow_hs) + (size_t)qt * TILE;
           const int qrow0 = x.tok0 + qt * TILE;
@@ -308,9 +340,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
             tma_load_3d(st + C::TILE_BYTES + (lane - C::NBOX) * C::BOX_BYTES, &tdo, (lane - C::NBOX) * 64, qrow0,
                         q_head, bar_q(s));
           else if (lane == 2 * C::NBOX)
-            bulk_load(st + 2 * C::TILE_BYTES, p.lse2 + roff, 512, bar_q(s));
-          else if (lane == 2 * C::NBOX + 1)
-            bulk_load(st + 2 * C::TILE_BYTES + 512, p.dsum + roff, 512, bar_q(s));
+            bulk_load(st + 2 * C::TILE_BYTES, p.qx + roff * QX_ROW_BYTES, (uint32_t)QX_TILE_BYTES, bar_q(s));
           ++n;
           ++nu;
         }
@@ -356,11 +386,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       const uint32_t d_ring = (uint32_t)sdesc_sw128(s_base + OFF_RING, 16, 1024);              // K-major
       const uint32_t d_ring_mn = (uint32_t)sdesc_sw128(s_base + OFF_RING, C::BOX_BYTES, 1024);  // MN-major
       auto desc = [&](uint32_t lo) { return ((uint64_t)hi << 32) | lo; };
+      // the statistics steps: plain K-major operands, two 2 KB planes
+      const uint32_t hi_x = (uint32_t)(sdesc_plain(0, QX_TILE_BYTES / 2, 128) >> 32);
+      const uint32_t d_ck = (uint32_t)sdesc_plain(s_base + OFF_CONST, QX_TILE_BYTES / 2, 128);
+      const uint32_t d_cv = (uint32_t)sdesc_plain(s_base + OFF_CONST + QX_TILE_BYTES, QX_TILE_BYTES / 2, 128);
+      const uint32_t d_qx = (uint32_t)sdesc_plain(s_base + OFF_RING + 2 * C::TILE_BYTES, QX_TILE_BYTES / 2, 128);
+      auto desc_x = [&](uint32_t lo) { return ((uint64_t)hi_x << 32) | lo; };
       auto kstep = [](int kk) { return (uint32_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4); };
       auto issue_st = [&](int slot) {   // S^T = K Q^T
         const uint32_t qd = d_ring + (uint32_t)slot * STAGE16;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) mma_ss_e(tmem + 0, desc(d_k + kstep(kk)), desc(qd + kstep(kk)), id_s, kk > 0);
+        mma_ss_e(tmem + 0, desc_x(d_ck), desc_x(d_qx + (uint32_t)slot * STAGE16), id_s, 1u);   // - lse2 / c
         mma_commit_e(bar_s);
       };
       auto issue_dpt = [&](int slot) {  // dP^T = V dO^T
@@ -368,6 +405,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss_e(tmem + 128, desc(d_v + kstep(kk)), desc(dd + kstep(kk)), id_s, kk > 0);
+        mma_ss_e(tmem + 128, desc_x(d_cv), desc_x(d_qx + (uint32_t)slot * STAGE16), id_s, 1u);   // - D
         mma_commit_e(bar_dp);
       };
       int s = 0;
@@ -459,19 +497,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       for (int h = 0; h < g && ok; ++h) {
         for (int qt = x.qt_first; qt < x.nqt; ++qt) {
           if (!tile_pair_visible(p, qt, kt)) continue;
-          const int s = i % NS;
-          const float* lse2 = reinterpret_cast<const float*>(smem + OFF_RING + s * STAGE + 2 * C::TILE_BYTES);
-          const float* dsum = lse2 + 128;
-          const float4* l4 = reinterpret_cast<const float4*>(lse2) + 16 * hf;
-          const float4* d4 = reinterpret_cast<const float4*>(dsum) + 16 * hf;
-          // this warpgroup's 64 lse2 values go to registers while S^T is
-          // still being computed (the same for every lane: broadcast loads),
-          // so that phase A does not wait on shared-memory loads
-          ok = wait_bar(bar_q(s), (i / NS) & 1, wc);
-          float4 Lr[16];
-#pragma unroll
-          for (int j4 = 0; j4 < 16; ++j4) Lr[j4] = l4[j4];
-          ok = ok && wait_bar(bar_s, i & 1, wc);
+          ok = wait_bar(bar_s, i & 1, wc);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
           // key r sees query column j iff 0 <= base + j - r < window: j >= lo
@@ -481,7 +507,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
           const bool cedge = causal && base < TILE - 1;
           const bool wedge = base + (TILE - 1) >= window_of(p);
           const int hi = wedge ? window_of(p) + r - base : TILE;
-          // phase A: P^T = 2^(S^T c - lse2) for this warpgroup's 64 query columns,
+          // phase A: P^T = 2^((S^T - lse2/c) c) for this warpgroup's 64 query columns,
           // kept in fp32 for phase B and rounded to bf16 pairs for dV = P^T dO.
           // Masked tiles (the diagonal, a window's edge) take their own copy of
           // the loop so that the others carry no mask arithmetic at all.
@@ -492,11 +518,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
             const int lo = cedge ? r - base : 0;        // visible query columns: lo <= j < hi
 #pragma unroll
             for (int j4 = 0; j4 < 16; ++j4) {
-              const float4 L = Lr[j4];
               const int col = cb + 4 * j4;
               float x0, x1, x2, x3;
-              fma2(x0, x1, __uint_as_float(sr[4 * j4 + 0]), __uint_as_float(sr[4 * j4 + 1]), c, c, -L.x, -L.y);
-              fma2(x2, x3, __uint_as_float(sr[4 * j4 + 2]), __uint_as_float(sr[4 * j4 + 3]), c, c, -L.z, -L.w);
+              mul2(x0, x1, __uint_as_float(sr[4 * j4 + 0]), __uint_as_float(sr[4 * j4 + 1]), c, c);
+              mul2(x2, x3, __uint_as_float(sr[4 * j4 + 2]), __uint_as_float(sr[4 * j4 + 3]), c, c);
               float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
               if constexpr (decltype(masked)::value) {
                 p0 = (col + 0 >= lo && col + 0 < hi) ? p0 : 0.f;
@@ -520,26 +545,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
           }
           tc_fence_before();
           mbar_arrive(bar_p);
-          float4 Dr[16];   // D likewise, before the wait for dP^T
-#pragma unroll
-          for (int j4 = 0; j4 < 16; ++j4) Dr[j4] = d4[j4];
           ok = wait_bar(bar_dp, i & 1, wc);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
-          // phase B: dS^T = P^T * (dP^T - D) for the same 64 columns; the bf16
-          // pairs go over the first 32 dP^T columns of the half
+          // phase B: dS^T = P^T * (dP^T - D) for the same 64 columns (the
+          // accumulator holds dP^T - D); the bf16 pairs go over the first 32
+          // dP^T columns of the half
           {
             uint32_t dr[64];
             tmem_ld64(tmem + lane_off + 128 + cb, dr);
             uint32_t ds[32];
 #pragma unroll
             for (int j4 = 0; j4 < 16; ++j4) {
-              const float4 Dv = Dr[j4];
-              float t0, t1, t2, t3, d0, d1, d2, d3;
-              add2(t0, t1, __uint_as_float(dr[4 * j4 + 0]), __uint_as_float(dr[4 * j4 + 1]), -Dv.x, -Dv.y);
-              add2(t2, t3, __uint_as_float(dr[4 * j4 + 2]), __uint_as_float(dr[4 * j4 + 3]), -Dv.z, -Dv.w);
-              mul2(d0, d1, pf[4 * j4 + 0], pf[4 * j4 + 1], t0, t1);
-              mul2(d2, d3, pf[4 * j4 + 2], pf[4 * j4 + 3], t2, t3);
+              float d0, d1, d2, d3;
+              mul2(d0, d1, pf[4 * j4 + 0], pf[4 * j4 + 1], __uint_as_float(dr[4 * j4 + 0]), __uint_as_float(dr[4 * j4 + 1]));
+              mul2(d2, d3, pf[4 * j4 + 2], pf[4 * j4 + 3], __uint_as_float(dr[4 * j4 + 2]), __uint_as_float(dr[4 * j4 + 3]));
               ds[2 * j4] = pack_bf16(d0, d1);
               ds[2 * j4 + 1] = pack_bf16(d2, d3);
             }
@@ -1053,8 +1073,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
 }
 
 template <int D>
-constexpr uint32_t dkdv_smem() {   // K, V, the ring, 8 x 1 KB of epilogue staging, alignment slack
-  return 2 * BwdCfg<D>::TILE_BYTES + BwdCfg<D>::NS * (2 * BwdCfg<D>::TILE_BYTES + 1024) + 8 * 1024 + 1024;
+constexpr uint32_t dkdv_smem() {   // K, V, the ring, the constant operands, 8 x 1 KB of epilogue staging, alignment
+  return 2 * BwdCfg<D>::TILE_BYTES + BwdCfg<D>::NS * (2 * BwdCfg<D>::TILE_BYTES + (uint32_t)QX_TILE_BYTES) +
+         2 * (uint32_t)QX_TILE_BYTES + 8 * 1024 + 1024;
 }
 template <int D, bool F32>
 cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

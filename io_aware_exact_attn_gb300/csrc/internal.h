@@ -55,10 +55,27 @@ struct FwdParams {
   int32_t* tile_counts;       // per-CTA debug record (DEBUG_FIELDS int32 each), or null
 };
 
+// The backward statistics of a call (in its workspace, or the static
+// scratch), for `rows` padded query rows: D, then LSE * log2(e) (float32, one
+// per row, each array rounded up to 256 bytes), then the dK/dV kernel's
+// per-row statistics operand: QX_ROW_BYTES per row in blocks of 128 rows
+// (QX_TILE_BYTES, written by the preprocessing kernel, which describes it).
+constexpr size_t QX_ROW_BYTES = 32;
+constexpr size_t QX_TILE_BYTES = QX_ROW_BYTES * TILE;
+struct StatsLayout {
+  size_t lse2_off, qx_off, bytes;   // byte offsets from the start, total size
+};
+constexpr StatsLayout stats_layout(int64_t rows) {
+  const size_t arr = ((size_t)rows * sizeof(float) + 255) & ~(size_t)255;
+  const size_t qx = ((size_t)rows + TILE - 1) / TILE * QX_TILE_BYTES;
+  return {arr, 2 * arr, 2 * arr + ((qx + 255) & ~(size_t)255)};
+}
+
 // Backward parameter block (kernels 2 and 3 of attn_bwd and attn_partial_bwd).
 struct BwdParams {
   const float* lse2;        // LSE * log2(e), [B*Hq][Np], +inf on padding rows
   const float* dsum;        // D = rowsum(dO*O), [B*Hq][Np], 0 on padding rows
+  const uint8_t* qx;        // the statistics operand, QX_ROW_BYTES per lse2 row
   int Np;                   // Nq rounded up to a multiple of 128
   void* dq;                 // bf16 (or f32) [B,Hq,*,d], heads dq_hs rows apart
   void* dk;                 // bf16 (or f32) [B,Hkv,*,d], heads dkv_hs rows apart
@@ -151,13 +168,13 @@ cudaError_t launch_merge(const float* const* o_parts, const float* const* lse_pa
 
 // Rows of head h of o / dout start at h * in_hs (in rows of d), of lse at h * in_hs.
 cudaError_t launch_bwd_preprocess(const void* o, const void* dout, const float* lse, float* dsum, float* lse2,
-                                  int64_t heads, int N, int Np, int64_t in_hs, int d, cudaStream_t s);
+                                  uint8_t* qx, int64_t heads, int N, int Np, int64_t in_hs, int d, cudaStream_t s);
 // Malformed sequences (seq_range_ok in schedule.h) count as empty and set
 // the bounds bit of *status.
 cudaError_t launch_varlen_pad(const int* cu_seqlens, int B, int64_t total, int max_len, int* pcu,
                               unsigned int* status, cudaStream_t s);
 cudaError_t launch_bwd_preprocess_varlen(const void* o, const void* dout, const float* lse, float* dsum, float* lse2,
-                                         int heads, int64_t total, const int* cu_seqlens, const int* pcu, int B,
+                                         uint8_t* qx, int heads, int64_t total, const int* cu_seqlens, const int* pcu, int B,
                                          int max_len, int64_t padded_rows_bound, int d, cudaStream_t s);
 
 // out_f32: dq / dk / dv are float32 (stored, or added with p.accumulate).

@@ -125,17 +125,40 @@ __global__ void __launch_bounds__(32) varlen_pad_kernel(const int* __restrict__ 
 // kernels; groups of d/8 lanes per row, 8 bf16 per lane.  Both outputs are
 // [heads][Np] with Np = N rounded up to a whole tile; rows past N (and rows
 // whose LSE is -inf, i.e. that saw no key) get D = 0 and lse2 = +inf, which
-// makes every recomputed probability of such a row exactly 0.  Head h's rows
+// makes every recomputed probability of such a row exactly 0.
+//
+// qx: the same two statistics as one 16-element bf16 row per query row i,
+// the B operand of one extra K = 16 step of the dK/dV kernel's S^T and dP^T
+// products.  With l = -lse2_i (-2^100 in place of -inf) and e = -D_i, each
+// split into three bf16 terms whose sum is the float32 value to about 2^-24
+// relative (x = x_h + x_m + x_l, each term the rounding of what the earlier
+// ones leave), the row is
+//   [l_h l_m l_l  l_h l_m l_l  l_h l_m l_l  e_h e_m e_l  0 0 0 0].
+// Against the kernel's constant A rows (the split of 1/c, c = scale*log2 e,
+// under the first nine columns; ones under the next three) the extra step
+// adds l / c to S^T and -D to dP^T, so the kernel's elementwise phases need
+// no per-column loads.  Layout: blocks of 128 rows (tile t of the padded
+// rows at t * QX_TILE_BYTES), each two planes of 2 KB (columns 0-7, then
+// 8-15), 16 bytes per row: the K-major core-matrix layout without swizzle.  Head h's rows
 // of O, dO and LSE start in_hs rows apart (a chunk of a longer sequence when
 // in_hs > N).  Ragged
 // batches (RAGGED): O, dO token-major [total][heads][d], LSE [heads][total],
 // outputs [heads][pcu[B]] with sequence b's rows from pcu[b] (see above).
+// x as three bf16 values (returned as the floats they hold) whose sum is x to
+// about 2^-24 relative: each is x minus the earlier ones, rounded to bf16
+// (the differences are exact in float32).
+__device__ __forceinline__ void split3_bf16(float x, float* h, float* m, float* l) {
+  *h = __bfloat162float(__float2bfloat16_rn(x));
+  *m = __bfloat162float(__float2bfloat16_rn(x - *h));
+  *l = __bfloat162float(__float2bfloat16_rn(x - *h - *m));
+}
+
 template <int D, bool RAGGED>
 __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ dout,
                                                          const float* __restrict__ lse,
                                                          float* __restrict__ dsum, float* __restrict__ lse2,
-                                                         int64_t heads, int N, int Np, int64_t in_hs,
+                                                         uint8_t* __restrict__ qx, int64_t heads, int N, int Np, int64_t in_hs,
                                                          const int* __restrict__ cu,
                                                          const int* __restrict__ pcu, int B, int64_t total,
                                                          int max_len) {
@@ -194,6 +217,13 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
       }
       dsum[prow] = valid ? acc : 0.f;
       lse2[prow] = l2;
+      float lh, lm, ll, eh, em, el;
+      split3_bf16(l2 == INFINITY ? -0x1p100f : -l2, &lh, &lm, &ll);
+      split3_bf16(valid ? -acc : 0.f, &eh, &em, &el);
+      uint8_t* row = qx + (size_t)(prow / TILE) * QX_TILE_BYTES + (size_t)(prow % TILE) * 16;
+      *reinterpret_cast<uint4*>(row) = make_uint4(pack_bf16(lh, lm), pack_bf16(ll, lh), pack_bf16(lm, ll),
+                                                  pack_bf16(lh, lm));
+      *reinterpret_cast<uint4*>(row + QX_TILE_BYTES / 2) = make_uint4(pack_bf16(ll, eh), pack_bf16(em, el), 0u, 0u);
     }
   }
 }
@@ -247,16 +277,16 @@ cudaError_t launch_merge(const float* const* o_parts, const float* const* lse_pa
 }
 
 cudaError_t launch_bwd_preprocess(const void* o, const void* dout, const float* lse, float* dsum, float* lse2,
-                                  int64_t heads, int N, int Np, int64_t in_hs, int d, cudaStream_t s) {
+                                  uint8_t* qx, int64_t heads, int N, int Np, int64_t in_hs, int d, cudaStream_t s) {
   const int rpw = 32 / (d / 8);
   const int grid = grid_for((heads * Np + rpw - 1) / rpw);
   const auto* po = static_cast<const __nv_bfloat16*>(o);
   const auto* pd = static_cast<const __nv_bfloat16*>(dout);
   if (d == 128)
-    preprocess_kernel<128, false><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, N, Np, in_hs, nullptr, nullptr,
+    preprocess_kernel<128, false><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, qx, heads, N, Np, in_hs, nullptr, nullptr,
                                                        0, 0, 0);
   else
-    preprocess_kernel<64, false><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, N, Np, in_hs, nullptr, nullptr,
+    preprocess_kernel<64, false><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, qx, heads, N, Np, in_hs, nullptr, nullptr,
                                                       0, 0, 0);
   return cudaGetLastError();
 }
@@ -268,17 +298,17 @@ cudaError_t launch_varlen_pad(const int* cu_seqlens, int B, int64_t total, int m
 }
 
 cudaError_t launch_bwd_preprocess_varlen(const void* o, const void* dout, const float* lse, float* dsum, float* lse2,
-                                         int heads, int64_t total, const int* cu_seqlens, const int* pcu, int B,
+                                         uint8_t* qx, int heads, int64_t total, const int* cu_seqlens, const int* pcu, int B,
                                          int max_len, int64_t padded_rows_bound, int d, cudaStream_t s) {
   const int rpw = 32 / (d / 8);
   const int grid = grid_for((heads * padded_rows_bound + rpw - 1) / rpw);
   const auto* po = static_cast<const __nv_bfloat16*>(o);
   const auto* pd = static_cast<const __nv_bfloat16*>(dout);
   if (d == 128)
-    preprocess_kernel<128, true><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, 0, 0, 0, cu_seqlens, pcu, B,
+    preprocess_kernel<128, true><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, qx, heads, 0, 0, 0, cu_seqlens, pcu, B,
                                                       total, max_len);
   else
-    preprocess_kernel<64, true><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, heads, 0, 0, 0, cu_seqlens, pcu, B,
+    preprocess_kernel<64, true><<<grid, 256, 0, s>>>(po, pd, lse, dsum, lse2, qx, heads, 0, 0, 0, cu_seqlens, pcu, B,
                                                      total, max_len);
   return cudaGetLastError();
 }

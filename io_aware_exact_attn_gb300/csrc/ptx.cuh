@@ -246,6 +246,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
          ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// Shared-memory descriptor without swizzle for a K-major operand stored as
+// core matrices of 8 rows x 16 bytes (each contiguous): kstride_bytes between
+// core matrices adjacent along K (bits 16-29), group_bytes between 8-row
+// groups (bits 32-45); checked on GB300 against a host product.
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t kstride_bytes, uint32_t group_bytes) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((kstride_bytes >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((group_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
 // ---- TMEM loads/stores (32 data-path lanes x 32 bit, 32 columns).  The wait
 // is inside the same asm statement so no use of the registers can be
 // scheduled before the data has landed.

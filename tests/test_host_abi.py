@@ -81,7 +81,8 @@ def test_argument_validation_without_gpu(lib):
     assert lib.attn_merge_lse(arr, arr, 65, _ptr(good), 0, None, 1, 1, 4, 64, 0, None) == -1
     # bwd workspace size and check
     need = lib.attn_bwd_workspace_bytes(2, 4, 2, 100, 64)
-    assert need == ((2 * 2 * 4 * 128 * 4 + 255) // 256) * 256
+    rows = 2 * 4 * 128   # padded query rows: D and LSE*log2 e (float32), then 32 bytes each
+    assert need == 2 * ((rows * 4 + 255) // 256) * 256 + rows * 32
     p = [_ptr(good)] * 10
     assert lib.attn_bwd(*p, need - 256, 2, 4, 2, 100, 64, 0.125, None, None) == -6
     # chunked backward: workspace, pointer, offset and size checks come before any device call

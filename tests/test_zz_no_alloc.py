@@ -21,7 +21,7 @@ from _gpu_helpers import assert_grad, f64, make
 def test_static_scratch_rejects_oversized_problem_without_a_gpu():
     lib = _ffi.lib()
     p = C.c_void_p(4096)
-    # 2 * 32 * 65536 query rows = 2^22 > 2^21: refused before any device work
+    # 2 * 32 * 65536 query rows = 2^22 > 2^20: refused before any device work
     rc = lib.attn_bwd_static_scratch(p, p, p, p, p, p, p, p, p, 2, 32, 32, 65536, 128, 0.088, None, None)
     assert rc == -6
     assert b"static scratch" in lib.attn_last_error_message()
