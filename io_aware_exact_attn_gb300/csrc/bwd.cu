@@ -39,14 +39,19 @@ struct BwdCfg {
   static constexpr int NBOX = D / 64;
   static constexpr uint32_t BOX_BYTES = 128 * 128;
   static constexpr uint32_t TILE_BYTES = NBOX * BOX_BYTES;
-  static constexpr int NS = (D == 128) ? 2 : 4;  // ring depth
+  // dK/dV rings: {Q_i, statistics block of tile i} QS deep, dO_i OS deep.
+  // dO_i is last read by dV_i, Q_i by dK_i a product later, and S^T_{i+1}
+  // (which needs Q_{i+1}) is issued right after dV_i, so the Q slots are the
+  // ones that must be refilled well ahead
+  static constexpr int QS = (D == 128) ? 3 : 4;
+  static constexpr int OS = (D == 128) ? 1 : 2;
   // both kernels: 12 warps; the control warpgroup gives registers back to the
-  // two elementwise warpgroups: 128*88 + 256*200 = 62464 <= 384*168 (launch
-  // allotment).  The dK/dV control warps walk a run of units and keep two
-  // kinds of operand descriptors: ptxas reports spills for them at 80, none at
-  // 88; the elementwise warps need no more than 200
+  // two elementwise warpgroups: 128*112 + 256*176 = 59392 <= 384*168 (launch
+  // allotment).  The dK/dV control warps walk a run of units over two rings
+  // with three kinds of operand descriptors: ptxas reports spills for them up
+  // to 104, none at 112; the elementwise warps need no more than 176
   static constexpr int SPLIT_THREADS = 384;
-  static constexpr uint32_t REGS_CTRL = 88, REGS_ELEM = 200;
+  static constexpr uint32_t REGS_CTRL = 112, REGS_ELEM = 176;
 };
 
 // The sliding window includes the causal rule.
@@ -118,10 +123,10 @@ __host__ __device__ constexpr uint32_t half_col(int kk) { return kk < 4 ? kk * 8
 // dK / dV
 // Tensor memory: S^T [0,128) (P^T bf16 overwrites [0,64)), dP^T [128,256)
 // (dS^T bf16 overwrites [128,192)), dV [256,256+d), dK [256+d,256+2d).
-// Shared memory: K, V (resident per unit), NS-deep ring of {Q_i, dO_i, the
-// statistics operand of query tile i}, the two constant A operands of the
-// statistics steps, and 1 KB per elementwise warp to stage the epilogue's
-// rows.
+// Shared memory: K, V (resident per unit), a ring of {Q_i, the statistics
+// operand of query tile i} and one of dO_i, the two constant A operands of
+// the statistics steps, and 1 KB per elementwise warp to stage the
+// epilogue's rows.
 // Each S^T and dP^T product has one more K = 16 step whose B operand is the
 // query tile's block of the statistics operand (the preprocessing kernel
 // writes it: -lse2 and -D as bf16 triples) and whose A operand is constant:
@@ -200,15 +205,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                 const BwdParams p) {
   using C = BwdCfg<D>;
-  constexpr int NS = C::NS;
+  constexpr int QS = C::QS, OS = C::OS;
   constexpr uint32_t OFF_V = C::TILE_BYTES;
-  constexpr uint32_t OFF_RING = 2 * C::TILE_BYTES;
-  constexpr uint32_t STAGE = 2 * C::TILE_BYTES + (uint32_t)QX_TILE_BYTES;   // Q, dO, statistics block
-  constexpr uint32_t OFF_CONST = OFF_RING + NS * STAGE;   // constant A operands: K side, V side
+  constexpr uint32_t OFF_QR = 2 * C::TILE_BYTES;                             // Q ring
+  constexpr uint32_t QSTAGE = C::TILE_BYTES + (uint32_t)QX_TILE_BYTES;        // Q, statistics block
+  constexpr uint32_t OFF_OR = OFF_QR + QS * QSTAGE;                          // dO ring
+  constexpr uint32_t OFF_CONST = OFF_OR + OS * C::TILE_BYTES;   // constant A operands: K side, V side
   constexpr uint32_t OFF_EPI = OFF_CONST + 2 * (uint32_t)QX_TILE_BYTES;   // 8 x 1 KB epilogue staging
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bars[1 + 2 * NS + 9];
+  __shared__ __align__(8) uint64_t bars[1 + 2 * QS + 2 * OS + 9];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ KvUnit units[MAX_KV_RUN];   // this CTA's units, decoded once
@@ -218,16 +224,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
   const uint32_t s_base = smem_u32(smem);
   const uint32_t bar_kv = smem_u32(&bars[0]);
   auto bar_q = [&](int s) { return smem_u32(&bars[1 + s]); };
-  auto bar_qfree = [&](int s) { return smem_u32(&bars[1 + NS + s]); };
-  const uint32_t bar_s = smem_u32(&bars[1 + 2 * NS + 0]);
-  const uint32_t bar_dp = smem_u32(&bars[1 + 2 * NS + 1]);
-  const uint32_t bar_p = smem_u32(&bars[1 + 2 * NS + 2]);
-  const uint32_t bar_ds = smem_u32(&bars[1 + 2 * NS + 3]);
-  const uint32_t bar_dv = smem_u32(&bars[1 + 2 * NS + 4]);
-  const uint32_t bar_dk = smem_u32(&bars[1 + 2 * NS + 5]);
-  const uint32_t bar_done = smem_u32(&bars[1 + 2 * NS + 6]);
-  const uint32_t bar_kvfree = smem_u32(&bars[1 + 2 * NS + 7]);   // a unit's K and V are read by no further MMA
-  const uint32_t bar_accfree = smem_u32(&bars[1 + 2 * NS + 8]);  // a unit's dV, dK have been read out
+  auto bar_qfree = [&](int s) { return smem_u32(&bars[1 + QS + s]); };
+  auto bar_o = [&](int s) { return smem_u32(&bars[1 + 2 * QS + s]); };
+  auto bar_ofree = [&](int s) { return smem_u32(&bars[1 + 2 * QS + OS + s]); };
+  constexpr int B0 = 1 + 2 * QS + 2 * OS;
+  const uint32_t bar_s = smem_u32(&bars[B0 + 0]);
+  const uint32_t bar_dp = smem_u32(&bars[B0 + 1]);
+  const uint32_t bar_p = smem_u32(&bars[B0 + 2]);
+  const uint32_t bar_ds = smem_u32(&bars[B0 + 3]);
+  const uint32_t bar_dv = smem_u32(&bars[B0 + 4]);
+  const uint32_t bar_dk = smem_u32(&bars[B0 + 5]);
+  const uint32_t bar_done = smem_u32(&bars[B0 + 6]);
+  const uint32_t bar_kvfree = smem_u32(&bars[B0 + 7]);   // a unit's K and V are read by no further MMA
+  const uint32_t bar_accfree = smem_u32(&bars[B0 + 8]);  // a unit's dV, dK have been read out
 
   const int64_t u_begin = (int64_t)blockIdx.x * p.kv_run;
   const int run = (int)min((int64_t)p.kv_run, p.kv_units - u_begin);   // units of this CTA: u_begin + j
@@ -247,9 +256,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(bar_kv, 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < QS; ++s) {
       mbar_init(bar_q(s), 1);
       mbar_init(bar_qfree(s), 1);
+    }
+    for (int s = 0; s < OS; ++s) {
+      mbar_init(bar_o(s), 1);
+      mbar_init(bar_ofree(s), 1);
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
@@ -301,7 +314,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
    if (warp == 0) {
     // ---------------------------------------------------------- producer
     // one lane per TMA copy (copies issued by one thread are serialised)
-    int n = 0;    // stages loaded, over all units
+    int n = 0;    // query tiles whose Q (with its statistics block) was loaded, over all units
+    int no = 0;   // query tiles whose dO was loaded
     int uc = 0;   // units whose K and V were loaded
     bool ok = true;
     for (int ju = 0; ju < run && ok; ++ju) {
@@ -326,22 +340,29 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
         const int q_head = p.cu_seqlens != nullptr ? hq : x.b * p.Hq + hq;
         for (int qt = x.qt_first; qt < x.nqt && ok; ++qt) {
           if (!tile_pair_visible(p, qt, x.kt)) continue;
-          const int s = n % NS;
-          if (n >= NS) ok = wait_bar(bar_qfree(s), ((n / NS) - 1) & 1, wc);
-          if (!(ok = __all_sync(0xffffffffu, ok))) break;
-          const uint32_t st = s_base + OFF_RING + s * STAGE;
-          if (lane == 0) mbar_arrive_expect_tx(bar_q(s), 2 * C::TILE_BYTES + (uint32_t)QX_TILE_BYTES);
-          __syncwarp();
           const size_t roff = (size_t)(x.lrow_b + hq * x.lrow_hs) + (size_t)qt * TILE;
           const int qrow0 = x.tok0 + qt * TILE;
+          const int s = n % QS;
+          if (n >= QS) ok = wait_bar(bar_qfree(s), ((n / QS) - 1) & 1, wc);
+          if (!(ok = __all_sync(0xffffffffu, ok))) break;
+          const uint32_t st = s_base + OFF_QR + s * QSTAGE;
+          if (lane == 0) mbar_arrive_expect_tx(bar_q(s), C::TILE_BYTES + (uint32_t)QX_TILE_BYTES);
+          __syncwarp();
           if (lane < C::NBOX)
             tma_load_3d(st + lane * C::BOX_BYTES, &tq, lane * 64, qrow0, q_head, bar_q(s));
-          else if (lane < 2 * C::NBOX)
-            tma_load_3d(st + C::TILE_BYTES + (lane - C::NBOX) * C::BOX_BYTES, &tdo, (lane - C::NBOX) * 64, qrow0,
-                        q_head, bar_q(s));
-          else if (lane == 2 * C::NBOX)
-            bulk_load(st + 2 * C::TILE_BYTES, p.qx + roff * QX_ROW_BYTES, (uint32_t)QX_TILE_BYTES, bar_q(s));
+          else if (lane == C::NBOX)
+            bulk_load(st + C::TILE_BYTES, p.qx + roff * QX_ROW_BYTES, (uint32_t)QX_TILE_BYTES, bar_q(s));
           ++n;
+          const int so = no % OS;
+          if (no >= OS) ok = wait_bar(bar_ofree(so), ((no / OS) - 1) & 1, wc);
+          if (!(ok = __all_sync(0xffffffffu, ok))) break;
+          const uint32_t sto = s_base + OFF_OR + so * C::TILE_BYTES;
+          if (lane == 0) mbar_arrive_expect_tx(bar_o(so), C::TILE_BYTES);
+          __syncwarp();
+          if (lane > C::NBOX && lane <= 2 * C::NBOX)   // other lanes than the Q copies'
+            tma_load_3d(sto + (lane - C::NBOX - 1) * C::BOX_BYTES, &tdo, (lane - C::NBOX - 1) * 64, qrow0, q_head,
+                        bar_o(so));
+          ++no;
           ++nu;
         }
       }
@@ -356,7 +377,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
     }
     if ((!ok || abort_flag) && lane == 0) {   // drain the copies still in flight
       if (uc > 0) wait_bar(bar_kv, (uint32_t)(uc - 1) & 1u, wc, false);
-      for (int j = n - NS < 0 ? 0 : n - NS; j < n; ++j) wait_bar(bar_q(j % NS), (j / NS) & 1, wc, false);
+      for (int j = n - QS < 0 ? 0 : n - QS; j < n; ++j) wait_bar(bar_q(j % QS), (j / QS) & 1, wc, false);
+      for (int j = no - OS < 0 ? 0 : no - OS; j < no; ++j) wait_bar(bar_o(j % OS), (j / OS) & 1, wc, false);
     }
    } else if (warp == 1) {
     {
@@ -379,37 +401,40 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       // is converged), which feeds the pipe faster than a one-lane loop.
       const uint32_t id_s = idesc_bf16(128, 128, false, false);
       const uint32_t id_acc = idesc_bf16(128, D, false, true);
-      constexpr uint32_t STAGE16 = STAGE >> 4, TILE16 = C::TILE_BYTES >> 4;
+      constexpr uint32_t QSTAGE16 = QSTAGE >> 4, TILE16 = C::TILE_BYTES >> 4;
       const uint32_t hi = (uint32_t)(sdesc_sw128(0, 16, 1024) >> 32);
       const uint32_t d_k = (uint32_t)sdesc_sw128(s_base, 16, 1024);
       const uint32_t d_v = (uint32_t)sdesc_sw128(s_base + OFF_V, 16, 1024);
-      const uint32_t d_ring = (uint32_t)sdesc_sw128(s_base + OFF_RING, 16, 1024);              // K-major
-      const uint32_t d_ring_mn = (uint32_t)sdesc_sw128(s_base + OFF_RING, C::BOX_BYTES, 1024);  // MN-major
+      const uint32_t d_q = (uint32_t)sdesc_sw128(s_base + OFF_QR, 16, 1024);               // K-major
+      const uint32_t d_o = (uint32_t)sdesc_sw128(s_base + OFF_OR, 16, 1024);
+      const uint32_t d_q_mn = (uint32_t)sdesc_sw128(s_base + OFF_QR, C::BOX_BYTES, 1024);  // MN-major
+      const uint32_t d_o_mn = (uint32_t)sdesc_sw128(s_base + OFF_OR, C::BOX_BYTES, 1024);
       auto desc = [&](uint32_t lo) { return ((uint64_t)hi << 32) | lo; };
       // the statistics steps: plain K-major operands, two 2 KB planes
       const uint32_t hi_x = (uint32_t)(sdesc_plain(0, QX_TILE_BYTES / 2, 128) >> 32);
       const uint32_t d_ck = (uint32_t)sdesc_plain(s_base + OFF_CONST, QX_TILE_BYTES / 2, 128);
       const uint32_t d_cv = (uint32_t)sdesc_plain(s_base + OFF_CONST + QX_TILE_BYTES, QX_TILE_BYTES / 2, 128);
-      const uint32_t d_qx = (uint32_t)sdesc_plain(s_base + OFF_RING + 2 * C::TILE_BYTES, QX_TILE_BYTES / 2, 128);
+      const uint32_t d_qx = (uint32_t)sdesc_plain(s_base + OFF_QR + C::TILE_BYTES, QX_TILE_BYTES / 2, 128);
       auto desc_x = [&](uint32_t lo) { return ((uint64_t)hi_x << 32) | lo; };
       auto kstep = [](int kk) { return (uint32_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4); };
-      auto issue_st = [&](int slot) {   // S^T = K Q^T
-        const uint32_t qd = d_ring + (uint32_t)slot * STAGE16;
+      auto issue_st = [&](int qslot) {   // S^T = K Q^T
+        const uint32_t qd = d_q + (uint32_t)qslot * QSTAGE16;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) mma_ss_e(tmem + 0, desc(d_k + kstep(kk)), desc(qd + kstep(kk)), id_s, kk > 0);
-        mma_ss_e(tmem + 0, desc_x(d_ck), desc_x(d_qx + (uint32_t)slot * STAGE16), id_s, 1u);   // - lse2 / c
+        mma_ss_e(tmem + 0, desc_x(d_ck), desc_x(d_qx + (uint32_t)qslot * QSTAGE16), id_s, 1u);   // - lse2 / c
         mma_commit_e(bar_s);
       };
-      auto issue_dpt = [&](int slot) {  // dP^T = V dO^T
-        const uint32_t dd = d_ring + (uint32_t)slot * STAGE16 + TILE16;
+      auto issue_dpt = [&](int oslot, int qslot) {  // dP^T = V dO^T
+        const uint32_t dd = d_o + (uint32_t)oslot * TILE16;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss_e(tmem + 128, desc(d_v + kstep(kk)), desc(dd + kstep(kk)), id_s, kk > 0);
-        mma_ss_e(tmem + 128, desc_x(d_cv), desc_x(d_qx + (uint32_t)slot * STAGE16), id_s, 1u);   // - D
+        mma_ss_e(tmem + 128, desc_x(d_cv), desc_x(d_qx + (uint32_t)qslot * QSTAGE16), id_s, 1u);   // - D
         mma_commit_e(bar_dp);
       };
-      int s = 0;
-      uint32_t spar = 0;   // ring slot of the next query tile and the parity of its fill
+      // ring slots of the next query tile and the parities of their fills
+      int s = 0, so = 0;
+      uint32_t spar = 0, sopar = 0;
       int itot = 0;        // query tiles whose dV and dK products were issued, over all units
       int uc = 0;          // units started
       bool ok = true;
@@ -421,16 +446,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
           if (!(ok = wt(bar_q(s), spar))) break;
           tc_fence_after();
           issue_st(s);
-          issue_dpt(s);
+          if (!(ok = wt(bar_o(so), sopar))) break;
+          tc_fence_after();
+          issue_dpt(so, s);
         }
         if (ntile <= 1) mma_commit_e(bar_kvfree);   // no later S^T or dP^T reads this unit's K and V
         int i = 0;   // after the loop: query tiles of this unit whose dV and dK products were issued
         for (; i < ntile; ++i) {
           const bool more = i + 1 < ntile;
-          const int sn = (s + 1 == NS) ? 0 : s + 1;
-          const uint32_t snpar = (s + 1 == NS) ? spar ^ 1u : spar;
+          const int sn = (s + 1 == QS) ? 0 : s + 1;
+          const uint32_t snpar = (s + 1 == QS) ? spar ^ 1u : spar;
+          const int son = (so + 1 == OS) ? 0 : so + 1;
+          const uint32_t sonpar = (so + 1 == OS) ? sopar ^ 1u : sopar;
           const uint32_t par = (uint32_t)itot & 1u;
-          const uint32_t md = d_ring_mn + (uint32_t)s * STAGE16;
+          const uint32_t mq = d_q_mn + (uint32_t)s * QSTAGE16, mo = d_o_mn + (uint32_t)so * TILE16;
           // dV += P^T dO   (dO as an MN-major operand: N = d, K = query rows);
           // the first dV of a unit overwrites the accumulator the previous
           // unit's epilogue reads
@@ -439,9 +468,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < TILE / 16; ++kk)
-            mma_ts_e(tmem + 256, tmem + half_col(kk), desc(md + TILE16 + (uint32_t)kk * (2048 >> 4)), id_acc,
+            mma_ts_e(tmem + 256, tmem + half_col(kk), desc(mo + (uint32_t)kk * (2048 >> 4)), id_acc,
                      (i > 0 || kk > 0));
           mma_commit_e(bar_dv);
+          mma_commit_e(bar_ofree(so));   // dP^T_i and dV_i have read dO_i
           if (more) {
             if (!(ok = wt(bar_q(sn), snpar))) break;
             tc_fence_after();
@@ -452,16 +482,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < TILE / 16; ++kk)
-            mma_ts_e(tmem + 256 + D, tmem + 128 + half_col(kk), desc(md + (uint32_t)kk * (2048 >> 4)), id_acc,
+            mma_ts_e(tmem + 256 + D, tmem + 128 + half_col(kk), desc(mq + (uint32_t)kk * (2048 >> 4)), id_acc,
                      (i > 0 || kk > 0));
           mma_commit_e(bar_dk);
           mma_commit_e(bar_qfree(s));
           if (more) {
-            issue_dpt(sn);
+            if (!(ok = wt(bar_o(son), sonpar))) break;
+            tc_fence_after();
+            issue_dpt(son, sn);
             if (i + 2 == ntile) mma_commit_e(bar_kvfree);   // the unit's last S^T and dP^T are issued
           }
           s = sn;
           spar = snpar;
+          so = son;
+          sopar = sonpar;
           ++itot;
         }
         if (p.dkdv_counts != nullptr && lane == 0) p.dkdv_counts[(size_t)DEBUG_FIELDS * (u_begin + ju) + 5] = i;
@@ -1074,8 +1108,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
 
 template <int D>
 constexpr uint32_t dkdv_smem() {   // K, V, the ring, the constant operands, 8 x 1 KB of epilogue staging, alignment
-  return 2 * BwdCfg<D>::TILE_BYTES + BwdCfg<D>::NS * (2 * BwdCfg<D>::TILE_BYTES + (uint32_t)QX_TILE_BYTES) +
-         2 * (uint32_t)QX_TILE_BYTES + 8 * 1024 + 1024;
+  return 2 * BwdCfg<D>::TILE_BYTES + BwdCfg<D>::QS * (BwdCfg<D>::TILE_BYTES + (uint32_t)QX_TILE_BYTES) +
+         BwdCfg<D>::OS * BwdCfg<D>::TILE_BYTES + 2 * (uint32_t)QX_TILE_BYTES + 8 * 1024 + 1024;
 }
 template <int D, bool F32>
 cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
