@@ -53,6 +53,7 @@ KERNEL_SOURCES = {
     "bwd_preprocess": ["merge.cu", "ptx.cuh", "internal.h"],
     "merge": ["merge.cu", "ptx.cuh", "internal.h"],
     "fwd_fp8": ["fwd_fp8.cu", "ptx.cuh", "schedule.h", "internal.h"],
+    "decode": ["fwd.cu", "ptx.cuh", "schedule.h", "internal.h"],   # the forward kernel in decode mode
 }
 
 
