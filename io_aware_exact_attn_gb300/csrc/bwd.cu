@@ -1034,8 +1034,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
       }
     }
     if (ok && !abort_flag) {
-      // dQ MMAs complete in issue order: the last one covers them all
+      // dQ MMAs complete in issue order: the last one covers them all.  With
+      // no key tile the Q and dO copies were still issued, and their memory
+      // stages the rows below: wait until they have landed
       if (j > 0) ok = __all_sync(0xffffffffu, wait_bar(bar_dq(j - 1), ((j - 1) >> 1) & 1, wc));
+      else ok = __all_sync(0xffffffffu, wait_bar(bar_qdo, 0, wc));
       if (ok) {
         tc_fence_after();
         // each warpgroup writes its half of the dQ rows (D / 2 columns, scaled

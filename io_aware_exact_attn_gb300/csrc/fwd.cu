@@ -479,8 +479,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       const bool have = it > 0;
       if (have) {
         ok = wait_bar(bar_o(t), (it - 1) & 1, wc);
-        ok = __all_sync(0xffffffffu, ok);
+      } else {   // no key tile: the bf16 rows below are staged where the Q copy may still be landing
+        ok = wait_bar(bar_q, 0, wc);
       }
+      ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
         const bool valid_row = qrow < u.nq;

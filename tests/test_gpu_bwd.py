@@ -70,15 +70,19 @@ def test_bwd_block_sparse(cib, d):
     check_full(1, 2, 2, N, d, "block_sparse", bm, cib)
 
 
-def test_bwd_empty_block_row_and_column():
-    N, d = 512, 64
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_empty_block_row_and_column(d):
+    """A query tile that sees no key tile (its dQ rows, staged at d = 128 where
+    its Q copy lands, are 0) and a key tile nobody sees (dK, dV = 0)."""
+    N = 512
     bm = np.ones((4, 4), bool)
     bm[1, :] = False          # rows 128..255 see nothing
     bm[:, 2] = False          # keys 256..383 seen by nobody
     (q, k, v, do), (dq, dk, dv) = run(1, 2, 2, N, d, "block_sparse", bm)
     assert torch.all(dq[:, :, 128:256] == 0)
     assert torch.all(dk[:, :, 256:384] == 0) and torch.all(dv[:, :, 256:384] == 0)
-    gq, gk, gv = oracle.attention_backward(f64(q), f64(k), f64(v), f64(do), 1 / 8, mask_spec("block_sparse", bm))
+    gq, gk, gv = oracle.attention_backward(f64(q), f64(k), f64(v), f64(do), 1 / np.sqrt(d),
+                                           mask_spec("block_sparse", bm))
     assert_grad(f64(dq), gq)
     assert_grad(f64(dk), gk)
     assert_grad(f64(dv), gv)

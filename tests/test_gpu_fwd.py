@@ -78,9 +78,11 @@ def test_block_sparse_special_masks():
     assert torch.equal(o3, o4) and torch.equal(l3, l4)
 
 
-def test_fully_masked_rows():
-    """A block row with no kept block: O = 0 and LSE = -inf for its rows."""
-    N, d = 384, 64
+@pytest.mark.parametrize("d", [64, 128])
+def test_fully_masked_rows(d):
+    """A block row with no kept block: O = 0 and LSE = -inf for its rows (the
+    bf16 rows of such a tile are staged where its Q copy lands)."""
+    N = 384
     q, k, v, _ = make(1, 1, 1, N, d)
     bm = np.ones((3, 3), bool)
     bm[1, :] = False
@@ -88,7 +90,7 @@ def test_fully_masked_rows():
     torch.cuda.synchronize()
     assert torch.all(o[0, 0, 128:256] == 0)
     assert torch.all(torch.isneginf(l[0, 0, 128:256]))
-    o_ref, l_ref = oracle.attention_forward(f64(q), f64(k), f64(v), 1 / 8, mask_spec("block_sparse", bm))
+    o_ref, l_ref = oracle.attention_forward(f64(q), f64(k), f64(v), 1 / np.sqrt(d), mask_spec("block_sparse", bm))
     assert_o_lse(f64(o), f64(l), o_ref, l_ref)
 
 
