@@ -163,3 +163,42 @@ def test_chunked_forward_backward_helpers_match_monolithic():
     assert float((lse - l_m).abs().max()) <= 2e-3
     for name, got, want in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
         assert_grad(f64(got), f64(want), f"helpers {name}")
+
+
+def test_preprocess_writes_the_statistics_operand():
+    """The workspace of attn_bwd_preprocess: D (rowsum(dO * O), checked against
+    the oracle's forward output) and LSE * log2 e as float32, then per padded
+    row 16 bf16 values [l l l, l l l, l l l, e e e, 0 0 0 0] (l = -LSE log2 e,
+    e = -D, each a three-term split) in 128-row blocks of two 16-byte planes;
+    the three terms sum to the float32 value to 2^-20 relative and padding rows
+    hold -2^100 and 0."""
+    B, Hq, Nq, d = 1, 2, 200, 64
+    q, k, v, do = make(B, Hq, Hq, Nq, d)
+    o, lse = api.attn_fwd(q, k, v, causal=True)
+    ws = api.attn_bwd_preprocess(o, lse, do)
+    torch.cuda.synchronize()
+    Np = 256
+    rows = B * Hq * Np
+    arr = (rows * 4 + 255) // 256 * 256
+    raw = ws.cpu()
+    dsum = raw[:rows * 4].view(torch.float32).double().numpy()
+    lse2 = raw[arr:arr + rows * 4].view(torch.float32).double().numpy()
+    qx = raw[2 * arr:2 * arr + rows * 32].view(torch.bfloat16).double().numpy().reshape(rows // 128, 2, 128, 8)
+    qx = np.concatenate([qx[:, 0], qx[:, 1]], axis=-1).reshape(rows, 16)   # row-major [row][16]
+    valid = np.zeros(rows, bool)
+    for h in range(B * Hq):
+        valid[h * Np:h * Np + Nq] = True
+    # D against the oracle's O and the same dO
+    of, _ = oracle.attention_forward(f64(q), f64(k), f64(v), 1 / math.sqrt(d), mask_spec("causal"))
+    d_ref = (of * f64(do)).sum(-1).reshape(-1)
+    np.testing.assert_allclose(dsum[valid], d_ref, rtol=2e-2, atol=2e-2)
+    np.testing.assert_allclose(lse2[valid], lse.cpu().double().numpy().reshape(-1) * math.log2(math.e), rtol=1e-6)
+    assert np.all(dsum[~valid] == 0) and np.all(np.isposinf(lse2[~valid]))
+    l3 = qx[:, 0:3].sum(1)
+    for rep in (3, 6):   # the lse2 triple three times
+        assert np.array_equal(qx[:, rep:rep + 3], qx[:, 0:3])
+    e3 = qx[:, 9:12].sum(1)
+    assert np.all(qx[:, 12:] == 0)
+    np.testing.assert_allclose(l3[valid], -lse2[valid], rtol=2 ** -20, atol=0)
+    np.testing.assert_allclose(e3[valid], -dsum[valid], rtol=2 ** -20, atol=1e-30)
+    assert np.all(l3[~valid] == -2.0 ** 100) and np.all(e3[~valid] == 0)

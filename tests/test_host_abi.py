@@ -83,6 +83,12 @@ def test_argument_validation_without_gpu(lib):
     need = lib.attn_bwd_workspace_bytes(2, 4, 2, 100, 64)
     rows = 2 * 4 * 128   # padded query rows: D and LSE*log2 e (float32), then 32 bytes each
     assert need == 2 * ((rows * 4 + 255) // 256) * 256 + rows * 32
+    # ragged: (B+1) ints, then the same statistics for Hq * (total + 127 B) rows, the
+    # 32-byte rows in whole 128-row blocks
+    vrows = 4 * (1000 + 127 * 3)
+    vneed = ((4 * 4 + 255) // 256) * 256 + 2 * ((vrows * 4 + 255) // 256) * 256 + \
+        (((vrows + 127) // 128) * 4096 + 255) // 256 * 256
+    assert lib.attn_varlen_bwd_workspace_bytes(3, 1000, 4) == vneed
     p = [_ptr(good)] * 10
     assert lib.attn_bwd(*p, need - 256, 2, 4, 2, 100, 64, 0.125, None, None) == -6
     # chunked backward: workspace, pointer, offset and size checks come before any device call
