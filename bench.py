@@ -98,11 +98,22 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def code_text(src):
+    """A source file's code with its comments and blank lines removed, so that
+    editing a comment does not mark the ncu summaries of its kernels stale
+    (string literals in these sources hold no comment markers)."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in src.splitlines())
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def source_hash(kernel):
+    """Hash of the code (comments excluded) a kernel is compiled from; an ncu
+    summary whose recorded hash differs was taken on other code."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES.get(kernel, []):
-        with open(os.path.join(ROOT, "io_aware_exact_attn_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "io_aware_exact_attn_gb300", "csrc", f)) as fh:
+            h.update(code_text(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

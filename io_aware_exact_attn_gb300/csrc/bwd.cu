@@ -10,20 +10,25 @@
 //   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  dQ = scale dS K,
 //   dK = scale dS^T Q.
 // Two kernels, both TMA-fed with tcgen05 accumulators in tensor memory:
-//   dkdv_kernel  one CTA per 128-key tile of one (batch, kv head); loops over
-//                the query tiles that see the key tile, for every query head of
-//                the GQA group, so dK and dV need no atomics.  Per query tile:
-//                S^T = K Q^T, dP^T = V dO^T (tensor cores), P^T and dS^T
-//                (softmax warpgroup, written back to tensor memory as bf16),
-//                dV += P^T dO, dK += dS^T Q (A operand from tensor memory).
+//   dkdv_kernel  a run of 128-key tiles of (batch, kv head) per CTA; loops
+//                over the query tiles that see each key tile, for every query
+//                head of the GQA group, so dK and dV need no atomics.  Per
+//                query tile: S^T - lse2/c = K Q^T and dP^T - D = V dO^T
+//                (tensor cores; the per-query statistics enter through one
+//                extra K = 16 step of each product), P^T and dS^T
+//                (elementwise warpgroups, written back to tensor memory as
+//                bf16), dV += P^T dO, dK += dS^T Q (A operand from tensor
+//                memory).
 //   dq_kernel    one CTA per 128-row query tile of one (batch, query head);
 //                loops over the key tiles it sees: S = Q K^T, dP = dO V^T,
 //                dS = P * (dP - D), dQ += dS K, dQ accumulated in fp32 in
 //                tensor memory and scaled / rounded once at the end.
-// Warp roles (12 warps): warp 0 TMA producer, warp 1 MMA issuer (one elected lane,
-// owns the TMEM allocation), warps 2-3 idle, warps 4-11 elementwise work in
-// two warpgroups that split the 128 columns of every tile row between them
-// (warp w owns TMEM lanes 32*(w%4)..+31; one thread per row and half).
+// Warp roles (12 warps): warp 0 TMA producer (the dQ kernel's second
+// producer is warp 2), warp 1 MMA issuer (one elected lane, owns the TMEM
+// allocation), warps 4-11 elementwise work in two warpgroups that split the
+// 128 columns of every tile row between them (warp w owns TMEM lanes
+// 32*(w%4)..+31; one thread per row and half); warps 1-3 of the dK/dV kernel
+// first decode the run's units.
 #include <type_traits>
 
 #include "internal.h"
