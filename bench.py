@@ -83,11 +83,13 @@ def kernel_work(w):
     }
 
 
-def executed_gemms(kernel):
+def executed_gemms(kernel, d):
     """N x N x d products each kernel runs per step, counted or not: the dQ
-    kernel recomputes S and dP next to its dQ product, so the backward runs
-    seven products for the five the metric's 2.5x convention credits."""
-    return {"fwd": 2, "bwd_dkdv": 4, "bwd_dq": 3}.get(kernel)
+    kernel recomputes S and dP next to its dQ product, and the dK/dV
+    kernel's S^T and dP^T products each have one more K = 16 step (the
+    per-query statistics), so the backward runs 7 + 32/d products for the five
+    the metric's 2.5x convention credits."""
+    return {"fwd": 2, "bwd_dkdv": 4 + 2 * 16 / d, "bwd_dq": 3}.get(kernel)
 
 
 def load_peaks():
@@ -399,7 +401,7 @@ def main():
         if kind == "tensor":
             entry["tflops"] = amount / (avg * 1e-3) / 1e12
             gem = 2.0 * w["B"] * w["Hq"] * w["N"] * w["N"] * w["d"] * (0.5 if w["mask"] == "causal" else 1.0)
-            entry["tflops_executed"] = executed_gemms(name) * gem / (avg * 1e-3) / 1e12
+            entry["tflops_executed"] = executed_gemms(name, w["d"]) * gem / (avg * 1e-3) / 1e12
         elif kind == "hbm":
             entry["gbs"] = amount / (avg * 1e-3) / 1e9
         kernels[name] = entry
