@@ -47,3 +47,29 @@ def test_static_scratch_backward_matches_attn_bwd(cuda_lib):
             assert torch.equal(got, want), f"{name} B{B} H{Hq}/{Hkv} N{N} d{d}"
             assert_grad(f64(got), f64(want), f"{name} B{B} H{Hq}/{Hkv} N{N} d{d}")
         assert api.get_status() == 0
+
+
+@pytest.mark.gpu
+def test_static_scratch_at_its_row_limit(cuda_lib):
+    """The largest call the static scratch takes (B*Hq*ceil(N/128)*128 = 2^20
+    query rows, so the statistics operand ends at the array's last byte) gives
+    the same gradients as attn_bwd; one row tile more is refused."""
+    lib = cuda_lib
+    B, Hq, Hkv, N, d = 1, 16, 4, 65536, 64
+    q, k, v, do = make(B, Hq, Hkv, N, d)
+    o, lse = api.attn_fwd(q, k, v, causal=True)
+    ref = api.attn_bwd(q, k, v, o, lse, do, causal=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    m, _ = api.mask_desc(causal=True)
+    stream = torch.cuda.current_stream().cuda_stream
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(), dq.data_ptr(),
+            dk.data_ptr(), dv.data_ptr())
+    rc = lib.attn_bwd_static_scratch(*args, B, Hq, Hkv, N, d, 1.0 / d ** 0.5, C.byref(m), stream)
+    assert rc == 0, lib.attn_last_error_message()
+    torch.cuda.synchronize()
+    for name, got, want in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        assert torch.equal(got, want), name
+    assert api.get_status() == 0
+    # 2^20 + 128 rows: refused before any device work
+    rc = lib.attn_bwd_static_scratch(*args, B, Hq, Hkv, N + 8, d, 1.0 / d ** 0.5, C.byref(m), stream)
+    assert rc == -6
