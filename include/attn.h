@@ -161,7 +161,8 @@ int attn_merge_lse(const float* const* o_parts, const float* const* lse_parts,
  * pass needs no recomputed forward; "FlashAttention-2" reviews, second review
  * items 2-3: LSE saved for the backward pass, query-derivative update
  * restructured).  Three launches on `stream`:
- *   1. D = rowsum(dO * O) per query row (float32, into the workspace);
+ *   1. D = rowsum(dO * O) and LSE * log2 e per query row (float32, and as
+ *      the dK/dV kernel's bf16 statistics operand; into the workspace);
  *   2. dK, dV per key tile, looping over the query tiles (and the query heads
  *      of its GQA group) that see it;
  *   3. dQ per query tile, accumulated in float32 on chip, looping over the key
@@ -262,7 +263,8 @@ int attn_varlen_fwd(const void* q, const void* k, const void* v, void* o, float*
  *   dq          device bf16 [total, Hq, d]    dk, dv device bf16 [total, Hkv, d]
  *   workspace   device, >= attn_varlen_bwd_workspace_bytes(B, total, Hq)
  *               bytes, 256-byte aligned; caller-owned.  It holds the
- *               per-sequence tile-padded offsets and D, LSE*log2 e per row.
+ *               per-sequence tile-padded offsets and the per-row statistics
+ *               of attn_bwd's workspace.
  * GQA: dK / dV sum over the query heads of a group, as in attn_bwd.
  */
 int attn_varlen_bwd(const void* q, const void* k, const void* v, const void* o,
