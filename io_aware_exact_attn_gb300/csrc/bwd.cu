@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
   constexpr uint32_t OFF_EPI = OFF_CONST + 2 * (uint32_t)QX_TILE_BYTES;   // 8 x 1 KB epilogue staging
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bars[1 + 2 * QS + 2 * OS + 9];
+  __shared__ __align__(8) uint64_t bars[1 + 2 * QS + 2 * OS + 10];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ KvUnit units[MAX_KV_RUN];   // this CTA's units, decoded once
@@ -235,7 +235,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
   constexpr int B0 = 1 + 2 * QS + 2 * OS;
   const uint32_t bar_s = smem_u32(&bars[B0 + 0]);
   const uint32_t bar_dp = smem_u32(&bars[B0 + 1]);
-  const uint32_t bar_p = smem_u32(&bars[B0 + 2]);
+  const uint32_t bar_p = smem_u32(&bars[B0 + 2]);    // P^T of the second 32 columns of each half written
+  const uint32_t bar_pa = smem_u32(&bars[B0 + 9]);   // P^T of the first 32 columns of each half written
   const uint32_t bar_ds = smem_u32(&bars[B0 + 3]);
   const uint32_t bar_dv = smem_u32(&bars[B0 + 4]);
   const uint32_t bar_dk = smem_u32(&bars[B0 + 5]);
@@ -272,6 +273,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
     mbar_init(bar_p, 256);
+    mbar_init(bar_pa, 256);
     mbar_init(bar_ds, 256);
     mbar_init(bar_dv, 1);
     mbar_init(bar_dk, 1);
@@ -465,16 +467,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
           const uint32_t sonpar = (so + 1 == OS) ? sopar ^ 1u : sopar;
           const uint32_t par = (uint32_t)itot & 1u;
           const uint32_t mq = d_q_mn + (uint32_t)s * QSTAGE16, mo = d_o_mn + (uint32_t)so * TILE16;
-          // dV += P^T dO   (dO as an MN-major operand: N = d, K = query rows);
-          // the first dV of a unit overwrites the accumulator the previous
-          // unit's epilogue reads
-          if (!(ok = wt(bar_p, par))) break;
+          // dV += P^T dO   (dO as an MN-major operand: N = d, K = query rows),
+          // in the order phase A hands P^T over: first the k-steps of the
+          // first 32 query columns of each half (0, 1, 4, 5), while the
+          // elementwise warps still compute the rest, then 2, 3, 6, 7.  The
+          // first dV of a unit overwrites the accumulator the previous unit's
+          // epilogue reads
+          if (!(ok = wt(bar_pa, par))) break;
           if (i == 0 && uc > 0 && !(ok = wt(bar_accfree, (uint32_t)(uc - 1) & 1u))) break;
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < TILE / 16; ++kk)
-            mma_ts_e(tmem + 256, tmem + half_col(kk), desc(mo + (uint32_t)kk * (2048 >> 4)), id_acc,
-                     (i > 0 || kk > 0));
+          for (int q = 0; q < 4; ++q) {
+            const int kk = (q & 1) + 4 * (q >> 1);
+            mma_ts_e(tmem + 256, tmem + half_col(kk), desc(mo + (uint32_t)kk * (2048 >> 4)), id_acc, (i > 0 || q > 0));
+          }
+          if (!(ok = wt(bar_p, par))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int kk = 2 + (q & 1) + 4 * (q >> 1);
+            mma_ts_e(tmem + 256, tmem + half_col(kk), desc(mo + (uint32_t)kk * (2048 >> 4)), id_acc, 1u);
+          }
           mma_commit_e(bar_dv);
           mma_commit_e(bar_ofree(so));   // dP^T_i and dV_i have read dO_i
           if (more) {
@@ -547,17 +560,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
           const bool wedge = base + (TILE - 1) >= window_of(p);
           const int hi = wedge ? window_of(p) + r - base : TILE;
           // phase A: P^T = 2^((S^T - lse2/c) c) for this warpgroup's 64 query columns,
-          // kept in fp32 for phase B and rounded to bf16 pairs for dV = P^T dO.
-          // Masked tiles (the diagonal, a window's edge) take their own copy of
-          // the loop so that the others carry no mask arithmetic at all.
+          // kept in fp32 for phase B and rounded to bf16 pairs for dV = P^T dO,
+          // in two passes of 32 columns, each handed to the tensor core as
+          // soon as it is written (its pairs go over the first 16 of the
+          // columns it has read).  Masked tiles (the diagonal, a window's
+          // edge) take their own copy of the loop so that the others carry no
+          // mask arithmetic at all.
           float pf[64];
-          auto phase_a = [&](auto masked) {
-            uint32_t sr[64];
-            tmem_ld64(tmem + lane_off + cb, sr);
-            const int lo = cedge ? r - base : 0;        // visible query columns: lo <= j < hi
+          const int lo = cedge ? r - base : 0;        // visible query columns: lo <= j < hi
+          auto phase_a = [&](auto masked, auto pass) {
+            constexpr int G = decltype(pass)::value;
+            uint32_t sr[32];
+            tmem_ld32(tmem + lane_off + cb + 32 * G, sr);
 #pragma unroll
-            for (int j4 = 0; j4 < 16; ++j4) {
-              const int col = cb + 4 * j4;
+            for (int j4 = 0; j4 < 8; ++j4) {
+              const int col = cb + 32 * G + 4 * j4;
               float x0, x1, x2, x3;
               mul2(x0, x1, __uint_as_float(sr[4 * j4 + 0]), __uint_as_float(sr[4 * j4 + 1]), c, c);
               mul2(x2, x3, __uint_as_float(sr[4 * j4 + 2]), __uint_as_float(sr[4 * j4 + 3]), c, c);
@@ -568,22 +585,25 @@ __global__ void __launch_bounds__(BwdCfg<D>::SPLIT_THREADS, 1)
                 p2 = (col + 2 >= lo && col + 2 < hi) ? p2 : 0.f;
                 p3 = (col + 3 >= lo && col + 3 < hi) ? p3 : 0.f;
               }
-              pf[4 * j4 + 0] = p0;
-              pf[4 * j4 + 1] = p1;
-              pf[4 * j4 + 2] = p2;
-              pf[4 * j4 + 3] = p3;
+              pf[32 * G + 4 * j4 + 0] = p0;
+              pf[32 * G + 4 * j4 + 1] = p1;
+              pf[32 * G + 4 * j4 + 2] = p2;
+              pf[32 * G + 4 * j4 + 3] = p3;
             }
-          };
-          if (cedge || wedge) phase_a(std::true_type{});
-          else phase_a(std::false_type{});
-          {
-            uint32_t pk[32];
+            uint32_t pk[16];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) pk[j] = pack_bf16(pf[2 * j], pf[2 * j + 1]);
-            tmem_st32(tmem + lane_off + cb, pk);
+            for (int j = 0; j < 16; ++j) pk[j] = pack_bf16(pf[32 * G + 2 * j], pf[32 * G + 2 * j + 1]);
+            tmem_st16(tmem + lane_off + cb + 16 * G, pk);
+            tc_fence_before();
+            mbar_arrive(G == 0 ? bar_pa : bar_p);
+          };
+          if (cedge || wedge) {
+            phase_a(std::true_type{}, std::integral_constant<int, 0>{});
+            phase_a(std::true_type{}, std::integral_constant<int, 1>{});
+          } else {
+            phase_a(std::false_type{}, std::integral_constant<int, 0>{});
+            phase_a(std::false_type{}, std::integral_constant<int, 1>{});
           }
-          tc_fence_before();
-          mbar_arrive(bar_p);
           ok = wait_bar(bar_dp, i & 1, wc);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
