@@ -524,13 +524,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           }
         }
         if constexpr (!OUT_F32) {
-          // bf16 rows staged through the Q tiles (no MMA reads them once this
-          // tile's last P.V has completed), so each store covers whole rows
+          // bf16 rows staged through a Q tile, so each store covers whole
+          // rows.  Tile t stages in Q_t: no MMA reads it once this tile's last
+          // P.V has completed.  Alternating decode loads Q_0 alone and both
+          // tiles' S read it, so an S of tile 1 may still be reading Q_0 when
+          // tile 0 ends: there tile 0 stages in the unused Q_1 and tile 1, whose
+          // last P.V follows every other MMA of the unit, in Q_0.
           const int wrow = trow0 + wq * 32;   // this warp's first local row
+          const int region = u.alternate ? 1 - t : t;
           char* base = reinterpret_cast<char*>(static_cast<__nv_bfloat16*>(p.o) +
                                                (size_t)(split_off * D + (int64_t)u.bh * p.o_hs +
                                                         (u.seq0 + wrow) * p.o_rs));
-          warp_store_rows<D / 8>(s_base + (uint32_t)(warp - 4) * (32u * D * 2), ob, base,
+          warp_store_rows<D / 8>(s_base + (uint32_t)(region * 4 + wq) * (32u * D * 2), ob, base,
                                  (size_t)p.o_rs * sizeof(__nv_bfloat16), u.nq - wrow);
         }
         if (valid_row && p.lse != nullptr)
